@@ -1,0 +1,409 @@
+"""Benchmark of the deformable convolution layer (forward + backward) on GB300.
+
+One step = one forward and one backward pass of the layer over one batch of
+synthetic input, through the C ABI (offset convolution + bilinear sampling
+fused in K1, main convolution GEMM, and the backward kernels).  Inputs are
+resident in HBM when the timed region starts; L2 is flushed (a 256 MiB write,
+outside the timed events) before every timed step.  The step is captured once
+in a CUDA graph and replayed.
+
+Prints one JSON line.  ``--impl reference`` times the fp64 CPU oracle instead
+(the reference arm: a deliberately slow, obviously correct program on the host
+cores), on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "deform-conv layer fwd+bwd ms and GFLOP/s; sampling-stage HBM GB/s vs GB300 peak"
+FLUSH_BYTES = 256 << 20
+
+# DRAM traffic of one K1 launch from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by the workload; valid only while the kernel
+# source hashes to the recorded value.
+K1_TRAFFIC = {}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="res3_bf16")
+    ap.add_argument("--eager", action="store_true", help="no CUDA graph")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="budget of the oracle's CPU-baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if os.environ.get("DC_BENCH_GLOO") is None else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v, device):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def source_hash(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of the SM clock and throttle reasons."""
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.out.flush()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                if self.uuid and parts[0] != self.uuid:
+                    continue
+                rows.append(parts)
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def cpu_baseline(wl, seconds):
+    """The oracle, as it stands, on image 0 of the workload (fwd + bwd),
+    repeated until `seconds` have passed (at least once)."""
+    import torch
+
+    import oracle
+    from deformable_convolution_gb300 import workloads as W
+    d = W.generate(wl)
+    one = {k: (None if v is None else (v[:1] if k in ("x", "offset_add", "grad_y") else v))
+           for k, v in d.items()}
+    p1 = wl.problem(1)
+    op = oracle.Problem(1, p1.c_in, p1.h, p1.w, p1.c_out, p1.kh, p1.kw, p1.stride, p1.pad,
+                        p1.dil, p1.offset_groups)
+    f64 = lambda t: None if t is None else t.double().numpy()  # noqa: E731
+    args = [f64(one[k]) for k in ("x", "w_off", "b_off", "w", "offset_add")]
+    flops = 3 * W.conv_flops(p1)
+    runs, t0 = 0, time.perf_counter()
+    while True:
+        y, off = oracle.forward(op, *args)
+        oracle.backward(op, args[0], args[1], args[3], off, f64(one["grad_y"]))
+        runs += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    per = el / runs
+    return {"value": flops / per / 1e9, "unit": "GFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"image 0 of {wl.name} (N=1 of {wl.n}), fwd+bwd in fp64, {runs} run(s), "
+                      f"{per * 1e3:.0f} ms each", "ms_per_image": per * 1e3}
+
+
+def run_reference(args, world, rank):
+    from deformable_convolution_gb300 import workloads as W
+    if rank != 0:
+        return
+    wl = W.WORKLOADS[args.workload]
+    p = wl.problem()
+    flops_full = 3 * W.conv_flops(p)
+    for _ in range(args.warmup):
+        cpu_baseline(wl, 0.0)
+    t = []
+    info = None
+    for _ in range(args.steps):
+        info = cpu_baseline(wl, 0.0)
+        t.append(info["ms_per_image"])
+    ms_img = sum(t) / len(t)
+    gflops = info["value"]
+    line = {"impl": "reference", "metric": METRIC, "value": gflops, "unit": "GFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_img * wl.n, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "n": wl.n, "c_in": wl.c_in, "c_out": wl.c_out,
+                       "h": wl.h, "w": wl.w, "k": wl.k, "offset_groups": wl.groups,
+                       "step": "image 0 of the batch per step (oracle, host cores); "
+                               "ms_per_step extrapolated x N"},
+            "cpu_baseline": {"value": gflops, "unit": "GFLOP/s", "cores": info["cores"],
+                             "kind": "oracle", "sample": info["sample"]},
+            "e2e": {"value": gflops, "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "flops_per_step": flops_full}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    import torch
+
+    from deformable_convolution_gb300 import binding as B
+    from deformable_convolution_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = W.WORKLOADS[args.workload]
+    p = wl.problem()
+    d = W.generate(wl)
+    t = {k: (None if v is None else v.to(dev)) for k, v in d.items()}
+    s = p.shapes()
+    y = torch.empty(s["y"], dtype=p.torch_dtype, device=dev)
+    off = torch.empty(s["offset"], dtype=torch.float32, device=dev)
+    gx = torch.empty(s["x"], dtype=torch.float32, device=dev)
+    gwo = torch.empty(s["w_off"], dtype=torch.float32, device=dev)
+    gbo = torch.empty(s["b_off"], dtype=torch.float32, device=dev)
+    gw = torch.empty(s["w"], dtype=torch.float32, device=dev)
+    goff = torch.empty(s["offset"], dtype=torch.float32, device=dev)
+    ws = B.workspace(p, True, dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        B.deform_conv_fwd(p, t["x"], t["w_off"], t["b_off"], t["w"], t["offset_add"], y, off,
+                          None, ws)
+        B.deform_conv_bwd(p, t["x"], t["w_off"], t["w"], off, t["grad_y"], gx, gwo, gbo, gw,
+                          goff, ws)
+
+    launches_before = B.launch_count()
+    with torch.cuda.stream(stream):
+        step()  # first call (attributes, module load) outside any capture
+    torch.cuda.synchronize(dev)
+    launches_per_step = B.launch_count() - launches_before
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        torch.cuda.synchronize(dev)
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            flush.fill_(1)
+            run_step()
+    torch.cuda.synchronize(dev)
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = "GPU-" + str(props.uuid) if hasattr(props, "uuid") else None
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            run_step()
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    total_ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends))
+    total_ms = max_over_ranks(world, total_ms, dev)
+    ms_step = total_ms / args.steps
+    flops_step = 3 * W.conv_flops(p)
+    value = flops_step * world / (ms_step / 1e3) / 1e9
+
+    line = {"metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": wl.dtype_name, "data": "synthetic",
+            "config": {"workload": wl.name, "n": wl.n, "c_in": wl.c_in, "c_out": wl.c_out,
+                       "h": wl.h, "w": wl.w, "k": wl.k, "stride": wl.stride, "pad": wl.pad,
+                       "dil": wl.dil, "offset_groups": wl.groups,
+                       "offsets": f"N(0,{wl.sigma}) px" + (
+                           f" + {wl.outlier_p:.0%} outliers at +-{wl.outlier_px} px"
+                           if wl.outlier_p else ""),
+                       "l2": "flushed (256 MiB write) before every timed step",
+                       "graph": graph is not None, "parallelism": f"replicas x{world}"},
+            "flops_per_step": flops_step, "wall_s_timed_region": wall,
+            "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
+
+    if rank == 0:
+        line["roofline"] = k1_roofline(p, t, dev, stream, flush, wl)
+        line["e2e"] = e2e(p, d, dev, stream, flops_step)
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+            line["cpu_baseline"].pop("ms_per_image", None)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def k1_bytes(p, has_add):
+    """Algorithmic bytes of one K1 launch: read x and w_off once, write the
+    deformed map and the fp32 offsets (and read offset_add when given)."""
+    elt = 2 if p.dtype == 1 else 4
+    P = p.n * p.ho * p.wo
+    b = p.n * p.c_in * p.h * p.w * elt + p.n_off * p.c_in * p.kh * p.kw * elt
+    b += p.c_in * p.kh * p.kw * P * elt + p.n_off * P * 4
+    if has_add:
+        b += p.n_off * P * 4
+    return b
+
+
+def k1_roofline(p, t, dev, stream, flush, wl, iters=200):
+    import torch
+
+    from deformable_convolution_gb300 import binding as B
+    col = torch.empty(p.shapes()["col"], dtype=p.torch_dtype, device=dev)
+    off = torch.empty(p.shapes()["offset"], dtype=torch.float32, device=dev)
+
+    def launch():
+        B.deform_conv_sample(p, t["x"], t["w_off"], t["b_off"], t["offset_add"], None, col, off)
+
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            flush.fill_(3)
+            launch()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(iters)]
+        torch.cuda.synchronize(dev)
+        for a, b in ev:
+            flush.fill_(7)
+            a.record(stream)
+            launch()
+            b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in ev) / iters
+    nbytes = k1_bytes(p, t["offset_add"] is not None)
+    peaks, src = measured_peaks()
+    achieved = nbytes / (ms / 1e3) / 1e9
+    src_hash = source_hash(os.path.join(ROOT, "deformable_convolution_gb300", "csrc",
+                                        "k1_sample.cu"))
+    rec = K1_TRAFFIC.get(wl.name)
+    traffic = rec["bytes"] if rec and rec["source"] == src_hash else None
+    return {"kernel": "k1_fused_sample (offset conv + bilinear sampling)", "bound": "hbm",
+            "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{src} (hbm_gbs, burst)",
+            "traffic": traffic, "algorithmic_bytes": nbytes, "ms_per_launch": ms}
+
+
+def e2e(p, d, dev, stream, flops_step, iters=20):
+    """Same metric through the ABI with host buffers: every step copies its
+    inputs from pinned host memory and reads the outputs back."""
+    import torch
+
+    from deformable_convolution_gb300 import binding as B
+    host = {k: (None if v is None else v.pin_memory()) for k, v in d.items()}
+    devt = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in d.items()}
+    s = p.shapes()
+    outs = dict(y=torch.empty(s["y"], dtype=p.torch_dtype, device=dev),
+                off=torch.empty(s["offset"], dtype=torch.float32, device=dev),
+                gx=torch.empty(s["x"], dtype=torch.float32, device=dev),
+                gwo=torch.empty(s["w_off"], dtype=torch.float32, device=dev),
+                gbo=torch.empty(s["b_off"], dtype=torch.float32, device=dev),
+                gw=torch.empty(s["w"], dtype=torch.float32, device=dev),
+                goff=torch.empty(s["offset"], dtype=torch.float32, device=dev))
+    hout = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in outs.items()}
+    ws = B.workspace(p, True, dev)
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = sum(v.numel() * v.element_size() for v in hout.values())
+
+    def one():
+        for k, v in host.items():
+            if v is not None:
+                devt[k].copy_(v, non_blocking=True)
+        B.deform_conv_fwd(p, devt["x"], devt["w_off"], devt["b_off"], devt["w"],
+                          devt["offset_add"], outs["y"], outs["off"], None, ws)
+        B.deform_conv_bwd(p, devt["x"], devt["w_off"], devt["w"], outs["off"], devt["grad_y"],
+                          outs["gx"], outs["gwo"], outs["gbo"], outs["gw"], outs["goff"], ws)
+        for k, v in outs.items():
+            hout[k].copy_(v, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            one()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(iters):
+            one()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / iters
+    return {"value": flops_step / (ms / 1e3) / 1e9, "unit": "GFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,261 @@
+"""Thin Python binding of the C ABI in ``include/deform_conv.h``.
+
+Argument marshalling only: every function here checks tensor shapes and
+dtypes, passes raw device pointers and the current CUDA stream to the library
+and turns a non-OK status into ``DcError``.  All arithmetic runs in the CUDA
+kernels of ``libdeformconv.so``; nothing here computes any part of the layer.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
+import torch
+
+from . import _native
+
+DC_OK, DC_ERR_INVALID_ARG, DC_ERR_UNSUPPORTED, DC_ERR_WORKSPACE, DC_ERR_CUDA, DC_ERR_TIMEOUT = range(6)
+DC_F32, DC_BF16 = 0, 1
+_TORCH_DTYPE = {DC_F32: torch.float32, DC_BF16: torch.bfloat16}
+
+# every symbol include/deform_conv.h declares
+EXPORTED_SYMBOLS = (
+    "dc_out_h", "dc_out_w", "deform_conv_workspace_size", "deform_conv_fwd",
+    "deform_conv_bwd", "deform_conv_sample", "dc_status_string", "dc_build_info",
+    "dc_launch_count",
+)
+
+
+class DcProblem(ctypes.Structure):
+    """Mirror of ``dc_problem``."""
+    _fields_ = [(name, ctypes.c_int) for name in (
+        "n", "c_in", "h", "w", "c_out", "kh", "kw", "stride_h", "stride_w",
+        "pad_h", "pad_w", "dil_h", "dil_w", "offset_groups", "dtype", "halo_margin")]
+
+
+class DcError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}")
+
+
+_configured = False
+
+
+def lib() -> ctypes.CDLL:
+    global _configured
+    L = _native.load()
+    if not _configured:
+        vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        pp = ctypes.POINTER(DcProblem)
+        L.dc_out_h.argtypes = [pp]
+        L.dc_out_h.restype = i
+        L.dc_out_w.argtypes = [pp]
+        L.dc_out_w.restype = i
+        L.deform_conv_workspace_size.argtypes = [pp, i, ctypes.POINTER(sz)]
+        L.deform_conv_workspace_size.restype = i
+        L.deform_conv_fwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.deform_conv_fwd.restype = i
+        L.deform_conv_bwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.deform_conv_bwd.restype = i
+        L.deform_conv_sample.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.deform_conv_sample.restype = i
+        L.dc_status_string.argtypes = [i]
+        L.dc_status_string.restype = ctypes.c_char_p
+        L.dc_build_info.argtypes = []
+        L.dc_build_info.restype = ctypes.c_char_p
+        L.dc_launch_count.argtypes = []
+        L.dc_launch_count.restype = ctypes.c_ulonglong
+        _configured = True
+    return L
+
+
+def status_string(status: int) -> str:
+    return lib().dc_status_string(int(status)).decode()
+
+
+def build_info() -> str:
+    return lib().dc_build_info().decode()
+
+
+def launch_count() -> int:
+    return int(lib().dc_launch_count())
+
+
+@dataclass(frozen=True)
+class Problem:
+    """One deformable layer: NCHW input, 3x3-style kernel geometry, dtype."""
+    n: int
+    c_in: int
+    h: int
+    w: int
+    c_out: int
+    kh: int = 3
+    kw: int = 3
+    stride: tuple = (1, 1)
+    pad: tuple = (1, 1)
+    dil: tuple = (1, 1)
+    offset_groups: int = 1
+    dtype: int = DC_F32
+    halo_margin: int = -1
+
+    def __post_init__(self):
+        for f in ("stride", "pad", "dil"):
+            v = getattr(self, f)
+            if isinstance(v, int):
+                object.__setattr__(self, f, (v, v))
+
+    def c_struct(self) -> DcProblem:
+        return DcProblem(self.n, self.c_in, self.h, self.w, self.c_out, self.kh, self.kw,
+                         self.stride[0], self.stride[1], self.pad[0], self.pad[1],
+                         self.dil[0], self.dil[1], self.offset_groups, self.dtype,
+                         self.halo_margin)
+
+    @property
+    def torch_dtype(self):
+        return _TORCH_DTYPE[self.dtype]
+
+    @property
+    def ho(self):
+        return (self.h + 2 * self.pad[0] - self.dil[0] * (self.kh - 1) - 1) // self.stride[0] + 1
+
+    @property
+    def wo(self):
+        return (self.w + 2 * self.pad[1] - self.dil[1] * (self.kw - 1) - 1) // self.stride[1] + 1
+
+    @property
+    def n_off(self):
+        return 2 * self.offset_groups * self.kh * self.kw
+
+    def shapes(self):
+        return dict(x=(self.n, self.c_in, self.h, self.w),
+                    w_off=(self.n_off, self.c_in, self.kh, self.kw),
+                    b_off=(self.n_off,),
+                    w=(self.c_out, self.c_in, self.kh, self.kw),
+                    offset=(self.n, self.n_off, self.ho, self.wo),
+                    y=(self.n, self.c_out, self.ho, self.wo),
+                    col=(self.c_in * self.kh * self.kw, self.n, self.ho * self.wo))
+
+
+def _ptr(t, name, shape=None, dtype=None, optional=False):
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status, what):
+    if status != DC_OK:
+        raise DcError(status, what)
+
+
+def deform_conv_workspace_size(p: Problem, backward: bool) -> int:
+    out = ctypes.c_size_t(0)
+    st = p.c_struct()
+    _check(lib().deform_conv_workspace_size(ctypes.byref(st), 1 if backward else 0,
+                                            ctypes.byref(out)), "deform_conv_workspace_size")
+    return int(out.value)
+
+
+def out_hw(p: Problem):
+    st = p.c_struct()
+    return lib().dc_out_h(ctypes.byref(st)), lib().dc_out_w(ctypes.byref(st))
+
+
+def deform_conv_fwd(p: Problem, x, w_off, b_off, w, offset_add, y, offset_out=None,
+                    slowpath_count=None, ws=None, stream=None):
+    s = p.shapes()
+    dt, f32 = p.torch_dtype, torch.float32
+    st = p.c_struct()
+    ws_ptr = _ptr(ws, "ws", dtype=torch.uint8)
+    _check(lib().deform_conv_fwd(
+        ctypes.byref(st), _ptr(x, "x", s["x"], dt), _ptr(w_off, "w_off", s["w_off"], dt),
+        _ptr(b_off, "b_off", s["b_off"], f32, True), _ptr(w, "w", s["w"], dt),
+        _ptr(offset_add, "offset_add", s["offset"], f32, True), _ptr(y, "y", s["y"], dt),
+        _ptr(offset_out, "offset_out", s["offset"], f32, True),
+        _ptr(slowpath_count, "slowpath_count", (1,), torch.int64, True),
+        ws_ptr, ctypes.c_size_t(ws.numel()), _stream(stream)), "deform_conv_fwd")
+
+
+def deform_conv_bwd(p: Problem, x, w_off, w, offset, grad_y, grad_x, grad_w_off, grad_b_off,
+                    grad_w, grad_offset=None, ws=None, stream=None):
+    s = p.shapes()
+    dt, f32 = p.torch_dtype, torch.float32
+    st = p.c_struct()
+    ws_ptr = _ptr(ws, "ws", dtype=torch.uint8)
+    _check(lib().deform_conv_bwd(
+        ctypes.byref(st), _ptr(x, "x", s["x"], dt), _ptr(w_off, "w_off", s["w_off"], dt),
+        _ptr(w, "w", s["w"], dt), _ptr(offset, "offset", s["offset"], f32),
+        _ptr(grad_y, "grad_y", s["y"], dt), _ptr(grad_x, "grad_x", s["x"], f32),
+        _ptr(grad_w_off, "grad_w_off", s["w_off"], f32),
+        _ptr(grad_b_off, "grad_b_off", s["b_off"], f32, True),
+        _ptr(grad_w, "grad_w", s["w"], f32),
+        _ptr(grad_offset, "grad_offset", s["offset"], f32, True),
+        ws_ptr, ctypes.c_size_t(ws.numel()), _stream(stream)), "deform_conv_bwd")
+
+
+def deform_conv_sample(p: Problem, x, w_off, b_off, offset_add, offset_in, col,
+                       offset_out=None, slowpath_count=None, stream=None):
+    s = p.shapes()
+    dt, f32 = p.torch_dtype, torch.float32
+    st = p.c_struct()
+    _check(lib().deform_conv_sample(
+        ctypes.byref(st), _ptr(x, "x", s["x"], dt),
+        _ptr(w_off, "w_off", s["w_off"], dt, True),
+        _ptr(b_off, "b_off", s["b_off"], f32, True),
+        _ptr(offset_add, "offset_add", s["offset"], f32, True),
+        _ptr(offset_in, "offset_in", s["offset"], f32, True),
+        _ptr(col, "col", s["col"], dt),
+        _ptr(offset_out, "offset_out", s["offset"], f32, True),
+        _ptr(slowpath_count, "slowpath_count", (1,), torch.int64, True),
+        _stream(stream)), "deform_conv_sample")
+
+
+# ---------------------------------------------------------------- conveniences
+# Allocate outputs with torch (device memory is PyTorch's job) and call the ABI.
+
+def workspace(p: Problem, backward: bool, device="cuda"):
+    return torch.empty(max(deform_conv_workspace_size(p, backward), 1), dtype=torch.uint8,
+                       device=device)
+
+
+def forward(p: Problem, x, w_off, b_off, w, offset_add=None, ws=None, stream=None,
+            slowpath_count=None):
+    """Returns (y, offsets)."""
+    s = p.shapes()
+    y = torch.empty(s["y"], dtype=p.torch_dtype, device=x.device)
+    off = torch.empty(s["offset"], dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(p, False, x.device)
+    deform_conv_fwd(p, x, w_off, b_off, w, offset_add, y, off, slowpath_count, ws, stream)
+    return y, off
+
+
+def backward(p: Problem, x, w_off, w, offset, grad_y, ws=None, stream=None):
+    """Returns dict(grad_x, grad_w_off, grad_b_off, grad_w, grad_offset)."""
+    s = p.shapes()
+    dev = x.device
+    out = dict(grad_x=torch.empty(s["x"], dtype=torch.float32, device=dev),
+               grad_w_off=torch.empty(s["w_off"], dtype=torch.float32, device=dev),
+               grad_b_off=torch.empty(s["b_off"], dtype=torch.float32, device=dev),
+               grad_w=torch.empty(s["w"], dtype=torch.float32, device=dev),
+               grad_offset=torch.empty(s["offset"], dtype=torch.float32, device=dev))
+    if ws is None:
+        ws = workspace(p, True, dev)
+    deform_conv_bwd(p, x, w_off, w, offset, grad_y, out["grad_x"], out["grad_w_off"],
+                    out["grad_b_off"], out["grad_w"], out["grad_offset"], ws, stream)
+    return out

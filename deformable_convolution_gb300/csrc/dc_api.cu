@@ -1,0 +1,321 @@
+// The C ABI (include/deform_conv.h): argument checks, workspace plan and the
+// launch sequences of the forward and backward passes.
+//
+// Forward ("The argument in one glance / This paper's idea" on the explainer
+// page "DefT: Boosting Scalability of Deformable Convolution Operations on
+// GPUs"): K1 fuses the offset convolution with the bilinear interpolation and
+// writes the deformed map; the main convolution is a separate dense GEMM over
+// that map.  Backward: K1 replays the deformed map from the saved offsets, two
+// GEMMs give the map's gradient and the main weights' gradient, K3 scatters
+// the map's gradient into grad_x and reduces the offset gradient, and K4 runs
+// the offset convolution's backward.
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "dc_common.cuh"
+
+namespace dc {
+
+static std::atomic<unsigned long long> g_launches{0};
+void note_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+cudaError_t launch_gemm_fwd(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
+cudaError_t launch_gemm_gcol(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
+cudaError_t launch_gemm_gw(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
+
+namespace {
+
+constexpr int kDefaultMargin = 3;
+constexpr int kMaxMargin = 64;
+constexpr int kMaxTaps = 49;
+constexpr size_t kMaxSampleSmem = 200 * 1024;
+
+size_t elt_size(dc_dtype dt) { return dt == DC_BF16 ? 2 : 4; }
+
+long long round_up(long long v, long long m) { return (v + m - 1) / m * m; }
+
+dc_status make_geom(const dc_problem* p, Geom* g, int* margin) {
+  if (!p) return DC_ERR_INVALID_ARG;
+  if (p->n <= 0 || p->c_in <= 0 || p->h <= 0 || p->w <= 0 || p->c_out <= 0 || p->kh <= 0 ||
+      p->kw <= 0 || p->stride_h <= 0 || p->stride_w <= 0 || p->pad_h < 0 || p->pad_w < 0 ||
+      p->dil_h <= 0 || p->dil_w <= 0 || p->offset_groups <= 0 ||
+      p->c_in % p->offset_groups != 0)
+    return DC_ERR_INVALID_ARG;
+  if (p->dtype != DC_F32 && p->dtype != DC_BF16) return DC_ERR_INVALID_ARG;
+  if (p->halo_margin < -1) return DC_ERR_INVALID_ARG;
+  const long long eh = (long long)p->h + 2LL * p->pad_h - (long long)p->dil_h * (p->kh - 1) - 1;
+  const long long ew = (long long)p->w + 2LL * p->pad_w - (long long)p->dil_w * (p->kw - 1) - 1;
+  if (eh < 0 || ew < 0) return DC_ERR_INVALID_ARG;
+  g->n = p->n;
+  g->c_in = p->c_in;
+  g->h = p->h;
+  g->w = p->w;
+  g->c_out = p->c_out;
+  g->kh = p->kh;
+  g->kw = p->kw;
+  g->sh = p->stride_h;
+  g->sw = p->stride_w;
+  g->ph = p->pad_h;
+  g->pw = p->pad_w;
+  g->dh = p->dil_h;
+  g->dw = p->dil_w;
+  g->groups = p->offset_groups;
+  g->ho = (int)(eh / p->stride_h + 1);
+  g->wo = (int)(ew / p->stride_w + 1);
+  g->K = p->kh * p->kw;
+  g->M = 2 * p->offset_groups * g->K;
+  g->cg = p->c_in / p->offset_groups;
+  g->kdim = p->c_in * g->K;
+  g->hw = (long long)p->h * p->w;
+  g->howo = (long long)g->ho * g->wo;
+  // limits of this build
+  if (g->K > kMaxTaps) return DC_ERR_UNSUPPORTED;
+  if ((long long)p->c_in * g->K > (1LL << 30) || (long long)p->n * p->c_in * g->hw > (1LL << 40) ||
+      g->howo * p->n > (1LL << 31))
+    return DC_ERR_UNSUPPORTED;
+  *margin = p->halo_margin < 0 ? kDefaultMargin : p->halo_margin;
+  if (*margin > kMaxMargin) return DC_ERR_UNSUPPORTED;
+  if (sample_smem_bytes(*g, p->dtype, *margin) > kMaxSampleSmem) return DC_ERR_UNSUPPORTED;
+  return DC_OK;
+}
+
+// Workspace carve-up.  The column buffer keeps each image's pixel run padded
+// to a multiple of 8 elements so that every row starts 16-byte aligned.
+struct Plan {
+  ColLayout col, gcol;
+  size_t col_off, gcol_off, off_off, total;
+};
+
+Plan make_plan(const Geom& g, dc_dtype dt, int backward) {
+  Plan pl{};
+  const long long pitch = round_up(g.howo, 8);
+  pl.col.img = pitch;
+  pl.col.row = pitch * g.n;
+  pl.gcol = pl.col;
+  size_t at = 0;
+  auto take = [&](size_t bytes) {
+    const size_t here = at;
+    at = (size_t)round_up((long long)(at + bytes), 256);
+    return here;
+  };
+  pl.col_off = take((size_t)g.kdim * pl.col.row * elt_size(dt));
+  pl.off_off = take((size_t)g.n * g.M * g.howo * sizeof(float));
+  pl.gcol_off = backward ? take((size_t)g.kdim * pl.gcol.row * sizeof(float)) : 0;
+  pl.total = at;
+  return pl;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+dc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DC_OK : DC_ERR_CUDA; }
+
+}  // namespace
+}  // namespace dc
+
+using namespace dc;
+
+extern "C" {
+
+int dc_out_h(const dc_problem* prob) {
+  Geom g;
+  int m;
+  return make_geom(prob, &g, &m) == DC_OK ? g.ho : 0;
+}
+
+int dc_out_w(const dc_problem* prob) {
+  Geom g;
+  int m;
+  return make_geom(prob, &g, &m) == DC_OK ? g.wo : 0;
+}
+
+dc_status deform_conv_workspace_size(const dc_problem* prob, int backward, size_t* bytes) {
+  if (!bytes) return DC_ERR_INVALID_ARG;
+  Geom g;
+  int margin;
+  const dc_status st = make_geom(prob, &g, &margin);
+  if (st != DC_OK) return st;
+  *bytes = make_plan(g, prob->dtype, backward ? 1 : 0).total;
+  return DC_OK;
+}
+
+dc_status deform_conv_fwd(const dc_problem* prob, const void* x, const void* w_off,
+                          const float* b_off, const void* w, const float* offset_add, void* y,
+                          float* offset_out, unsigned long long* slowpath_count, void* ws,
+                          size_t ws_bytes, void* stream) {
+  Geom g;
+  int margin;
+  dc_status st = make_geom(prob, &g, &margin);
+  if (st != DC_OK) return st;
+  if (!x || !w_off || !w || !y) return DC_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, w_off, b_off, w, offset_add, y, offset_out, slowpath_count, ws};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return DC_ERR_UNSUPPORTED;
+  const Plan pl = make_plan(g, prob->dtype, 0);
+  if (!ws || ws_bytes < pl.total) return DC_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* wsb = static_cast<char*>(ws);
+
+  SampleArgs sa{};
+  sa.g = g;
+  sa.x = x;
+  sa.w_off = w_off;
+  sa.b_off = b_off;
+  sa.off_add = offset_add;
+  sa.off_in = nullptr;
+  sa.col = wsb + pl.col_off;
+  sa.col_layout = pl.col;
+  sa.off_out = offset_out;
+  sa.slow_count = slowpath_count;
+  sa.margin = margin;
+  st = cuda_status(launch_sample(sa, prob->dtype, s));
+  if (st != DC_OK) return st;
+
+  GemmArgs ga{};
+  ga.g = g;
+  ga.w = w;
+  ga.col = sa.col;
+  ga.col_layout = pl.col;
+  ga.y = y;
+  return cuda_status(launch_gemm_fwd(ga, prob->dtype, s));
+}
+
+dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_off, const void* w,
+                          const float* offset, const void* grad_y, float* grad_x,
+                          float* grad_w_off, float* grad_b_off, float* grad_w,
+                          float* grad_offset, void* ws, size_t ws_bytes, void* stream) {
+  Geom g;
+  int margin;
+  dc_status st = make_geom(prob, &g, &margin);
+  if (st != DC_OK) return st;
+  if (!x || !w_off || !w || !offset || !grad_y || !grad_x || !grad_w_off || !grad_w)
+    return DC_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, w_off, w, offset, grad_y, grad_x, grad_w_off, grad_b_off, grad_w,
+                        grad_offset, ws};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return DC_ERR_UNSUPPORTED;
+  const Plan pl = make_plan(g, prob->dtype, 1);
+  if (!ws || ws_bytes < pl.total) return DC_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* wsb = static_cast<char*>(ws);
+  float* goff = grad_offset ? grad_offset : reinterpret_cast<float*>(wsb + pl.off_off);
+
+  st = cuda_status(cudaMemsetAsync(grad_x, 0, sizeof(float) * g.n * g.c_in * g.hw, s));
+  if (st != DC_OK) return st;
+  st = cuda_status(cudaMemsetAsync(grad_w, 0, sizeof(float) * g.c_out * g.kdim, s));
+  if (st != DC_OK) return st;
+
+  // deformed map, replayed from the saved offsets
+  SampleArgs sa{};
+  sa.g = g;
+  sa.x = x;
+  sa.w_off = w_off;
+  sa.off_in = offset;
+  sa.col = wsb + pl.col_off;
+  sa.col_layout = pl.col;
+  sa.margin = margin;
+  st = cuda_status(launch_sample(sa, prob->dtype, s));
+  if (st != DC_OK) return st;
+
+  GemmArgs ga{};
+  ga.g = g;
+  ga.w = w;
+  ga.col = sa.col;
+  ga.col_layout = pl.col;
+  ga.gy = grad_y;
+  ga.gcol = reinterpret_cast<float*>(wsb + pl.gcol_off);
+  ga.gcol_layout = pl.gcol;
+  ga.gw = grad_w;
+  st = cuda_status(launch_gemm_gcol(ga, prob->dtype, s));
+  if (st != DC_OK) return st;
+  st = cuda_status(launch_gemm_gw(ga, prob->dtype, s));
+  if (st != DC_OK) return st;
+
+  ScatterArgs ka{};
+  ka.g = g;
+  ka.x = x;
+  ka.off = offset;
+  ka.gcol = ga.gcol;
+  ka.gcol_layout = pl.gcol;
+  ka.gx = grad_x;
+  ka.goff = goff;
+  st = cuda_status(launch_scatter(ka, prob->dtype, s));
+  if (st != DC_OK) return st;
+
+  OffconvBwdArgs oa{};
+  oa.g = g;
+  oa.x = x;
+  oa.w_off = w_off;
+  oa.goff = goff;
+  oa.gx = grad_x;
+  oa.gw_off = grad_w_off;
+  oa.gb_off = grad_b_off;
+  return cuda_status(launch_offconv_bwd(oa, prob->dtype, s));
+}
+
+dc_status deform_conv_sample(const dc_problem* prob, const void* x, const void* w_off,
+                             const float* b_off, const float* offset_add, const float* offset_in,
+                             void* col, float* offset_out, unsigned long long* slowpath_count,
+                             void* stream) {
+  Geom g;
+  int margin;
+  dc_status st = make_geom(prob, &g, &margin);
+  if (st != DC_OK) return st;
+  if (!x || !col || (!offset_in && !w_off)) return DC_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, w_off, b_off, offset_add, offset_in, col, offset_out, slowpath_count};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return DC_ERR_UNSUPPORTED;
+  SampleArgs sa{};
+  sa.g = g;
+  sa.x = x;
+  sa.w_off = w_off;
+  sa.b_off = offset_in ? nullptr : b_off;
+  sa.off_add = offset_in ? nullptr : offset_add;
+  sa.off_in = offset_in;
+  sa.col = col;
+  sa.col_layout.img = g.howo;
+  sa.col_layout.row = g.howo * g.n;
+  sa.off_out = offset_out;
+  sa.slow_count = slowpath_count;
+  sa.margin = margin;
+  return cuda_status(launch_sample(sa, prob->dtype, static_cast<cudaStream_t>(stream)));
+}
+
+const char* dc_status_string(dc_status status) {
+  switch (status) {
+    case DC_OK: return "DC_OK: success";
+    case DC_ERR_INVALID_ARG: return "DC_ERR_INVALID_ARG: invalid problem size or missing argument";
+    case DC_ERR_UNSUPPORTED: return "DC_ERR_UNSUPPORTED: no path for this problem (alignment, dtype or size)";
+    case DC_ERR_WORKSPACE: return "DC_ERR_WORKSPACE: workspace missing or too small";
+    case DC_ERR_CUDA: return "DC_ERR_CUDA: a CUDA launch or runtime call failed";
+    case DC_ERR_TIMEOUT: return "DC_ERR_TIMEOUT: a bounded device wait expired";
+  }
+  return "unknown dc_status";
+}
+
+unsigned long long dc_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* dc_build_info(void) {
+  return "deformable_convolution_gb300: sm_103a, CUDA "
+#define DC_STR2(x) #x
+#define DC_STR(x) DC_STR2(x)
+         DC_STR(__CUDACC_VER_MAJOR__) "." DC_STR(__CUDACC_VER_MINOR__);
+}
+
+}  // extern "C"
+
+namespace dc {
+
+// GEMM dispatch: CUDA cores for now.
+cudaError_t launch_gemm_fwd(const GemmArgs& a, dc_dtype dt, cudaStream_t s) {
+  return launch_gemm_fwd_simt(a, dt, s);
+}
+cudaError_t launch_gemm_gcol(const GemmArgs& a, dc_dtype dt, cudaStream_t s) {
+  return launch_gemm_gcol_simt(a, dt, s);
+}
+cudaError_t launch_gemm_gw(const GemmArgs& a, dc_dtype dt, cudaStream_t s) {
+  return launch_gemm_gw_simt(a, dt, s);
+}
+
+}  // namespace dc

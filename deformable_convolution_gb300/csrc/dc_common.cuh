@@ -1,0 +1,139 @@
+// Shared definitions of the CUDA library (device helpers, derived geometry,
+// kernel launch entry points).  Nothing here is visible through the C ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/deform_conv.h"
+
+namespace dc {
+
+// Layer geometry with the derived sizes every kernel needs.
+struct Geom {
+  int n, c_in, h, w, c_out, kh, kw;
+  int sh, sw, ph, pw, dh, dw;
+  int groups;
+  int ho, wo;
+  int K;     // taps per filter, kh * kw
+  int M;     // offset channels, 2 * groups * K
+  int cg;    // input channels per offset group
+  int kdim;  // main-GEMM reduction length, c_in * K
+  long long hw, howo;
+};
+
+// Pitches of the deformed map ("column") buffer [kdim][n][howo(+pad)]:
+// element (row r, image b, pixel q) lives at r * row + b * img + q.
+struct ColLayout {
+  long long row;
+  long long img;
+};
+
+__host__ __device__ inline long long ceil_div_ll(long long a, long long b) {
+  return (a + b - 1) / b;
+}
+
+__device__ __forceinline__ float ld_f(const float* p) { return *p; }
+__device__ __forceinline__ float ld_f(const __nv_bfloat16* p) {
+  return __bfloat162float(*p);
+}
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) {
+  return v;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// Bilinear blend of the four corners around a fractional point ("Why it fell
+// short": four neighbouring pixels averaged by weight).  Every caller goes
+// through this one sequence of roundings, so the on-chip and global-memory
+// paths of a kernel give bitwise identical samples.
+__device__ __forceinline__ float blend4(float ly, float lx, float v00, float v01,
+                                        float v10, float v11) {
+  const float hy = 1.0f - ly, hx = 1.0f - lx;
+  float s = __fmul_rn(__fmul_rn(hy, hx), v00);
+  s = __fmaf_rn(__fmul_rn(hy, lx), v01, s);
+  s = __fmaf_rn(__fmul_rn(ly, hx), v10, s);
+  s = __fmaf_rn(__fmul_rn(ly, lx), v11, s);
+  return s;
+}
+
+// A sampling point can touch the image only if -1 <= p < extent on both axes
+// (p = -1 still gives the right-sided derivative a nonzero value at row 0);
+// outside, the sample and both of its derivatives are zero.  NaN is outside.
+__device__ __forceinline__ bool touches_image(float py, float px, int H, int W) {
+  return py >= -1.0f && py < (float)H && px >= -1.0f && px < (float)W;
+}
+
+// ---------------------------------------------------------------- launchers
+// All return the launch's cudaError_t; the ABI layer maps it to a status.
+
+// Host-side count of kernels enqueued by this library (dc_launch_count).
+void note_launches(unsigned n);
+
+struct SampleArgs {
+  Geom g;
+  const void* x;
+  const void* w_off;
+  const float* b_off;
+  const float* off_add;
+  const float* off_in;  // non-null: sample these offsets, skip the offset conv
+  void* col;
+  ColLayout col_layout;
+  float* off_out;  // may be null: offsets are then kept on chip only
+  unsigned long long* slow_count;
+  int margin;
+};
+cudaError_t launch_sample(const SampleArgs& a, dc_dtype dt, cudaStream_t s);
+size_t sample_smem_bytes(const Geom& g, dc_dtype dt, int margin);
+
+// Main-convolution GEMMs on the column layout (batched over images).
+struct GemmArgs {
+  Geom g;
+  const void* w;      // [c_out][kdim]
+  const void* col;    // column buffer, dtype
+  ColLayout col_layout;
+  const void* gy;     // [n][c_out][howo], dtype
+  void* y;            // [n][c_out][howo], dtype (forward)
+  float* gcol;        // column-layout gradient, fp32 (backward)
+  ColLayout gcol_layout;
+  float* gw;          // [c_out][kdim] fp32, accumulated with atomics (backward)
+};
+// CUDA-core (fp32 arithmetic) versions, any layout pitch.
+cudaError_t launch_gemm_fwd_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
+cudaError_t launch_gemm_gcol_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
+cudaError_t launch_gemm_gw_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
+
+// Backward of the sampling step: grad_x (atomics) and the offset gradient.
+struct ScatterArgs {
+  Geom g;
+  const void* x;
+  const float* off;
+  const float* gcol;
+  ColLayout gcol_layout;
+  float* gx;
+  float* goff;
+};
+cudaError_t launch_scatter(const ScatterArgs& a, dc_dtype dt, cudaStream_t s);
+
+// Backward of the offset convolution.
+struct OffconvBwdArgs {
+  Geom g;
+  const void* x;
+  const void* w_off;
+  const float* goff;
+  float* gx;        // += transposed convolution of goff
+  float* gw_off;    // overwritten
+  float* gb_off;    // overwritten, may be null
+};
+cudaError_t launch_offconv_bwd(const OffconvBwdArgs& a, dc_dtype dt, cudaStream_t s);
+
+}  // namespace dc

@@ -1,0 +1,158 @@
+/*
+ * deform_conv.h -- C ABI of the GB300 (sm_103a) deformable convolution layer.
+ *
+ * The layer follows the explainer page "DefT: Boosting Scalability of
+ * Deformable Convolution Operations on GPUs" (ASPLOS 2023):
+ *   - "The argument in one glance / What people did": three operators -- an
+ *     offset convolution, a bilinear interpolation that builds the deformed
+ *     feature map, and the main convolution over that map;
+ *   - "Following a deformable layer through DefT", Step 1 of 5: a fractional
+ *     (y, x) offset for every filter position at every output location, added
+ *     to the base sampling coordinate;
+ *   - "The argument in one glance / Why it fell short": each displaced sample
+ *     blends its four neighbouring pixels by their bilinear weights;
+ *   - "This paper's idea" / "Why it works": the offset convolution and the
+ *     interpolation run fused in one kernel over an output-spatial tile whose
+ *     input halo, padded by a margin sized to the offset distribution, is staged
+ *     on chip; the main convolution stays a separate dense GEMM.
+ * Written out: y[n,o,p0] = sum_{c,k} w[o,c,k] * xbar[n,c](p0*s - pad + k*dil +
+ * dp[n,g(c),k,p0]), with xbar read by bilinear interpolation and zero outside
+ * the image.
+ *
+ * Conventions (the page fixes none of these; they are this library's):
+ *   - All tensors are dense, contiguous, row-major, on the current CUDA device.
+ *     x, y: NCHW.  w: [C_out, C_in, Kh, Kw].  w_off: [2*G*Kh*Kw, C_in, Kh, Kw].
+ *     x, y, w and w_off are in the problem's dtype; b_off, offsets and every
+ *     gradient are float32.
+ *   - The offset convolution uses the main convolution's kernel size, stride,
+ *     padding and dilation and has a bias b_off, so its output grid is the
+ *     output grid [N, 2*G*Kh*Kw, Ho, Wo].
+ *   - Offset channel 2*(g*Kh*Kw + k) is the row shift and 2*(g*Kh*Kw + k) + 1
+ *     the column shift of tap k = i*Kw + j in offset group g; input channel c
+ *     belongs to group c / (C_in / G).
+ *   - Corners outside [0,H) x [0,W) contribute zero.  At an integer sampling
+ *     coordinate the lower corner is floor(p), so offset gradients there are
+ *     right-sided differences.
+ *   - Ownership: the caller allocates every buffer, including the workspace.
+ *     The library allocates no device memory, keeps no per-call state, and
+ *     never synchronises; all work is enqueued on `stream` (a cudaStream_t; 0
+ *     is the legacy default stream).  Calls on different streams must not
+ *     share a workspace.
+ *   - Errors: arguments are checked on the host before anything is launched.
+ *     A non-DC_OK status means nothing was enqueued, except DC_ERR_CUDA from a
+ *     launch, after which earlier kernels of the same call may have run.
+ *   - Pointers must be 16-byte aligned.  Gradient outputs are overwritten.
+ */
+#ifndef DEFORM_CONV_H_
+#define DEFORM_CONV_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DC_OK = 0,
+  DC_ERR_INVALID_ARG = 1, /* bad size, C_in % G != 0, Ho or Wo < 1, NULL required pointer */
+  DC_ERR_UNSUPPORTED = 2, /* valid problem this build has no path for (alignment, dtype, size) */
+  DC_ERR_WORKSPACE = 3,   /* workspace pointer NULL or smaller than the query returned */
+  DC_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed */
+  DC_ERR_TIMEOUT = 5      /* a bounded on-device wait expired (reported by dc_device_error) */
+} dc_status;
+
+typedef enum { DC_F32 = 0, DC_BF16 = 1 } dc_dtype;
+
+/* Geometry of one deformable layer.  halo_margin is the number of extra pixels
+ * the fused sampling kernel stages around each output tile's receptive field
+ * ("The idea": tile padding sized to the offset distribution); -1 selects the
+ * library default (3 px).  It changes speed only, never results: taps that
+ * fall outside the staged tile are read from global memory. */
+typedef struct {
+  int n, c_in, h, w, c_out, kh, kw;
+  int stride_h, stride_w, pad_h, pad_w, dil_h, dil_w;
+  int offset_groups;
+  dc_dtype dtype;
+  int halo_margin;
+} dc_problem;
+
+/* Output height/width of the problem (0 if the problem is invalid). */
+int dc_out_h(const dc_problem* prob);
+int dc_out_w(const dc_problem* prob);
+
+/* Bytes of device workspace deform_conv_fwd (backward = 0) or deform_conv_bwd
+ * (backward = 1) needs for this problem.  Writes *bytes; returns
+ * DC_ERR_INVALID_ARG / DC_ERR_UNSUPPORTED for problems the calls would reject. */
+dc_status deform_conv_workspace_size(const dc_problem* prob, int backward, size_t* bytes);
+
+/* Forward pass of the whole layer ("What people did": offset convolution ->
+ * bilinear interpolation -> main convolution; the first two fused, "This
+ * paper's idea").
+ *   x          [N, C_in, H, W]                 dtype, required
+ *   w_off      [2GK, C_in, Kh, Kw]             dtype, required (offset conv weights)
+ *   b_off      [2GK]                           float32, NULL = zero bias
+ *   w          [C_out, C_in, Kh, Kw]           dtype, required (main weights)
+ *   offset_add [N, 2GK, Ho, Wo]                float32, NULL = none; added to the
+ *                                              offset-conv output before sampling
+ *   y          [N, C_out, Ho, Wo]              dtype, required, overwritten
+ *   offset_out [N, 2GK, Ho, Wo]                float32, NULL = not returned; the
+ *                                              offsets used (input to the backward)
+ *   slowpath_count  one unsigned 64-bit counter, NULL = not counted; the number
+ *                   of taps read outside the staged tile is ADDED to it
+ *   ws, ws_bytes    workspace from deform_conv_workspace_size(prob, 0, ...)
+ * Accumulation is float32 for both dtypes; bf16 outputs are rounded to nearest
+ * even. */
+dc_status deform_conv_fwd(const dc_problem* prob, const void* x, const void* w_off,
+                          const float* b_off, const void* w, const float* offset_add,
+                          void* y, float* offset_out, unsigned long long* slowpath_count,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* Backward pass: gradients of sum(y * grad_y) at the saved offsets.
+ *   x, w_off, w   as in the forward pass
+ *   offset        [N, 2GK, Ho, Wo] float32, required: offset_out of the forward
+ *   grad_y        [N, C_out, Ho, Wo] dtype, required
+ *   grad_x        [N, C_in, H, W] float32, required (sampling + offset-conv paths)
+ *   grad_w_off    [2GK, C_in, Kh, Kw] float32, required
+ *   grad_b_off    [2GK] float32, NULL = not returned
+ *   grad_w        [C_out, C_in, Kh, Kw] float32, required
+ *   grad_offset   [N, 2GK, Ho, Wo] float32, NULL = not returned; gradient with
+ *                 respect to the offsets (equivalently to offset_add)
+ *   ws, ws_bytes  workspace from deform_conv_workspace_size(prob, 1, ...)
+ * Float32 atomics make grad_x, grad_w and grad_w_off reproducible only up to
+ * summation order. */
+dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_off,
+                          const void* w, const float* offset, const void* grad_y,
+                          float* grad_x, float* grad_w_off, float* grad_b_off,
+                          float* grad_w, float* grad_offset, void* ws, size_t ws_bytes,
+                          void* stream);
+
+/* The fused offset-convolution + bilinear-interpolation stage alone ("This
+ * paper's idea": the kernel whose arithmetic intensity the fusion raises),
+ * returning the deformed feature map ("What people did before, and where it
+ * broke": the unrolled map the interpolation materialises).
+ *   col        [C_in*Kh*Kw, N, Ho*Wo] dtype, required; row c*Kh*Kw + k holds
+ *              channel c sampled at tap k for every output pixel
+ *   offset_add, b_off, offset_out, slowpath_count as in deform_conv_fwd
+ * If `offset_in` is non-NULL the offset convolution is skipped and those
+ * offsets [N, 2GK, Ho, Wo] are sampled instead (w_off and b_off are ignored). */
+dc_status deform_conv_sample(const dc_problem* prob, const void* x, const void* w_off,
+                             const float* b_off, const float* offset_add,
+                             const float* offset_in, void* col, float* offset_out,
+                             unsigned long long* slowpath_count, void* stream);
+
+/* Static description of a status code. */
+const char* dc_status_string(dc_status status);
+
+/* Library build description (architecture, version). */
+const char* dc_build_info(void);
+
+/* Number of kernels this library has enqueued in this process so far (host
+ * counter, incremented per launch; memsets are not counted).  Lets a caller
+ * count the launches of a region of work, e.g. of a captured CUDA graph. */
+unsigned long long dc_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DEFORM_CONV_H_ */

@@ -1,0 +1,117 @@
+"""Host-side contract of the C ABI: builds, loads, exports every declared
+symbol, and rejects bad arguments on the host before launching anything.
+None of these tests needs a GPU (no call here reaches a kernel launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from deformable_convolution_gb300 import _native, binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                            text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_builds_and_exports_every_declared_symbol():
+    _native.build()
+    lib = ctypes.CDLL(_native.LIB_PATH)
+    names = declared_functions()
+    assert "deform_conv_fwd" in names and "deform_conv_bwd" in names
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(B.EXPORTED_SYMBOLS) == set(names)
+
+
+def test_build_info_and_status_strings():
+    assert "sm_103a" in B.build_info()
+    for s in range(6):
+        assert B.status_string(s).startswith("DC_")
+
+
+def problem(**kw):
+    base = dict(n=2, c_in=4, h=9, w=7, c_out=3)
+    base.update(kw)
+    return B.Problem(**base)
+
+
+def ws_size(p, backward=False):
+    out = ctypes.c_size_t(0)
+    st = p.c_struct()
+    return B.lib().deform_conv_workspace_size(ctypes.byref(st), int(backward), ctypes.byref(out)), out.value
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(c_in=5, offset_groups=2), B.DC_ERR_INVALID_ARG),
+    (dict(n=0), B.DC_ERR_INVALID_ARG),
+    (dict(h=1, pad=0), B.DC_ERR_INVALID_ARG),
+    (dict(stride=0), B.DC_ERR_INVALID_ARG),
+    (dict(dtype=7), B.DC_ERR_INVALID_ARG),
+    (dict(halo_margin=-2), B.DC_ERR_INVALID_ARG),
+    (dict(kh=9, kw=9, pad=4), B.DC_ERR_UNSUPPORTED),
+    (dict(halo_margin=1000), B.DC_ERR_UNSUPPORTED),
+])
+def test_invalid_problems_are_rejected(kw, status):
+    st, _ = ws_size(problem(**kw))
+    assert st == status
+    assert B.out_hw(problem(**kw)) == (0, 0)
+
+
+def test_output_size_and_workspace():
+    p = problem(h=9, w=7, stride=(2, 1), pad=(1, 0), dil=(1, 2))
+    assert B.out_hw(p) == ((9 + 2 - 2 - 1) // 2 + 1, (7 - 4 - 1) + 1)
+    st, fwd = ws_size(p)
+    assert st == B.DC_OK and fwd > 0
+    st, bwd = ws_size(p, True)
+    assert st == B.DC_OK and bwd > fwd
+
+
+def _call_fwd(p, ptrs, ws_bytes):
+    st = p.c_struct()
+    vp = ctypes.c_void_p
+    return B.lib().deform_conv_fwd(ctypes.byref(st), *[vp(v) if v else None for v in ptrs],
+                                   ctypes.c_size_t(ws_bytes), None)
+
+
+def test_fwd_argument_checks_fail_before_any_launch():
+    # fake, never dereferenced device addresses: every check below happens on
+    # the host before the first launch
+    p = problem()
+    _, need = ws_size(p)
+    good = [0x10000 * (i + 1) for i in range(9)]  # x w_off b_off w add y off slow ws
+    bad = list(good)
+    bad[0] = 0
+    assert _call_fwd(p, bad, need) == B.DC_ERR_INVALID_ARG
+    bad = list(good)
+    bad[3] += 4
+    assert _call_fwd(p, bad, need) == B.DC_ERR_UNSUPPORTED
+    assert _call_fwd(p, good, need - 1) == B.DC_ERR_WORKSPACE
+    bad = list(good)
+    bad[8] = 0
+    assert _call_fwd(p, bad, need) == B.DC_ERR_WORKSPACE
+    assert _call_fwd(problem(c_in=3, offset_groups=2), good, need) == B.DC_ERR_INVALID_ARG
+
+
+def test_bwd_argument_checks_fail_before_any_launch():
+    p = problem()
+    _, need = ws_size(p, True)
+    st = p.c_struct()
+    vp = ctypes.c_void_p
+    ptrs = [vp(0x10000 * (i + 1)) for i in range(11)]
+    ptrs[5] = None  # grad_x missing
+    rc = B.lib().deform_conv_bwd(ctypes.byref(st), *ptrs, ctypes.c_size_t(need), None)
+    assert rc == B.DC_ERR_INVALID_ARG
+    ptrs = [vp(0x10000 * (i + 1)) for i in range(11)]
+    rc = B.lib().deform_conv_bwd(ctypes.byref(st), *ptrs, ctypes.c_size_t(need // 2), None)
+    assert rc == B.DC_ERR_WORKSPACE

@@ -1,0 +1,187 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs, element by element.
+
+Full-size workloads whose oracle run stays within seconds are compared
+whole (the tiny layer, the res3-style layer the benchmark times, the res4
+layer).  The two largest (early layer, training-stack layer) run on the GPU at
+full batch in the benchmark's launch configuration and are compared image by
+image on image 0 (batch items are independent), with the batch-summed weight
+gradients checked on a one-image run."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deformable_convolution_gb300 import binding as B
+from deformable_convolution_gb300 import workloads as W
+
+from parity import (TOL, check_layer, f64, gpu_backward, gpu_forward, oracle_backward,
+                    oracle_forward, oracle_problem, rel_err)
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+
+@pytest.mark.parametrize("name", ["tiny_f32", "res3_f32", "res3_bf16", "res4_bf16"])
+def test_workload_full(name):
+    wl = W.WORKLOADS[name]
+    p = wl.problem()
+    d = W.generate(wl)
+    errs = check_layer(p, d)
+    print(name, errs)
+
+
+@pytest.mark.parametrize("name", ["early_bf16", "stack_bf16"])
+def test_workload_batch_slice(name):
+    wl = W.WORKLOADS[name]
+    p = wl.problem()
+    d = W.generate(wl)
+    tol = TOL[p.dtype]
+    one = {k: (None if v is None else (v[:1].contiguous() if k in ("x", "offset_add", "grad_y") else v))
+           for k, v in d.items()}
+    p1 = wl.problem(1)
+    # forward at full batch, image 0 against the oracle
+    y, off, _ = gpu_forward(p, d)
+    y_ref, off_ref = oracle_forward(p1, one)
+    assert rel_err(f64(y[:1]), y_ref) <= tol
+    assert rel_err(f64(off[:1]), off_ref) <= tol
+    # backward at full batch with the oracle's offsets for every image
+    op = oracle_problem(p)
+    off_all = oracle.offsets(op, f64(d["x"]), f64(d["w_off"]), f64(d["b_off"]), f64(d["offset_add"]))
+    off32 = torch.from_numpy(off_all).float()
+    g = gpu_backward(p, d, off32)
+    ref = oracle_backward(p1, one, off32[:1].double().numpy())
+    for k in ("grad_x", "grad_offset"):
+        assert rel_err(f64(g[k][:1]), ref[k]) <= tol, k
+    # batch-summed weight gradients on the one-image problem
+    g1 = gpu_backward(p1, one, off32[:1])
+    for k in ("grad_w", "grad_w_off", "grad_b_off"):
+        assert rel_err(f64(g1[k]), ref[k]) <= tol, k
+
+
+def random_inputs(p, seed, off_scale=1.5):
+    gen = torch.Generator().manual_seed(seed)
+    s = p.shapes()
+    dt = p.torch_dtype
+    x = (torch.rand(s["x"], generator=gen) * 2 - 1).to(dt)
+    w_off = (torch.randn(s["w_off"], generator=gen) * off_scale /
+             np.sqrt(p.c_in * p.kh * p.kw / 3.0)).to(dt)
+    b_off = torch.randn(s["b_off"], generator=gen) * 0.5
+    w = (torch.randn(s["w"], generator=gen) / np.sqrt(p.c_in * p.kh * p.kw)).to(dt)
+    add = torch.randn(s["offset"], generator=gen) * 0.5
+    gy = torch.randn(s["y"], generator=gen).to(dt)
+    return dict(x=x, w_off=w_off, b_off=b_off, w=w, offset_add=add, grad_y=gy)
+
+
+EDGE_GEOMETRIES = [
+    # n, c_in, h, w, c_out, kh, kw, stride, pad, dil, groups
+    (1, 1, 1, 1, 1, 1, 1, 1, 0, 1, 1),
+    (2, 1, 3, 4, 2, 3, 3, 1, 1, 1, 1),
+    (1, 2, 5, 3, 3, 3, 3, 2, 1, 1, 2),
+    (3, 3, 7, 9, 5, 3, 3, 1, 2, 2, 3),
+    (2, 4, 6, 5, 1, 2, 3, (2, 1), (0, 1), (1, 2), 2),
+    (1, 5, 17, 19, 7, 3, 3, 1, 1, 1, 1),
+    (2, 8, 33, 21, 16, 3, 3, 2, 1, 1, 4),
+    (1, 3, 11, 40, 2, 5, 5, 1, 2, 1, 1),
+    (1, 16, 9, 130, 24, 3, 3, 1, 1, 1, 2),
+]
+
+
+@pytest.mark.parametrize("geom", EDGE_GEOMETRIES)
+@pytest.mark.parametrize("dtype", [B.DC_F32, B.DC_BF16])
+def test_edge_geometries(geom, dtype):
+    n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups = geom
+    p = B.Problem(n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups, dtype)
+    check_layer(p, random_inputs(p, 100 + h * w + c_in))
+
+
+@pytest.mark.parametrize("dtype", [B.DC_F32, B.DC_BF16])
+def test_fast_and_slow_paths_agree_bitwise(dtype):
+    """Margin 0 sends most taps to the global-memory path, a wide margin keeps
+    them on chip: the deformed maps must be identical bit for bit."""
+    p = B.Problem(2, 16, 23, 29, 8, 3, 3, 1, 1, 1, 2, dtype)
+    d = random_inputs(p, 7, off_scale=3.0)
+    dd = {k: v.cuda() for k, v in d.items()}
+    cols = []
+    counts = []
+    for margin in (0, 2, 12):
+        q = B.Problem(2, 16, 23, 29, 8, 3, 3, 1, 1, 1, 2, dtype, margin)
+        col = torch.empty(q.shapes()["col"], dtype=q.torch_dtype, device="cuda")
+        cnt = torch.zeros(1, dtype=torch.int64, device="cuda")
+        B.deform_conv_sample(q, dd["x"], dd["w_off"], dd["b_off"], dd["offset_add"], None, col,
+                             slowpath_count=cnt)
+        torch.cuda.synchronize()
+        cols.append(col.cpu())
+        counts.append(int(cnt.item()))
+    assert counts[0] > counts[1] > counts[2]
+    assert torch.equal(cols[0].view(torch.int16 if dtype else torch.int32),
+                       cols[1].view(torch.int16 if dtype else torch.int32))
+    assert torch.equal(cols[0].view(torch.int16 if dtype else torch.int32),
+                       cols[2].view(torch.int16 if dtype else torch.int32))
+
+
+@pytest.mark.parametrize("dtype", [B.DC_F32, B.DC_BF16])
+def test_column_matches_oracle(dtype):
+    p = B.Problem(2, 6, 13, 11, 4, 3, 3, 1, 1, 1, 3, dtype)
+    d = random_inputs(p, 8)
+    dd = {k: v.cuda() for k, v in d.items()}
+    col = torch.empty(p.shapes()["col"], dtype=p.torch_dtype, device="cuda")
+    off = torch.empty(p.shapes()["offset"], dtype=torch.float32, device="cuda")
+    B.deform_conv_sample(p, dd["x"], dd["w_off"], dd["b_off"], dd["offset_add"], None, col, off)
+    torch.cuda.synchronize()
+    op = oracle_problem(p)
+    off_ref = oracle.offsets(op, f64(d["x"]), f64(d["w_off"]), f64(d["b_off"]), f64(d["offset_add"]))
+    assert rel_err(f64(off), off_ref) <= 1e-5
+    # sample both at the same offsets
+    col2 = torch.empty_like(col)
+    off32 = torch.from_numpy(off_ref).float().cuda()
+    B.deform_conv_sample(p, dd["x"], None, None, None, off32, col2)
+    torch.cuda.synchronize()
+    ref = oracle.column(op, f64(d["x"]), off32.double().cpu().numpy())  # [n, c, k, ho, wo]
+    ref = ref.reshape(p.n, p.c_in * 9, p.ho * p.wo).transpose(1, 0, 2)
+    tol = 1e-6 if dtype == B.DC_F32 else 8e-3
+    assert rel_err(f64(col2), ref) <= tol
+
+
+def test_zero_and_integer_offsets():
+    p = B.Problem(2, 8, 12, 10, 6, 3, 3, 1, 1, 1, 2, B.DC_F32)
+    d = random_inputs(p, 9)
+    d["w_off"] = torch.zeros_like(d["w_off"])
+    d["offset_add"] = None
+    d["b_off"] = torch.zeros_like(d["b_off"])
+    check_layer(p, d)
+    d["b_off"] = torch.randint(-3, 4, d["b_off"].shape).float()
+    check_layer(p, d)
+
+
+def test_far_outside_offsets():
+    p = B.Problem(1, 4, 8, 8, 3, 3, 3, 1, 1, 1, 1, B.DC_F32)
+    d = random_inputs(p, 10)
+    d["offset_add"] = torch.full(p.shapes()["offset"], 1e4)
+    y, off, cnt = gpu_forward(p, d)
+    assert torch.count_nonzero(y).item() == 0
+    g = gpu_backward(p, d, off.cpu())
+    assert torch.count_nonzero(g["grad_offset"]).item() == 0
+
+
+def test_hand_worked_layer():
+    import json
+    import os
+    gold = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "hand_worked.json")))
+    L = gold["layer"]
+    p = B.Problem(1, 1, 2, 3, 1, 1, 1, 1, 0, 1, 1, B.DC_F32)
+    x = torch.tensor(gold["plane"], dtype=torch.float32).reshape(1, 1, 2, 3).cuda()
+    y, off = B.forward(p, x, torch.zeros(2, 1, 1, 1, device="cuda"),
+                       torch.tensor(L["b_off"], device="cuda"),
+                       torch.full((1, 1, 1, 1), L["w_main"], device="cuda"))
+    assert y.cpu().reshape(2, 3).tolist() == L["y"]
+
+
+def test_repeated_calls_are_deterministic_forward():
+    wl = W.WORKLOADS["res3_bf16"]
+    p = wl.problem()
+    d = W.generate(wl)
+    y1, off1, _ = gpu_forward(p, d)
+    y2, off2, _ = gpu_forward(p, d)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(off1, off2)
