@@ -30,7 +30,9 @@
  *   - input channel c belongs to offset group c / (C_in / G);
  *   - corners outside [0,H) x [0,W) contribute zero, with no clamping;
  *   - at an integer coordinate the lower corner is floor(p), so the derivative
- *     of the sample with respect to p is the right-sided difference.
+ *     of the sample with respect to p is the right-sided difference;
+ *   - floor(p) is an integer decision, so it is taken on the float32 value of
+ *     the coordinate, the precision the GPU kernels form it in (orc_cell).
  *
  * The backward pass is the exact derivative of that definition, written out
  * step by step in fp64.  Loops are parallelised with OpenMP only over indices
@@ -84,17 +86,23 @@ static int orc_near_image(int H, int W, double py, double px) {
 }
 
 /* Bilinear sample of one plane at the fractional point (py, px), written as
- * the blend of the four neighbouring pixels ("Why it fell short"). */
-double orc_bilinear(const double *plane, int H, int W, double py, double px) {
-  if (!orc_near_image(H, W, py, px)) return 0.0;
-  double fy = floor(py), fx = floor(px);
-  long a = (long)fy, b = (long)fx;
-  double ly = py - fy, lx = px - fx;
+ * the blend of the four neighbouring pixels ("Why it fell short").  The cell
+ * (lower corner) is (cy, cx); the plain definition takes cy = floor(py),
+ * cx = floor(px), which is what orc_bilinear below does. */
+static double orc_bilinear_cell(const double *plane, int H, int W, double py,
+                                double px, double cy, double cx) {
+  long a = (long)cy, b = (long)cx;
+  double ly = py - cy, lx = px - cx;
   double hy = 1.0 - ly, hx = 1.0 - lx;
   return hy * hx * orc_pixel(plane, H, W, a, b) +
          hy * lx * orc_pixel(plane, H, W, a, b + 1) +
          ly * hx * orc_pixel(plane, H, W, a + 1, b) +
          ly * lx * orc_pixel(plane, H, W, a + 1, b + 1);
+}
+
+double orc_bilinear(const double *plane, int H, int W, double py, double px) {
+  if (!orc_near_image(H, W, py, px)) return 0.0;
+  return orc_bilinear_cell(plane, H, W, py, px, floor(py), floor(px));
 }
 
 /* The same sample as a sum over every pixel of the image with the triangular
@@ -115,16 +123,13 @@ double orc_bilinear_closed_form(const double *plane, int H, int W, double py,
   return s;
 }
 
-/* Derivatives of the bilinear sample with respect to py and px, with the lower
- * corner at floor(p) (right-sided difference at integer coordinates). */
-void orc_bilinear_grad(const double *plane, int H, int W, double py, double px,
-                       double *d_py, double *d_px) {
-  *d_py = 0.0;
-  *d_px = 0.0;
-  if (!orc_near_image(H, W, py, px)) return;
-  double fy = floor(py), fx = floor(px);
-  long a = (long)fy, b = (long)fx;
-  double ly = py - fy, lx = px - fx;
+/* Derivatives of the bilinear sample with respect to py and px inside the
+ * cell (cy, cx) (with cy = floor(py): right-sided difference at integers). */
+static void orc_bilinear_grad_cell(const double *plane, int H, int W, double py,
+                                   double px, double cy, double cx,
+                                   double *d_py, double *d_px) {
+  long a = (long)cy, b = (long)cx;
+  double ly = py - cy, lx = px - cx;
   double v00 = orc_pixel(plane, H, W, a, b);
   double v01 = orc_pixel(plane, H, W, a, b + 1);
   double v10 = orc_pixel(plane, H, W, a + 1, b);
@@ -133,14 +138,20 @@ void orc_bilinear_grad(const double *plane, int H, int W, double py, double px,
   *d_px = (1.0 - ly) * (v01 - v00) + ly * (v11 - v10);
 }
 
-/* Adjoint of orc_bilinear with respect to the plane: adds g times each corner's
- * weight to that corner, for the corners inside the image. */
-static void orc_bilinear_scatter(double *plane, int H, int W, double py,
-                                 double px, double g) {
+void orc_bilinear_grad(const double *plane, int H, int W, double py, double px,
+                       double *d_py, double *d_px) {
+  *d_py = 0.0;
+  *d_px = 0.0;
   if (!orc_near_image(H, W, py, px)) return;
-  double fy = floor(py), fx = floor(px);
-  long a = (long)fy, b = (long)fx;
-  double ly = py - fy, lx = px - fx;
+  orc_bilinear_grad_cell(plane, H, W, py, px, floor(py), floor(px), d_py, d_px);
+}
+
+/* Adjoint of the sample with respect to the plane: adds g times each corner's
+ * weight to that corner, for the corners inside the image. */
+static void orc_bilinear_scatter_cell(double *plane, int H, int W, double py,
+                                      double px, double cy, double cx, double g) {
+  long a = (long)cy, b = (long)cx;
+  double ly = py - cy, lx = px - cx;
   double hy = 1.0 - ly, hx = 1.0 - lx;
   long ya[2] = {a, a + 1}, xb[2] = {b, b + 1};
   double wy[2] = {hy, ly}, wx[2] = {hx, lx};
@@ -149,6 +160,18 @@ static void orc_bilinear_scatter(double *plane, int H, int W, double py,
       if (ya[u] < 0 || ya[u] >= H || xb[v] < 0 || xb[v] >= W) continue;
       plane[ya[u] * W + xb[v]] += wy[u] * wx[v] * g;
     }
+}
+
+/* Cell of a sampling coordinate base + shift.  floor() turns the coordinate
+ * into an integer (which four pixels are blended, and on which side of a
+ * pixel line the derivative is taken), so that decision is made in the
+ * precision the GPU kernels form the coordinate in: float32, on
+ * fl32(fl32(base) + fl32(shift)).  The weights inside the cell stay fp64.
+ * Away from pixel lines this is floor(base + shift) exactly; within a float32
+ * rounding of a line it picks the same side as the kernels. */
+double orc_cell(long base, double shift) {
+  float p32 = (float)base + (float)shift;
+  return floor((double)p32);
 }
 
 /* Step 1 of 5: offset convolution.
@@ -188,10 +211,12 @@ int orc_offsets(const orc_problem *p, const double *x, const double *w_off,
 }
 
 /* Sampling point of tap (i, j) at output (ho, wo) of image n for offset
- * group g: base grid position plus the learned shift (Step 1 of 5). */
-static void orc_sample_point(const orc_problem *p, const double *off, int n,
-                             int g, int i, int j, int ho, int wo, double *py,
-                             double *px) {
+ * group g: base grid position plus the learned shift (Step 1 of 5).  Returns
+ * 0 when no corner can touch the image (sample and derivatives are zero),
+ * else 1 with the point (py, px) and its cell (cy, cx). */
+static int orc_sample_point(const orc_problem *p, const double *off, int n,
+                            int g, int i, int j, int ho, int wo, double *py,
+                            double *px, double *cy, double *cx) {
   const int Ho = orc_out_h(p), Wo = orc_out_w(p);
   const int K = p->kh * p->kw, M = 2 * p->groups * K;
   const int k = i * p->kw + j;
@@ -199,8 +224,14 @@ static void orc_sample_point(const orc_problem *p, const double *off, int n,
   const long base = (long)n * M * HoWo + (long)ho * Wo + wo;
   double dy = off[base + (long)(2 * (g * K + k)) * HoWo];
   double dx = off[base + (long)(2 * (g * K + k) + 1) * HoWo];
-  *py = (double)((long)ho * p->stride_h - p->pad_h + (long)i * p->dil_h) + dy;
-  *px = (double)((long)wo * p->stride_w - p->pad_w + (long)j * p->dil_w) + dx;
+  long by = (long)ho * p->stride_h - p->pad_h + (long)i * p->dil_h;
+  long bx = (long)wo * p->stride_w - p->pad_w + (long)j * p->dil_w;
+  *py = (double)by + dy;
+  *px = (double)bx + dx;
+  if (!orc_near_image(p->h, p->w, *py, *px)) return 0;
+  *cy = orc_cell(by, dy);
+  *cx = orc_cell(bx, dx);
+  return 1;
 }
 
 /* The deformed ("unrolled") feature map, col[n, c, k, ho, wo] = bilinear
@@ -224,9 +255,11 @@ int orc_column(const orc_problem *p, const double *x, const double *off,
           double *dst = col + (((long)n * p->c_in + c) * K + k) * HoWo;
           for (int ho = 0; ho < Ho; ++ho)
             for (int wo = 0; wo < Wo; ++wo) {
-              double py, px;
-              orc_sample_point(p, off, n, g, i, j, ho, wo, &py, &px);
-              dst[(long)ho * Wo + wo] = orc_bilinear(plane, p->h, p->w, py, px);
+              double py, px, cy, cx;
+              double v = 0.0;
+              if (orc_sample_point(p, off, n, g, i, j, ho, wo, &py, &px, &cy, &cx))
+                v = orc_bilinear_cell(plane, p->h, p->w, py, px, cy, cx);
+              dst[(long)ho * Wo + wo] = v;
             }
         }
     }
@@ -254,10 +287,10 @@ int orc_column_adjoint(const orc_problem *p, const double *off,
           const double *src = gcol + (((long)n * p->c_in + c) * K + k) * HoWo;
           for (int ho = 0; ho < Ho; ++ho)
             for (int wo = 0; wo < Wo; ++wo) {
-              double py, px;
-              orc_sample_point(p, off, n, g, i, j, ho, wo, &py, &px);
-              orc_bilinear_scatter(plane, p->h, p->w, py, px,
-                                   src[(long)ho * Wo + wo]);
+              double py, px, cy, cx;
+              if (orc_sample_point(p, off, n, g, i, j, ho, wo, &py, &px, &cy, &cx))
+                orc_bilinear_scatter_cell(plane, p->h, p->w, py, px, cy, cx,
+                                          src[(long)ho * Wo + wo]);
             }
         }
     }
@@ -374,18 +407,19 @@ int orc_backward(const orc_problem *p, const double *x, const double *w_off,
           double *gdx = gdy + HoWo;
           for (int ho = 0; ho < Ho; ++ho)
             for (int wo = 0; wo < Wo; ++wo) {
-              double py, px, sy = 0.0, sx = 0.0;
-              orc_sample_point(p, off, n, g, i, j, ho, wo, &py, &px);
-              for (int c = g * Cg; c < (g + 1) * Cg; ++c) {
-                const double *plane = x + ((long)n * p->c_in + c) * HW;
-                const double gc =
-                    gcol[(((long)n * p->c_in + c) * K + k) * HoWo +
-                         (long)ho * Wo + wo];
-                double dpy, dpx;
-                orc_bilinear_grad(plane, p->h, p->w, py, px, &dpy, &dpx);
-                sy += gc * dpy;
-                sx += gc * dpx;
-              }
+              double py, px, cy, cx, sy = 0.0, sx = 0.0;
+              if (orc_sample_point(p, off, n, g, i, j, ho, wo, &py, &px, &cy, &cx))
+                for (int c = g * Cg; c < (g + 1) * Cg; ++c) {
+                  const double *plane = x + ((long)n * p->c_in + c) * HW;
+                  const double gc =
+                      gcol[(((long)n * p->c_in + c) * K + k) * HoWo +
+                           (long)ho * Wo + wo];
+                  double dpy, dpx;
+                  orc_bilinear_grad_cell(plane, p->h, p->w, py, px, cy, cx, &dpy,
+                                         &dpx);
+                  sy += gc * dpy;
+                  sx += gc * dpx;
+                }
               gdy[(long)ho * Wo + wo] = sy;
               gdx[(long)ho * Wo + wo] = sx;
             }

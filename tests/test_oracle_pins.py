@@ -382,3 +382,29 @@ def test_rejects_bad_problems():
     with pytest.raises(ValueError):
         oracle.offsets(oracle.Problem(1, 3, 1, 4, 2, kh=3, kw=3, pad=0), x[:, :, :1],
                        np.zeros((18, 3, 3, 3)))
+
+
+# ---------------------------------------------------------------- cell decision
+
+
+def test_cell_is_decided_on_the_float32_coordinate():
+    """floor() of a sampling coordinate is an integer decision and is taken on
+    the float32 value base + shift (the kernels' precision).  A shift that is
+    just below 1 in fp64 but rounds to 1.0 in float32 puts the sample in the
+    next cell: the offset gradient is the right-sided difference there."""
+    p = oracle.Problem(1, 1, 8, 3, 1, 1, 1, 1, 0, 1, 1)
+    rng = np.random.default_rng(19)
+    x = rng.standard_normal((1, 1, 8, 3))
+    w = np.ones((1, 1, 1, 1))
+    gy = np.zeros((1, 1, 8, 3))
+    gy[0, 0, 3, 1] = 1.0
+    off = np.zeros((1, 2, 8, 3))
+    shift = 0.99999999
+    off[0, 0, 3, 1] = shift
+    assert np.floor(np.float32(3) + np.float32(shift)) == 4.0
+    assert np.floor(3 + shift) == 3.0
+    g = oracle.backward(p, x, np.zeros((2, 1, 1, 1)), w, off, gy)
+    assert g["grad_offset"][0, 0, 3, 1] == x[0, 0, 5, 1] - x[0, 0, 4, 1]
+    # the sample itself is continuous across the line
+    col = oracle.column(p, x, off)
+    assert abs(col[0, 0, 0, 3, 1] - x[0, 0, 4, 1]) < 1e-7
