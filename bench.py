@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="budget of the oracle's CPU-baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--roofline-iters", type=int, default=200)
+    ap.add_argument("--e2e-iters", type=int, default=20)
     return ap.parse_args()
 
 
@@ -298,8 +300,8 @@ def main():
             "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
 
     if rank == 0:
-        line["roofline"] = k1_roofline(p, t, dev, stream, flush, wl)
-        line["e2e"] = e2e(p, d, dev, stream, flops_step)
+        line["roofline"] = k1_roofline(p, t, dev, stream, flush, wl, args.roofline_iters)
+        line["e2e"] = e2e(p, d, dev, stream, flops_step, args.e2e_iters)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
             line["cpu_baseline"].pop("ms_per_image", None)

@@ -22,8 +22,9 @@ _TORCH_DTYPE = {DC_F32: torch.float32, DC_BF16: torch.bfloat16}
 EXPORTED_SYMBOLS = (
     "dc_out_h", "dc_out_w", "deform_conv_workspace_size", "deform_conv_fwd",
     "deform_conv_bwd", "deform_conv_sample", "dc_status_string", "dc_build_info",
-    "dc_launch_count",
+    "dc_launch_count", "deform_conv_fwd_noalloc",
 )
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class DcProblem(ctypes.Structure):
@@ -64,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.dc_status_string.restype = ctypes.c_char_p
         L.dc_build_info.argtypes = []
         L.dc_build_info.restype = ctypes.c_char_p
+        L.deform_conv_fwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.deform_conv_fwd_noalloc.restype = i
         L.dc_launch_count.argtypes = []
         L.dc_launch_count.restype = ctypes.c_ulonglong
         _configured = True
@@ -189,6 +192,22 @@ def deform_conv_fwd(p: Problem, x, w_off, b_off, w, offset_add, y, offset_out=No
         _ptr(offset_out, "offset_out", s["offset"], f32, True),
         _ptr(slowpath_count, "slowpath_count", (1,), torch.int64, True),
         ws_ptr, ctypes.c_size_t(ws.numel()), _stream(stream)), "deform_conv_fwd")
+
+
+def deform_conv_fwd_noalloc(p: Problem, x, w_off, b_off, w, offset_add, y, offset_out=None,
+                            slowpath_count=None, stream=None):
+    """Forward pass with the library's fixed scratch array instead of a
+    workspace (for callers that cannot allocate device memory)."""
+    s = p.shapes()
+    dt, f32 = p.torch_dtype, torch.float32
+    st = p.c_struct()
+    _check(lib().deform_conv_fwd_noalloc(
+        ctypes.byref(st), _ptr(x, "x", s["x"], dt), _ptr(w_off, "w_off", s["w_off"], dt),
+        _ptr(b_off, "b_off", s["b_off"], f32, True), _ptr(w, "w", s["w"], dt),
+        _ptr(offset_add, "offset_add", s["offset"], f32, True), _ptr(y, "y", s["y"], dt),
+        _ptr(offset_out, "offset_out", s["offset"], f32, True),
+        _ptr(slowpath_count, "slowpath_count", (1,), torch.int64, True),
+        _stream(stream)), "deform_conv_fwd_noalloc")
 
 
 def deform_conv_bwd(p: Problem, x, w_off, w, offset, grad_y, grad_x, grad_w_off, grad_b_off,

@@ -140,6 +140,30 @@ dc_status deform_conv_sample(const dc_problem* prob, const void* x, const void* 
                              const float* offset_in, void* col, float* offset_out,
                              unsigned long long* slowpath_count, void* stream);
 
+/* Forward pass without a caller-provided workspace.  The paper has no
+ * counterpart to this entry point; it exists for callers that cannot allocate
+ * device memory -- loops that must not allocate once running, plug-ins whose
+ * host framework owns all device memory, call sites that could not handle an
+ * allocation failure.  Arguments and results are those of deform_conv_fwd
+ * minus ws/ws_bytes.
+ *   - Scratch: a fixed array of DC_NOALLOC_SCRATCH_BYTES inside this library,
+ *     held on every GPU that loads the library until the process exits.
+ *     Problems whose forward workspace (deform_conv_workspace_size(prob, 0))
+ *     exceeds it are rejected with DC_ERR_WORKSPACE before anything runs.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on each device looks up the array's device address on
+ *     that device (cudaGetSymbolAddress); make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; nothing there needs to start at zero.  Calls whose work
+ *     overlaps on the GPU (other streams, other host threads) race on the
+ *     array: serialise them. */
+#define DC_NOALLOC_SCRATCH_BYTES (32u << 20)
+dc_status deform_conv_fwd_noalloc(const dc_problem* prob, const void* x, const void* w_off,
+                                  const float* b_off, const void* w, const float* offset_add,
+                                  void* y, float* offset_out,
+                                  unsigned long long* slowpath_count, void* stream);
+
 /* Static description of a status code. */
 const char* dc_status_string(dc_status status);
 
