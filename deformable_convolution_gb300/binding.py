@@ -22,7 +22,7 @@ _TORCH_DTYPE = {DC_F32: torch.float32, DC_BF16: torch.bfloat16}
 EXPORTED_SYMBOLS = (
     "dc_out_h", "dc_out_w", "deform_conv_workspace_size", "deform_conv_fwd",
     "deform_conv_bwd", "deform_conv_sample", "dc_status_string", "dc_build_info",
-    "dc_launch_count", "deform_conv_fwd_noalloc",
+    "dc_launch_count", "deform_conv_fwd_noalloc", "dc_device_error",
 )
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.dc_build_info.restype = ctypes.c_char_p
         L.deform_conv_fwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.deform_conv_fwd_noalloc.restype = i
+        L.dc_device_error.argtypes = [i]
+        L.dc_device_error.restype = i
         L.dc_launch_count.argtypes = []
         L.dc_launch_count.restype = ctypes.c_ulonglong
         _configured = True
@@ -79,6 +81,11 @@ def status_string(status: int) -> str:
 
 def build_info() -> str:
     return lib().dc_build_info().decode()
+
+
+def device_error(clear: bool = False) -> int:
+    """DC_ERR_TIMEOUT if a bounded device wait expired (synchronises)."""
+    return int(lib().dc_device_error(1 if clear else 0))
 
 
 def launch_count() -> int:

@@ -5,10 +5,10 @@
 // page "DefT: Boosting Scalability of Deformable Convolution Operations on
 // GPUs"): K1 fuses the offset convolution with the bilinear interpolation and
 // writes the deformed map; the main convolution is a separate dense GEMM over
-// that map.  Backward: K1 replays the deformed map from the saved offsets, two
-// GEMMs give the map's gradient and the main weights' gradient, K3 scatters
-// the map's gradient into grad_x and reduces the offset gradient, and K4 runs
-// the offset convolution's backward.
+// that map.  Backward: a GEMM gives the deformed map's gradient; K3 scatters
+// it into grad_x, reduces the offset gradient, runs the offset convolution's
+// backward and replays the deformed map; a second GEMM gives the main
+// weights' gradient from that map.
 #include <stdint.h>
 #include <string.h>
 
@@ -78,6 +78,7 @@ dc_status make_geom(const dc_problem* p, Geom* g, int* margin) {
   *margin = p->halo_margin < 0 ? kDefaultMargin : p->halo_margin;
   if (*margin > kMaxMargin) return DC_ERR_UNSUPPORTED;
   if (sample_smem_bytes(*g, p->dtype, *margin) > kMaxSampleSmem) return DC_ERR_UNSUPPORTED;
+  if (bwd_smem_bytes(*g, p->dtype, *margin) > kMaxSampleSmem) return DC_ERR_UNSUPPORTED;
   return DC_OK;
 }
 
@@ -201,27 +202,23 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
   char* wsb = static_cast<char*>(ws);
   float* goff = grad_offset ? grad_offset : reinterpret_cast<float*>(wsb + pl.off_off);
 
+  // atomic targets start at zero
   st = cuda_status(cudaMemsetAsync(grad_x, 0, sizeof(float) * g.n * g.c_in * g.hw, s));
   if (st != DC_OK) return st;
   st = cuda_status(cudaMemsetAsync(grad_w, 0, sizeof(float) * g.c_out * g.kdim, s));
   if (st != DC_OK) return st;
-
-  // deformed map, replayed from the saved offsets
-  SampleArgs sa{};
-  sa.g = g;
-  sa.x = x;
-  sa.w_off = w_off;
-  sa.off_in = offset;
-  sa.col = wsb + pl.col_off;
-  sa.col_layout = pl.col;
-  sa.margin = margin;
-  st = cuda_status(launch_sample(sa, prob->dtype, s));
+  st = cuda_status(cudaMemsetAsync(grad_w_off, 0, sizeof(float) * g.M * g.kdim, s));
   if (st != DC_OK) return st;
+  if (grad_b_off) {
+    st = cuda_status(cudaMemsetAsync(grad_b_off, 0, sizeof(float) * g.M, s));
+    if (st != DC_OK) return st;
+  }
 
+  // gradient of the deformed map: gcol = w^T grad_y
   GemmArgs ga{};
   ga.g = g;
   ga.w = w;
-  ga.col = sa.col;
+  ga.col = wsb + pl.col_off;
   ga.col_layout = pl.col;
   ga.gy = grad_y;
   ga.gcol = reinterpret_cast<float*>(wsb + pl.gcol_off);
@@ -229,29 +226,27 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
   ga.gw = grad_w;
   st = cuda_status(launch_gemm_gcol(ga, prob->dtype, s));
   if (st != DC_OK) return st;
-  st = cuda_status(launch_gemm_gw(ga, prob->dtype, s));
+
+  // sampling and offset-conv backward; replays the deformed map for grad_w
+  BwdArgs ba{};
+  ba.g = g;
+  ba.x = x;
+  ba.w_off = w_off;
+  ba.off = offset;
+  ba.gcol = ga.gcol;
+  ba.gcol_layout = pl.gcol;
+  ba.col = wsb + pl.col_off;
+  ba.col_layout = pl.col;
+  ba.gx = grad_x;
+  ba.goff = goff;
+  ba.gw_off = grad_w_off;
+  ba.gb_off = grad_b_off;
+  ba.margin = margin;
+  st = cuda_status(launch_band_bwd(ba, prob->dtype, s));
   if (st != DC_OK) return st;
 
-  ScatterArgs ka{};
-  ka.g = g;
-  ka.x = x;
-  ka.off = offset;
-  ka.gcol = ga.gcol;
-  ka.gcol_layout = pl.gcol;
-  ka.gx = grad_x;
-  ka.goff = goff;
-  st = cuda_status(launch_scatter(ka, prob->dtype, s));
-  if (st != DC_OK) return st;
-
-  OffconvBwdArgs oa{};
-  oa.g = g;
-  oa.x = x;
-  oa.w_off = w_off;
-  oa.goff = goff;
-  oa.gx = grad_x;
-  oa.gw_off = grad_w_off;
-  oa.gb_off = grad_b_off;
-  return cuda_status(launch_offconv_bwd(oa, prob->dtype, s));
+  // main weight gradient from the replayed map
+  return cuda_status(launch_gemm_gw(ga, prob->dtype, s));
 }
 
 dc_status deform_conv_sample(const dc_problem* prob, const void* x, const void* w_off,
@@ -307,14 +302,19 @@ const char* dc_build_info(void) {
 
 namespace dc {
 
-// GEMM dispatch: CUDA cores for now.
+// GEMM dispatch: bf16 problems whose rows are 16-byte aligned run on the
+// tensor cores; float32 problems (whose tolerance a bf16/tf32 contraction would
+// not hold) and unaligned shapes run on CUDA cores.
 cudaError_t launch_gemm_fwd(const GemmArgs& a, dc_dtype dt, cudaStream_t s) {
+  if (dt == DC_BF16 && tc_gemm_supported(a.g)) return launch_gemm_fwd_tc(a, s);
   return launch_gemm_fwd_simt(a, dt, s);
 }
 cudaError_t launch_gemm_gcol(const GemmArgs& a, dc_dtype dt, cudaStream_t s) {
+  if (dt == DC_BF16 && tc_gemm_supported(a.g)) return launch_gemm_gcol_tc(a, s);
   return launch_gemm_gcol_simt(a, dt, s);
 }
 cudaError_t launch_gemm_gw(const GemmArgs& a, dc_dtype dt, cudaStream_t s) {
+  if (dt == DC_BF16 && tc_gemm_supported(a.g)) return launch_gemm_gw_tc(a, s);
   return launch_gemm_gw_simt(a, dt, s);
 }
 

@@ -1,0 +1,217 @@
+// Band tiling shared by the fused forward kernel (K1) and the fused backward
+// kernel (K3).
+//
+// The explainer page "DefT: Boosting Scalability of Deformable Convolution
+// Operations on GPUs" tiles by the output's spatial dimensions and pads each
+// tile's input window by a margin sized to the offset distribution ("Why it
+// works", "The idea").  Here a tile is a band of R full-width output rows
+// (at most kBandPx pixels); its input window is the band's receptive field plus
+// `margin` pixels on each side.  Channels are split into slices of CPC, one
+// slice per CTA of a thread-block cluster.
+#pragma once
+
+#include "dc_common.cuh"
+
+namespace dc {
+namespace band {
+
+constexpr int kThreads = 256;
+constexpr int kBandPx = 128;  // largest band; smaller ones are tried when shared memory is short
+constexpr int kMaxCluster = 8;
+
+struct Shape {
+  int R, TW, tiles_w, tiles_h, npx;
+  int in_rows, in_cols;  // receptive field of the band
+  int rows, cols;        // staged window (receptive field + 2 * margin)
+  int plane;             // padded 32-bit words per staged plane
+};
+
+// Words per plane, rounded so that consecutive planes start 8 banks apart.
+__host__ inline int pad_plane(int v) {
+  int p = (v + 31) / 32 * 32 + 8;
+  if (p - 32 >= v) p -= 32;
+  return p;
+}
+
+// Band of at most `px` output pixels: full-width rows when the output is at
+// most `px` wide, else `px`-wide row segments.
+__host__ inline Shape make_shape(const Geom& g, int margin, int px) {
+  Shape s{};
+  if (g.wo <= px) {
+    s.TW = g.wo;
+    s.R = px / g.wo;
+    if (s.R > g.ho) s.R = g.ho;
+    if (s.R < 1) s.R = 1;
+  } else {
+    s.TW = px;
+    s.R = 1;
+  }
+  s.npx = s.R * s.TW;
+  s.tiles_w = (int)ceil_div_ll(g.wo, s.TW);
+  s.tiles_h = (int)ceil_div_ll(g.ho, s.R);
+  s.in_rows = (s.R - 1) * g.sh + (g.kh - 1) * g.dh + 1;
+  s.in_cols = (s.TW - 1) * g.sw + (g.kw - 1) * g.dw + 1;
+  s.rows = s.in_rows + 2 * margin;
+  s.cols = s.in_cols + 2 * margin;
+  s.plane = pad_plane(s.rows * s.cols);
+  return s;
+}
+
+// Per (pixel, tap, group) sampling state.
+struct Tap {
+  bool inside, fast;
+  float ly, lx;
+  int y0, x0;  // lower corner, image coordinates
+};
+
+__device__ __forceinline__ Tap make_tap(float py, float pxf, const Geom& g, int ylo, int xlo,
+                                        int rows, int cols) {
+  Tap t;
+  t.inside = touches_image(py, pxf, g.h, g.w);
+  t.fast = false;
+  t.ly = t.lx = 0.f;
+  t.y0 = t.x0 = 0;
+  if (t.inside) {
+    const float fy = floorf(py), fx = floorf(pxf);
+    t.ly = py - fy;
+    t.lx = pxf - fx;
+    t.y0 = (int)fy;
+    t.x0 = (int)fx;
+    const int ry = t.y0 - ylo, rx = t.x0 - xlo;
+    t.fast = ry >= 0 && ry + 1 < rows && rx >= 0 && rx + 1 < cols;
+  }
+  return t;
+}
+
+template <typename T>
+__device__ __forceinline__ float gload(const T* plane, const Geom& g, int y, int x) {
+  return (y >= 0 && y < g.h && x >= 0 && x < g.w) ? ld_f(plane + (long long)y * g.w + x) : 0.0f;
+}
+
+__device__ __forceinline__ uint32_t bf16_bits(const __nv_bfloat16* p) {
+  return (uint32_t)(*reinterpret_cast<const unsigned short*>(p));
+}
+
+__device__ __forceinline__ uint32_t raw_bits(const __nv_bfloat16* p) { return bf16_bits(p); }
+__device__ __forceinline__ uint32_t raw_bits(const float* p) { return __float_as_uint(*p); }
+
+// Walks the flattened index of a [A x B] grid in steps of `step` without
+// divisions after the first element (step is split once into step = da*B + db).
+struct Walk2 {
+  int a, b, da, db, B;
+  __device__ __forceinline__ void init(int start, int step, int nb) {
+    B = nb;
+    a = start / nb;
+    b = start - a * nb;
+    da = step / nb;
+    db = step - da * nb;
+  }
+  __device__ __forceinline__ void next() {
+    b += db;
+    a += da;
+    if (b >= B) {
+      b -= B;
+      a += 1;
+    }
+  }
+};
+
+// Same for a [A x B x C] grid.
+struct Walk3 {
+  int a, b, c, da, db, dc, B, C;
+  __device__ __forceinline__ void init(int start, int step, int nb, int nc) {
+    B = nb;
+    C = nc;
+    const int bc = nb * nc;
+    a = start / bc;
+    int r = start - a * bc;
+    b = r / nc;
+    c = r - b * nc;
+    da = step / bc;
+    r = step - da * bc;
+    db = r / nc;
+    dc = r - db * nc;
+  }
+  __device__ __forceinline__ void next() {
+    c += dc;
+    b += db;
+    a += da;
+    if (c >= C) {
+      c -= C;
+      b += 1;
+    }
+    if (b >= B) {
+      b -= B;
+      a += 1;
+    }
+  }
+};
+
+// Stages the window [ylo, ylo+rows) x [xlo, xlo+cols) of channels
+// [c_begin, c_begin + cpc) of image `img` into shared memory, zero outside the
+// image and beyond c_in.  bf16: one 32-bit word per pixel per channel pair
+// (low half = even channel); fp32: one word per pixel per channel.  Plane u
+// starts at dst + u * plane.  Each thread keeps kBatch independent global loads
+// in flight; lanes run along window rows, so loads are coalesced.
+template <typename T>
+__device__ __forceinline__ void stage_window(const T* __restrict__ x, const Geom& g,
+                                             long long img, int c_begin, int cpc, int ylo,
+                                             int xlo, int rows, int cols, int plane,
+                                             uint32_t* dst) {
+  constexpr bool kPairs = sizeof(T) == 2;
+  constexpr int kBatch = 8;
+  const int units = kPairs ? cpc / 2 : cpc;
+  Walk3 w;
+  w.init(threadIdx.x, kThreads, rows, cols);
+  while (w.a < units) {
+    uint32_t v[kBatch];
+    int at[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      v[j] = 0u;
+      at[j] = -1;
+      if (w.a < units) {
+        const int u = w.a;
+        at[j] = u * plane + w.b * cols + w.c;
+        const int yy = ylo + w.b, xx = xlo + w.c;
+        if (yy >= 0 && yy < g.h && xx >= 0 && xx < g.w) {
+          const long long pix = (long long)yy * g.w + xx;
+          if (kPairs) {
+            const int c0 = c_begin + 2 * u;
+            if (c0 < g.c_in) v[j] = raw_bits(x + img + (long long)c0 * g.hw + pix);
+            if (c0 + 1 < g.c_in) v[j] |= raw_bits(x + img + (long long)(c0 + 1) * g.hw + pix) << 16;
+          } else {
+            const int c = c_begin + u;
+            if (c < g.c_in) v[j] = raw_bits(x + img + (long long)c * g.hw + pix);
+          }
+        }
+        w.next();
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j)
+      if (at[j] >= 0) dst[at[j]] = v[j];
+  }
+}
+
+// Per-band table of output pixels: packs (row in band, column in band) into
+// one int so inner loops need no division by the band width.
+__device__ __forceinline__ void fill_pixel_table(int* tab, int npx, int TW) {
+  for (int px = threadIdx.x; px < npx; px += kThreads) {
+    const int r = px / TW;
+    tab[px] = (r << 16) | (px - r * TW);
+  }
+}
+
+// Value of channel `cl` (relative to the slice) at staged word offset `pos`.
+template <typename T>
+__device__ __forceinline__ float staged(const uint32_t* xs, int plane, int cl, int pos) {
+  if (sizeof(T) == 2) {
+    const uint32_t w = xs[(cl >> 1) * plane + pos];
+    return __uint_as_float(((cl & 1) ? w : (w << 16)) & 0xffff0000u);
+  }
+  return __uint_as_float(xs[cl * plane + pos]);
+}
+
+}  // namespace band
+}  // namespace dc

@@ -107,33 +107,35 @@ struct GemmArgs {
   ColLayout gcol_layout;
   float* gw;          // [c_out][kdim] fp32, accumulated with atomics (backward)
 };
+// Tensor-core (tcgen05, bf16) versions; need tc_gemm_supported(g).
+bool tc_gemm_supported(const Geom& g);
+cudaError_t launch_gemm_fwd_tc(const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_gcol_tc(const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_gw_tc(const GemmArgs& a, cudaStream_t s);
 // CUDA-core (fp32 arithmetic) versions, any layout pitch.
 cudaError_t launch_gemm_fwd_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
 cudaError_t launch_gemm_gcol_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
 cudaError_t launch_gemm_gw_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
 
-// Backward of the sampling step: grad_x (atomics) and the offset gradient.
-struct ScatterArgs {
-  Geom g;
-  const void* x;
-  const float* off;
-  const float* gcol;
-  ColLayout gcol_layout;
-  float* gx;
-  float* goff;
-};
-cudaError_t launch_scatter(const ScatterArgs& a, dc_dtype dt, cudaStream_t s);
-
-// Backward of the offset convolution.
-struct OffconvBwdArgs {
+// Fused backward of the sampling step and of the offset convolution (K3):
+// grad_x (atomics; zeroed by the caller), the offset gradient, grad_w_off and
+// grad_b_off (atomics; zeroed by the caller), and the replayed deformed map.
+struct BwdArgs {
   Geom g;
   const void* x;
   const void* w_off;
-  const float* goff;
-  float* gx;        // += transposed convolution of goff
-  float* gw_off;    // overwritten
-  float* gb_off;    // overwritten, may be null
+  const float* off;
+  const float* gcol;
+  ColLayout gcol_layout;
+  void* col;  // may be null: deformed map not written
+  ColLayout col_layout;
+  float* gx;
+  float* goff;
+  float* gw_off;
+  float* gb_off;  // may be null
+  int margin;
 };
-cudaError_t launch_offconv_bwd(const OffconvBwdArgs& a, dc_dtype dt, cudaStream_t s);
+cudaError_t launch_band_bwd(const BwdArgs& a, dc_dtype dt, cudaStream_t s);
+size_t bwd_smem_bytes(const Geom& g, dc_dtype dt, int margin);
 
 }  // namespace dc

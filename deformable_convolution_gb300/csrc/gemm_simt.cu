@@ -7,8 +7,10 @@
 //   forward  y[b][o][q]     = sum_r w[o][r] * col[r][b][q]
 //   backward gcol[r][b][q]  = sum_o w[o][r] * gy[b][o][q]
 //            gw[o][r]      += sum_{b,q} gy[b][o][q] * col[r][b][q]
-// This file is the float32 path (a tensor-core path would not hold the
-// float32 tolerance); bf16 problems use the tcgen05 kernels in gemm_tc.cu.
+// This file is the float32 path (a bf16/tf32 tensor-core contraction would
+// not hold the float32 tolerance) and the path for bf16 shapes whose rows are
+// not 16-byte aligned; other bf16 problems use the tcgen05 kernels in
+// gemm_tc.cu.
 #include "dc_common.cuh"
 
 namespace dc {

@@ -1,0 +1,480 @@
+// Main-convolution GEMMs on the 5th-generation tensor cores (bf16 inputs,
+// fp32 accumulation in tensor memory).
+//
+// Explainer page "DefT: Boosting Scalability of Deformable Convolution
+// Operations on GPUs", "The argument in one glance / This paper's idea" and
+// "The idea": the main convolution over the deformed map is left as a dense
+// GEMM -- the one step of the layer that is a true contraction.  On GB300 it
+// runs here as a hand-written tcgen05 kernel instead of a library call.
+// With the column layout col[kdim][image][pixel]:
+//   FWD   y[b][o][q]    = sum_r   w[o][r]  * col[r][b][q]     A = w   (K-major)
+//                                                              B = col (MN-major)
+//   GCOL  gcol[r][b][q] = sum_o   w[o][r]  * gy[b][o][q]      A = w^T (MN-major)
+//                                                              B = gy  (MN-major)
+//   GW    gw[o][r]     += sum_b,q gy[b][o][q] * col[r][b][q]  A = gy  (K-major)
+//                                                              B = col (K-major)
+// One CTA computes one 128 x BN output tile (GW: one K-split of it).
+// Warp roles: warps 0-3 read the accumulator out of tensor memory (one TMEM
+// lane quarter each), warp 4 issues TMA loads into a ring of shared-memory
+// stages, warp 5 issues tcgen05.mma (one thread) and commits each stage back to
+// the producer.  All operand tiles use the 128-byte swizzle.  Every mbarrier
+// wait is bounded: on expiry the kernel raises the library's device error flag,
+// skips the rest of its work, frees its tensor memory and returns.
+#include <cuda.h>
+
+#include "dc_common.cuh"
+
+namespace dc {
+
+__device__ unsigned int g_dc_device_error;
+
+namespace {
+
+constexpr int kBM = 128, kBK = 64;
+constexpr int kThreads = 192;
+constexpr uint32_t kSpinLimit = 1u << 24;
+enum Kind { FWD = 0, GCOL = 1, GW = 2 };
+
+struct TcArgs {
+  int c_out, kdim, howo, nimg;
+  int kb_total;          // k-blocks of the whole reduction
+  int kb_per_split;      // GW: k-blocks per CTA along blockIdx.z
+  int qblocks;           // GW: k-blocks per image (ceil(howo / 64))
+  void* out;
+  long long out_row, out_img;  // GCOL: gcol pitches (elements)
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait; false (and the device error flag raised) on expiry.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  atomicOr(&g_dc_device_error, 1u);
+  return false;
+}
+
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
+                                       int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
+                                       int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: 128-byte swizzle, sm_100 descriptor version.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M = 128, N = bn.
+__host__ __device__ constexpr uint32_t idesc_bf16(int bn, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(bn >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <int KIND, int BN>
+struct Cfg {
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStage = kABytes + kBBytes;
+  // GCOL reduces over C_out only (a few k-blocks): two stages, so that three
+  // CTAs fit on an SM; the long reductions keep a deeper ring.
+  static constexpr int kStages = KIND == GCOL ? 2 : (BN >= 128 ? 4 : 6);
+  static constexpr int kTmemCols = BN < 32 ? 32 : BN;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256;
+  static constexpr int kAMn = KIND == GCOL ? 1 : 0;
+  static constexpr int kBMn = KIND == GW ? 0 : 1;
+};
+
+template <int KIND, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+            TcArgs a) {
+  using C = Cfg<KIND, BN>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* done = empty + C::kStages;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * BN;
+  const int z = blockIdx.z;
+  int kb_begin = 0, kb_end = a.kb_total;
+  if (KIND == GW) {
+    kb_begin = z * a.kb_per_split;
+    kb_end = min(a.kb_total, kb_begin + a.kb_per_split);
+  }
+  const int nkb = kb_end > kb_begin ? kb_end - kb_begin : 0;
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_holder)),
+                 "r"((uint32_t)C::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % C::kStages;
+        if (i >= C::kStages && !mbar_wait(&empty[s], ((i / C::kStages) - 1) & 1)) break;
+        unsigned char* sa = smem + s * C::kStage;
+        unsigned char* sb = sa + C::kABytes;
+        mbar_expect_tx(&full[s], C::kStage);
+        const int kb = kb_begin + i;
+        if (KIND == FWD) {
+          tma_2d(sa, &tmA, &full[s], kb * kBK, m0);
+#pragma unroll
+          for (int h = 0; h < BN / 64; ++h) tma_3d(sb + h * 8192, &tmB, &full[s], n0 + 64 * h, z, kb * kBK);
+        } else if (KIND == GCOL) {
+          tma_2d(sa, &tmA, &full[s], m0, kb * kBK);
+          tma_2d(sa + 8192, &tmA, &full[s], m0 + 64, kb * kBK);
+#pragma unroll
+          for (int h = 0; h < BN / 64; ++h) tma_3d(sb + h * 8192, &tmB, &full[s], n0 + 64 * h, kb * kBK, z);
+        } else {
+          const int img = kb / a.qblocks, q0 = (kb - img * a.qblocks) * kBK;
+          tma_3d(sa, &tmA, &full[s], q0, m0, img);
+          tma_3d(sb, &tmB, &full[s], q0, img, n0);
+        }
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = idesc_bf16(BN, C::kAMn, C::kBMn);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % C::kStages;
+        if (!mbar_wait(&full[s], (i / C::kStages) & 1)) break;
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + s * C::kStage);
+        const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          // K-major: step 32 bytes inside the 128-byte swizzled row;
+          // MN-major: step 16 k-rows = two 1024-byte swizzle atoms
+          const uint64_t da = C::kAMn ? sdesc(sa + kk * 2048, 8192, 1024) : sdesc(sa + kk * 32, 16, 1024);
+          const uint64_t db = C::kBMn ? sdesc(sb + kk * 2048, 8192, 1024) : sdesc(sb + kk * 32, 16, 1024);
+          umma(tmem, da, db, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&empty[s]);
+      }
+      umma_commit(done);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue (warps 0-3)
+    const bool ok = mbar_wait(done, 0);
+    tc_fence_after();
+    const int row = warp * 32 + lane;
+    const int m = m0 + row;
+    const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tbase + c * 32, r);
+      if (!ok || nkb == 0) continue;
+      const int n_first = n0 + c * 32;
+      if (KIND == FWD) {
+        if (m >= a.c_out) continue;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
+                             ((long long)z * a.c_out + m) * a.howo + n_first;
+        if (n_first + 32 <= a.howo) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 pk;
+            uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[v * 8 + 2 * e]),
+                                                        __uint_as_float(r[v * 8 + 2 * e + 1]));
+              pw[e] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(dst + v * 8) = pk;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (n_first + j < a.howo) dst[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+        }
+      } else if (KIND == GCOL) {
+        if (m >= a.kdim) continue;
+        float* dst = static_cast<float*>(a.out) + (long long)m * a.out_row +
+                     (long long)z * a.out_img + n_first;
+        if (n_first + 32 <= a.howo) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            *reinterpret_cast<float4*>(dst + v * 4) =
+                make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                            __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (n_first + j < a.howo) dst[j] = __uint_as_float(r[j]);
+        }
+      } else {
+        if (m >= a.c_out) continue;
+        float* dst = static_cast<float*>(a.out) + (long long)m * a.kdim + n_first;
+        if (n_first + 32 <= a.kdim) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            atomicAdd(reinterpret_cast<float4*>(dst + v * 4),
+                      make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                  __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (n_first + j < a.kdim) atomicAdd(dst + j, __uint_as_float(r[j]));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"((uint32_t)C::kTmemCols)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// bf16 tensor map, 128-byte swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+              const cuuint64_t* strides, const cuuint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KIND, int BN>
+cudaError_t launch(const CUtensorMap& A, const CUtensorMap& B, const TcArgs& a, dim3 grid,
+                   cudaStream_t s) {
+  using C = Cfg<KIND, BN>;
+  auto k = tc_gemm<KIND, BN>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kThreads, C::kSmem, s>>>(A, B, a);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+// column buffer as a 3-D tensor {pixel (true extent), image, row}
+bool col_map(CUtensorMap* m, const void* col, const Geom& g, const ColLayout& L, cuuint32_t box_rows) {
+  const cuuint64_t dims[3] = {(cuuint64_t)g.howo, (cuuint64_t)g.n, (cuuint64_t)g.kdim};
+  const cuuint64_t strides[2] = {(cuuint64_t)L.img * 2, (cuuint64_t)L.row * 2};
+  const cuuint32_t box[3] = {64, 1, box_rows};
+  return make_map(m, col, 3, dims, strides, box);
+}
+
+// grad_y as a 3-D tensor {pixel, channel, image}
+bool gy_map(CUtensorMap* m, const void* gy, const Geom& g, cuuint32_t box_ch) {
+  const cuuint64_t dims[3] = {(cuuint64_t)g.howo, (cuuint64_t)g.c_out, (cuuint64_t)g.n};
+  const cuuint64_t strides[2] = {(cuuint64_t)g.howo * 2, (cuuint64_t)g.c_out * g.howo * 2};
+  const cuuint32_t box[3] = {64, box_ch, 1};
+  return make_map(m, gy, 3, dims, strides, box);
+}
+
+// main weights as a 2-D tensor {kdim, c_out}
+bool w_map(CUtensorMap* m, const void* w, const Geom& g, cuuint32_t box0, cuuint32_t box1) {
+  const cuuint64_t dims[2] = {(cuuint64_t)g.kdim, (cuuint64_t)g.c_out};
+  const cuuint64_t strides[1] = {(cuuint64_t)g.kdim * 2};
+  const cuuint32_t box[2] = {box0, box1};
+  return make_map(m, w, 2, dims, strides, box);
+}
+
+int pick_fwd_bn(const Geom& g) {
+  const long long tiles128 = ceil_div_ll(g.howo, 128) * ceil_div_ll(g.c_out, kBM) * g.n;
+  return tiles128 >= 148 ? 128 : 64;
+}
+
+}  // namespace
+
+// The tensor-core path needs 16-byte aligned rows for every tensor map.
+bool tc_gemm_supported(const Geom& g) {
+  return g.kdim % 8 == 0 && g.howo % 8 == 0 && encode_fn() != nullptr;
+}
+
+cudaError_t launch_gemm_fwd_tc(const GemmArgs& ga, cudaStream_t s) {
+  const Geom& g = ga.g;
+  CUtensorMap A, B;
+  if (!w_map(&A, ga.w, g, 64, 128)) return cudaErrorInvalidValue;
+  if (!col_map(&B, ga.col, g, ga.col_layout, 64)) return cudaErrorInvalidValue;
+  TcArgs a{};
+  a.c_out = g.c_out;
+  a.kdim = g.kdim;
+  a.howo = (int)g.howo;
+  a.nimg = g.n;
+  a.kb_total = (int)ceil_div_ll(g.kdim, kBK);
+  a.out = ga.y;
+  const int bn = pick_fwd_bn(g);
+  dim3 grid((unsigned)ceil_div_ll(g.howo, bn), (unsigned)ceil_div_ll(g.c_out, kBM), (unsigned)g.n);
+  return bn == 128 ? launch<FWD, 128>(A, B, a, grid, s) : launch<FWD, 64>(A, B, a, grid, s);
+}
+
+cudaError_t launch_gemm_gcol_tc(const GemmArgs& ga, cudaStream_t s) {
+  const Geom& g = ga.g;
+  CUtensorMap A, B;
+  if (!w_map(&A, ga.w, g, 64, 64)) return cudaErrorInvalidValue;
+  if (!gy_map(&B, ga.gy, g, 64)) return cudaErrorInvalidValue;
+  TcArgs a{};
+  a.c_out = g.c_out;
+  a.kdim = g.kdim;
+  a.howo = (int)g.howo;
+  a.nimg = g.n;
+  a.kb_total = (int)ceil_div_ll(g.c_out, kBK);
+  a.out = ga.gcol;
+  a.out_row = ga.gcol_layout.row;
+  a.out_img = ga.gcol_layout.img;
+  dim3 grid((unsigned)ceil_div_ll(g.howo, 128), (unsigned)ceil_div_ll(g.kdim, kBM), (unsigned)g.n);
+  return launch<GCOL, 128>(A, B, a, grid, s);
+}
+
+cudaError_t launch_gemm_gw_tc(const GemmArgs& ga, cudaStream_t s) {
+  const Geom& g = ga.g;
+  CUtensorMap A, B;
+  if (!gy_map(&A, ga.gy, g, 128)) return cudaErrorInvalidValue;
+  if (!col_map(&B, ga.col, g, ga.col_layout, 128)) return cudaErrorInvalidValue;
+  TcArgs a{};
+  a.c_out = g.c_out;
+  a.kdim = g.kdim;
+  a.howo = (int)g.howo;
+  a.nimg = g.n;
+  a.qblocks = (int)ceil_div_ll(g.howo, kBK);
+  a.kb_total = a.qblocks * g.n;
+  a.out = ga.gw;
+  const long long tiles = ceil_div_ll(g.kdim, 128) * ceil_div_ll(g.c_out, kBM);
+  long long splits = ceil_div_ll(2 * 148, tiles);
+  if (splits > a.kb_total) splits = a.kb_total;
+  if (splits < 1) splits = 1;
+  a.kb_per_split = (int)ceil_div_ll(a.kb_total, splits);
+  splits = ceil_div_ll(a.kb_total, a.kb_per_split);
+  dim3 grid((unsigned)ceil_div_ll(g.kdim, 128), (unsigned)ceil_div_ll(g.c_out, kBM), (unsigned)splits);
+  return launch<GW, 128>(A, B, a, grid, s);
+}
+
+}  // namespace dc
+
+// Reads (and optionally clears) the flag bounded device waits raise on expiry.
+extern "C" dc_status dc_device_error(int clear) {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, dc::g_dc_device_error, sizeof(v)) != cudaSuccess) return DC_ERR_CUDA;
+  if (clear && v) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(dc::g_dc_device_error, &zero, sizeof(zero)) != cudaSuccess)
+      return DC_ERR_CUDA;
+  }
+  return v ? DC_ERR_TIMEOUT : DC_OK;
+}

@@ -11,294 +11,446 @@
 //     near-zero) offset distribution, so out-of-tile reads are rare; the ones
 //     that remain take a guarded path to global memory.
 //
-// One CTA owns a TH x TW tile of output pixels of one image.  The input halo
-// of that tile (receptive field plus `margin` pixels on every side) is staged
-// in shared memory a chunk of channels at a time, zero-filled outside the
-// image.  Pass 1 accumulates the offset convolution for the tile's pixels over
-// all channel chunks; pass 2 restages each chunk and samples every (channel,
-// tap, pixel) from shared memory, or from global memory for taps whose corners
-// leave the staged window.  The deformed map is written with pixels fastest
-// (coalesced), one row per (channel, tap).
-#include "dc_common.cuh"
+// GB300 mapping.  The output is cut into bands of R full-width rows (at most
+// 128 pixels).  A thread-block cluster of up to 8 CTAs owns one band of one
+// image; CTA r of the cluster owns a slice of CPC input channels.  Each CTA
+// stages its channel slice of the band's input halo (receptive field plus
+// `margin` pixels per side, zero outside the image) in shared memory once;
+// that one copy serves both phases:
+//   phase 1  partial offset convolution over the CTA's channels (bf16: mma.sync
+//            m16n8k16 tensor-core tiles, fp32 accumulate; fp32: CUDA cores),
+//            then the cluster adds the partials through distributed shared
+//            memory -- every CTA ends with the band's complete offsets on chip;
+//   phase 2  bilinear sampling of the CTA's channels at every tap, from shared
+//            memory, or from global memory for taps whose corners leave the
+//            staged window.  Rows of the deformed map are written pixel-fastest,
+//            so a band's full-width rows land as one contiguous run.
+// In replay mode (offsets given) phase 1 is skipped and no cluster is formed.
+#include <cooperative_groups.h>
+
+#include "dc_band.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace dc {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kTH = 8, kTW = 16;       // output tile
-constexpr int kTilePx = kTH * kTW;
-constexpr int kAccMax = 8;              // offset accumulators per thread
+using band::kThreads;
+using band::Tap;
+using band::gload;
+using band::make_tap;
+constexpr int kMaxPx = band::kBandPx;  // largest band (output pixels)
+constexpr int kNtMax = 9;              // n8 tiles of offset channels per mma pass
+constexpr int kMaxCluster = band::kMaxCluster;
+constexpr size_t kSmemBudget = 112 * 1024;
 
-struct Window {
-  int y_lo, x_lo, rows, cols;
+struct Plan {
+  int R, TW;              // band: R output rows x TW output columns
+  int tiles_w, tiles_h;
+  int npx;                // R * TW
+  int ps;                 // pixel stride of the per-band offset arrays
+  int cpc;                // channels per CTA (multiple of 16)
+  int csize;              // CTAs per cluster = channel slices
+  int rows, cols;         // staged window
+  int plane;              // padded words (bf16 pairs) or floats (fp32) per staged channel (pair)
+  int mp;                 // offset channels padded to a multiple of 8
+  size_t off_halo, off_w, off_part, off_offs, off_tab, smem;
 };
 
-__host__ __device__ inline Window make_window(const Geom& g, int ho0, int wo0, int margin) {
-  Window w;
-  w.y_lo = ho0 * g.sh - g.ph - margin;
-  w.x_lo = wo0 * g.sw - g.pw - margin;
-  w.rows = (kTH - 1) * g.sh + (g.kh - 1) * g.dh + 1 + 2 * margin;
-  w.cols = (kTW - 1) * g.sw + (g.kw - 1) * g.dw + 1 + 2 * margin;
-  return w;
+__host__ size_t plan_bytes(Plan& p, const Geom& g, bool bf16, bool replay) {
+  const int units = bf16 ? p.cpc / 2 : p.cpc;  // staged planes
+  size_t at = 0;
+  p.off_halo = at;
+  at += (size_t)units * p.plane * 4;
+  p.off_w = at;
+  if (!replay) at += bf16 ? (size_t)g.K * (p.cpc / 2) * p.mp * 4 : (size_t)p.cpc * g.K * p.mp * 4;
+  p.off_part = at;
+  if (!replay) at += (size_t)p.mp * p.ps * 4;
+  p.off_offs = at;
+  at += (size_t)g.M * p.ps * 4;
+  p.off_tab = at;  // pixel table [ps] + tap offsets [K]
+  at += (size_t)(p.ps + g.K) * 4;
+  p.smem = at;
+  return at;
 }
 
-__host__ __device__ inline int chunk_channels(const Geom& g, int margin, size_t elt) {
-  // channels per staged chunk: keep the halo chunk near 48 KB
-  Window w = make_window(g, 0, 0, margin);
-  long long per_c = (long long)w.rows * w.cols * (long long)elt;
-  long long cc = (48 * 1024) / per_c;
-  if (cc < 1) cc = 1;
-  if (cc > g.c_in) cc = g.c_in;
-  if (cc > 32) cc = 32;
-  return (int)cc;
-}
-
-__host__ __device__ inline int offset_chunk(const Geom& g) {
-  // offset channels computed per pass so that each thread holds <= kAccMax
-  int mc = kAccMax * kThreads / kTilePx;
-  return mc < g.M ? mc : g.M;
-}
-
-template <typename T>
-__device__ void stage_halo(const T* __restrict__ x, const Geom& g, int n, int c0, int cc,
-                           const Window& win, T* xs) {
-  const int plane = win.rows * win.cols;
-  const int total = cc * plane;
-  for (int idx = threadIdx.x; idx < total; idx += kThreads) {
-    const int cl = idx / plane;
-    const int rem = idx - cl * plane;
-    const int r = rem / win.cols;
-    const int q = rem - r * win.cols;
-    const int c = c0 + cl;
-    const int yy = win.y_lo + r, xx = win.x_lo + q;
-    T v = from_f<T>(0.0f);
-    if (c < g.c_in && yy >= 0 && yy < g.h && xx >= 0 && xx < g.w)
-      v = x[(((long long)n * g.c_in + c) * g.h + yy) * g.w + xx];
-    xs[idx] = v;
+// Largest band (128, 64 or 32 pixels) and widest channel slice (32 or 16, and
+// wider when 8 CTAs of 32 would not cover C_in) whose shared memory fits.
+__host__ Plan make_plan(const Geom& g, dc_dtype dt, int margin, bool replay) {
+  const bool bf16 = dt == DC_BF16;
+  const int c16 = (g.c_in + 15) / 16 * 16;
+  int cmin = 16;
+  while ((c16 + cmin - 1) / cmin > kMaxCluster) cmin += 16;
+  Plan best{};
+  for (int px = kMaxPx; px >= 32; px /= 2) {
+    const band::Shape sh = band::make_shape(g, margin, px);
+    for (int cpc = (c16 <= 16 ? 16 : (cmin > 32 ? cmin : 32)); cpc >= cmin; cpc -= 16) {
+      Plan p{};
+      p.R = sh.R;
+      p.TW = sh.TW;
+      p.npx = sh.npx;
+      p.ps = px;
+      p.tiles_w = sh.tiles_w;
+      p.tiles_h = sh.tiles_h;
+      p.rows = sh.rows;
+      p.cols = sh.cols;
+      p.plane = sh.plane;
+      p.mp = (g.M + 7) / 8 * 8;
+      p.cpc = cpc;
+      p.csize = (g.c_in + cpc - 1) / cpc;
+      plan_bytes(p, g, bf16, replay);
+      if (best.smem == 0 || p.smem < best.smem) best = p;
+      if (p.smem <= kSmemBudget) return p;
+    }
   }
+  return best;  // over budget: the caller rejects the problem
+}
+
+__device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+using band::bf16_bits;
+
+__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
-    k1_fused_sample(SampleArgs a, int tiles_w, int cc, int mc) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+__device__ __forceinline__ float sample_global(const T* plane, const Geom& g, const Tap& t) {
+  return blend4(t.ly, t.lx, gload(plane, g, t.y0, t.x0), gload(plane, g, t.y0, t.x0 + 1),
+                gload(plane, g, t.y0 + 1, t.x0), gload(plane, g, t.y0 + 1, t.x0 + 1));
+}
+
+template <typename T, bool kReplay>
+__global__ void __launch_bounds__(kThreads) k1_band_sample(SampleArgs a, Plan pl) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  constexpr bool kBf16 = sizeof(T) == 2;
   const Geom g = a.g;
   const T* __restrict__ x = static_cast<const T*>(a.x);
   T* __restrict__ col = static_cast<T*>(a.col);
 
-  const int n = blockIdx.y;
-  const int tile = blockIdx.x;
-  const int ho0 = (tile / tiles_w) * kTH;
-  const int wo0 = (tile % tiles_w) * kTW;
-  const Window win = make_window(g, ho0, wo0, a.margin);
-  const int plane = win.rows * win.cols;
+  const int rank = (int)(blockIdx.x % pl.csize);
+  const int tw_idx = (int)(blockIdx.x / pl.csize);
+  const int band_idx = blockIdx.y;
+  const int n = blockIdx.z;
+  const int ho0 = band_idx * pl.R, wo0 = tw_idx * pl.TW;
+  const int c_begin = rank * pl.cpc;
+  const int c_end = min(g.c_in, c_begin + pl.cpc);
+  const int g_begin = c_begin / g.cg;
+  const int ylo = ho0 * g.sh - g.ph - a.margin;
+  const int xlo = wo0 * g.sw - g.pw - a.margin;
+  const int tid = threadIdx.x;
+  const int PL = pl.plane;
+  const int npx = pl.npx;
+  const int PS = pl.ps;
+  const long long img = (long long)n * g.c_in * g.hw;
 
-  // shared memory: [offsets: kTilePx x M floats][w_off chunk: mc x cc x K floats][halo: cc x plane T]
-  float* offs = reinterpret_cast<float*>(smem_raw);
-  float* wsm = offs + (size_t)kTilePx * g.M;
-  T* xs = reinterpret_cast<T*>(wsm + (size_t)mc * cc * g.K);
+  uint32_t* xw = reinterpret_cast<uint32_t*>(smem + pl.off_halo);  // staged input words
+  float* offs = reinterpret_cast<float*>(smem + pl.off_offs);      // [M][PS]
+  int* pix = reinterpret_cast<int*>(smem + pl.off_tab);            // (row << 16 | col) in band
+  int* tapoff = pix + PS;                                          // window offset of tap k
 
-  const long long howo = g.howo;
-
-  // ---------------------------------------------------------------- pass 1
-  if (a.off_in == nullptr) {
-    const T* __restrict__ w_off = static_cast<const T*>(a.w_off);
-    for (int m0 = 0; m0 < g.M; m0 += mc) {
-      const int mcur = min(mc, g.M - m0);
-      float acc[kAccMax];
-#pragma unroll
-      for (int r = 0; r < kAccMax; ++r) acc[r] = 0.0f;
-      for (int c0 = 0; c0 < g.c_in; c0 += cc) {
-        const int ccur = min(cc, g.c_in - c0);
-        __syncthreads();
-        stage_halo<T>(x, g, n, c0, cc, win, xs);
-        for (int idx = threadIdx.x; idx < mcur * cc * g.K; idx += kThreads) {
-          const int mm = idx / (cc * g.K);
-          const int rem = idx - mm * cc * g.K;
-          const int cl = rem / g.K;
-          const int k = rem - cl * g.K;
-          float v = 0.0f;
-          if (cl < ccur)
-            v = ld_f(w_off + ((long long)(m0 + mm) * g.c_in + c0 + cl) * g.K + k);
-          wsm[idx] = v;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int r = 0; r < kAccMax; ++r) {
-          const int pair = threadIdx.x + r * kThreads;
-          if (pair >= kTilePx * mcur) break;
-          const int mm = pair / kTilePx;
-          const int px = pair - mm * kTilePx;
-          const int ty = px / kTW, tx = px - (px / kTW) * kTW;
-          if (ho0 + ty >= g.ho || wo0 + tx >= g.wo) continue;
-          float s = acc[r];
-          for (int cl = 0; cl < ccur; ++cl) {
-            const T* xp = xs + cl * plane + (ty * g.sh + a.margin) * win.cols + tx * g.sw + a.margin;
-            const float* wp = wsm + (mm * cc + cl) * g.K;
-            for (int i = 0; i < g.kh; ++i)
-              for (int j = 0; j < g.kw; ++j)
-                s = __fmaf_rn(wp[i * g.kw + j], to_f(xp[i * g.dh * win.cols + j * g.dw]), s);
-          }
-          acc[r] = s;
-        }
-      }
-      // finish: bias, external shift, write to smem and to the offset output
-#pragma unroll
-      for (int r = 0; r < kAccMax; ++r) {
-        const int pair = threadIdx.x + r * kThreads;
-        if (pair >= kTilePx * mcur) break;
-        const int mm = pair / kTilePx;
-        const int px = pair - mm * kTilePx;
-        const int ty = px / kTW, tx = px - (px / kTW) * kTW;
-        const int ho = ho0 + ty, wo = wo0 + tx;
-        if (ho >= g.ho || wo >= g.wo) continue;
-        const int m = m0 + mm;
-        float v = acc[r];
-        if (a.b_off) v += a.b_off[m];
-        const long long oi = ((long long)n * g.M + m) * howo + (long long)ho * g.wo + wo;
-        if (a.off_add) v += a.off_add[oi];
-        offs[px * g.M + m] = v;
-        if (a.off_out) a.off_out[oi] = v;
-      }
-    }
-  } else {
-    for (int idx = threadIdx.x; idx < kTilePx * g.M; idx += kThreads) {
-      const int m = idx / kTilePx;
-      const int px = idx - m * kTilePx;
-      const int ho = ho0 + px / kTW, wo = wo0 + px % kTW;
-      float v = 0.0f;
-      if (ho < g.ho && wo < g.wo)
-        v = a.off_in[((long long)n * g.M + m) * howo + (long long)ho * g.wo + wo];
-      offs[px * g.M + m] = v;
-    }
+  band::fill_pixel_table(pix, npx, pl.TW);
+  for (int k = tid; k < g.K; k += kThreads) {
+    const int i = k / g.kw;
+    tapoff[k] = i * g.dh * pl.cols + (k - i * g.kw) * g.dw;
   }
-  __syncthreads();
 
-  // count the (pixel, tap, group) sampling points that leave the staged window
-  if (a.slow_count) {
-    unsigned long long local = 0;
-    for (int pair = threadIdx.x; pair < kTilePx * g.K; pair += kThreads) {
-      const int k = pair / kTilePx;
-      const int px = pair - k * kTilePx;
-      const int ty = px / kTW, tx = px % kTW;
-      if (ho0 + ty >= g.ho || wo0 + tx >= g.wo) continue;
-      const int i = k / g.kw, j = k - (k / g.kw) * g.kw;
-      for (int gg = 0; gg < g.groups; ++gg) {
-        const float py = (float)((ho0 + ty) * g.sh - g.ph + i * g.dh) + offs[px * g.M + 2 * (gg * g.K + k)];
-        const float pxf = (float)((wo0 + tx) * g.sw - g.pw + j * g.dw) + offs[px * g.M + 2 * (gg * g.K + k) + 1];
-        if (!touches_image(py, pxf, g.h, g.w)) continue;
-        const int y0 = (int)floorf(py) - win.y_lo, x0 = (int)floorf(pxf) - win.x_lo;
-        if (y0 < 0 || y0 + 1 >= win.rows || x0 < 0 || x0 + 1 >= win.cols) ++local;
+  // ---------------------------------------------------------------- stage halo
+  band::stage_window<T>(x, g, img, c_begin, pl.cpc, ylo, xlo, pl.rows, pl.cols, PL, xw);
+
+  if (!kReplay) {
+    // -------------------------------------------------------------- weights
+    const T* __restrict__ w_off = static_cast<const T*>(a.w_off);
+    if (kBf16) {
+      uint32_t* wb = reinterpret_cast<uint32_t*>(smem + pl.off_w);  // [K][cpc/2][mp]
+      const int cpp = pl.cpc / 2;
+      const __nv_bfloat16* wsrc = reinterpret_cast<const __nv_bfloat16*>(w_off);
+      band::Walk3 w;
+      w.init(tid, kThreads, cpp, pl.mp);
+      while (w.a < g.K) {
+        const int k = w.a, cp = w.b, m = w.c;
+        const int c0 = c_begin + 2 * cp;
+        uint32_t lo = 0, hi = 0;
+        if (m < g.M && c0 < g.c_in) lo = bf16_bits(wsrc + ((long long)m * g.c_in + c0) * g.K + k);
+        if (m < g.M && c0 + 1 < g.c_in)
+          hi = bf16_bits(wsrc + ((long long)m * g.c_in + c0 + 1) * g.K + k);
+        wb[(k * cpp + cp) * pl.mp + m] = lo | (hi << 16);
+        w.next();
       }
+    } else {
+      float* wf = reinterpret_cast<float*>(smem + pl.off_w);  // [cpc][K][mp]
+      band::Walk3 w;
+      w.init(tid, kThreads, g.K, pl.mp);
+      while (w.a < pl.cpc) {
+        const int cl = w.a, k = w.b, m = w.c;
+        const int c = c_begin + cl;
+        float v = 0.f;
+        if (m < g.M && c < g.c_in) v = ld_f(w_off + ((long long)m * g.c_in + c) * g.K + k);
+        wf[(cl * g.K + k) * pl.mp + m] = v;
+        w.next();
+      }
+    }
+    __syncthreads();
+
+    // -------------------------------------------------------------- phase 1
+    float* part = reinterpret_cast<float*>(smem + pl.off_part);  // [mp][PS]
+    if (kBf16) {
+      const uint32_t* wb = reinterpret_cast<const uint32_t*>(smem + pl.off_w);
+      const int warp = tid >> 5, lane = tid & 31;
+      const int gid = lane >> 2, tig = lane & 3;
+      const int mtiles = (npx + 15) / 16;
+      const int cpp = pl.cpc / 2;
+      for (int mt = warp; mt < mtiles; mt += kThreads / 32) {
+        const int r0 = mt * 16 + gid, r1 = r0 + 8;
+        const int e0 = pix[r0 < npx ? r0 : 0], e1 = pix[r1 < npx ? r1 : 0];
+        const int b0 = ((e0 >> 16) * g.sh + a.margin) * pl.cols + (e0 & 0xffff) * g.sw + a.margin;
+        const int b1 = ((e1 >> 16) * g.sh + a.margin) * pl.cols + (e1 & 0xffff) * g.sw + a.margin;
+        for (int nt0 = 0; nt0 < pl.mp / 8; nt0 += kNtMax) {
+          const int ntn = min(kNtMax, pl.mp / 8 - nt0);
+          float acc[kNtMax][4];
+#pragma unroll
+          for (int t = 0; t < kNtMax; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+          for (int k = 0; k < g.K; ++k) {
+            const int toff = tapoff[k];
+            for (int cpb = 0; cpb < cpp; cpb += 8) {
+              uint32_t af[4];
+              const uint32_t* xa = xw + (cpb + tig) * PL + toff;
+              af[0] = xa[b0];
+              af[1] = xa[b1];
+              af[2] = xa[4 * PL + b0];
+              af[3] = xa[4 * PL + b1];
+              const uint32_t* wk = wb + ((k * cpp) + cpb + tig) * pl.mp + nt0 * 8 + gid;
+#pragma unroll
+              for (int t = 0; t < kNtMax; ++t)
+                if (t < ntn) mma_bf16_16816(acc[t], af, wk[t * 8], wk[4 * pl.mp + t * 8]);
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < kNtMax; ++t) {
+            if (t >= ntn) continue;
+            const int m = (nt0 + t) * 8 + 2 * tig;
+            if (r0 < npx) {
+              part[m * PS + r0] = acc[t][0];
+              part[(m + 1) * PS + r0] = acc[t][1];
+            }
+            if (r1 < npx) {
+              part[m * PS + r1] = acc[t][2];
+              part[(m + 1) * PS + r1] = acc[t][3];
+            }
+          }
+        }
+      }
+    } else {
+      const float* wf = reinterpret_cast<const float*>(smem + pl.off_w);
+      const float* xf = reinterpret_cast<const float*>(xw);
+      constexpr int kMc = 12;
+      const int ngrp = (g.M + kMc - 1) / kMc;
+      band::Walk2 w;
+      w.init(tid, kThreads, npx);
+      while (w.a < ngrp) {
+        const int m0 = w.a * kMc, px = w.b;
+        const int e = pix[px];
+        const int base = ((e >> 16) * g.sh + a.margin) * pl.cols + (e & 0xffff) * g.sw + a.margin;
+        float acc[kMc];
+#pragma unroll
+        for (int t = 0; t < kMc; ++t) acc[t] = 0.f;
+        for (int cl = 0; cl < pl.cpc; ++cl) {
+          const float* xc = xf + cl * PL + base;
+          const float* wc = wf + cl * g.K * pl.mp + m0;
+          for (int k = 0; k < g.K; ++k) {
+            const float xv = xc[tapoff[k]];
+            const float4* wv = reinterpret_cast<const float4*>(wc + k * pl.mp);
+#pragma unroll
+            for (int t4 = 0; t4 < kMc / 4; ++t4) {
+              if (m0 + 4 * t4 >= pl.mp) break;
+              const float4 w4 = wv[t4];
+              acc[4 * t4 + 0] = __fmaf_rn(w4.x, xv, acc[4 * t4 + 0]);
+              acc[4 * t4 + 1] = __fmaf_rn(w4.y, xv, acc[4 * t4 + 1]);
+              acc[4 * t4 + 2] = __fmaf_rn(w4.z, xv, acc[4 * t4 + 2]);
+              acc[4 * t4 + 3] = __fmaf_rn(w4.w, xv, acc[4 * t4 + 3]);
+            }
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < kMc; ++t)
+          if (m0 + t < g.M) part[(m0 + t) * PS + px] = acc[t];
+        w.next();
+      }
+    }
+
+    // -------------------------------------------------------------- cluster reduction
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    {
+      band::Walk2 w;
+      w.init(tid, kThreads, npx);
+      while (w.a < g.M) {
+        const int m = w.a, px = w.b;
+        float v = 0.f;
+        for (int r = 0; r < pl.csize; ++r) v += cluster.map_shared_rank(part, r)[m * PS + px];
+        const int e = pix[px];
+        const int ho = ho0 + (e >> 16), wo = wo0 + (e & 0xffff);
+        if (ho < g.ho && wo < g.wo) {
+          if (a.b_off) v += a.b_off[m];
+          const long long oi = ((long long)n * g.M + m) * g.howo + (long long)ho * g.wo + wo;
+          if (a.off_add) v += a.off_add[oi];
+          if (a.off_out && rank == 0) a.off_out[oi] = v;
+        }
+        offs[m * PS + px] = v;
+        w.next();
+      }
+    }
+    cluster.sync();  // peers have finished reading this CTA's partials
+  } else {
+    __syncthreads();  // pixel table
+    band::Walk2 w;
+    w.init(tid, kThreads, npx);
+    while (w.a < g.M) {
+      const int m = w.a, px = w.b;
+      const int e = pix[px];
+      const int ho = ho0 + (e >> 16), wo = wo0 + (e & 0xffff);
+      float v = 0.f;
+      if (ho < g.ho && wo < g.wo)
+        v = a.off_in[((long long)n * g.M + m) * g.howo + (long long)ho * g.wo + wo];
+      offs[m * PS + px] = v;
+      w.next();
+    }
+    __syncthreads();
+  }
+
+  // ---------------------------------------------------------------- slow-path count
+  if (a.slow_count && rank == 0) {
+    unsigned long long local = 0;
+    band::Walk2 w;
+    w.init(tid, kThreads, npx);
+    while (w.a < g.K) {
+      const int k = w.a, px = w.b;
+      const int e = pix[px];
+      const int ho = ho0 + (e >> 16), wo = wo0 + (e & 0xffff);
+      if (ho < g.ho && wo < g.wo) {
+        const int i = k / g.kw, j = k - (k / g.kw) * g.kw;
+        const float by = (float)(ho * g.sh - g.ph + i * g.dh);
+        const float bx = (float)(wo * g.sw - g.pw + j * g.dw);
+        for (int gg = 0; gg < g.groups; ++gg) {
+          const Tap t = make_tap(by + offs[(2 * (gg * g.K + k)) * PS + px],
+                                 bx + offs[(2 * (gg * g.K + k) + 1) * PS + px], g, ylo, xlo,
+                                 pl.rows, pl.cols);
+          if (t.inside && !t.fast) ++local;
+        }
+      }
+      w.next();
     }
     for (int o = 16; o > 0; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
-    if ((threadIdx.x & 31) == 0 && local) atomicAdd(a.slow_count, local);
+    if ((tid & 31) == 0 && local) atomicAdd(a.slow_count, local);
   }
 
-  // ---------------------------------------------------------------- pass 2
-  for (int c0 = 0; c0 < g.c_in; c0 += cc) {
-    const int ccur = min(cc, g.c_in - c0);
-    __syncthreads();
-    stage_halo<T>(x, g, n, c0, cc, win, xs);
-    __syncthreads();
-    for (int pair = threadIdx.x; pair < kTilePx * g.K; pair += kThreads) {
-      const int k = pair / kTilePx;
-      const int px = pair - k * kTilePx;
-      const int ty = px / kTW, tx = px % kTW;
-      const int ho = ho0 + ty, wo = wo0 + tx;
-      if (ho >= g.ho || wo >= g.wo) continue;
-      const int i = k / g.kw, j = k - (k / g.kw) * g.kw;
-      const float by = (float)(ho * g.sh - g.ph + i * g.dh);
-      const float bx = (float)(wo * g.sw - g.pw + j * g.dw);
-      const long long q = (long long)n * a.col_layout.img + (long long)ho * g.wo + wo;
-      int gcur = -1;
-      float ly = 0.f, lx = 0.f;
-      int y0 = 0, x0 = 0;
-      bool inside = false, fast = false;
-      for (int cl = 0; cl < ccur; ++cl) {
-        const int c = c0 + cl;
-        const int gg = c / g.cg;
-        if (gg != gcur) {
-          gcur = gg;
-          const float py = by + offs[px * g.M + 2 * (gg * g.K + k)];
-          const float pxf = bx + offs[px * g.M + 2 * (gg * g.K + k) + 1];
-          inside = touches_image(py, pxf, g.h, g.w);
-          if (inside) {
-            const float fy = floorf(py), fx = floorf(pxf);
-            ly = py - fy;
-            lx = pxf - fx;
-            y0 = (int)fy;
-            x0 = (int)fx;
-            const int ry = y0 - win.y_lo, rx = x0 - win.x_lo;
-            fast = ry >= 0 && ry + 1 < win.rows && rx >= 0 && rx + 1 < win.cols;
+  // ---------------------------------------------------------------- phase 2
+  const long long cstride = (long long)g.K * a.col_layout.row;  // next channel's row
+  band::Walk2 w;
+  w.init(tid, kThreads, npx);
+  while (w.a < g.K) {
+    const int k = w.a, px = w.b;
+    w.next();
+    const int e = pix[px];
+    const int ho = ho0 + (e >> 16), wo = wo0 + (e & 0xffff);
+    if (ho >= g.ho || wo >= g.wo) continue;
+    const int i = k / g.kw, j = k - i * g.kw;
+    const float by = (float)(ho * g.sh - g.ph + i * g.dh);
+    const float bx = (float)(wo * g.sw - g.pw + j * g.dw);
+    T* crow = col + (long long)k * a.col_layout.row + (long long)n * a.col_layout.img +
+              (long long)ho * g.wo + wo;
+    // channels in runs that share one offset group (one sampling point)
+    int c = c_begin;
+    for (int gg = g_begin; c < c_end; ++gg) {
+      const int run_end = min(c_end, (gg + 1) * g.cg);
+      const Tap t = make_tap(by + offs[(2 * (gg * g.K + k)) * PS + px],
+                             bx + offs[(2 * (gg * g.K + k) + 1) * PS + px], g, ylo, xlo, pl.rows,
+                             pl.cols);
+      const int sbase = (t.y0 - ylo) * pl.cols + (t.x0 - xlo);
+      while (c < run_end) {
+        const int rel = c - c_begin;
+        if (kBf16 && !(rel & 1) && c + 1 < run_end) {
+          float s0 = 0.f, s1 = 0.f;
+          if (t.inside) {
+            if (t.fast) {
+              const uint32_t* wp = xw + (rel >> 1) * PL + sbase;
+              const uint32_t w00 = wp[0], w01 = wp[1], w10 = wp[pl.cols], w11 = wp[pl.cols + 1];
+              s0 = blend4(t.ly, t.lx, lo_bf16(w00), lo_bf16(w01), lo_bf16(w10), lo_bf16(w11));
+              s1 = blend4(t.ly, t.lx, hi_bf16(w00), hi_bf16(w01), hi_bf16(w10), hi_bf16(w11));
+            } else {
+              s0 = sample_global(x + img + (long long)c * g.hw, g, t);
+              s1 = sample_global(x + img + (long long)(c + 1) * g.hw, g, t);
+            }
           }
-        }
-        float s = 0.0f;
-        if (inside) {
-          float v00, v01, v10, v11;
-          if (fast) {
-            const T* p = xs + cl * plane + (y0 - win.y_lo) * win.cols + (x0 - win.x_lo);
-            v00 = to_f(p[0]);
-            v01 = to_f(p[1]);
-            v10 = to_f(p[win.cols]);
-            v11 = to_f(p[win.cols + 1]);
-          } else {
-            const T* base = x + ((long long)n * g.c_in + c) * g.hw;
-            const bool r0 = y0 >= 0 && y0 < g.h, r1 = y0 + 1 >= 0 && y0 + 1 < g.h;
-            const bool q0 = x0 >= 0 && x0 < g.w, q1 = x0 + 1 >= 0 && x0 + 1 < g.w;
-            v00 = (r0 && q0) ? ld_f(base + (long long)y0 * g.w + x0) : 0.0f;
-            v01 = (r0 && q1) ? ld_f(base + (long long)y0 * g.w + x0 + 1) : 0.0f;
-            v10 = (r1 && q0) ? ld_f(base + (long long)(y0 + 1) * g.w + x0) : 0.0f;
-            v11 = (r1 && q1) ? ld_f(base + (long long)(y0 + 1) * g.w + x0 + 1) : 0.0f;
+          crow[(long long)c * cstride] = from_f<T>(s0);
+          crow[(long long)(c + 1) * cstride] = from_f<T>(s1);
+          c += 2;
+        } else {
+          float s = 0.f;
+          if (t.inside) {
+            if (t.fast) {
+              const int pos = sbase;
+              s = blend4(t.ly, t.lx, band::staged<T>(xw, PL, rel, pos),
+                         band::staged<T>(xw, PL, rel, pos + 1),
+                         band::staged<T>(xw, PL, rel, pos + pl.cols),
+                         band::staged<T>(xw, PL, rel, pos + pl.cols + 1));
+            } else {
+              s = sample_global(x + img + (long long)c * g.hw, g, t);
+            }
           }
-          s = blend4(ly, lx, v00, v01, v10, v11);
+          crow[(long long)c * cstride] = from_f<T>(s);
+          c += 1;
         }
-        col[(long long)(c * g.K + k) * a.col_layout.row + q] = from_f<T>(s);
       }
     }
   }
 }
 
-template <typename T>
-size_t smem_for(const Geom& g, int margin, int cc, int mc) {
-  Window w = make_window(g, 0, 0, margin);
-  return (size_t)kTilePx * g.M * 4 + (size_t)mc * cc * g.K * 4 +
-         (size_t)cc * w.rows * w.cols * sizeof(T);
+template <typename T, bool kReplay>
+cudaError_t launch_t(const SampleArgs& a, const Plan& pl, cudaStream_t s) {
+  auto kern = k1_band_sample<T, kReplay>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)pl.smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(pl.csize * pl.tiles_w), (unsigned)pl.tiles_h, (unsigned)a.g.n);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  unsigned nattr = 0;
+  if (!kReplay) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)pl.csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    nattr = 1;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = nattr;
+  e = cudaLaunchKernelEx(&cfg, kern, a, pl);
+  note_launches(1);
+  return e;
 }
 
 }  // namespace
 
 size_t sample_smem_bytes(const Geom& g, dc_dtype dt, int margin) {
-  const size_t elt = dt == DC_BF16 ? 2 : 4;
-  const int cc = chunk_channels(g, margin, elt);
-  const int mc = offset_chunk(g);
-  return dt == DC_BF16 ? smem_for<__nv_bfloat16>(g, margin, cc, mc)
-                       : smem_for<float>(g, margin, cc, mc);
+  return make_plan(g, dt, margin, false).smem;
 }
 
 cudaError_t launch_sample(const SampleArgs& a, dc_dtype dt, cudaStream_t s) {
-  const Geom& g = a.g;
-  const int tiles_h = (int)ceil_div_ll(g.ho, kTH), tiles_w = (int)ceil_div_ll(g.wo, kTW);
-  const size_t elt = dt == DC_BF16 ? 2 : 4;
-  const int cc = chunk_channels(g, a.margin, elt);
-  const int mc = offset_chunk(g);
-  const size_t smem = sample_smem_bytes(g, dt, a.margin);
-  dim3 grid(tiles_h * tiles_w, g.n);
-  cudaError_t e;
-  if (dt == DC_BF16) {
-    auto k = k1_fused_sample<__nv_bfloat16>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, smem, s>>>(a, tiles_w, cc, mc);
-    note_launches(1);
-  } else {
-    auto k = k1_fused_sample<float>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, smem, s>>>(a, tiles_w, cc, mc);
-    note_launches(1);
-  }
-  return cudaGetLastError();
+  const bool replay = a.off_in != nullptr;
+  const Plan pl = make_plan(a.g, dt, a.margin, replay);
+  if (dt == DC_BF16)
+    return replay ? launch_t<__nv_bfloat16, true>(a, pl, s) : launch_t<__nv_bfloat16, false>(a, pl, s);
+  return replay ? launch_t<float, true>(a, pl, s) : launch_t<float, false>(a, pl, s);
 }
 
 }  // namespace dc

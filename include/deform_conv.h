@@ -170,6 +170,13 @@ const char* dc_status_string(dc_status status);
 /* Library build description (architecture, version). */
 const char* dc_build_info(void);
 
+/* DC_ERR_TIMEOUT if a bounded on-device wait of this library's kernels has
+ * expired since the flag was last cleared on the current device, else DC_OK
+ * (DC_ERR_CUDA if the flag cannot be read).  Synchronises with the device.
+ * clear != 0 resets the flag.  An expired wait means the kernel skipped the
+ * rest of its work: its outputs are not valid. */
+dc_status dc_device_error(int clear);
+
 /* Number of kernels this library has enqueued in this process so far (host
  * counter, incremented per launch; memsets are not counted).  Lets a caller
  * count the launches of a region of work, e.g. of a captured CUDA graph. */
