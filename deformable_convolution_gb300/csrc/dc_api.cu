@@ -30,7 +30,7 @@ namespace {
 constexpr int kDefaultMargin = 3;
 constexpr int kMaxMargin = 64;
 constexpr int kMaxTaps = 49;
-constexpr size_t kMaxSampleSmem = 200 * 1024;
+constexpr size_t kMaxSmem = 225 * 1024;  // dynamic shared memory per CTA on sm_103a is 227 KB
 
 size_t elt_size(dc_dtype dt) { return dt == DC_BF16 ? 2 : 4; }
 
@@ -77,8 +77,7 @@ dc_status make_geom(const dc_problem* p, Geom* g, int* margin) {
     return DC_ERR_UNSUPPORTED;
   *margin = p->halo_margin < 0 ? kDefaultMargin : p->halo_margin;
   if (*margin > kMaxMargin) return DC_ERR_UNSUPPORTED;
-  if (sample_smem_bytes(*g, p->dtype, *margin) > kMaxSampleSmem) return DC_ERR_UNSUPPORTED;
-  if (bwd_smem_bytes(*g, p->dtype, *margin) > kMaxSampleSmem) return DC_ERR_UNSUPPORTED;
+  if (sample_smem_bytes(*g, p->dtype, *margin) > kMaxSmem) return DC_ERR_UNSUPPORTED;
   return DC_OK;
 }
 
@@ -137,6 +136,7 @@ dc_status deform_conv_workspace_size(const dc_problem* prob, int backward, size_
   int margin;
   const dc_status st = make_geom(prob, &g, &margin);
   if (st != DC_OK) return st;
+  if (backward && bwd_smem_bytes(g, prob->dtype, margin) > kMaxSmem) return DC_ERR_UNSUPPORTED;
   *bytes = make_plan(g, prob->dtype, backward ? 1 : 0).total;
   return DC_OK;
 }
@@ -192,6 +192,7 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
   if (st != DC_OK) return st;
   if (!x || !w_off || !w || !offset || !grad_y || !grad_x || !grad_w_off || !grad_w)
     return DC_ERR_INVALID_ARG;
+  if (bwd_smem_bytes(g, prob->dtype, margin) > kMaxSmem) return DC_ERR_UNSUPPORTED;
   const void* ptrs[] = {x, w_off, w, offset, grad_y, grad_x, grad_w_off, grad_b_off, grad_w,
                         grad_offset, ws};
   for (const void* p : ptrs)

@@ -159,7 +159,7 @@ __device__ __forceinline__ void stage_window(const T* __restrict__ x, const Geom
                                              int xlo, int rows, int cols, int plane,
                                              uint32_t* dst) {
   constexpr bool kPairs = sizeof(T) == 2;
-  constexpr int kBatch = 8;
+  constexpr int kBatch = 16;
   const int units = kPairs ? cpc / 2 : cpc;
   Walk3 w;
   w.init(threadIdx.x, kThreads, rows, cols);

@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/deform_conv.h"
+#include "deform_conv.h"
 
 namespace dc {
 

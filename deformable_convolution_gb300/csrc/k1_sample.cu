@@ -54,7 +54,8 @@ struct Plan {
   int rows, cols;         // staged window
   int plane;              // padded words (bf16 pairs) or floats (fp32) per staged channel (pair)
   int mp;                 // offset channels padded to a multiple of 8
-  size_t off_halo, off_w, off_part, off_offs, off_tab, smem;
+  int qcap;  // capacity of the deferred slow-tap queue
+  size_t off_halo, off_w, off_part, off_offs, off_tab, off_q, smem;
 };
 
 __host__ size_t plan_bytes(Plan& p, const Geom& g, bool bf16, bool replay) {
@@ -70,12 +71,25 @@ __host__ size_t plan_bytes(Plan& p, const Geom& g, bool bf16, bool replay) {
   at += (size_t)g.M * p.ps * 4;
   p.off_tab = at;  // pixel table [ps] + tap offsets [K]
   at += (size_t)(p.ps + g.K) * 4;
+  {
+    int ngroups = 1;  // most offset groups any channel slice touches
+    for (int r = 0; r * p.cpc < g.c_in; ++r) {
+      const int lo = r * p.cpc, hi = (r + 1) * p.cpc < g.c_in ? (r + 1) * p.cpc : g.c_in;
+      const int ng = (hi - 1) / g.cg - lo / g.cg + 1;
+      if (ng > ngroups) ngroups = ng;
+    }
+    p.qcap = p.npx * g.K * (ngroups < 4 ? ngroups : 4);
+  }
+  p.off_q = at;  // queue counter + entries (overflow is handled in place)
+  at += (size_t)(1 + p.qcap) * 4;
   p.smem = at;
   return at;
 }
 
 // Largest band (128, 64 or 32 pixels) and widest channel slice (32 or 16, and
-// wider when 8 CTAs of 32 would not cover C_in) whose shared memory fits.
+// wider when 8 CTAs of 32 would not cover C_in) whose shared memory fits.  (Slices
+// of 16 double the CTAs per band, but 8-CTA clusters then no longer fit in one
+// wave on GB300.)
 __host__ Plan make_plan(const Geom& g, dc_dtype dt, int margin, bool replay) {
   const bool bf16 = dt == DC_BF16;
   const int c16 = (g.c_in + 15) / 16 * 16;
@@ -89,7 +103,7 @@ __host__ Plan make_plan(const Geom& g, dc_dtype dt, int margin, bool replay) {
       p.R = sh.R;
       p.TW = sh.TW;
       p.npx = sh.npx;
-      p.ps = px;
+      p.ps = px + 8;  // rows of the per-band arrays start 8 banks apart
       p.tiles_w = sh.tiles_w;
       p.tiles_h = sh.tiles_h;
       p.rows = sh.rows;
@@ -154,6 +168,9 @@ __global__ void __launch_bounds__(kThreads) k1_band_sample(SampleArgs a, Plan pl
   float* offs = reinterpret_cast<float*>(smem + pl.off_offs);      // [M][PS]
   int* pix = reinterpret_cast<int*>(smem + pl.off_tab);            // (row << 16 | col) in band
   int* tapoff = pix + PS;                                          // window offset of tap k
+  int* nslow = reinterpret_cast<int*>(smem + pl.off_q);            // deferred slow taps
+  int* slowq = nslow + 1;
+  if (tid == 0) *nslow = 0;
 
   band::fill_pixel_table(pix, npx, pl.TW);
   for (int k = tid; k < g.K; k += kThreads) {
@@ -173,15 +190,27 @@ __global__ void __launch_bounds__(kThreads) k1_band_sample(SampleArgs a, Plan pl
       const __nv_bfloat16* wsrc = reinterpret_cast<const __nv_bfloat16*>(w_off);
       band::Walk3 w;
       w.init(tid, kThreads, cpp, pl.mp);
+      constexpr int kB = 8;
       while (w.a < g.K) {
-        const int k = w.a, cp = w.b, m = w.c;
-        const int c0 = c_begin + 2 * cp;
-        uint32_t lo = 0, hi = 0;
-        if (m < g.M && c0 < g.c_in) lo = bf16_bits(wsrc + ((long long)m * g.c_in + c0) * g.K + k);
-        if (m < g.M && c0 + 1 < g.c_in)
-          hi = bf16_bits(wsrc + ((long long)m * g.c_in + c0 + 1) * g.K + k);
-        wb[(k * cpp + cp) * pl.mp + m] = lo | (hi << 16);
-        w.next();
+        uint32_t v[kB];
+        int at[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          v[j] = 0u;
+          at[j] = -1;
+          if (w.a < g.K) {
+            const int k = w.a, cp = w.b, m = w.c;
+            const int c0 = c_begin + 2 * cp;
+            if (m < g.M && c0 < g.c_in) v[j] = bf16_bits(wsrc + ((long long)m * g.c_in + c0) * g.K + k);
+            if (m < g.M && c0 + 1 < g.c_in)
+              v[j] |= bf16_bits(wsrc + ((long long)m * g.c_in + c0 + 1) * g.K + k) << 16;
+            at[j] = (k * cpp + cp) * pl.mp + m;
+            w.next();
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kB; ++j)
+          if (at[j] >= 0) wb[at[j]] = v[j];
       }
     } else {
       float* wf = reinterpret_cast<float*>(smem + pl.off_w);  // [cpc][K][mp]
@@ -288,22 +317,43 @@ __global__ void __launch_bounds__(kThreads) k1_band_sample(SampleArgs a, Plan pl
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
     {
+      // four (m, px) items per round, their remote loads all in flight
       band::Walk2 w;
       w.init(tid, kThreads, npx);
       while (w.a < g.M) {
-        const int m = w.a, px = w.b;
-        float v = 0.f;
-        for (int r = 0; r < pl.csize; ++r) v += cluster.map_shared_rank(part, r)[m * PS + px];
-        const int e = pix[px];
-        const int ho = ho0 + (e >> 16), wo = wo0 + (e & 0xffff);
-        if (ho < g.ho && wo < g.wo) {
-          if (a.b_off) v += a.b_off[m];
-          const long long oi = ((long long)n * g.M + m) * g.howo + (long long)ho * g.wo + wo;
-          if (a.off_add) v += a.off_add[oi];
-          if (a.off_out && rank == 0) a.off_out[oi] = v;
+        int mm[4], pp[4];
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          mm[j] = -1;
+          v[j] = 0.f;
+          if (w.a < g.M) {
+            mm[j] = w.a;
+            pp[j] = w.b;
+            w.next();
+          }
         }
-        offs[m * PS + px] = v;
-        w.next();
+        for (int r = 0; r < pl.csize; ++r) {
+          const float* rp = cluster.map_shared_rank(part, r);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (mm[j] >= 0) v[j] += rp[mm[j] * PS + pp[j]];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (mm[j] < 0) continue;
+          const int m = mm[j], px = pp[j];
+          float vv = v[j];
+          const int e = pix[px];
+          const int ho = ho0 + (e >> 16), wo = wo0 + (e & 0xffff);
+          if (ho < g.ho && wo < g.wo) {
+            if (a.b_off) vv += a.b_off[m];
+            const long long oi = ((long long)n * g.M + m) * g.howo + (long long)ho * g.wo + wo;
+            if (a.off_add) vv += a.off_add[oi];
+            if (a.off_out && rank == 0) a.off_out[oi] = vv;
+          }
+          offs[m * PS + px] = vv;
+        }
       }
     }
     cluster.sync();  // peers have finished reading this CTA's partials
@@ -373,6 +423,15 @@ __global__ void __launch_bounds__(kThreads) k1_band_sample(SampleArgs a, Plan pl
                              bx + offs[(2 * (gg * g.K + k) + 1) * PS + px], g, ylo, xlo, pl.rows,
                              pl.cols);
       const int sbase = (t.y0 - ylo) * pl.cols + (t.x0 - xlo);
+      if (t.inside && !t.fast) {
+        // out-of-window tap: queued for the cooperative pass below, so that
+        // this warp does not wait on global memory for one lane
+        const int qi = atomicAdd(nslow, 1);
+        if (qi < pl.qcap) {
+          slowq[qi] = px | (k << 8) | ((gg - g_begin) << 16);
+          c = run_end;
+        }
+      }
       while (c < run_end) {
         const int rel = c - c_begin;
         if (kBf16 && !(rel & 1) && c + 1 < run_end) {
@@ -409,6 +468,27 @@ __global__ void __launch_bounds__(kThreads) k1_band_sample(SampleArgs a, Plan pl
         }
       }
     }
+  }
+
+  // ---------------------------------------------------------------- deferred slow taps
+  // all lanes together: one (queued tap, channel) pair per thread, corners read
+  // from global memory with the same blend as the on-chip path
+  __syncthreads();
+  const int nq = min(*nslow, pl.qcap);
+  for (int task = tid; task < nq * pl.cpc; task += kThreads) {
+    const int ent = task / pl.cpc, jj = task - ent * pl.cpc;
+    const int code = slowq[ent];
+    const int px = code & 0xff, k = (code >> 8) & 0xff, gg = g_begin + (code >> 16);
+    const int c = max(c_begin, gg * g.cg) + jj;
+    if (c >= min(c_end, (gg + 1) * g.cg)) continue;
+    const int e = pix[px];
+    const int ho = ho0 + (e >> 16), wo = wo0 + (e & 0xffff);
+    const int i = k / g.kw, j = k - i * g.kw;
+    const Tap t = make_tap((float)(ho * g.sh - g.ph + i * g.dh) + offs[(2 * (gg * g.K + k)) * PS + px],
+                           (float)(wo * g.sw - g.pw + j * g.dw) + offs[(2 * (gg * g.K + k) + 1) * PS + px],
+                           g, ylo, xlo, pl.rows, pl.cols);
+    col[(long long)k * a.col_layout.row + (long long)n * a.col_layout.img + (long long)ho * g.wo + wo +
+        (long long)c * cstride] = from_f<T>(sample_global(x + img + (long long)c * g.hw, g, t));
   }
 }
 

@@ -39,14 +39,15 @@ using band::gload;
 using band::make_tap;
 constexpr int kMaxPx = band::kBandPx;
 constexpr int kMaxCluster = band::kMaxCluster;
-constexpr size_t kSmemBudget = 110 * 1024;
+constexpr size_t kSmemBudget = 112 * 1024;
 
 struct Plan {
   int R, TW, tiles_w, tiles_h, npx;
   int ps;  // pixel stride of the per-band offset arrays
   int cpc, csize;
   int rows, cols, plane;
-  size_t off_halo, off_gx, off_offs, off_part, off_tab, smem;
+  int qcap;  // capacity of the deferred slow-tap queue
+  size_t off_halo, off_gx, off_offs, off_part, off_tab, off_q, smem;
 };
 
 // Largest band (128, 64 or 32 pixels) and widest channel slice whose shared
@@ -65,7 +66,7 @@ __host__ Plan make_plan(const Geom& g, dc_dtype dt, int margin) {
       p.R = sh.R;
       p.TW = sh.TW;
       p.npx = sh.npx;
-      p.ps = px;
+      p.ps = px + 8;  // rows of the per-band arrays start 8 banks apart
       p.tiles_w = sh.tiles_w;
       p.tiles_h = sh.tiles_h;
       p.rows = sh.rows;
@@ -84,6 +85,17 @@ __host__ Plan make_plan(const Geom& g, dc_dtype dt, int margin) {
       at += (size_t)g.M * p.ps * 4;
       p.off_tab = at;  // pixel table [ps] + tap offsets [K]
       at += (size_t)(p.ps + g.K) * 4;
+      {
+        int ngroups = 1;  // most offset groups any channel slice touches
+        for (int r = 0; r * cpc < g.c_in; ++r) {
+          const int lo = r * cpc, hi = (r + 1) * cpc < g.c_in ? (r + 1) * cpc : g.c_in;
+          const int ng = (hi - 1) / g.cg - lo / g.cg + 1;
+          if (ng > ngroups) ngroups = ng;
+        }
+        p.qcap = p.npx * g.K * (ngroups < 4 ? ngroups : 4);
+      }
+      p.off_q = at;  // queue counter + entries (overflow is handled in place)
+      at += (size_t)(1 + p.qcap) * 4;
       p.smem = at;
       if (best.smem == 0 || p.smem < best.smem) best = p;
       if (p.smem <= kSmemBudget) return p;
@@ -97,6 +109,9 @@ __device__ __forceinline__ void gadd(float* plane, const Geom& g, int y, int x, 
 }
 
 constexpr int kOffconvMmaMaxM = 80;
+
+__device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 __device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0,
                                                uint32_t b1) {
@@ -225,30 +240,140 @@ __device__ void offconv_bwd_mma(const __nv_bfloat16* __restrict__ w_off, float* 
       const int oc1 = orow1 < NK ? orow1 / g.K : 0, ok1 = orow1 < NK ? orow1 - oc1 * g.K : 0;
       float* dst0 = gxs + oc0 * PL + tapoff[ok0] + window0;
       float* dst1 = gxs + oc1 * PL + tapoff[ok1] + window0;
-      for (int nt = 0; nt < ntiles; ++nt) {
-        const int q = nt * 8 + gid;  // this lane's B column (pixel)
-        const int qc = q < npx ? q : 0;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      // four pixel tiles per round: all their loads and mma first, then the
+      // round's shared-memory atomics
+      constexpr int kNt = 4;
+      for (int nt0 = 0; nt0 < ntiles; nt0 += kNt) {
+        float acc[kNt][4];
 #pragma unroll
-        for (int ks = 0; ks < 5; ++ks) {
-          if (ks >= ksteps) break;
-          const int m = ks * 16 + 2 * tig;
-          auto gv = [&](int mm) { return (mm < M && q < npx) ? goff[mm * PS + qc] : 0.f; };
-          const uint32_t b0 = pack_bf16(gv(m), gv(m + 1));
-          const uint32_t b1 = pack_bf16(gv(m + 8), gv(m + 9));
-          mma_bf16_16816(acc, af[ks], b0, b1);
+        for (int tt = 0; tt < kNt; ++tt) {
+          acc[tt][0] = acc[tt][1] = acc[tt][2] = acc[tt][3] = 0.f;
+          const int q = (nt0 + tt) * 8 + gid;  // this lane's B column (pixel)
+          const int qc = q < npx ? q : 0;
+#pragma unroll
+          for (int ks = 0; ks < 5; ++ks) {
+            if (ks >= ksteps) break;
+            const int m = ks * 16 + 2 * tig;
+            auto gv = [&](int mm) { return (mm < M && q < npx) ? goff[mm * PS + qc] : 0.f; };
+            const uint32_t b0 = pack_bf16(gv(m), gv(m + 1));
+            const uint32_t b1 = pack_bf16(gv(m + 8), gv(m + 9));
+            mma_bf16_16816(acc[tt], af[ks], b0, b1);
+          }
         }
         // D: rows orow0/orow1, columns pixels nt*8 + 2*tig (+1)
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int px = nt * 8 + 2 * tig + (h & 1);
-          const bool row_ok = (h >> 1) ? orow1 < NK : orow0 < NK;
-          if (!row_ok || px >= npx) continue;
-          const int e = pix[px];
-          const int pos = (e >> 16) * g.sh * pl.cols + (e & 0xffff) * g.sw;
-          if (acc[h] != 0.f) atomicAdd(((h >> 1) ? dst1 : dst0) + pos, acc[h]);
+        for (int tt = 0; tt < kNt; ++tt) {
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int px = (nt0 + tt) * 8 + 2 * tig + (h & 1);
+            const bool row_ok = (h >> 1) ? orow1 < NK : orow0 < NK;
+            if (!row_ok || px >= npx) continue;
+            const int e = pix[px];
+            const int pos = (e >> 16) * g.sh * pl.cols + (e & 0xffff) * g.sw;
+            if (acc[tt][h] != 0.f) atomicAdd(((h >> 1) ? dst1 : dst0) + pos, acc[tt][h]);
+          }
         }
       }
+    }
+  }
+}
+
+
+// Sampling backward of one on-chip tap over `count` consecutive channels of
+// the slice starting at slice channel `cl0`: reads gcol, the four staged
+// corners, writes the replayed sample, adds the offset-gradient terms to
+// sdy/sdx and scatters the corner weights times gcol into the grad_x window
+// (shared-memory atomics).  Loads of a batch of channels are issued before any
+// of the batch's atomics.  bf16: channel pairs share one corner word load.
+template <typename T>
+__device__ __forceinline__ void band_bwd_run(const uint32_t* __restrict__ xw, int PL, int cols,
+                                             int sbase, int cl0, int count,
+                                             const float* __restrict__ gp, long long gstride,
+                                             T* cp, long long cstride, float* gxp, float ly,
+                                             float lx, float w00, float w01, float w10, float w11,
+                                             float& sdy, float& sdx) {
+  const float hy = 1.0f - ly, hx = 1.0f - lx;
+  auto one = [&](float gc, float v00, float v01, float v10, float v11, int ch) {
+    sdy = __fmaf_rn(gc, hx * (v10 - v00) + lx * (v11 - v01), sdy);
+    sdx = __fmaf_rn(gc, hy * (v01 - v00) + ly * (v11 - v10), sdx);
+    if (cp) cp[(long long)ch * cstride] = from_f<T>(blend4(ly, lx, v00, v01, v10, v11));
+  };
+  auto scatter = [&](float gc, int ch) {
+    float* q = gxp + ch * PL;
+    atomicAdd(q, w00 * gc);
+    atomicAdd(q + 1, w01 * gc);
+    atomicAdd(q + cols, w10 * gc);
+    atomicAdd(q + cols + 1, w11 * gc);
+  };
+  int ch = 0;
+  if (sizeof(T) == 2) {
+    const uint32_t* xs = xw + sbase;
+    if (cl0 & 1) {  // odd start: high half of a pair word
+      const uint32_t* wp = xs + (cl0 >> 1) * PL;
+      const float gc = __ldg(gp);
+      one(gc, hi_bf16(wp[0]), hi_bf16(wp[1]), hi_bf16(wp[cols]), hi_bf16(wp[cols + 1]), 0);
+      scatter(gc, 0);
+      ch = 1;
+    }
+    constexpr int kPairs = 4;  // 8 channels per batch
+    for (; ch + 2 * kPairs <= count; ch += 2 * kPairs) {
+      uint32_t a00[kPairs], a01[kPairs], a10[kPairs], a11[kPairs];
+      float g0[kPairs], g1[kPairs];
+#pragma unroll
+      for (int u = 0; u < kPairs; ++u) {
+        const uint32_t* wp = xs + ((cl0 + ch) >> 1) * PL + u * PL;
+        a00[u] = wp[0];
+        a01[u] = wp[1];
+        a10[u] = wp[cols];
+        a11[u] = wp[cols + 1];
+        g0[u] = __ldg(gp + (long long)(ch + 2 * u) * gstride);
+        g1[u] = __ldg(gp + (long long)(ch + 2 * u + 1) * gstride);
+      }
+#pragma unroll
+      for (int u = 0; u < kPairs; ++u) {
+        one(g0[u], lo_bf16(a00[u]), lo_bf16(a01[u]), lo_bf16(a10[u]), lo_bf16(a11[u]), ch + 2 * u);
+        one(g1[u], hi_bf16(a00[u]), hi_bf16(a01[u]), hi_bf16(a10[u]), hi_bf16(a11[u]), ch + 2 * u + 1);
+      }
+#pragma unroll
+      for (int u = 0; u < kPairs; ++u) {
+        scatter(g0[u], ch + 2 * u);
+        scatter(g1[u], ch + 2 * u + 1);
+      }
+    }
+    for (; ch < count; ++ch) {
+      const int cl = cl0 + ch;
+      const uint32_t* wp = xs + (cl >> 1) * PL;
+      const float gc = __ldg(gp + (long long)ch * gstride);
+      if (cl & 1)
+        one(gc, hi_bf16(wp[0]), hi_bf16(wp[1]), hi_bf16(wp[cols]), hi_bf16(wp[cols + 1]), ch);
+      else
+        one(gc, lo_bf16(wp[0]), lo_bf16(wp[1]), lo_bf16(wp[cols]), lo_bf16(wp[cols + 1]), ch);
+      scatter(gc, ch);
+    }
+  } else {
+    const float* xs = reinterpret_cast<const float*>(xw) + sbase + cl0 * PL;
+    constexpr int kB = 8;
+    for (; ch + kB <= count; ch += kB) {
+      float v00[kB], v01[kB], v10[kB], v11[kB], gc[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        const float* wp = xs + (ch + u) * PL;
+        v00[u] = wp[0];
+        v01[u] = wp[1];
+        v10[u] = wp[cols];
+        v11[u] = wp[cols + 1];
+        gc[u] = __ldg(gp + (long long)(ch + u) * gstride);
+      }
+#pragma unroll
+      for (int u = 0; u < kB; ++u) one(gc[u], v00[u], v01[u], v10[u], v11[u], ch + u);
+#pragma unroll
+      for (int u = 0; u < kB; ++u) scatter(gc[u], ch + u);
+    }
+    for (; ch < count; ++ch) {
+      const float* wp = xs + ch * PL;
+      const float gc = __ldg(gp + (long long)ch * gstride);
+      one(gc, wp[0], wp[1], wp[cols], wp[cols + 1], ch);
+      scatter(gc, ch);
     }
   }
 }
@@ -287,6 +412,8 @@ __global__ void __launch_bounds__(kThreads, 2) k3_band_bwd(BwdArgs a, Plan pl) {
   float* part = reinterpret_cast<float*>(smem + pl.off_part);  // [M][PS]
   int* pix = reinterpret_cast<int*>(smem + pl.off_tab);        // (row << 16 | col) in band
   int* tapoff = pix + PS;                                      // window offset of tap k
+  int* nslow = reinterpret_cast<int*>(smem + pl.off_q);        // deferred slow taps
+  int* slowq = nslow + 1;
   float* goff = offs;
 
   // ---------------------------------------------------------------- staging
@@ -298,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 2) k3_band_bwd(BwdArgs a, Plan pl) {
   band::stage_window<T>(x, g, img, c_begin, pl.cpc, ylo, xlo, pl.rows, pl.cols, PL, xw);
   for (int idx = tid; idx < pl.cpc * PL; idx += kThreads) gxs[idx] = 0.f;
   for (int idx = tid; idx < M * PS; idx += kThreads) part[idx] = 0.f;
+  if (tid == 0) *nslow = 0;
   __syncthreads();
   {
     band::Walk2 w;
@@ -343,39 +471,45 @@ __global__ void __launch_bounds__(kThreads, 2) k3_band_bwd(BwdArgs a, Plan pl) {
         const float hy = 1.0f - t.ly, hx = 1.0f - t.lx;
         const float w00 = hy * hx, w01 = hy * t.lx, w10 = t.ly * hx, w11 = t.ly * t.lx;
         float sdy = 0.f, sdx = 0.f;
-        for (; c < run_end; ++c) {
-          const int cl = c - c_begin;
-          float s = 0.f;
-          if (t.inside) {
-            const float gc = grow[(long long)c * gstride];
-            float v00, v01, v10, v11;
-            if (t.fast) {
-              v00 = band::staged<T>(xw, PL, cl, sbase);
-              v01 = band::staged<T>(xw, PL, cl, sbase + 1);
-              v10 = band::staged<T>(xw, PL, cl, sbase + pl.cols);
-              v11 = band::staged<T>(xw, PL, cl, sbase + pl.cols + 1);
-              float* gp = gxs + cl * PL + sbase;
-              atomicAdd(gp, w00 * gc);
-              atomicAdd(gp + 1, w01 * gc);
-              atomicAdd(gp + pl.cols, w10 * gc);
-              atomicAdd(gp + pl.cols + 1, w11 * gc);
-            } else {
-              const T* xp = x + img + (long long)c * g.hw;
-              v00 = gload(xp, g, t.y0, t.x0);
-              v01 = gload(xp, g, t.y0, t.x0 + 1);
-              v10 = gload(xp, g, t.y0 + 1, t.x0);
-              v11 = gload(xp, g, t.y0 + 1, t.x0 + 1);
-              float* gp = a.gx + img + (long long)c * g.hw;
-              gadd(gp, g, t.y0, t.x0, w00 * gc);
-              gadd(gp, g, t.y0, t.x0 + 1, w01 * gc);
-              gadd(gp, g, t.y0 + 1, t.x0, w10 * gc);
-              gadd(gp, g, t.y0 + 1, t.x0 + 1, w11 * gc);
-            }
-            s = blend4(t.ly, t.lx, v00, v01, v10, v11);
+        if (t.inside && !t.fast) {
+          // out-of-window tap: queued for the cooperative pass below, so that
+          // this warp does not wait on global memory for one lane
+          const int qi = atomicAdd(nslow, 1);
+          if (qi < pl.qcap) {
+            slowq[qi] = px | (k << 8) | ((gg - g_begin) << 16);
+            c = run_end;
+          }
+        }
+        if (!t.inside) {
+          if (crow)
+            for (; c < run_end; ++c) crow[(long long)c * cstride] = from_f<T>(0.f);
+          c = run_end;
+        }
+        if (c < run_end && !t.fast) {
+          // queue full: this out-of-window tap is handled here, from global memory
+          for (; c < run_end; ++c) {
+            const float gc = __ldg(grow + (long long)c * gstride);
+            const T* xp = x + img + (long long)c * g.hw;
+            const float v00 = gload(xp, g, t.y0, t.x0), v01 = gload(xp, g, t.y0, t.x0 + 1);
+            const float v10 = gload(xp, g, t.y0 + 1, t.x0), v11 = gload(xp, g, t.y0 + 1, t.x0 + 1);
+            float* gq = a.gx + img + (long long)c * g.hw;
+            gadd(gq, g, t.y0, t.x0, w00 * gc);
+            gadd(gq, g, t.y0, t.x0 + 1, w01 * gc);
+            gadd(gq, g, t.y0 + 1, t.x0, w10 * gc);
+            gadd(gq, g, t.y0 + 1, t.x0 + 1, w11 * gc);
             sdy = __fmaf_rn(gc, hx * (v10 - v00) + t.lx * (v11 - v01), sdy);
             sdx = __fmaf_rn(gc, hy * (v01 - v00) + t.ly * (v11 - v10), sdx);
+            if (crow) crow[(long long)c * cstride] = from_f<T>(blend4(t.ly, t.lx, v00, v01, v10, v11));
           }
-          if (crow) crow[(long long)c * cstride] = from_f<T>(s);
+        }
+        if (c < run_end) {
+          // on-chip tap: gcol, corners, blend, offset-gradient terms, scatter
+          const float* gp = grow + (long long)c * gstride;
+          T* cp = crow ? crow + (long long)c * cstride : nullptr;
+          float* gxp = gxs + (c - c_begin) * PL + sbase;
+          band_bwd_run<T>(xw, PL, pl.cols, sbase, c - c_begin, run_end - c, gp, gstride, cp,
+                          cstride, gxp, t.ly, t.lx, w00, w01, w10, w11, sdy, sdx);
+          c = run_end;
         }
         part[(2 * (gg * g.K + k)) * PS + px] = sdy;
         part[(2 * (gg * g.K + k) + 1) * PS + px] = sdx;
@@ -383,24 +517,84 @@ __global__ void __launch_bounds__(kThreads, 2) k3_band_bwd(BwdArgs a, Plan pl) {
     }
   }
 
+  // ---------------------------------------------------------------- deferred slow taps
+  // all lanes together: one (queued tap, channel) pair per thread, corners and
+  // grad_x updates in global memory, offset-gradient terms added to `part`
+  __syncthreads();
+  {
+    const int nq = min(*nslow, pl.qcap);
+    const long long gstride = (long long)g.K * a.gcol_layout.row;
+    const long long cstride = (long long)g.K * a.col_layout.row;
+    for (int task = tid; task < nq * pl.cpc; task += kThreads) {
+      const int ent = task / pl.cpc, jj = task - ent * pl.cpc;
+      const int code = slowq[ent];
+      const int px = code & 0xff, k = (code >> 8) & 0xff, gg = g_begin + (code >> 16);
+      const int c = max(c_begin, gg * g.cg) + jj;
+      if (c >= min(c_end, (gg + 1) * g.cg)) continue;
+      const int e = pix[px];
+      const int ho = ho0 + (e >> 16), wo = wo0 + (e & 0xffff);
+      const int i = k / g.kw, j = k - i * g.kw;
+      const Tap t = make_tap((float)(ho * g.sh - g.ph + i * g.dh) + offs[(2 * (gg * g.K + k)) * PS + px],
+                             (float)(wo * g.sw - g.pw + j * g.dw) + offs[(2 * (gg * g.K + k) + 1) * PS + px],
+                             g, ylo, xlo, pl.rows, pl.cols);
+      const long long qo = (long long)ho * g.wo + wo;
+      const float gc = __ldg(a.gcol + (long long)k * a.gcol_layout.row + (long long)n * a.gcol_layout.img +
+                             qo + (long long)c * gstride);
+      const T* xp = x + img + (long long)c * g.hw;
+      const float v00 = gload(xp, g, t.y0, t.x0), v01 = gload(xp, g, t.y0, t.x0 + 1);
+      const float v10 = gload(xp, g, t.y0 + 1, t.x0), v11 = gload(xp, g, t.y0 + 1, t.x0 + 1);
+      const float hy = 1.0f - t.ly, hx = 1.0f - t.lx;
+      float* gp = a.gx + img + (long long)c * g.hw;
+      gadd(gp, g, t.y0, t.x0, hy * hx * gc);
+      gadd(gp, g, t.y0, t.x0 + 1, hy * t.lx * gc);
+      gadd(gp, g, t.y0 + 1, t.x0, t.ly * hx * gc);
+      gadd(gp, g, t.y0 + 1, t.x0 + 1, t.ly * t.lx * gc);
+      atomicAdd(part + (2 * (gg * g.K + k)) * PS + px, gc * (hx * (v10 - v00) + t.lx * (v11 - v01)));
+      atomicAdd(part + (2 * (gg * g.K + k) + 1) * PS + px, gc * (hy * (v01 - v00) + t.ly * (v11 - v10)));
+      if (col)
+        col[(long long)k * a.col_layout.row + (long long)n * a.col_layout.img + qo + (long long)c * cstride] =
+            from_f<T>(blend4(t.ly, t.lx, v00, v01, v10, v11));
+    }
+  }
+
   // ---------------------------------------------------------------- offset gradient, cluster sum
   cg::cluster_group cluster = cg::this_cluster();
   cluster.sync();
   {
+    // four (m, px) items per round, their remote loads all in flight
     band::Walk2 w;
     w.init(tid, kThreads, npx);
     while (w.a < M) {
-      const int m = w.a, px = w.b;
-      float v = 0.f;
-      for (int r = 0; r < pl.csize; ++r) v += cluster.map_shared_rank(part, r)[m * PS + px];
-      const int e = pix[px];
-      const int ho = ho0 + (e >> 16), wo = wo0 + (e & 0xffff);
-      const bool valid = ho < g.ho && wo < g.wo;
-      if (!valid) v = 0.f;
-      goff[m * PS + px] = v;
-      if (valid && rank == 0)
-        a.goff[((long long)n * M + m) * g.howo + (long long)ho * g.wo + wo] = v;
-      w.next();
+      int mm[4], pp[4];
+      float v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        mm[j] = -1;
+        v[j] = 0.f;
+        if (w.a < M) {
+          mm[j] = w.a;
+          pp[j] = w.b;
+          w.next();
+        }
+      }
+      for (int r = 0; r < pl.csize; ++r) {
+        const float* rp = cluster.map_shared_rank(part, r);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (mm[j] >= 0) v[j] += rp[mm[j] * PS + pp[j]];
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (mm[j] < 0) continue;
+        const int m = mm[j], px = pp[j];
+        const int e = pix[px];
+        const int ho = ho0 + (e >> 16), wo = wo0 + (e & 0xffff);
+        const bool valid = ho < g.ho && wo < g.wo;
+        const float vv = valid ? v[j] : 0.f;
+        goff[m * PS + px] = vv;
+        if (valid && rank == 0)
+          a.goff[((long long)n * M + m) * g.howo + (long long)ho * g.wo + wo] = vv;
+      }
     }
   }
   cluster.sync();  // peers have read this CTA's partials; goff complete here
