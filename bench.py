@@ -29,17 +29,26 @@ if ROOT not in sys.path:
 
 METRIC = "deform-conv layer fwd+bwd ms and GFLOP/s; sampling-stage HBM GB/s vs GB300 peak"
 FLUSH_BYTES = 256 << 20
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
-# DRAM traffic of one K1 launch from an ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum), keyed by the workload; valid only while the kernel
-# source hashes to the recorded value.
-K1_TRAFFIC = {}
+# DRAM traffic of one launch from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by (workload, kernel); valid only while the
+# kernel's source file hashes to the recorded value (else reported as null).
+TRAFFIC = {
+    # ncu --set full of k1_band_sample, res3 bf16 (profiles/k1_band_sample_res3_bf16.md):
+    # the deformed map and the offsets stay in L2, only x is read from DRAM
+    ("res3_bf16", "k1_band_sample"): {"bytes": 2176000 + 768, "source": "779e1724db30fbf1"},
+}
+KERNEL_SOURCES = {
+    "k1_band_sample": "k1_sample.cu", "k3_band_bwd": "k3_band_bwd.cu",
+    "gemm_fwd": "gemm_tc.cu", "gemm_gcol": "gemm_tc.cu", "gemm_gw": "gemm_tc.cu",
+}
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="res3_bf16")
@@ -300,7 +309,14 @@ def main():
             "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
 
     if rank == 0:
-        line["roofline"] = k1_roofline(p, t, dev, stream, flush, wl, args.roofline_iters)
+        kernels = kernel_breakdown(p, wl, step, dev, stream, flush)
+        dom = dict(kernels[0])
+        line["roofline"] = {k: dom[k] for k in ("kernel", "bound", "achieved", "peak", "unit", "frac",
+                                                "traffic", "ms_per_launch", "peak_source")
+                            if k in dom}
+        line["roofline"]["note"] = "dominant kernel of the step (longest per-launch time)"
+        line["kernels"] = kernels
+        line["sampling_stage"] = k1_roofline(p, t, dev, stream, flush, wl, args.roofline_iters)
         line["e2e"] = e2e(p, d, dev, stream, flops_step, args.e2e_iters)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
@@ -309,6 +325,87 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def traffic_for(workload, kernel):
+    rec = TRAFFIC.get((workload, kernel))
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "deformable_convolution_gb300", "csrc", KERNEL_SOURCES[kernel])
+    return rec["bytes"] if rec["source"] == source_hash(src) else None
+
+
+def kernel_costs(p, has_add):
+    """Algorithmic bytes (HBM-bound kernels) or flops (GEMMs) of one launch of
+    each kernel of the forward + backward step."""
+    elt = 2 if p.dtype == 1 else 4
+    P = p.n * p.ho * p.wo
+    kdim = p.c_in * p.kh * p.kw
+    x_b = p.n * p.c_in * p.h * p.w * elt
+    off_b = p.n_off * P * 4
+    gemm = 2.0 * p.c_out * kdim * P
+    k3 = (x_b + off_b + kdim * P * 4 + p.n_off * kdim * elt      # read x, offsets, gcol, w_off
+          + p.n * p.c_in * p.h * p.w * 4 + off_b + kdim * P * elt  # write grad_x, grad_offset, map
+          + p.n_off * kdim * 4)                                     # write grad_w_off
+    return {
+        "k1_band_sample": ("hbm", k1_bytes(p, has_add)),
+        "gemm_fwd": ("tensor", gemm), "gemm_gcol": ("tensor", gemm), "gemm_gw": ("tensor", gemm),
+        "k3_band_bwd": ("hbm", k3),
+        "memsets": ("hbm", 4 * (p.n * p.c_in * p.h * p.w + p.c_out * kdim + p.n_off * kdim + p.n_off)),
+    }
+
+
+def kernel_breakdown(p, wl, step, dev, stream, flush, iters=40):
+    """Every kernel of the step timed with CUDA events on its stream (the
+    library's dc_kernel_timing), eager launches, L2 flushed before each step."""
+    import torch
+
+    from deformable_convolution_gb300 import binding as B
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            flush.fill_(5)
+            step()
+        torch.cuda.synchronize(dev)
+        B.kernel_timing(True)
+        for _ in range(iters):
+            flush.fill_(9)
+            step()
+    torch.cuda.synchronize(dev)
+    recs = B.kernel_times()
+    B.kernel_timing(False)
+    tot, cnt = {}, {}
+    for name, ms in recs:
+        if ms >= 0:
+            tot[name] = tot.get(name, 0.0) + ms
+            cnt[name] = cnt.get(name, 0) + 1
+    costs = kernel_costs(p, wl.outlier_p > 0)
+    peaks, src = measured_peaks()
+    step_ms = sum(tot[k] / cnt[k] for k in tot)
+    out = []
+    for name in tot:
+        ms = tot[name] / cnt[name]
+        bound, amount = costs.get(name, ("hbm", 0.0))
+        if bound == "tensor" and p.dtype != 1:
+            # float32 problems run the GEMMs on CUDA cores: FFMA peak of the part
+            bound = "alu"
+            achieved = amount / (ms / 1e3) / 1e12
+            peak, unit = FP32_ALU_TFLOPS, "TFLOP/s"
+            peak_src = "derived: 152 SMs x 128 fp32 lanes x 2 flop x 2.07 GHz"
+        elif bound == "tensor":
+            achieved = amount / (ms / 1e3) / 1e12
+            peak, unit = peaks["bf16_tflops_sustained"], "TFLOP/s"
+            peak_src = f"{src} (bf16_tflops_sustained)"
+        else:
+            achieved = amount / (ms / 1e3) / 1e9
+            peak, unit = peaks["hbm_gbs"], "GB/s"
+            peak_src = f"{src} (hbm_gbs)"
+        out.append({"kernel": name, "ms_per_launch": ms, "share": ms / step_ms, "bound": bound,
+                    "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                    "peak_source": peak_src,
+                    ("algorithmic_flops" if bound == "tensor" else "algorithmic_bytes"): amount,
+                    "traffic": traffic_for(wl.name, name)})
+    out.sort(key=lambda r: -r["ms_per_launch"])
+    return out
 
 
 def k1_bytes(p, has_add):
@@ -360,8 +457,7 @@ def k1_roofline(p, t, dev, stream, flush, wl, iters=200):
     achieved = nbytes / (ms / 1e3) / 1e9
     src_hash = source_hash(os.path.join(ROOT, "deformable_convolution_gb300", "csrc",
                                         "k1_sample.cu"))
-    rec = K1_TRAFFIC.get(wl.name)
-    traffic = rec["bytes"] if rec and rec["source"] == src_hash else None
+    traffic = traffic_for(wl.name, "k1_band_sample")
     return {"kernel": "k1_band_sample (offset conv + bilinear sampling)", "bound": "hbm",
             "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{src} (hbm_gbs, burst)",

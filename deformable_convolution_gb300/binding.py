@@ -22,7 +22,8 @@ _TORCH_DTYPE = {DC_F32: torch.float32, DC_BF16: torch.bfloat16}
 EXPORTED_SYMBOLS = (
     "dc_out_h", "dc_out_w", "deform_conv_workspace_size", "deform_conv_fwd",
     "deform_conv_bwd", "deform_conv_sample", "dc_status_string", "dc_build_info",
-    "dc_launch_count", "deform_conv_fwd_noalloc", "dc_device_error",
+    "dc_launch_count", "deform_conv_fwd_noalloc", "dc_device_error", "dc_kernel_timing",
+    "dc_kernel_times",
 )
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -67,6 +68,10 @@ def lib() -> ctypes.CDLL:
         L.dc_build_info.restype = ctypes.c_char_p
         L.deform_conv_fwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.deform_conv_fwd_noalloc.restype = i
+        L.dc_kernel_timing.argtypes = [i]
+        L.dc_kernel_timing.restype = None
+        L.dc_kernel_times.argtypes = [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float), i]
+        L.dc_kernel_times.restype = i
         L.dc_device_error.argtypes = [i]
         L.dc_device_error.restype = i
         L.dc_launch_count.argtypes = []
@@ -86,6 +91,20 @@ def build_info() -> str:
 def device_error(clear: bool = False) -> int:
     """DC_ERR_TIMEOUT if a bounded device wait expired (synchronises)."""
     return int(lib().dc_device_error(1 if clear else 0))
+
+
+def kernel_timing(enable: bool) -> None:
+    """Start/stop CUDA-event timing of every launch the library enqueues."""
+    lib().dc_kernel_timing(1 if enable else 0)
+
+
+def kernel_times(capacity: int = 256):
+    """[(kernel name, ms)] of the launches recorded since timing was enabled
+    (waits for them); clears the record."""
+    names = (ctypes.c_char_p * capacity)()
+    ms = (ctypes.c_float * capacity)()
+    n = lib().dc_kernel_times(names, ms, capacity)
+    return [(names[i].decode(), float(ms[i])) for i in range(n)]
 
 
 def launch_count() -> int:

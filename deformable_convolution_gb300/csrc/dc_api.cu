@@ -13,6 +13,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "dc_common.cuh"
 
@@ -20,6 +21,45 @@ namespace dc {
 
 static std::atomic<unsigned long long> g_launches{0};
 void note_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+// Per-launch timing (dc_kernel_timing): when enabled, every kernel the ABI
+// enqueues is bracketed by two CUDA events on its stream; dc_kernel_times
+// reads the records of the calls made since timing was (re)enabled.  Off by
+// default; events are host/driver objects, no device memory is allocated.
+namespace {
+constexpr int kMaxTimed = 256;
+struct TimedLaunch {
+  const char* name;
+  cudaEvent_t a, b;
+};
+std::mutex g_timing_mu;
+bool g_timing = false;
+TimedLaunch g_timed[kMaxTimed];
+int g_ntimed = 0;
+int g_nevents = 0;  // event pairs created so far (reused across calls)
+
+template <typename F>
+cudaError_t timed(const char* name, cudaStream_t s, F&& launch) {
+  int slot = -1;
+  if (g_timing) {
+    std::lock_guard<std::mutex> lock(g_timing_mu);
+    if (g_ntimed < kMaxTimed) {
+      slot = g_ntimed++;
+      if (slot >= g_nevents) {
+        if (cudaEventCreate(&g_timed[slot].a) != cudaSuccess ||
+            cudaEventCreate(&g_timed[slot].b) != cudaSuccess)
+          return cudaErrorUnknown;
+        g_nevents = slot + 1;
+      }
+      g_timed[slot].name = name;
+    }
+  }
+  if (slot >= 0) cudaEventRecord(g_timed[slot].a, s);
+  const cudaError_t e = launch();
+  if (slot >= 0) cudaEventRecord(g_timed[slot].b, s);
+  return e;
+}
+}  // namespace
 
 cudaError_t launch_gemm_fwd(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
 cudaError_t launch_gemm_gcol(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
@@ -170,7 +210,7 @@ dc_status deform_conv_fwd(const dc_problem* prob, const void* x, const void* w_o
   sa.off_out = offset_out;
   sa.slow_count = slowpath_count;
   sa.margin = margin;
-  st = cuda_status(launch_sample(sa, prob->dtype, s));
+  st = cuda_status(timed("k1_band_sample", s, [&] { return launch_sample(sa, prob->dtype, s); }));
   if (st != DC_OK) return st;
 
   GemmArgs ga{};
@@ -179,7 +219,7 @@ dc_status deform_conv_fwd(const dc_problem* prob, const void* x, const void* w_o
   ga.col = sa.col;
   ga.col_layout = pl.col;
   ga.y = y;
-  return cuda_status(launch_gemm_fwd(ga, prob->dtype, s));
+  return cuda_status(timed("gemm_fwd", s, [&] { return launch_gemm_fwd(ga, prob->dtype, s); }));
 }
 
 dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_off, const void* w,
@@ -203,18 +243,6 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
   char* wsb = static_cast<char*>(ws);
   float* goff = grad_offset ? grad_offset : reinterpret_cast<float*>(wsb + pl.off_off);
 
-  // atomic targets start at zero
-  st = cuda_status(cudaMemsetAsync(grad_x, 0, sizeof(float) * g.n * g.c_in * g.hw, s));
-  if (st != DC_OK) return st;
-  st = cuda_status(cudaMemsetAsync(grad_w, 0, sizeof(float) * g.c_out * g.kdim, s));
-  if (st != DC_OK) return st;
-  st = cuda_status(cudaMemsetAsync(grad_w_off, 0, sizeof(float) * g.M * g.kdim, s));
-  if (st != DC_OK) return st;
-  if (grad_b_off) {
-    st = cuda_status(cudaMemsetAsync(grad_b_off, 0, sizeof(float) * g.M, s));
-    if (st != DC_OK) return st;
-  }
-
   // gradient of the deformed map: gcol = w^T grad_y
   GemmArgs ga{};
   ga.g = g;
@@ -225,7 +253,16 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
   ga.gcol = reinterpret_cast<float*>(wsb + pl.gcol_off);
   ga.gcol_layout = pl.gcol;
   ga.gw = grad_w;
-  st = cuda_status(launch_gemm_gcol(ga, prob->dtype, s));
+  // the GCOL launch also clears the buffers later kernels accumulate into
+  ga.zero.p[0] = grad_x;
+  ga.zero.n[0] = (long long)g.n * g.c_in * g.hw;
+  ga.zero.p[1] = grad_w;
+  ga.zero.n[1] = (long long)g.c_out * g.kdim;
+  ga.zero.p[2] = grad_w_off;
+  ga.zero.n[2] = (long long)g.M * g.kdim;
+  ga.zero.p[3] = grad_b_off;
+  ga.zero.n[3] = grad_b_off ? g.M : 0;
+  st = cuda_status(timed("gemm_gcol", s, [&] { return launch_gemm_gcol(ga, prob->dtype, s); }));
   if (st != DC_OK) return st;
 
   // sampling and offset-conv backward; replays the deformed map for grad_w
@@ -243,11 +280,11 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
   ba.gw_off = grad_w_off;
   ba.gb_off = grad_b_off;
   ba.margin = margin;
-  st = cuda_status(launch_band_bwd(ba, prob->dtype, s));
+  st = cuda_status(timed("k3_band_bwd", s, [&] { return launch_band_bwd(ba, prob->dtype, s); }));
   if (st != DC_OK) return st;
 
   // main weight gradient from the replayed map
-  return cuda_status(launch_gemm_gw(ga, prob->dtype, s));
+  return cuda_status(timed("gemm_gw", s, [&] { return launch_gemm_gw(ga, prob->dtype, s); }));
 }
 
 dc_status deform_conv_sample(const dc_problem* prob, const void* x, const void* w_off,
@@ -275,7 +312,8 @@ dc_status deform_conv_sample(const dc_problem* prob, const void* x, const void* 
   sa.off_out = offset_out;
   sa.slow_count = slowpath_count;
   sa.margin = margin;
-  return cuda_status(launch_sample(sa, prob->dtype, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(timed("k1_band_sample", s, [&] { return launch_sample(sa, prob->dtype, s); }));
 }
 
 const char* dc_status_string(dc_status status) {
@@ -288,6 +326,27 @@ const char* dc_status_string(dc_status status) {
     case DC_ERR_TIMEOUT: return "DC_ERR_TIMEOUT: a bounded device wait expired";
   }
   return "unknown dc_status";
+}
+
+void dc_kernel_timing(int enable) {
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  g_timing = enable != 0;
+  g_ntimed = 0;
+}
+
+int dc_kernel_times(const char** names, float* ms, int capacity) {
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  const int n = g_ntimed < capacity ? g_ntimed : capacity;
+  for (int i = 0; i < n; ++i) {
+    float t = -1.f;
+    if (cudaEventSynchronize(g_timed[i].b) != cudaSuccess ||
+        cudaEventElapsedTime(&t, g_timed[i].a, g_timed[i].b) != cudaSuccess)
+      t = -1.f;
+    if (names) names[i] = g_timed[i].name;
+    if (ms) ms[i] = t;
+  }
+  g_ntimed = 0;
+  return n;
 }
 
 unsigned long long dc_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

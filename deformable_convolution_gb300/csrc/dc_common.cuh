@@ -95,6 +95,30 @@ struct SampleArgs {
 cudaError_t launch_sample(const SampleArgs& a, dc_dtype dt, cudaStream_t s);
 size_t sample_smem_bytes(const Geom& g, dc_dtype dt, int margin);
 
+// Buffers a kernel zeroes as a side job (up to four float arrays); CTA `part`
+// of `nparts` clears its share of each, float4 where aligned.
+struct ZeroArgs {
+  float* p[4];
+  long long n[4];
+};
+
+__device__ __forceinline__ void zero_share(const ZeroArgs& z, long long part, long long nparts,
+                                           int tid, int nthreads) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (!z.p[i] || z.n[i] <= 0) continue;
+    const long long chunk = (ceil_div_ll(z.n[i], nparts) + 3) / 4 * 4;
+    const long long lo = part * chunk;
+    long long hi = lo + chunk;
+    if (hi > z.n[i]) hi = z.n[i];
+    float* p = z.p[i];
+    long long e = lo + 4LL * tid;
+    for (; e + 4 <= hi; e += 4LL * nthreads)
+      *reinterpret_cast<float4*>(p + e) = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (; e < hi; ++e) p[e] = 0.f;
+  }
+}
+
 // Main-convolution GEMMs on the column layout (batched over images).
 struct GemmArgs {
   Geom g;
@@ -106,6 +130,7 @@ struct GemmArgs {
   float* gcol;        // column-layout gradient, fp32 (backward)
   ColLayout gcol_layout;
   float* gw;          // [c_out][kdim] fp32, accumulated with atomics (backward)
+  ZeroArgs zero;      // GCOL kernels clear these (the backward's atomic targets)
 };
 // Tensor-core (tcgen05, bf16) versions; need tc_gemm_supported(g).
 bool tc_gemm_supported(const Geom& g);

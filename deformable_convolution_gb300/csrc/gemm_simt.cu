@@ -27,6 +27,7 @@ struct StridedGemm {
   long long b_z, b_k, b_n;
   long long c_z, c_m, c_n;
   int atomic;  // 1: atomically add fp32 into C, 0: store
+  ZeroArgs zero;  // buffers this launch clears as a side job (GCOL)
 };
 
 template <typename TA, typename TB, typename TC>
@@ -36,6 +37,11 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ float Bs[BK][BN + 4];
   const int z = blockIdx.z;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  {
+    const long long nparts = (long long)gridDim.x * gridDim.y * gridDim.z;
+    const long long part = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
+    zero_share(p.zero, part, nparts, threadIdx.x, kThreads);
+  }
   const TA* Az = A + (long long)z * p.a_z;
   const TB* Bz = B + (long long)z * p.b_z;
   const int tid = threadIdx.x;
@@ -128,6 +134,7 @@ cudaError_t launch_gemm_gcol_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s
   p.b_z = (long long)g.c_out * g.howo; p.b_k = g.howo; p.b_n = 1;
   p.c_z = a.gcol_layout.img; p.c_m = a.gcol_layout.row; p.c_n = 1;
   p.atomic = 0;
+  p.zero = a.zero;
   if (dt == DC_BF16)
     return run<__nv_bfloat16, __nv_bfloat16, float>(p, g.n, a.w, a.gy, a.gcol, s);
   return run<float, float, float>(p, g.n, a.w, a.gy, a.gcol, s);

@@ -42,6 +42,7 @@ struct TcArgs {
   int qblocks;           // GW: k-blocks per image (ceil(howo / 64))
   void* out;
   long long out_row, out_img;  // GCOL: gcol pitches (elements)
+  ZeroArgs zero;               // GCOL: the backward's atomic targets, cleared by warps 0-3
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -253,6 +254,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue (warps 0-3)
+    if (KIND == GCOL) {
+      // while the tensor cores work, clear this CTA's share of the buffers the
+      // rest of the backward pass accumulates into with atomics
+      const long long nparts = (long long)gridDim.x * gridDim.y * gridDim.z;
+      const long long part = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
+      zero_share(a.zero, part, nparts, threadIdx.x, 128);
+    }
     const bool ok = mbar_wait(done, 0);
     tc_fence_after();
     const int row = warp * 32 + lane;
@@ -438,6 +446,7 @@ cudaError_t launch_gemm_gcol_tc(const GemmArgs& ga, cudaStream_t s) {
   a.out = ga.gcol;
   a.out_row = ga.gcol_layout.row;
   a.out_img = ga.gcol_layout.img;
+  a.zero = ga.zero;
   dim3 grid((unsigned)ceil_div_ll(g.howo, 128), (unsigned)ceil_div_ll(g.kdim, kBM), (unsigned)g.n);
   return launch<GCOL, 128>(A, B, a, grid, s);
 }

@@ -177,6 +177,17 @@ const char* dc_build_info(void);
  * rest of its work: its outputs are not valid. */
 dc_status dc_device_error(int clear);
 
+/* Kernel timing (tracing).  dc_kernel_timing(1) starts recording: every
+ * kernel (and the backward pass's group of memsets) enqueued by the calls that
+ * follow is bracketed by two CUDA events on its stream, up to 256 launches;
+ * dc_kernel_timing(0) stops.  Timing is off by default; it must not be enabled
+ * while a stream is being captured into a CUDA graph.  dc_kernel_times waits
+ * for the recorded launches, writes up to `capacity` (static name, duration in
+ * ms) pairs in launch order (-1 for a launch that could not be timed), returns
+ * how many it wrote and clears the record.  names or ms may be NULL. */
+void dc_kernel_timing(int enable);
+int dc_kernel_times(const char** names, float* ms, int capacity);
+
 /* Number of kernels this library has enqueued in this process so far (host
  * counter, incremented per launch; memsets are not counted).  Lets a caller
  * count the launches of a region of work, e.g. of a captured CUDA graph. */
