@@ -41,6 +41,7 @@ TRAFFIC = {
 }
 KERNEL_SOURCES = {
     "k1_band_sample": "k1_sample.cu", "k3_band_bwd": "k3_band_bwd.cu",
+    "k4_offconv_bwd": "k4_offconv_bwd.cu",
     "gemm_fwd": "gemm_tc.cu", "gemm_gcol": "gemm_tc.cu", "gemm_gw": "gemm_tc.cu",
 }
 

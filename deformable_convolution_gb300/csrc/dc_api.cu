@@ -5,10 +5,11 @@
 // page "DefT: Boosting Scalability of Deformable Convolution Operations on
 // GPUs"): K1 fuses the offset convolution with the bilinear interpolation and
 // writes the deformed map; the main convolution is a separate dense GEMM over
-// that map.  Backward: a GEMM gives the deformed map's gradient; K3 scatters
-// it into grad_x, reduces the offset gradient, runs the offset convolution's
-// backward and replays the deformed map; a second GEMM gives the main
-// weights' gradient from that map.
+// that map.  Backward: a GEMM gives the deformed map's gradient (and clears
+// the buffers the later kernels accumulate into); K3 scatters it into grad_x,
+// accumulates the offset gradient and replays the deformed map; K4 runs the
+// offset convolution's backward; a second GEMM gives the main weights'
+// gradient from the replayed map.
 #include <stdint.h>
 #include <string.h>
 
@@ -176,7 +177,9 @@ dc_status deform_conv_workspace_size(const dc_problem* prob, int backward, size_
   int margin;
   const dc_status st = make_geom(prob, &g, &margin);
   if (st != DC_OK) return st;
-  if (backward && bwd_smem_bytes(g, prob->dtype, margin) > kMaxSmem) return DC_ERR_UNSUPPORTED;
+  if (backward && (bwd_smem_bytes(g, prob->dtype, margin) > kMaxSmem ||
+                   offconv_bwd_smem_bytes(g, prob->dtype) > kMaxSmem))
+    return DC_ERR_UNSUPPORTED;
   *bytes = make_plan(g, prob->dtype, backward ? 1 : 0).total;
   return DC_OK;
 }
@@ -232,7 +235,9 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
   if (st != DC_OK) return st;
   if (!x || !w_off || !w || !offset || !grad_y || !grad_x || !grad_w_off || !grad_w)
     return DC_ERR_INVALID_ARG;
-  if (bwd_smem_bytes(g, prob->dtype, margin) > kMaxSmem) return DC_ERR_UNSUPPORTED;
+  if (bwd_smem_bytes(g, prob->dtype, margin) > kMaxSmem ||
+      offconv_bwd_smem_bytes(g, prob->dtype) > kMaxSmem)
+    return DC_ERR_UNSUPPORTED;
   const void* ptrs[] = {x, w_off, w, offset, grad_y, grad_x, grad_w_off, grad_b_off, grad_w,
                         grad_offset, ws};
   for (const void* p : ptrs)
@@ -262,14 +267,15 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
   ga.zero.n[2] = (long long)g.M * g.kdim;
   ga.zero.p[3] = grad_b_off;
   ga.zero.n[3] = grad_b_off ? g.M : 0;
+  ga.zero.p[4] = goff;
+  ga.zero.n[4] = (long long)g.n * g.M * g.howo;
   st = cuda_status(timed("gemm_gcol", s, [&] { return launch_gemm_gcol(ga, prob->dtype, s); }));
   if (st != DC_OK) return st;
 
-  // sampling and offset-conv backward; replays the deformed map for grad_w
+  // sampling backward; replays the deformed map for grad_w
   BwdArgs ba{};
   ba.g = g;
   ba.x = x;
-  ba.w_off = w_off;
   ba.off = offset;
   ba.gcol = ga.gcol;
   ba.gcol_layout = pl.gcol;
@@ -277,10 +283,20 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
   ba.col_layout = pl.col;
   ba.gx = grad_x;
   ba.goff = goff;
-  ba.gw_off = grad_w_off;
-  ba.gb_off = grad_b_off;
   ba.margin = margin;
   st = cuda_status(timed("k3_band_bwd", s, [&] { return launch_band_bwd(ba, prob->dtype, s); }));
+  if (st != DC_OK) return st;
+
+  // offset-convolution backward on the completed offset gradient
+  OffconvBwdArgs oa{};
+  oa.g = g;
+  oa.x = x;
+  oa.w_off = w_off;
+  oa.goff = goff;
+  oa.gx = grad_x;
+  oa.gw_off = grad_w_off;
+  oa.gb_off = grad_b_off;
+  st = cuda_status(timed("k4_offconv_bwd", s, [&] { return launch_offconv_bwd(oa, prob->dtype, s); }));
   if (st != DC_OK) return st;
 
   // main weight gradient from the replayed map

@@ -95,17 +95,17 @@ struct SampleArgs {
 cudaError_t launch_sample(const SampleArgs& a, dc_dtype dt, cudaStream_t s);
 size_t sample_smem_bytes(const Geom& g, dc_dtype dt, int margin);
 
-// Buffers a kernel zeroes as a side job (up to four float arrays); CTA `part`
+// Buffers a kernel zeroes as a side job (up to six float arrays); CTA `part`
 // of `nparts` clears its share of each, float4 where aligned.
 struct ZeroArgs {
-  float* p[4];
-  long long n[4];
+  float* p[6];
+  long long n[6];
 };
 
 __device__ __forceinline__ void zero_share(const ZeroArgs& z, long long part, long long nparts,
                                            int tid, int nthreads) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 6; ++i) {
     if (!z.p[i] || z.n[i] <= 0) continue;
     const long long chunk = (ceil_div_ll(z.n[i], nparts) + 3) / 4 * 4;
     const long long lo = part * chunk;
@@ -142,13 +142,11 @@ cudaError_t launch_gemm_fwd_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s)
 cudaError_t launch_gemm_gcol_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
 cudaError_t launch_gemm_gw_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
 
-// Fused backward of the sampling step and of the offset convolution (K3):
-// grad_x (atomics; zeroed by the caller), the offset gradient, grad_w_off and
-// grad_b_off (atomics; zeroed by the caller), and the replayed deformed map.
+// Backward of the sampling step (K3): grad_x and the offset gradient goff
+// (float atomics into buffers cleared beforehand) and the replayed deformed map.
 struct BwdArgs {
   Geom g;
   const void* x;
-  const void* w_off;
   const float* off;
   const float* gcol;
   ColLayout gcol_layout;
@@ -156,11 +154,23 @@ struct BwdArgs {
   ColLayout col_layout;
   float* gx;
   float* goff;
-  float* gw_off;
-  float* gb_off;  // may be null
   int margin;
 };
 cudaError_t launch_band_bwd(const BwdArgs& a, dc_dtype dt, cudaStream_t s);
 size_t bwd_smem_bytes(const Geom& g, dc_dtype dt, int margin);
+
+// Backward of the offset convolution (K4) from the completed goff: adds into
+// grad_x, grad_w_off and grad_b_off (cleared beforehand).
+struct OffconvBwdArgs {
+  Geom g;
+  const void* x;
+  const void* w_off;
+  const float* goff;
+  float* gx;
+  float* gw_off;
+  float* gb_off;  // may be null
+};
+cudaError_t launch_offconv_bwd(const OffconvBwdArgs& a, dc_dtype dt, cudaStream_t s);
+size_t offconv_bwd_smem_bytes(const Geom& g, dc_dtype dt);
 
 }  // namespace dc
