@@ -73,6 +73,19 @@ __device__ __forceinline__ bool touches_image(float py, float px, int H, int W) 
   return py >= -1.0f && py < (float)H && px >= -1.0f && px < (float)W;
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream serialization attribute may start while its predecessor on the
+// stream is finishing; it must call pdl_wait() before touching anything the
+// predecessor writes (or reads and this kernel overwrites).  pdl_wait() is a
+// no-op for kernels launched without the attribute.  pdl_release() lets this
+// kernel's own dependent start its prologue; every kernel calls it only after
+// its own pdl_wait(), so a dependent's prologue may read anything produced two
+// or more launches earlier.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- launchers
 // All return the launch's cudaError_t; the ABI layer maps it to a status.
 

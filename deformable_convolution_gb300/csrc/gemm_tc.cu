@@ -203,6 +203,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // The forward GEMM reads the column K1 writes; GCOL is the first kernel of
+  // the backward call (launched without early start, so the wait is a no-op).
+  // The weight-gradient GEMM follows K4 but reads nothing K4 writes: it starts
+  // only once every K4 block has passed its own wait on K3 (which replays the
+  // column it reads, after GCOL cleared grad_w), so it runs beside K4 and
+  // waits for K4 only before it exits.
+  if (KIND != GW) pdl_wait();
 
   if (warp == 4) {
     if (lane == 0) {
@@ -230,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    pdl_release();
   } else if (warp == 5) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
@@ -252,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma_commit(done);
     }
+    pdl_release();
   } else {
     // -------------------------------------------------------------- epilogue (warps 0-3)
     if (KIND == GCOL) {
@@ -263,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const bool ok = mbar_wait(done, 0);
     tc_fence_after();
+    pdl_release();
     const int row = warp * 32 + lane;
     const int m = m0 + row;
     const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
@@ -332,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"((uint32_t)C::kTmemCols)
                  : "memory");
+  if (KIND == GW) pdl_wait();  // completes no earlier than K4
 }
 
 // ---------------------------------------------------------------- host side
@@ -374,9 +385,21 @@ cudaError_t launch(const CUtensorMap& A, const CUtensorMap& B, const TcArgs& a, 
   auto k = tc_gemm<KIND, BN>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, C::kSmem, s>>>(A, B, a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  // the forward GEMM follows K1 and the weight-gradient GEMM follows K4 in the
+  // same call: both may start their prologue early
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = KIND == GCOL ? 0 : 1;
+  e = cudaLaunchKernelEx(&cfg, k, A, B, a);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 // column buffer as a 3-D tensor {pixel (true extent), image, row}

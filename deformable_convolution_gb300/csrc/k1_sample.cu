@@ -374,6 +374,8 @@ __global__ void __launch_bounds__(kThreads) k1_band_sample(SampleArgs a, Plan pl
     __syncthreads();
   }
 
+  pdl_release();  // the forward GEMM may set up while the sampling runs
+
   // ---------------------------------------------------------------- slow-path count
   if (a.slow_count && rank == 0) {
     unsigned long long local = 0;

@@ -263,6 +263,10 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
     }
   }
   __syncthreads();
+  // x and the offsets come from the forward call; gcol and the cleared
+  // grad_x / offset-gradient buffers come from the GCOL GEMM just before
+  pdl_wait();
+  pdl_release();
 
   // ---------------------------------------------------------------- sampling backward
   {
@@ -422,8 +426,11 @@ cudaError_t launch_t(const BwdArgs& a, const Plan& pl, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = s;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, kern, a, pl);
   note_launches(1);
   return e;

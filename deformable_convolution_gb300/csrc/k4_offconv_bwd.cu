@@ -265,6 +265,10 @@ __global__ void __launch_bounds__(kThreads) k4_offconv_bwd(OffconvBwdArgs a, Pla
   }
   band::stage_window<T>(x, g, img, c_begin, pl.cpc, ylo, xlo, pl.rows, pl.cols, PL, xw);
   for (int idx = tid; idx < pl.cpc * PL; idx += kThreads) gxs[idx] = 0.f;
+  // the offset gradient is K3's output; grad_x / grad_w_off / grad_b_off were
+  // cleared by the GCOL GEMM before K3 started
+  pdl_wait();
+  pdl_release();
 
   if (tensor) {
     // positions of the band's pixels in the staged window (padding -> 0)
@@ -474,10 +478,19 @@ cudaError_t launch_t(const OffconvBwdArgs& a, const Plan& pl, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)pl.smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)(pl.nslices * pl.tiles_w), (unsigned)pl.tiles_h, (unsigned)a.g.n);
-  kern<<<grid, kThreads, pl.smem, s>>>(a, pl);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(pl.nslices * pl.tiles_w), (unsigned)pl.tiles_h, (unsigned)a.g.n);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kern, a, pl);
   note_launches(1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
