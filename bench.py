@@ -35,9 +35,14 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 # dram__bytes_write.sum), keyed by (workload, kernel); valid only while the
 # kernel's source file hashes to the recorded value (else reported as null).
 TRAFFIC = {
-    # ncu --set full of k1_band_sample, res3 bf16 (profiles/k1_band_sample_res3_bf16.md):
-    # the deformed map and the offsets stay in L2, only x is read from DRAM
-    ("res3_bf16", "k1_band_sample"): {"bytes": 2176000 + 768, "source": "779e1724db30fbf1"},
+    # ncu --set full, res3 bf16, one launch each (profiles/<kernel>_res3_bf16.md,
+    # profiles/tc_gemm_res3_bf16.md).  Writes mostly stay in the 129 MB L2.
+    ("res3_bf16", "k1_band_sample"): {"bytes": 2176256, "source": "9c5ad9459c81675a"},
+    ("res3_bf16", "k3_band_bwd"): {"bytes": 34691840 + 5888, "source": "ccb7bb3fdf278c8a"},
+    ("res3_bf16", "k4_offconv_bwd"): {"bytes": 5482752, "source": "1190cb609f794a95"},
+    ("res3_bf16", "gemm_fwd"): {"bytes": 14764800, "source": "38ef6860e950b566"},
+    ("res3_bf16", "gemm_gcol"): {"bytes": 2045184 + 106240, "source": "38ef6860e950b566"},
+    ("res3_bf16", "gemm_gw"): {"bytes": 16665600, "source": "38ef6860e950b566"},
 }
 KERNEL_SOURCES = {
     "k1_band_sample": "k1_sample.cu", "k3_band_bwd": "k3_band_bwd.cu",
@@ -345,14 +350,17 @@ def kernel_costs(p, has_add):
     x_b = p.n * p.c_in * p.h * p.w * elt
     off_b = p.n_off * P * 4
     gemm = 2.0 * p.c_out * kdim * P
-    k3 = (x_b + off_b + kdim * P * 4 + p.n_off * kdim * elt      # read x, offsets, gcol, w_off
-          + p.n * p.c_in * p.h * p.w * 4 + off_b + kdim * P * elt  # write grad_x, grad_offset, map
-          + p.n_off * kdim * 4)                                     # write grad_w_off
+    gx_b = p.n * p.c_in * p.h * p.w * 4
+    k3 = (x_b + off_b + kdim * P * 4       # read x, offsets, gcol
+          + gx_b + off_b + kdim * P * elt)  # write grad_x, grad_offset, replayed map
+    k4 = (x_b + off_b + p.n_off * kdim * elt  # read x, grad_offset, w_off
+          + 2 * gx_b                          # add into grad_x (read + write)
+          + p.n_off * (kdim + 1) * 4)         # write grad_w_off, grad_b_off
     return {
         "k1_band_sample": ("hbm", k1_bytes(p, has_add)),
         "gemm_fwd": ("tensor", gemm), "gemm_gcol": ("tensor", gemm), "gemm_gw": ("tensor", gemm),
         "k3_band_bwd": ("hbm", k3),
-        "memsets": ("hbm", 4 * (p.n * p.c_in * p.h * p.w + p.c_out * kdim + p.n_off * kdim + p.n_off)),
+        "k4_offconv_bwd": ("hbm", k4),
     }
 
 
