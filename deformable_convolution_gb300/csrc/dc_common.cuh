@@ -185,5 +185,9 @@ struct OffconvBwdArgs {
 };
 cudaError_t launch_offconv_bwd(const OffconvBwdArgs& a, dc_dtype dt, cudaStream_t s);
 size_t offconv_bwd_smem_bytes(const Geom& g, dc_dtype dt);
+// tensor-core variant (bf16, few offset channels), chosen by launch_offconv_bwd
+bool offconv_bwd_tc_supported(const Geom& g, dc_dtype dt);
+size_t offconv_bwd_tc_smem_bytes(const Geom& g);
+cudaError_t launch_offconv_bwd_tc(const OffconvBwdArgs& a, cudaStream_t s);
 
 }  // namespace dc

@@ -1,0 +1,415 @@
+// K4 on tensor cores: backward of the offset convolution ("Following a
+// deformable layer through DefT", Step 1 of 5, on the explainer page "DefT:
+// Boosting Scalability of Deformable Convolution Operations on GPUs") for bf16
+// problems with at most kMaxM offset channels.  With goff the completed
+// gradient of the offset convolution's output (summed over all channels by K3)
+// and one CTA per (band of output rows, slice of 16 input channels):
+//
+//   weight part  gw_off[m][c][k] += sum_px X[c,k][px] * goff[m][px]
+//                X[c,k][px] = x[c] at the window position tap k of pixel px reads
+//                (M = 16 channels of one tap, N = offset channels, K = pixels)
+//   input part   grad_x[c][q]   += sum_(k,m) w_off[m][c][k] * goff[m][px(q,k)]
+//                px(q,k) = the band pixel whose tap k reads window position q
+//                (M = 16 channels, N = window positions, K = (tap, offset channel))
+//   bias         gb_off[m]      += sum_px goff[m][px]   (slice 0 only)
+//
+// Both parts are dense mma.sync m16n8k16 contractions (bf16 operands, fp32
+// accumulation).  The input part is written as a gather over window positions
+// (the im2col of goff), so every grad_x element of the window is produced once
+// in registers and added to global memory with one atomic: there is no shared
+// grad_x window and no shared-memory atomic.  Every fragment register is one
+// 32-bit shared load: goff is packed twice (pixel pairs [m][px/2], offset-
+// channel pairs [px][m/2]), w_off^T as [(k,c)][m/2], and the input window as
+// pixel-pair words (x[q], x[q + stride]) so that the two pixels a register
+// holds are one word whenever they lie in the same band row.
+#include "dc_band.cuh"
+
+namespace dc {
+namespace {
+
+using band::kThreads;
+constexpr int kCpc = 16;  // channels per CTA: one mma row tile
+constexpr int kMaxM = 80;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMChunk = 5;  // offset-channel n-tiles per pass of the weight part
+constexpr int kQGroup = 2;  // window-position n-tiles per unit of the input part
+
+struct TcPlan {
+  int R, TW, tiles_w, tiles_h, npx, nslices;
+  int rows, cols, npos, nq;  // window (receptive field), positions, rounded to 8
+  int xplane;                // words per channel plane of the pair-packed window
+  int pxp, mp8, mp16;        // pixels to 16, offset channels to 8 and 16
+  int sa, sb, sw;            // word strides of ga [m][px/2], gb [px][m/2], wa [(k,c)][m/2]
+  size_t off_xp, off_goff, off_ga, off_gb, off_wa, off_pxq, off_pair, smem;
+};
+
+__host__ TcPlan make_tc_plan(const Geom& g, int px) {
+  const band::Shape sh = band::make_shape(g, 0, px);
+  TcPlan p{};
+  p.R = sh.R;
+  p.TW = sh.TW;
+  p.npx = sh.npx;
+  p.tiles_w = sh.tiles_w;
+  p.tiles_h = sh.tiles_h;
+  p.nslices = (g.c_in + kCpc - 1) / kCpc;
+  p.rows = sh.rows;
+  p.cols = sh.cols;
+  p.npos = sh.rows * sh.cols;
+  p.nq = (p.npos + 7) / 8 * 8;
+  p.xplane = band::pad_plane(p.npos);
+  p.pxp = (p.npx + 15) / 16 * 16;
+  p.mp8 = (g.M + 7) / 8 * 8;
+  p.mp16 = (g.M + 15) / 16 * 16;
+  p.sa = p.pxp / 2 + 4;
+  p.sb = p.mp16 / 2 + 4;
+  p.sw = p.mp16 / 2 + 4;
+  size_t at = 0;
+  p.off_xp = at;
+  at += (size_t)kCpc * p.xplane * 4;
+  p.off_goff = at;
+  at += (size_t)g.M * p.pxp * 4;
+  p.off_ga = at;
+  at += (size_t)p.mp8 * p.sa * 4;
+  p.off_gb = at;
+  at += (size_t)(p.pxp + 1) * p.sb * 4;  // last row: zeros (positions no pixel reaches)
+  p.off_wa = at;
+  at += (size_t)g.K * kCpc * p.sw * 4;
+  p.off_pair = at;
+  at += (size_t)(p.pxp / 2) * 8;
+  p.off_pxq = at;
+  at += ((size_t)g.K * p.nq * 2 + 15) / 16 * 16;
+  p.smem = at;
+  return p;
+}
+
+// Largest band that keeps three CTAs per SM, else two, else the smallest.
+__host__ TcPlan pick_tc_plan(const Geom& g) {
+  const size_t budgets[2] = {72 * 1024, 110 * 1024};
+  for (size_t budget : budgets)
+    for (int px = band::kBandPx; px >= 32; px /= 2) {
+      const TcPlan p = make_tc_plan(g, px);
+      if (p.smem <= budget) return p;
+    }
+  return make_tc_plan(g, 32);
+}
+
+__device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// The two input values of a pixel pair (2j, 2j+1) at tap offset `tap` as one
+// bf16-pair register.  e.x / e.y: window positions of the two pixels (-1 for
+// a padding pixel).  When the pair lies in one band row the word at e.x
+// already holds both (its high half is the value one column stride further).
+__device__ __forceinline__ uint32_t x_pair(const uint32_t* plane, int2 e, int tap, int sw) {
+  if (e.x < 0) return 0u;
+  uint32_t w = plane[e.x + tap];
+  if (e.y < 0) return w & 0xffffu;
+  if (e.y != e.x + sw) w = (w & 0xffffu) | (plane[e.y + tap] << 16);
+  return w;
+}
+
+__global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs a, TcPlan pl) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const Geom g = a.g;
+  const __nv_bfloat16* __restrict__ x = static_cast<const __nv_bfloat16*>(a.x);
+  const unsigned short* __restrict__ w_off = static_cast<const unsigned short*>(a.w_off);
+  const int slice = (int)(blockIdx.x % pl.nslices);
+  const int tw_idx = (int)(blockIdx.x / pl.nslices);
+  const int ho0 = blockIdx.y * pl.R, wo0 = tw_idx * pl.TW;
+  const int n = blockIdx.z;
+  const int c_begin = slice * kCpc;
+  const int ncur = min(g.c_in, c_begin + kCpc) - c_begin;
+  const int ylo = ho0 * g.sh - g.ph, xlo = wo0 * g.sw - g.pw;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int M = g.M, K = g.K;
+  const long long img = (long long)n * g.c_in * g.hw;
+
+  uint32_t* xp = reinterpret_cast<uint32_t*>(smem + pl.off_xp);      // [kCpc][xplane]
+  float* gt = reinterpret_cast<float*>(smem + pl.off_goff);          // [M][pxp]
+  uint32_t* ga = reinterpret_cast<uint32_t*>(smem + pl.off_ga);      // [mp8][sa]
+  uint32_t* gb = reinterpret_cast<uint32_t*>(smem + pl.off_gb);      // [pxp + 1][sb]
+  uint32_t* wa = reinterpret_cast<uint32_t*>(smem + pl.off_wa);      // [K * kCpc][sw]
+  int2* pair = reinterpret_cast<int2*>(smem + pl.off_pair);          // [pxp / 2]
+  unsigned short* pxq = reinterpret_cast<unsigned short*>(smem + pl.off_pxq);  // [K][nq]
+
+  // ---------------------------------------------------------------- prologue (inputs only)
+  // pixel-pair table: window positions of pixels 2j and 2j+1
+  for (int j = tid; j < pl.pxp / 2; j += kThreads) {
+    int2 e = make_int2(-1, -1);
+    const int p = 2 * j;
+    if (p < pl.npx) {
+      const int r = p / pl.TW, c = p - r * pl.TW;
+      e.x = r * g.sh * pl.cols + c * g.sw;
+      if (p + 1 < pl.npx) {
+        const int r1 = (p + 1) / pl.TW, c1 = p + 1 - r1 * pl.TW;
+        e.y = r1 * g.sh * pl.cols + c1 * g.sw;
+      }
+    }
+    pair[j] = e;
+  }
+  // px(q, k): the band pixel whose tap k reads window position q (pxp: none)
+  {
+    band::Walk2 w;
+    w.init(tid, kThreads, pl.nq);
+    while (w.a < K) {
+      const int k = w.a, q = w.b;
+      w.next();
+      int px = pl.pxp;
+      if (q < pl.npos) {
+        const int i = k / g.kw, j = k - i * g.kw;
+        const int qr = q / pl.cols, qc = q - qr * pl.cols;
+        const int r = qr - i * g.dh, c = qc - j * g.dw;
+        if (r >= 0 && c >= 0 && r % g.sh == 0 && c % g.sw == 0 && r / g.sh < pl.R &&
+            c / g.sw < pl.TW)
+          px = (r / g.sh) * pl.TW + c / g.sw;
+      }
+      pxq[k * pl.nq + q] = (unsigned short)px;
+    }
+  }
+  // input window of the slice as pixel-pair words (x[q], x[q + column stride]),
+  // zero outside the image and beyond c_in
+  {
+    constexpr int kB = 8;
+    const int total = kCpc * pl.npos;
+    band::Walk3 w;
+    w.init(tid, kThreads, pl.rows, pl.cols);
+    for (int base = tid; base < total; base += kThreads * kB) {
+      uint32_t v[kB];
+      int at[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        v[u] = 0u;
+        at[u] = -1;
+        if (w.a < kCpc) {
+          at[u] = w.a * pl.xplane + w.b * pl.cols + w.c;
+          const int c = c_begin + w.a, yy = ylo + w.b, xx = xlo + w.c;
+          if (c < g.c_in && yy >= 0 && yy < g.h) {
+            const __nv_bfloat16* row = x + img + (long long)c * g.hw + (long long)yy * g.w;
+            if (xx >= 0 && xx < g.w) v[u] = band::bf16_bits(row + xx);
+            if (xx + g.sw >= 0 && xx + g.sw < g.w) v[u] |= band::bf16_bits(row + xx + g.sw) << 16;
+          }
+          w.next();
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kB; ++u)
+        if (at[u] >= 0) xp[at[u]] = v[u];
+    }
+  }
+  // w_off^T as [(k, c)][offset-channel pair] words, zero for m >= M or c >= c_in
+  {
+    constexpr int kB = 4;
+    const int wpr = pl.mp16 / 2;  // words per row
+    const int total = K * kCpc * wpr;
+    const long long mstride = (long long)g.c_in * K;
+    band::Walk2 w;
+    w.init(tid, kThreads, wpr);
+    for (int base = tid; base < total; base += kThreads * kB) {
+      unsigned short lo[kB], hi[kB];
+      int at[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        lo[u] = hi[u] = 0;
+        at[u] = -1;
+        if (w.a < K * kCpc) {
+          const int row = w.a, j = w.b;
+          const int k = row / kCpc, cl = row - k * kCpc;
+          at[u] = row * pl.sw + j;
+          if (cl < ncur) {
+            const long long o = (long long)(c_begin + cl) * K + k;
+            if (2 * j < M) lo[u] = w_off[(2 * j) * mstride + o];
+            if (2 * j + 1 < M) hi[u] = w_off[(2 * j + 1) * mstride + o];
+          }
+          w.next();
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kB; ++u)
+        if (at[u] >= 0) wa[at[u]] = (uint32_t)lo[u] | ((uint32_t)hi[u] << 16);
+    }
+  }
+  // the offset gradient is K3's output; grad_x / grad_w_off / grad_b_off were
+  // cleared by the GCOL GEMM before K3 started
+  pdl_wait();
+  pdl_release();
+
+  // ---------------------------------------------------------------- the band's offset gradient
+  {
+    constexpr int kB = 8;
+    const int total = M * pl.pxp;
+    band::Walk2 w;
+    w.init(tid, kThreads, pl.pxp);
+    for (int base = tid; base < total; base += kThreads * kB) {
+      float v[kB];
+      int at[kB];
+#pragma unroll
+      for (int u = 0; u < kB; ++u) {
+        v[u] = 0.f;
+        at[u] = -1;
+        if (w.a < M) {
+          const int m = w.a, px = w.b;
+          at[u] = m * pl.pxp + px;
+          if (px < pl.npx) {
+            const int r = px / pl.TW;
+            const int ho = ho0 + r, wo = wo0 + px - r * pl.TW;
+            if (ho < g.ho && wo < g.wo)
+              v[u] = a.goff[((long long)n * M + m) * g.howo + (long long)ho * g.wo + wo];
+          }
+          w.next();
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kB; ++u)
+        if (at[u] >= 0) gt[at[u]] = v[u];
+    }
+  }
+  __syncthreads();
+  // packed copies: ga [m][pixel pair] (zero rows m >= M), gb [pixel][offset-channel
+  // pair] (zero row pxp), and the bias gradient from the fp32 values
+  for (int idx = tid; idx < pl.mp8 * (pl.pxp / 2); idx += kThreads) {
+    const int m = idx / (pl.pxp / 2), j = idx - m * (pl.pxp / 2);
+    ga[m * pl.sa + j] = m < M ? pack2(gt[m * pl.pxp + 2 * j], gt[m * pl.pxp + 2 * j + 1]) : 0u;
+  }
+  for (int idx = tid; idx < (pl.pxp + 1) * (pl.mp16 / 2); idx += kThreads) {
+    const int px = idx / (pl.mp16 / 2), j = idx - px * (pl.mp16 / 2);
+    float lo = 0.f, hi = 0.f;
+    if (px < pl.pxp) {
+      if (2 * j < M) lo = gt[(2 * j) * pl.pxp + px];
+      if (2 * j + 1 < M) hi = gt[(2 * j + 1) * pl.pxp + px];
+    }
+    gb[px * pl.sb + j] = pack2(lo, hi);
+  }
+  if (a.gb_off && slice == 0) {
+    for (int m = warp; m < M; m += kWarps) {
+      float s = 0.f;
+      for (int px = lane; px < pl.npx; px += 32) s += gt[m * pl.pxp + px];
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) atomicAdd(a.gb_off + m, s);
+    }
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- both contractions
+  // work units, round robin over the warps: K weight-part units (one tap each)
+  // then the input part in groups of kQGroup position tiles
+  const int qtiles = pl.nq / 8;
+  const int qunits = (qtiles + kQGroup - 1) / kQGroup;
+  const int mtiles8 = pl.mp8 / 8;
+  const int ksteps = pl.pxp / 16;
+  for (int unit = warp; unit < K + qunits; unit += kWarps) {
+    if (unit < K) {
+      // ---- weight part, tap k: rows = 16 channels, columns = offset channels
+      const int k = unit;
+      const int i = k / g.kw;
+      const int tap = i * g.dh * pl.cols + (k - i * g.kw) * g.dw;
+      const uint32_t* p0 = xp + gid * pl.xplane;
+      const uint32_t* p1 = xp + (gid + 8) * pl.xplane;
+      for (int mt0 = 0; mt0 < mtiles8; mt0 += kMChunk) {
+        float acc[kMChunk][4];
+#pragma unroll
+        for (int t = 0; t < kMChunk; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+        for (int ks = 0; ks < ksteps; ++ks) {
+          const int2 e0 = pair[ks * 8 + tig], e1 = pair[ks * 8 + tig + 4];
+          const uint32_t a0 = x_pair(p0, e0, tap, g.sw), a1 = x_pair(p1, e0, tap, g.sw);
+          const uint32_t a2 = x_pair(p0, e1, tap, g.sw), a3 = x_pair(p1, e1, tap, g.sw);
+#pragma unroll
+          for (int t = 0; t < kMChunk; ++t) {
+            if (mt0 + t >= mtiles8) break;
+            const uint32_t* b = ga + ((mt0 + t) * 8 + gid) * pl.sa + ks * 8 + tig;
+            mma16816(acc[t], a0, a1, a2, a3, b[0], b[4]);
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < kMChunk; ++t) {
+          if (mt0 + t >= mtiles8) break;
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int cl = gid + (h >> 1) * 8;
+            const int m = (mt0 + t) * 8 + 2 * tig + (h & 1);
+            if (cl < ncur && m < M)
+              atomicAdd(a.gw_off + ((long long)m * g.c_in + c_begin + cl) * K + k, acc[t][h]);
+          }
+        }
+      }
+    } else {
+      // ---- input part: rows = 16 channels, columns = window positions,
+      // reduction over (tap, offset channel)
+      const int nt0 = (unit - K) * kQGroup;
+      float acc[kQGroup][4];
+#pragma unroll
+      for (int t = 0; t < kQGroup; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+      for (int k = 0; k < K; ++k) {
+        int prow[kQGroup];
+#pragma unroll
+        for (int t = 0; t < kQGroup; ++t)
+          prow[t] = nt0 + t < qtiles ? (int)pxq[k * pl.nq + (nt0 + t) * 8 + gid] * pl.sb : pl.pxp * pl.sb;
+        const uint32_t* ar = wa + (k * kCpc + gid) * pl.sw + tig;
+        for (int mc = 0; mc < pl.mp16 / 16; ++mc) {
+          const uint32_t a0 = ar[mc * 8], a2 = ar[mc * 8 + 4];
+          const uint32_t a1 = ar[8 * pl.sw + mc * 8], a3 = ar[8 * pl.sw + mc * 8 + 4];
+#pragma unroll
+          for (int t = 0; t < kQGroup; ++t) {
+            const uint32_t* b = gb + prow[t] + mc * 8 + tig;
+            mma16816(acc[t], a0, a1, a2, a3, b[0], b[4]);
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kQGroup; ++t) {
+        if (nt0 + t >= qtiles) break;
+#pragma unroll
+        for (int hc = 0; hc < 2; ++hc) {
+          const int q = (nt0 + t) * 8 + 2 * tig + hc;
+          if (q >= pl.npos) continue;
+          const int qr = q / pl.cols, qc = q - qr * pl.cols;
+          const int yy = ylo + qr, xx = xlo + qc;
+          if (yy < 0 || yy >= g.h || xx < 0 || xx >= g.w) continue;
+          float* dst = a.gx + img + (long long)c_begin * g.hw + (long long)yy * g.w + xx;
+          if (gid < ncur && acc[t][hc] != 0.f) atomicAdd(dst + (long long)gid * g.hw, acc[t][hc]);
+          if (gid + 8 < ncur && acc[t][2 + hc] != 0.f)
+            atomicAdd(dst + (long long)(gid + 8) * g.hw, acc[t][2 + hc]);
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+bool offconv_bwd_tc_supported(const Geom& g, dc_dtype dt) { return dt == DC_BF16 && g.M <= kMaxM; }
+
+size_t offconv_bwd_tc_smem_bytes(const Geom& g) { return pick_tc_plan(g).smem; }
+
+cudaError_t launch_offconv_bwd_tc(const OffconvBwdArgs& a, cudaStream_t s) {
+  const TcPlan pl = pick_tc_plan(a.g);
+  cudaError_t e = cudaFuncSetAttribute(k4_offconv_bwd_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)pl.smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(pl.nslices * pl.tiles_w), (unsigned)pl.tiles_h, (unsigned)a.g.n);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k4_offconv_bwd_tc, a, pl);
+  note_launches(1);
+  return e;
+}
+
+}  // namespace dc
