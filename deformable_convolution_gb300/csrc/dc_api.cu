@@ -126,7 +126,8 @@ dc_status make_geom(const dc_problem* p, Geom* g, int* margin) {
 // to a multiple of 8 elements so that every row starts 16-byte aligned.
 struct Plan {
   ColLayout col, gcol;
-  size_t col_off, gcol_off, off_off, total;
+  size_t col_off, gcol_off, off_off, gmax_off, total;
+  int gmax_tx, gmax_ty;
 };
 
 Plan make_plan(const Geom& g, dc_dtype dt, int backward) {
@@ -144,6 +145,10 @@ Plan make_plan(const Geom& g, dc_dtype dt, int backward) {
   pl.col_off = take((size_t)g.kdim * pl.col.row * elt_size(dt));
   pl.off_off = take((size_t)g.n * g.M * g.howo * sizeof(float));
   pl.gcol_off = backward ? take((size_t)g.kdim * pl.gcol.row * sizeof(float)) : 0;
+  // per-tile max |gcol| written by the tensor-core GCOL GEMM (128 x 128 tiles)
+  pl.gmax_tx = (int)ceil_div_ll(g.howo, 128);
+  pl.gmax_ty = (int)ceil_div_ll(g.kdim, 128);
+  pl.gmax_off = backward ? take((size_t)g.n * pl.gmax_tx * pl.gmax_ty * 4 * sizeof(float)) : 0;
   pl.total = at;
   return pl;
 }
@@ -269,6 +274,10 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
   ga.zero.n[3] = grad_b_off ? g.M : 0;
   ga.zero.p[4] = goff;
   ga.zero.n[4] = (long long)g.n * g.M * g.howo;
+  // the tensor-core GCOL GEMM also reports max |gcol| per tile, from which K3
+  // scales its fixed-point grad_x accumulation
+  const bool tc_gcol = prob->dtype == DC_BF16 && tc_gemm_supported(g);
+  ga.gmax = tc_gcol ? reinterpret_cast<float*>(wsb + pl.gmax_off) : nullptr;
   st = cuda_status(timed("gemm_gcol", s, [&] { return launch_gemm_gcol(ga, prob->dtype, s); }));
   if (st != DC_OK) return st;
 
@@ -284,6 +293,9 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
   ba.gx = grad_x;
   ba.goff = goff;
   ba.margin = margin;
+  ba.gmax = ga.gmax;
+  ba.gmax_tx = pl.gmax_tx;
+  ba.gmax_ty = pl.gmax_ty;
   st = cuda_status(timed("k3_band_bwd", s, [&] { return launch_band_bwd(ba, prob->dtype, s); }));
   if (st != DC_OK) return st;
 

@@ -144,6 +144,7 @@ struct GemmArgs {
   ColLayout gcol_layout;
   float* gw;          // [c_out][kdim] fp32, accumulated with atomics (backward)
   ZeroArgs zero;      // GCOL kernels clear these (the backward's atomic targets)
+  float* gmax;        // tensor-core GCOL: max |gcol| per 128 x 128 tile (4 floats each), or null
 };
 // Tensor-core (tcgen05, bf16) versions; need tc_gemm_supported(g).
 bool tc_gemm_supported(const Geom& g);
@@ -168,6 +169,11 @@ struct BwdArgs {
   float* gx;
   float* goff;
   int margin;
+  // max |gcol| per 128 x 128 tile of the GCOL GEMM (4 floats per tile, tiles
+  // [image][row tile][pixel tile]); when given, K3 accumulates its grad_x window
+  // in fixed point scaled from it, else in float
+  const float* gmax;
+  int gmax_tx, gmax_ty;  // pixel tiles per image, row tiles
 };
 cudaError_t launch_band_bwd(const BwdArgs& a, dc_dtype dt, cudaStream_t s);
 size_t bwd_smem_bytes(const Geom& g, dc_dtype dt, int margin);

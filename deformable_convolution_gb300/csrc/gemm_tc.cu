@@ -43,7 +43,14 @@ struct TcArgs {
   void* out;
   long long out_row, out_img;  // GCOL: gcol pitches (elements)
   ZeroArgs zero;               // GCOL: the backward's atomic targets, cleared by warps 0-3
+  float* gmax;                 // GCOL: max |gcol| of each tile, one float per epilogue warp
 };
+
+// |v|, or +inf when v is not finite (so that a NaN is not lost by fmaxf)
+__device__ __forceinline__ float abs_or_inf(float v) {
+  const float m = fabsf(v);
+  return m <= 3.402823466e38f ? m : __int_as_float(0x7f800000);
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -276,6 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = warp * 32 + lane;
     const int m = m0 + row;
     const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
+    float amax = 0.f;  // GCOL: largest |value| this thread stores (+inf if not finite)
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t r[32];
@@ -314,10 +322,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<float4*>(dst + v * 4) =
                 make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
                             __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+#pragma unroll
+          for (int j = 0; j < 32; ++j) amax = fmaxf(amax, abs_or_inf(__uint_as_float(r[j])));
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (n_first + j < a.howo) dst[j] = __uint_as_float(r[j]);
+            if (n_first + j < a.howo) {
+              dst[j] = __uint_as_float(r[j]);
+              amax = fmaxf(amax, abs_or_inf(__uint_as_float(r[j])));
+            }
         }
       } else {
         if (m >= a.c_out) continue;
@@ -334,6 +347,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (n_first + j < a.kdim) atomicAdd(dst + j, __uint_as_float(r[j]));
         }
       }
+    }
+    if (KIND == GCOL && a.gmax) {
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const long long tile = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * z);
+      if (lane == 0) a.gmax[tile * 4 + warp] = amax;
     }
   }
   tc_fence_before();
@@ -470,6 +488,7 @@ cudaError_t launch_gemm_gcol_tc(const GemmArgs& ga, cudaStream_t s) {
   a.out_row = ga.gcol_layout.row;
   a.out_img = ga.gcol_layout.img;
   a.zero = ga.zero;
+  a.gmax = ga.gmax;
   dim3 grid((unsigned)ceil_div_ll(g.howo, 128), (unsigned)ceil_div_ll(g.kdim, kBM), (unsigned)g.n);
   return launch<GCOL, 128>(A, B, a, grid, s);
 }

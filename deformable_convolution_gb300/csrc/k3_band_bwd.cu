@@ -101,6 +101,12 @@ __device__ __forceinline__ void gadd(float* plane, const Geom& g, int y, int x, 
 }
 
 __device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
+
+// round(ws * gc) as an int, for |ws * gc| < 2^22: adding 1.5 * 2^23 puts the
+// rounded integer in the low mantissa bits (one rounding, to nearest even)
+__device__ __forceinline__ int to_fixed(float ws, float gc) {
+  return __float_as_int(__fmaf_rn(ws, gc, 12582912.0f)) - 0x4B400000;
+}
 __device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // Sampling backward of one on-chip tap over `count` consecutive channels of
@@ -109,7 +115,7 @@ __device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w 
 // sdy/sdx and scatters the corner weights times gcol into the grad_x window
 // (shared-memory atomics).  Loads of a batch of channels are issued before any
 // of the batch's atomics.  bf16: channel pairs share one corner word load.
-template <typename T>
+template <typename T, bool kFixed>
 __device__ __forceinline__ void band_bwd_run(const uint32_t* __restrict__ xw, int PL, int cols,
                                              int sbase, int cl0, int count,
                                              const float* __restrict__ gp, long long gstride,
@@ -123,11 +129,21 @@ __device__ __forceinline__ void band_bwd_run(const uint32_t* __restrict__ xw, in
     if (cp) cp[(long long)ch * cstride] = from_f<T>(blend4(ly, lx, v00, v01, v10, v11));
   };
   auto scatter = [&](float gc, int ch) {
-    float* q = gxp + ch * PL;
-    atomicAdd(q, w00 * gc);
-    atomicAdd(q + 1, w01 * gc);
-    atomicAdd(q + cols, w10 * gc);
-    atomicAdd(q + cols + 1, w11 * gc);
+    if (kFixed) {
+      // fixed point: the weights arrive pre-scaled; integer shared-memory
+      // atomics are several times faster than float ones
+      int* q = reinterpret_cast<int*>(gxp) + ch * PL;
+      atomicAdd(q, to_fixed(w00, gc));
+      atomicAdd(q + 1, to_fixed(w01, gc));
+      atomicAdd(q + cols, to_fixed(w10, gc));
+      atomicAdd(q + cols + 1, to_fixed(w11, gc));
+    } else {
+      float* q = gxp + ch * PL;
+      atomicAdd(q, w00 * gc);
+      atomicAdd(q + 1, w01 * gc);
+      atomicAdd(q + cols, w10 * gc);
+      atomicAdd(q + cols + 1, w11 * gc);
+    }
   };
   int ch = 0;
   if (sizeof(T) == 2) {
@@ -203,9 +219,10 @@ __device__ __forceinline__ void band_bwd_run(const uint32_t* __restrict__ xw, in
 }
 
 
-template <typename T>
+template <typename T, bool kFixed>
 __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
   extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int s_gmax;
   const Geom g = a.g;
   const T* __restrict__ x = static_cast<const T*>(a.x);
   T* __restrict__ col = static_cast<T*>(a.col);
@@ -246,7 +263,10 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
   band::stage_window<T>(x, g, img, c_begin, pl.cpc, ylo, xlo, pl.rows, pl.cols, PL, xw);
   for (int idx = tid; idx < pl.cpc * PL; idx += kThreads) gxs[idx] = 0.f;
   for (int idx = tid; idx < M * PS; idx += kThreads) part[idx] = 0.f;
-  if (tid == 0) *nslow = 0;
+  if (tid == 0) {
+    *nslow = 0;
+    s_gmax = 0;
+  }
   __syncthreads();
   {
     band::Walk2 w;
@@ -267,6 +287,42 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
   // grad_x / offset-gradient buffers come from the GCOL GEMM just before
   pdl_wait();
   pdl_release();
+
+  // fixed-point scale of the grad_x window: every contribution is
+  // |corner weight * gcol| <= G (the largest |gcol| of the GCOL tiles that
+  // cover this slice's rows and this band's pixels, weights <= 1), and a
+  // window element receives at most K * npx of them.  2^S keeps every sum
+  // below 2^30 and every single contribution below 2^21 (the range of
+  // to_fixed); the rounding error per contribution is 2^-(S+1) <= G * 2^-22.
+  float fscale = 1.f, finv = 1.f;
+  bool poison = false;  // a non-finite gcol in range: the window flushes NaN
+  if (kFixed) {
+    const int ty0 = (c_begin * g.K) / 128, ty1 = (c_end * g.K - 1) / 128;
+    const int p_lo = ho0 * g.wo + wo0;
+    const int p_hi = (min(ho0 + pl.R, g.ho) - 1) * g.wo + min(wo0 + pl.TW, g.wo) - 1;
+    const int tx0 = p_lo / 128, tx1 = p_hi / 128;
+    const int ntx = tx1 - tx0 + 1, nent = (ty1 - ty0 + 1) * ntx * 4;
+    for (int i = tid; i < nent; i += kThreads) {
+      const int e = i & 3, r = i >> 2;
+      const int ty = ty0 + r / ntx, tx = tx0 + r - (r / ntx) * ntx;
+      const float v = a.gmax[(((long long)n * a.gmax_ty + ty) * a.gmax_tx + tx) * 4 + e];
+      atomicMax(&s_gmax, __float_as_int(v));  // non-negative floats order like their bits
+    }
+    __syncthreads();
+    const float G = __int_as_float(s_gmax);
+    if (!(G <= 3.402823466e38f)) {
+      poison = true;
+    } else {
+      int eg;
+      frexpf(G, &eg);  // G < 2^eg
+      const int units = g.K * npx;
+      const int lg = 32 - __clz(units > 1 ? units - 1 : 1);  // ceil(log2(K * npx))
+      int S = min(30 - (eg + lg), 21 - eg);
+      S = max(-126, min(126, S));
+      fscale = ldexpf(1.0f, S);
+      finv = ldexpf(1.0f, -S);
+    }
+  }
 
   // ---------------------------------------------------------------- sampling backward
   {
@@ -332,8 +388,13 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
           const float* gp = grow + (long long)c * gstride;
           T* cp = crow ? crow + (long long)c * cstride : nullptr;
           float* gxp = gxs + (c - c_begin) * PL + sbase;
-          band_bwd_run<T>(xw, PL, pl.cols, sbase, c - c_begin, run_end - c, gp, gstride, cp,
-                          cstride, gxp, t.ly, t.lx, w00, w01, w10, w11, sdy, sdx);
+          if (kFixed)
+            band_bwd_run<T, true>(xw, PL, pl.cols, sbase, c - c_begin, run_end - c, gp, gstride, cp,
+                                  cstride, gxp, t.ly, t.lx, w00 * fscale, w01 * fscale,
+                                  w10 * fscale, w11 * fscale, sdy, sdx);
+          else
+            band_bwd_run<T, false>(xw, PL, pl.cols, sbase, c - c_begin, run_end - c, gp, gstride,
+                                   cp, cstride, gxp, t.ly, t.lx, w00, w01, w10, w11, sdy, sdx);
           c = run_end;
         }
         part[(2 * (gg * g.K + k)) * PS + px] = sdy;
@@ -409,15 +470,18 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
       w.next();
       const int yy = ylo + r, xx = xlo + q;
       if (yy < 0 || yy >= g.h || xx < 0 || xx >= g.w) continue;
-      const float v = gxs[cl * PL + r * pl.cols + q];
+      const int at = cl * PL + r * pl.cols + q;
+      const float v = kFixed ? (poison ? __int_as_float(0x7fc00000)
+                                       : (float)reinterpret_cast<const int*>(gxs)[at] * finv)
+                             : gxs[at];
       if (v != 0.f) atomicAdd(a.gx + img + (long long)(c_begin + cl) * g.hw + (long long)yy * g.w + xx, v);
     }
   }
 }
 
-template <typename T>
+template <typename T, bool kFixed>
 cudaError_t launch_t(const BwdArgs& a, const Plan& pl, cudaStream_t s) {
-  auto kern = k3_band_bwd<T>;
+  auto kern = k3_band_bwd<T, kFixed>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)pl.smem);
   if (e != cudaSuccess) return e;
@@ -444,7 +508,9 @@ size_t bwd_smem_bytes(const Geom& g, dc_dtype dt, int margin) {
 
 cudaError_t launch_band_bwd(const BwdArgs& a, dc_dtype dt, cudaStream_t s) {
   const Plan pl = make_plan(a.g, dt, a.margin);
-  return dt == DC_BF16 ? launch_t<__nv_bfloat16>(a, pl, s) : launch_t<float>(a, pl, s);
+  if (dt == DC_BF16)
+    return a.gmax ? launch_t<__nv_bfloat16, true>(a, pl, s) : launch_t<__nv_bfloat16, false>(a, pl, s);
+  return launch_t<float, false>(a, pl, s);
 }
 
 }  // namespace dc

@@ -32,7 +32,7 @@ constexpr int kCpc = 16;  // channels per CTA: one mma row tile
 constexpr int kMaxM = 80;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMChunk = 5;  // offset-channel n-tiles per pass of the weight part
-constexpr int kQGroup = 2;  // window-position n-tiles per unit of the input part
+constexpr int kQGroup = 4;  // window-position n-tiles per unit of the input part
 
 struct TcPlan {
   int R, TW, tiles_w, tiles_h, npx, nslices;
@@ -40,7 +40,7 @@ struct TcPlan {
   int xplane;                // words per channel plane of the pair-packed window
   int pxp, mp8, mp16;        // pixels to 16, offset channels to 8 and 16
   int sa, sb, sw;            // word strides of ga [m][px/2], gb [px][m/2], wa [(k,c)][m/2]
-  size_t off_xp, off_goff, off_ga, off_gb, off_wa, off_pxq, off_pair, smem;
+  size_t off_xp, off_ga, off_gb, off_wa, off_pair, off_gpos, smem;
 };
 
 __host__ TcPlan make_tc_plan(const Geom& g, int px) {
@@ -66,8 +66,6 @@ __host__ TcPlan make_tc_plan(const Geom& g, int px) {
   size_t at = 0;
   p.off_xp = at;
   at += (size_t)kCpc * p.xplane * 4;
-  p.off_goff = at;
-  at += (size_t)g.M * p.pxp * 4;
   p.off_ga = at;
   at += (size_t)p.mp8 * p.sa * 4;
   p.off_gb = at;
@@ -76,8 +74,8 @@ __host__ TcPlan make_tc_plan(const Geom& g, int px) {
   at += (size_t)g.K * kCpc * p.sw * 4;
   p.off_pair = at;
   at += (size_t)(p.pxp / 2) * 8;
-  p.off_pxq = at;
-  at += ((size_t)g.K * p.nq * 2 + 15) / 16 * 16;
+  p.off_gpos = at;
+  at += (size_t)p.pxp * 4;
   p.smem = at;
   return p;
 }
@@ -137,12 +135,11 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
   const long long img = (long long)n * g.c_in * g.hw;
 
   uint32_t* xp = reinterpret_cast<uint32_t*>(smem + pl.off_xp);      // [kCpc][xplane]
-  float* gt = reinterpret_cast<float*>(smem + pl.off_goff);          // [M][pxp]
   uint32_t* ga = reinterpret_cast<uint32_t*>(smem + pl.off_ga);      // [mp8][sa]
   uint32_t* gb = reinterpret_cast<uint32_t*>(smem + pl.off_gb);      // [pxp + 1][sb]
   uint32_t* wa = reinterpret_cast<uint32_t*>(smem + pl.off_wa);      // [K * kCpc][sw]
   int2* pair = reinterpret_cast<int2*>(smem + pl.off_pair);          // [pxp / 2]
-  unsigned short* pxq = reinterpret_cast<unsigned short*>(smem + pl.off_pxq);  // [K][nq]
+  int* gpos = reinterpret_cast<int*>(smem + pl.off_gpos);          // [pxp]
 
   // ---------------------------------------------------------------- prologue (inputs only)
   // pixel-pair table: window positions of pixels 2j and 2j+1
@@ -159,25 +156,18 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
     }
     pair[j] = e;
   }
-  // px(q, k): the band pixel whose tap k reads window position q (pxp: none)
-  {
-    band::Walk2 w;
-    w.init(tid, kThreads, pl.nq);
-    while (w.a < K) {
-      const int k = w.a, q = w.b;
-      w.next();
-      int px = pl.pxp;
-      if (q < pl.npos) {
-        const int i = k / g.kw, j = k - i * g.kw;
-        const int qr = q / pl.cols, qc = q - qr * pl.cols;
-        const int r = qr - i * g.dh, c = qc - j * g.dw;
-        if (r >= 0 && c >= 0 && r % g.sh == 0 && c % g.sw == 0 && r / g.sh < pl.R &&
-            c / g.sw < pl.TW)
-          px = (r / g.sh) * pl.TW + c / g.sw;
-      }
-      pxq[k * pl.nq + q] = (unsigned short)px;
+  // pixel -> offset within one goff plane (-1: padding or outside the output)
+  for (int px = tid; px < pl.pxp; px += kThreads) {
+    int v = -1;
+    if (px < pl.npx) {
+      const int r = px / pl.TW;
+      const int ho = ho0 + r, wo = wo0 + px - r * pl.TW;
+      if (ho < g.ho && wo < g.wo) v = ho * g.wo + wo;
     }
+    gpos[px] = v;
   }
+  // gb's last row stays zero: window positions that no pixel's tap reaches
+  for (int j = tid; j < pl.mp16 / 2; j += kThreads) gb[pl.pxp * pl.sb + j] = 0u;
   // input window of the slice as pixel-pair words (x[q], x[q + column stride]),
   // zero outside the image and beyond c_in
   {
@@ -245,58 +235,58 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
   pdl_wait();
   pdl_release();
 
+  __syncthreads();  // gpos
+
   // ---------------------------------------------------------------- the band's offset gradient
+  // packed straight from global memory: ga [m][pixel pair] (zero rows m >= M)
+  // and gb [pixel][offset-channel pair]; eight loads in flight per thread
   {
-    constexpr int kB = 8;
-    const int total = M * pl.pxp;
-    band::Walk2 w;
-    w.init(tid, kThreads, pl.pxp);
+    const float* gsrc = a.goff + (long long)n * M * g.howo;
+    const int wa_ = pl.pxp / 2, wb_ = pl.mp16 / 2;
+    const int nga = pl.mp8 * wa_, total = nga + pl.pxp * wb_;
+    auto gv = [&](int m, int px) {
+      const int o = gpos[px];
+      return (m < M && o >= 0) ? gsrc[(long long)m * g.howo + o] : 0.f;
+    };
+    constexpr int kB = 4;
     for (int base = tid; base < total; base += kThreads * kB) {
-      float v[kB];
+      float lo[kB], hi[kB];
       int at[kB];
 #pragma unroll
       for (int u = 0; u < kB; ++u) {
-        v[u] = 0.f;
+        const int idx = base + u * kThreads;
         at[u] = -1;
-        if (w.a < M) {
-          const int m = w.a, px = w.b;
-          at[u] = m * pl.pxp + px;
-          if (px < pl.npx) {
-            const int r = px / pl.TW;
-            const int ho = ho0 + r, wo = wo0 + px - r * pl.TW;
-            if (ho < g.ho && wo < g.wo)
-              v[u] = a.goff[((long long)n * M + m) * g.howo + (long long)ho * g.wo + wo];
-          }
-          w.next();
+        lo[u] = hi[u] = 0.f;
+        if (idx < nga) {
+          const int m = idx / wa_, j = idx - m * wa_;
+          at[u] = m * pl.sa + j;
+          lo[u] = gv(m, 2 * j);
+          hi[u] = gv(m, 2 * j + 1);
+        } else if (idx < total) {
+          const int r = idx - nga;
+          const int px = r / wb_, j = r - px * wb_;
+          at[u] = (1 << 30) | (px * pl.sb + j);
+          lo[u] = gv(2 * j, px);
+          hi[u] = gv(2 * j + 1, px);
         }
       }
 #pragma unroll
-      for (int u = 0; u < kB; ++u)
-        if (at[u] >= 0) gt[at[u]] = v[u];
+      for (int u = 0; u < kB; ++u) {
+        if (at[u] < 0) continue;
+        if (at[u] & (1 << 30))
+          gb[at[u] & ((1 << 30) - 1)] = pack2(lo[u], hi[u]);
+        else
+          ga[at[u]] = pack2(lo[u], hi[u]);
+      }
     }
-  }
-  __syncthreads();
-  // packed copies: ga [m][pixel pair] (zero rows m >= M), gb [pixel][offset-channel
-  // pair] (zero row pxp), and the bias gradient from the fp32 values
-  for (int idx = tid; idx < pl.mp8 * (pl.pxp / 2); idx += kThreads) {
-    const int m = idx / (pl.pxp / 2), j = idx - m * (pl.pxp / 2);
-    ga[m * pl.sa + j] = m < M ? pack2(gt[m * pl.pxp + 2 * j], gt[m * pl.pxp + 2 * j + 1]) : 0u;
-  }
-  for (int idx = tid; idx < (pl.pxp + 1) * (pl.mp16 / 2); idx += kThreads) {
-    const int px = idx / (pl.mp16 / 2), j = idx - px * (pl.mp16 / 2);
-    float lo = 0.f, hi = 0.f;
-    if (px < pl.pxp) {
-      if (2 * j < M) lo = gt[(2 * j) * pl.pxp + px];
-      if (2 * j + 1 < M) hi = gt[(2 * j + 1) * pl.pxp + px];
-    }
-    gb[px * pl.sb + j] = pack2(lo, hi);
-  }
-  if (a.gb_off && slice == 0) {
-    for (int m = warp; m < M; m += kWarps) {
-      float s = 0.f;
-      for (int px = lane; px < pl.npx; px += 32) s += gt[m * pl.pxp + px];
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) atomicAdd(a.gb_off + m, s);
+    if (a.gb_off && slice == 0) {
+      // bias gradient in fp32: one warp per offset channel
+      for (int m = warp; m < M; m += kWarps) {
+        float s = 0.f;
+        for (int px = lane; px < pl.npx; px += 32) s += gv(m, px);
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) atomicAdd(a.gb_off + m, s);
+      }
     }
   }
   __syncthreads();
@@ -305,6 +295,7 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
   // work units, round robin over the warps: K weight-part units (one tap each)
   // then the input part in groups of kQGroup position tiles
   const int qtiles = pl.nq / 8;
+  const bool unit_stride = g.sh == 1 && g.sw == 1;
   const int qunits = (qtiles + kQGroup - 1) / kQGroup;
   const int mtiles8 = pl.mp8 / 8;
   const int ksteps = pl.pxp / 16;
@@ -345,27 +336,60 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
       }
     } else {
       // ---- input part: rows = 16 channels, columns = window positions,
-      // reduction over (tap, offset channel)
+      // reduction over (tap, offset channel); the pixel each position reads
+      // through tap k is found on the fly.  Two accumulator chains (even and
+      // odd offset-channel blocks) halve the dependent mma sequence.
       const int nt0 = (unit - K) * kQGroup;
-      float acc[kQGroup][4];
+      int qr[kQGroup], qc[kQGroup];
 #pragma unroll
-      for (int t = 0; t < kQGroup; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-      for (int k = 0; k < K; ++k) {
-        int prow[kQGroup];
+      for (int t = 0; t < kQGroup; ++t) {
+        const int q = (nt0 + t) * 8 + gid;
+        qr[t] = -(1 << 20);  // no pixel
+        qc[t] = 0;
+        if (q < pl.npos) {
+          qr[t] = q / pl.cols;
+          qc[t] = q - qr[t] * pl.cols;
+        }
+      }
+      const int nmc = pl.mp16 / 16;
+      float acc[2][kQGroup][4];
 #pragma unroll
-        for (int t = 0; t < kQGroup; ++t)
-          prow[t] = nt0 + t < qtiles ? (int)pxq[k * pl.nq + (nt0 + t) * 8 + gid] * pl.sb : pl.pxp * pl.sb;
-        const uint32_t* ar = wa + (k * kCpc + gid) * pl.sw + tig;
-        for (int mc = 0; mc < pl.mp16 / 16; ++mc) {
-          const uint32_t a0 = ar[mc * 8], a2 = ar[mc * 8 + 4];
-          const uint32_t a1 = ar[8 * pl.sw + mc * 8], a3 = ar[8 * pl.sw + mc * 8 + 4];
+      for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int t = 0; t < kQGroup; ++t) acc[s][t][0] = acc[s][t][1] = acc[s][t][2] = acc[s][t][3] = 0.f;
+      for (int i = 0, k = 0; i < g.kh; ++i) {
+        for (int j = 0; j < g.kw; ++j, ++k) {
+          int prow[kQGroup];
 #pragma unroll
           for (int t = 0; t < kQGroup; ++t) {
-            const uint32_t* b = gb + prow[t] + mc * 8 + tig;
-            mma16816(acc[t], a0, a1, a2, a3, b[0], b[4]);
+            const int r = qr[t] - i * g.dh, c = qc[t] - j * g.dw;
+            int px = pl.pxp;
+            if (unit_stride) {
+              if (r >= 0 && r < pl.R && c >= 0 && c < pl.TW) px = r * pl.TW + c;
+            } else if (r >= 0 && c >= 0 && r % g.sh == 0 && c % g.sw == 0 && r / g.sh < pl.R &&
+                       c / g.sw < pl.TW) {
+              px = (r / g.sh) * pl.TW + c / g.sw;
+            }
+            prow[t] = px * pl.sb;
+          }
+          const uint32_t* ar = wa + (k * kCpc + gid) * pl.sw + tig;
+#pragma unroll
+          for (int mc = 0; mc < kMaxM / 16; ++mc) {
+            if (mc >= nmc) break;
+            const uint32_t a0 = ar[mc * 8], a2 = ar[mc * 8 + 4];
+            const uint32_t a1 = ar[8 * pl.sw + mc * 8], a3 = ar[8 * pl.sw + mc * 8 + 4];
+#pragma unroll
+            for (int t = 0; t < kQGroup; ++t) {
+              const uint32_t* b = gb + prow[t] + mc * 8 + tig;
+              mma16816(acc[mc & 1][t], a0, a1, a2, a3, b[0], b[4]);
+            }
           }
         }
       }
+#pragma unroll
+      for (int t = 0; t < kQGroup; ++t)
+#pragma unroll
+        for (int h = 0; h < 4; ++h) acc[0][t][h] += acc[1][t][h];
 #pragma unroll
       for (int t = 0; t < kQGroup; ++t) {
         if (nt0 + t >= qtiles) break;
@@ -377,9 +401,9 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
           const int yy = ylo + qr, xx = xlo + qc;
           if (yy < 0 || yy >= g.h || xx < 0 || xx >= g.w) continue;
           float* dst = a.gx + img + (long long)c_begin * g.hw + (long long)yy * g.w + xx;
-          if (gid < ncur && acc[t][hc] != 0.f) atomicAdd(dst + (long long)gid * g.hw, acc[t][hc]);
-          if (gid + 8 < ncur && acc[t][2 + hc] != 0.f)
-            atomicAdd(dst + (long long)(gid + 8) * g.hw, acc[t][2 + hc]);
+          if (gid < ncur && acc[0][t][hc] != 0.f) atomicAdd(dst + (long long)gid * g.hw, acc[0][t][hc]);
+          if (gid + 8 < ncur && acc[0][t][2 + hc] != 0.f)
+            atomicAdd(dst + (long long)(gid + 8) * g.hw, acc[0][t][2 + hc]);
         }
       }
     }
