@@ -46,12 +46,6 @@ struct TcArgs {
   float* gmax;                 // GCOL: max |gcol| of each tile, one float per epilogue warp
 };
 
-// |v|, or +inf when v is not finite (so that a NaN is not lost by fmaxf)
-__device__ __forceinline__ float abs_or_inf(float v) {
-  const float m = fabsf(v);
-  return m <= 3.402823466e38f ? m : __int_as_float(0x7f800000);
-}
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -283,7 +277,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = warp * 32 + lane;
     const int m = m0 + row;
     const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
-    float amax = 0.f;  // GCOL: largest |value| this thread stores (+inf if not finite)
+    // GCOL: bits of the largest |value| this thread stores; as integers the
+    // magnitudes order like the floats, and inf / NaN sort above every finite value
+    uint32_t amax = 0u;
 #pragma unroll 1
     for (int c = 0; c < BN / 32; ++c) {
       uint32_t r[32];
@@ -323,13 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
                             __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
 #pragma unroll
-          for (int j = 0; j < 32; ++j) amax = fmaxf(amax, abs_or_inf(__uint_as_float(r[j])));
+          for (int j = 0; j < 32; ++j) amax = max(amax, r[j] & 0x7fffffffu);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (n_first + j < a.howo) {
               dst[j] = __uint_as_float(r[j]);
-              amax = fmaxf(amax, abs_or_inf(__uint_as_float(r[j])));
+              amax = max(amax, r[j] & 0x7fffffffu);
             }
         }
       } else {
@@ -349,9 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (KIND == GCOL && a.gmax) {
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      for (int o = 16; o > 0; o >>= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       const long long tile = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * z);
-      if (lane == 0) a.gmax[tile * 4 + warp] = amax;
+      if (lane == 0) a.gmax[tile * 4 + warp] = __uint_as_float(amax);
     }
   }
   tc_fence_before();

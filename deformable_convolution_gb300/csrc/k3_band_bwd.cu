@@ -306,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
       const int e = i & 3, r = i >> 2;
       const int ty = ty0 + r / ntx, tx = tx0 + r - (r / ntx) * ntx;
       const float v = a.gmax[(((long long)n * a.gmax_ty + ty) * a.gmax_tx + tx) * 4 + e];
-      atomicMax(&s_gmax, __float_as_int(v));  // non-negative floats order like their bits
+      atomicMax(&s_gmax, __float_as_int(v));  // |values|: their bits order like the floats
+                                              // (a NaN sorts above inf)
     }
     __syncthreads();
     const float G = __int_as_float(s_gmax);

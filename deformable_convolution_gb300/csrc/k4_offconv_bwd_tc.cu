@@ -248,8 +248,56 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
       const int o = gpos[px];
       return (m < M && o >= 0) ? gsrc[(long long)m * g.howo + o] : 0.f;
     };
+    // full-width band with 16-byte aligned rows: the band's pixels are one
+    // contiguous run of each goff plane, read as float4; a warp covers 8
+    // offset-channel pairs x 4 pixel quads (conflicts on the packed stores stay
+    // two-way)
+    const int nvalid = (min(ho0 + pl.R, g.ho) - ho0) * g.wo;
+    const bool vec = pl.TW == g.wo && (g.howo & 3) == 0 && ((ho0 * g.wo) & 3) == 0 &&
+                     (nvalid & 3) == 0 && (reinterpret_cast<uintptr_t>(a.goff) & 15) == 0;
+    if (vec) {
+      const float* band0 = gsrc + (long long)ho0 * g.wo;
+      const int pblocks = pl.pxp / 16, nblk = (pl.mp16 / 16) * pblocks;
+      for (int blk0 = warp; blk0 < nblk; blk0 += 2 * kWarps) {
+        float4 f[2][2];
+        int jj[2], pq[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int blk = blk0 + u * kWarps;
+          const int jb = blk / pblocks, pb = blk - jb * pblocks;
+          jj[u] = jb * 8 + (lane >> 2);
+          pq[u] = pb * 4 + (lane & 3);
+          f[u][0] = f[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (blk < nblk && 4 * pq[u] < nvalid) {
+            if (2 * jj[u] < M)
+              f[u][0] = *reinterpret_cast<const float4*>(band0 + (long long)(2 * jj[u]) * g.howo + 4 * pq[u]);
+            if (2 * jj[u] + 1 < M)
+              f[u][1] = *reinterpret_cast<const float4*>(band0 + (long long)(2 * jj[u] + 1) * g.howo + 4 * pq[u]);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (blk0 + u * kWarps >= nblk) break;
+          const int j = jj[u], p4 = pq[u];
+          const float4 f0 = f[u][0], f1 = f[u][1];
+          if (2 * j < pl.mp8) {
+            ga[(2 * j) * pl.sa + 2 * p4] = pack2(f0.x, f0.y);
+            ga[(2 * j) * pl.sa + 2 * p4 + 1] = pack2(f0.z, f0.w);
+          }
+          if (2 * j + 1 < pl.mp8) {
+            ga[(2 * j + 1) * pl.sa + 2 * p4] = pack2(f1.x, f1.y);
+            ga[(2 * j + 1) * pl.sa + 2 * p4 + 1] = pack2(f1.z, f1.w);
+          }
+          uint32_t* gq = gb + (4 * p4) * pl.sb + j;
+          gq[0] = pack2(f0.x, f1.x);
+          gq[pl.sb] = pack2(f0.y, f1.y);
+          gq[2 * pl.sb] = pack2(f0.z, f1.z);
+          gq[3 * pl.sb] = pack2(f0.w, f1.w);
+        }
+      }
+    }
     constexpr int kB = 4;
-    for (int base = tid; base < total; base += kThreads * kB) {
+    for (int base = vec ? total : tid; base < total; base += kThreads * kB) {
       float lo[kB], hi[kB];
       int at[kB];
 #pragma unroll
@@ -395,10 +443,14 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
         if (nt0 + t >= qtiles) break;
 #pragma unroll
         for (int hc = 0; hc < 2; ++hc) {
+          // window position of accumulator column 2 * tig + hc: the lane whose
+          // gid is that column computed its (row, column) above
+          const int src = (2 * tig + hc) * 4;
+          const int qrow = __shfl_sync(0xffffffffu, qr[t], src);
+          const int qcol = __shfl_sync(0xffffffffu, qc[t], src);
           const int q = (nt0 + t) * 8 + 2 * tig + hc;
           if (q >= pl.npos) continue;
-          const int qr = q / pl.cols, qc = q - qr * pl.cols;
-          const int yy = ylo + qr, xx = xlo + qc;
+          const int yy = ylo + qrow, xx = xlo + qcol;
           if (yy < 0 || yy >= g.h || xx < 0 || xx >= g.w) continue;
           float* dst = a.gx + img + (long long)c_begin * g.hw + (long long)yy * g.w + xx;
           if (gid < ncur && acc[0][t][hc] != 0.f) atomicAdd(dst + (long long)gid * g.hw, acc[0][t][hc]);

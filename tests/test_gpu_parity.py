@@ -185,3 +185,33 @@ def test_repeated_calls_are_deterministic_forward():
     y2, off2, _ = gpu_forward(p, d)
     assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
     assert torch.equal(off1, off2)
+
+
+# bf16 problem whose GCOL GEMM runs on the tensor cores (C_in * K and Ho * Wo
+# multiples of 8), so K3 accumulates grad_x in fixed point scaled from the
+# per-tile max |gcol|; the relative error must not depend on the gradient's
+# magnitude
+SCALED_PROBLEM = (2, 32, 16, 16, 16, 3, 3, 1, 1, 1, 1)
+
+
+@pytest.mark.parametrize("scale", [1e-30, 1e-8, 1e6, 1e25])
+def test_backward_parity_at_extreme_gradient_scales(scale):
+    n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups = SCALED_PROBLEM
+    p = B.Problem(n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups, B.DC_BF16)
+    d = random_inputs(p, 77)
+    d["grad_y"] = (d["grad_y"].float() * scale).to(p.torch_dtype)
+    errs = check_layer(p, d)
+    print(scale, errs)
+
+
+def test_backward_non_finite_gradient_propagates():
+    n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups = SCALED_PROBLEM
+    p = B.Problem(n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups, B.DC_BF16)
+    d = random_inputs(p, 78)
+    d["grad_y"][0, 3, 5, 7] = float("nan")
+    y, off, _ = gpu_forward(p, d)
+    g = gpu_backward(p, d, off.cpu())
+    assert torch.isnan(g["grad_x"][0]).any()
+    # image 1 never sees the NaN: its gradient stays finite
+    assert torch.isfinite(g["grad_x"][1]).all()
+    assert B.device_error() == 0
