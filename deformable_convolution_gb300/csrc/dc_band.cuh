@@ -153,12 +153,71 @@ struct Walk3 {
 // (low half = even channel); fp32: one word per pixel per channel.  Plane u
 // starts at dst + u * plane.  Each thread keeps kBatch independent global loads
 // in flight; lanes run along window rows, so loads are coalesced.
+// Fast path of stage_window for bf16 when image rows are whole 8-byte
+// quads (W % 4 == 0, 8-byte aligned planes): a task is (channel pair, window
+// row, aligned 4-pixel quad of the image row); it reads one 8-byte quad of each
+// of the two channels and writes up to four pair words.  Quads lie either
+// wholly inside or wholly outside the image, so no load straddles an edge.
+__device__ __forceinline__ void stage_window_quads(const __nv_bfloat16* __restrict__ x,
+                                                   const Geom& g, long long img, int c_begin,
+                                                   int cpc, int ylo, int xlo, int rows, int cols,
+                                                   int plane, uint32_t* dst) {
+  constexpr int kBatch = 4;
+  const int q_lo = (xlo >= 0 ? xlo : xlo - 3) / 4;  // floor(xlo / 4)
+  const int q_hi = (xlo + cols - 1 >= 0 ? xlo + cols - 1 : xlo + cols - 4) / 4;
+  const int nq = q_hi - q_lo + 1;
+  const int units = cpc / 2;
+  Walk3 w;
+  w.init(threadIdx.x, kThreads, rows, nq);
+  while (w.a < units) {
+    uint2 v0[kBatch], v1[kBatch];
+    int uu[kBatch], rr[kBatch], qq[kBatch];
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      v0[j] = v1[j] = make_uint2(0u, 0u);
+      uu[j] = -1;
+      if (w.a < units) {
+        uu[j] = w.a;
+        rr[j] = w.b;
+        qq[j] = q_lo + w.c;
+        const int yy = ylo + w.b, x0 = 4 * qq[j];
+        if (yy >= 0 && yy < g.h && x0 >= 0 && x0 < g.w) {
+          const int c0 = c_begin + 2 * w.a;
+          const __nv_bfloat16* p = x + img + (long long)c0 * g.hw + (long long)yy * g.w + x0;
+          if (c0 < g.c_in) v0[j] = *reinterpret_cast<const uint2*>(p);
+          if (c0 + 1 < g.c_in) v1[j] = *reinterpret_cast<const uint2*>(p + g.hw);
+        }
+        w.next();
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kBatch; ++j) {
+      if (uu[j] < 0) continue;
+      // pixel i of the quad: low half = channel c0, high half = channel c0 + 1
+      const uint32_t pw[4] = {__byte_perm(v0[j].x, v1[j].x, 0x5410), __byte_perm(v0[j].x, v1[j].x, 0x7632),
+                              __byte_perm(v0[j].y, v1[j].y, 0x5410), __byte_perm(v0[j].y, v1[j].y, 0x7632)};
+      uint32_t* row = dst + uu[j] * plane + rr[j] * cols;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int col = 4 * qq[j] + i - xlo;
+        if (col >= 0 && col < cols) row[col] = pw[i];
+      }
+    }
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ void stage_window(const T* __restrict__ x, const Geom& g,
                                              long long img, int c_begin, int cpc, int ylo,
                                              int xlo, int rows, int cols, int plane,
                                              uint32_t* dst) {
   constexpr bool kPairs = sizeof(T) == 2;
+  if (kPairs && (g.w & 3) == 0 && (cpc & 1) == 0 &&
+      (reinterpret_cast<uintptr_t>(x) & 7) == 0) {
+    stage_window_quads(reinterpret_cast<const __nv_bfloat16*>(x), g, img, c_begin, cpc, ylo, xlo,
+                       rows, cols, plane, dst);
+    return;
+  }
   constexpr int kBatch = 16;
   const int units = kPairs ? cpc / 2 : cpc;
   Walk3 w;
