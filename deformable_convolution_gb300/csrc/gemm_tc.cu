@@ -98,6 +98,21 @@ __device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, uint64
       : "memory");
 }
 
+// TMA store of a shared-memory box (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void tma_store_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -164,7 +179,7 @@ struct Cfg {
 template <int KIND, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-            TcArgs a) {
+            const __grid_constant__ CUtensorMap tmC, TcArgs a) {
   using C = Cfg<KIND, BN>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
@@ -271,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long part = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
       zero_share(a.zero, part, nparts, threadIdx.x, 128);
     }
-    const bool ok = mbar_wait(done, 0);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0));
     tc_fence_after();
     pdl_release();
     const int row = warp * 32 + lane;
@@ -309,24 +324,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (n_first + j < a.howo) dst[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
         }
       } else if (KIND == GCOL) {
-        if (m >= a.kdim) continue;
-        float* dst = static_cast<float*>(a.out) + (long long)m * a.out_row +
-                     (long long)z * a.out_img + n_first;
-        if (n_first + 32 <= a.howo) {
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            *reinterpret_cast<float4*>(dst + v * 4) =
-                make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                            __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-#pragma unroll
-          for (int j = 0; j < 32; ++j) amax = max(amax, r[j] & 0x7fffffffu);
-        } else {
+        // this warp's 32 rows x 32 columns go through shared memory (the
+        // operand stages are free once `done` fired) in the 128-byte swizzled
+        // layout of the store map, then out with one TMA store; rows and
+        // columns beyond the tensor are clipped by the TMA unit
+        if (m < a.kdim) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (n_first + j < a.howo) {
-              dst[j] = __uint_as_float(r[j]);
-              amax = max(amax, r[j] & 0x7fffffffu);
-            }
+            if (n_first + j < a.howo) amax = max(amax, r[j] & 0x7fffffffu);
+        }
+        unsigned char* buf = smem + (warp * (BN / 32) + c) * 4096;
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          *reinterpret_cast<float4*>(buf + lane * 128 + ((v ^ (lane & 7)) << 4)) =
+              make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                          __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0 && m0 + warp * 32 < a.kdim && n_first < a.howo) {
+          tma_store_3d(&tmC, buf, n_first, z, m0 + warp * 32);
+          tma_store_commit();
         }
       } else {
         if (m >= a.c_out) continue;
@@ -344,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (KIND == GCOL && lane == 0) tma_store_wait_all();  // gcol written before exit
     if (KIND == GCOL && a.gmax) {
       for (int o = 16; o > 0; o >>= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       const long long tile = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * z);
@@ -383,18 +401,19 @@ EncodeTiledFn encode_fn() {
 
 // bf16 tensor map, 128-byte swizzle, zero fill outside the tensor.
 bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-              const cuuint64_t* strides, const cuuint32_t* box) {
+              const cuuint64_t* strides, const cuuint32_t* box,
+              CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims,
+  return fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims,
             strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int KIND, int BN>
-cudaError_t launch(const CUtensorMap& A, const CUtensorMap& B, const TcArgs& a, dim3 grid,
-                   cudaStream_t s) {
+cudaError_t launch(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Cm,
+                   const TcArgs& a, dim3 grid, cudaStream_t s) {
   using C = Cfg<KIND, BN>;
   auto k = tc_gemm<KIND, BN>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
@@ -411,7 +430,7 @@ cudaError_t launch(const CUtensorMap& A, const CUtensorMap& B, const TcArgs& a, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = KIND == GCOL ? 0 : 1;
-  e = cudaLaunchKernelEx(&cfg, k, A, B, a);
+  e = cudaLaunchKernelEx(&cfg, k, A, B, Cm, a);
   note_launches(1);
   return e;
 }
@@ -425,6 +444,15 @@ bool col_map(CUtensorMap* m, const void* col, const Geom& g, const ColLayout& L,
 }
 
 // grad_y as a 3-D tensor {pixel, channel, image}
+// gcol (fp32) as the store target of the GCOL epilogue: boxes of 32 pixels x
+// 32 rows of one image
+bool gcol_map(CUtensorMap* m, const float* gcol, const Geom& g, const ColLayout& L) {
+  const cuuint64_t dims[3] = {(cuuint64_t)g.howo, (cuuint64_t)g.n, (cuuint64_t)g.kdim};
+  const cuuint64_t strides[2] = {(cuuint64_t)L.img * 4, (cuuint64_t)L.row * 4};
+  const cuuint32_t box[3] = {32, 1, 32};
+  return make_map(m, gcol, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+}
+
 bool gy_map(CUtensorMap* m, const void* gy, const Geom& g, cuuint32_t box_ch) {
   const cuuint64_t dims[3] = {(cuuint64_t)g.howo, (cuuint64_t)g.c_out, (cuuint64_t)g.n};
   const cuuint64_t strides[2] = {(cuuint64_t)g.howo * 2, (cuuint64_t)g.c_out * g.howo * 2};
@@ -466,14 +494,15 @@ cudaError_t launch_gemm_fwd_tc(const GemmArgs& ga, cudaStream_t s) {
   a.out = ga.y;
   const int bn = pick_fwd_bn(g);
   dim3 grid((unsigned)ceil_div_ll(g.howo, bn), (unsigned)ceil_div_ll(g.c_out, kBM), (unsigned)g.n);
-  return bn == 128 ? launch<FWD, 128>(A, B, a, grid, s) : launch<FWD, 64>(A, B, a, grid, s);
+  return bn == 128 ? launch<FWD, 128>(A, B, A, a, grid, s) : launch<FWD, 64>(A, B, A, a, grid, s);
 }
 
 cudaError_t launch_gemm_gcol_tc(const GemmArgs& ga, cudaStream_t s) {
   const Geom& g = ga.g;
-  CUtensorMap A, B;
+  CUtensorMap A, B, Cm;
   if (!w_map(&A, ga.w, g, 64, 64)) return cudaErrorInvalidValue;
   if (!gy_map(&B, ga.gy, g, 64)) return cudaErrorInvalidValue;
+  if (!gcol_map(&Cm, ga.gcol, g, ga.gcol_layout)) return cudaErrorInvalidValue;
   TcArgs a{};
   a.c_out = g.c_out;
   a.kdim = g.kdim;
@@ -486,7 +515,7 @@ cudaError_t launch_gemm_gcol_tc(const GemmArgs& ga, cudaStream_t s) {
   a.zero = ga.zero;
   a.gmax = ga.gmax;
   dim3 grid((unsigned)ceil_div_ll(g.howo, 128), (unsigned)ceil_div_ll(g.kdim, kBM), (unsigned)g.n);
-  return launch<GCOL, 128>(A, B, a, grid, s);
+  return launch<GCOL, 128>(A, B, Cm, a, grid, s);
 }
 
 cudaError_t launch_gemm_gw_tc(const GemmArgs& ga, cudaStream_t s) {
@@ -509,7 +538,7 @@ cudaError_t launch_gemm_gw_tc(const GemmArgs& ga, cudaStream_t s) {
   a.kb_per_split = (int)ceil_div_ll(a.kb_total, splits);
   splits = ceil_div_ll(a.kb_total, a.kb_per_split);
   dim3 grid((unsigned)ceil_div_ll(g.kdim, 128), (unsigned)ceil_div_ll(g.c_out, kBM), (unsigned)splits);
-  return launch<GW, 128>(A, B, a, grid, s);
+  return launch<GW, 128>(A, B, A, a, grid, s);
 }
 
 }  // namespace dc
