@@ -17,11 +17,14 @@
 // a slice of 16 input channels (no cluster: slices only meet in the offset
 // gradient, which each CTA adds to global memory with fire-and-forget float
 // reductions).  It stages its slice of the band's input window (receptive
-// field + margin) once and keeps a float32 copy of grad_x over the same window
-// in shared memory; scatters land there with shared-memory atomics.  Taps
-// whose corners leave the window are queued and processed by all lanes
-// together from global memory.  The window is flushed to grad_x with one float
-// atomic per element (neighbouring bands' windows overlap).
+// field + margin) once and accumulates grad_x over the same window in shared
+// memory.  bf16 problems whose gcol comes from the tensor-core GEMM accumulate
+// in 32-bit fixed point (integer shared-memory atomics, several times faster
+// than float ones) with a per-CTA scale derived from the largest |gcol| of the
+// tiles it reads; other problems accumulate floats.  Taps whose corners leave
+// the window are queued and processed by all lanes together from global
+// memory.  The window is flushed to grad_x with float atomics (neighbouring
+// bands' windows overlap).
 #include "dc_band.cuh"
 
 namespace dc {
@@ -43,9 +46,6 @@ struct Plan {
   size_t off_halo, off_gx, off_offs, off_part, off_tab, off_q, smem;
 };
 
-// Largest band (128, 64 or 32 pixels) and widest channel slice whose shared
-// memory fits: staged input, grad_x window, offsets (reused for the offset
-// gradient) and this CTA's partial offset gradient.
 // Largest band (128, 64 or 32 pixels) whose shared memory fits, with slices
 // of 16 channels: staged input, grad_x window, offsets, this CTA's partial
 // offset gradient, pixel table and the slow-tap queue.
@@ -445,37 +445,83 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
   }
 
   // ---------------------------------------------------------------- offset gradient
-  // this slice's partial sums, added to grad_offset (cleared before the pass)
+  // this slice's partial sums, added to grad_offset (cleared before the pass);
+  // full-width bands with 16-byte aligned rows add float4 quads
   __syncthreads();
   {
-    band::Walk2 w;
-    w.init(tid, kThreads, npx);
-    while (w.a < M) {
-      const int m = w.a, px = w.b;
-      w.next();
-      const float v = part[m * PS + px];
-      if (v == 0.f) continue;
-      const int e = pix[px];
-      const int ho = ho0 + (e >> 16), wo = wo0 + (e & 0xffff);
-      if (ho < g.ho && wo < g.wo)
-        atomicAdd(a.goff + ((long long)n * M + m) * g.howo + (long long)ho * g.wo + wo, v);
+    const int nvalid = (min(ho0 + pl.R, g.ho) - ho0) * g.wo;
+    const bool vec = pl.TW == g.wo && (g.howo & 3) == 0 && ((ho0 * g.wo) & 3) == 0 &&
+                     (nvalid & 3) == 0 && (PS & 3) == 0 &&
+                     (reinterpret_cast<uintptr_t>(a.goff) & 15) == 0;
+    if (vec) {
+      band::Walk2 w;
+      w.init(tid, kThreads, nvalid / 4);
+      while (w.a < M) {
+        const int m = w.a, p4 = w.b;
+        w.next();
+        const float4 v = *reinterpret_cast<const float4*>(part + m * PS + 4 * p4);
+        if (v.x == 0.f && v.y == 0.f && v.z == 0.f && v.w == 0.f) continue;
+        atomicAdd(reinterpret_cast<float4*>(a.goff + ((long long)n * M + m) * g.howo +
+                                            (long long)ho0 * g.wo + 4 * p4),
+                  v);
+      }
+    } else {
+      band::Walk2 w;
+      w.init(tid, kThreads, npx);
+      while (w.a < M) {
+        const int m = w.a, px = w.b;
+        w.next();
+        const float v = part[m * PS + px];
+        if (v == 0.f) continue;
+        const int e = pix[px];
+        const int ho = ho0 + (e >> 16), wo = wo0 + (e & 0xffff);
+        if (ho < g.ho && wo < g.wo)
+          atomicAdd(a.goff + ((long long)n * M + m) * g.howo + (long long)ho * g.wo + wo, v);
+      }
     }
   }
 
   // ---------------------------------------------------------------- flush the grad_x window
+  // (neighbouring bands' windows overlap: float atomics).  With image rows of
+  // whole 16-byte quads, one float4 atomic per quad of an image row.
   {
-    band::Walk3 w;
-    w.init(tid, kThreads, pl.rows, pl.cols);
-    while (w.a < ncur) {
-      const int cl = w.a, r = w.b, q = w.c;
-      w.next();
-      const int yy = ylo + r, xx = xlo + q;
-      if (yy < 0 || yy >= g.h || xx < 0 || xx >= g.w) continue;
-      const int at = cl * PL + r * pl.cols + q;
-      const float v = kFixed ? (poison ? __int_as_float(0x7fc00000)
-                                       : (float)reinterpret_cast<const int*>(gxs)[at] * finv)
-                             : gxs[at];
-      if (v != 0.f) atomicAdd(a.gx + img + (long long)(c_begin + cl) * g.hw + (long long)yy * g.w + xx, v);
+    auto value = [&](int at) {
+      return kFixed ? (poison ? __int_as_float(0x7fc00000)
+                              : (float)reinterpret_cast<const int*>(gxs)[at] * finv)
+                    : gxs[at];
+    };
+    if ((g.w & 3) == 0 && (reinterpret_cast<uintptr_t>(a.gx) & 15) == 0) {
+      const int q_lo = (xlo >= 0 ? xlo : xlo - 3) / 4;
+      const int q_hi = (xlo + pl.cols - 1 >= 0 ? xlo + pl.cols - 1 : xlo + pl.cols - 4) / 4;
+      band::Walk3 w;
+      w.init(tid, kThreads, pl.rows, q_hi - q_lo + 1);
+      while (w.a < ncur) {
+        const int cl = w.a, r = w.b, x0 = 4 * (q_lo + w.c);
+        w.next();
+        const int yy = ylo + r;
+        if (yy < 0 || yy >= g.h || x0 < 0 || x0 >= g.w) continue;
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int q = x0 + i - xlo;
+          v[i] = (q >= 0 && q < pl.cols) ? value(cl * PL + r * pl.cols + q) : 0.f;
+        }
+        if (v[0] == 0.f && v[1] == 0.f && v[2] == 0.f && v[3] == 0.f) continue;
+        atomicAdd(reinterpret_cast<float4*>(a.gx + img + (long long)(c_begin + cl) * g.hw +
+                                            (long long)yy * g.w + x0),
+                  make_float4(v[0], v[1], v[2], v[3]));
+      }
+    } else {
+      band::Walk3 w;
+      w.init(tid, kThreads, pl.rows, pl.cols);
+      while (w.a < ncur) {
+        const int cl = w.a, r = w.b, q = w.c;
+        w.next();
+        const int yy = ylo + r, xx = xlo + q;
+        if (yy < 0 || yy >= g.h || xx < 0 || xx >= g.w) continue;
+        const float v = value(cl * PL + r * pl.cols + q);
+        if (v != 0.f) atomicAdd(a.gx + img + (long long)(c_begin + cl) * g.hw + (long long)yy * g.w + xx, v);
+      }
     }
   }
 }
