@@ -184,7 +184,52 @@ __global__ void __launch_bounds__(kThreads) k1_band_sample(SampleArgs a, Plan pl
   if (!kReplay) {
     // -------------------------------------------------------------- weights
     const T* __restrict__ w_off = static_cast<const T*>(a.w_off);
-    if (kBf16) {
+    const bool wvec = kBf16 && c_begin + pl.cpc <= g.c_in && ((g.c_in * g.K) & 7) == 0 &&
+                      ((pl.cpc * g.K) & 7) == 0 && (reinterpret_cast<uintptr_t>(w_off) & 15) == 0;
+    if (wvec) {
+      // each offset channel's slice w_off[m][c_begin ..][*] is one contiguous,
+      // 16-byte aligned run: read it as uint4 (eight weights), write the
+      // halves of the channel-pair words; padding rows m >= M are zero
+      uint32_t* wb = reinterpret_cast<uint32_t*>(smem + pl.off_w);  // [K][cpc/2][mp]
+      unsigned short* wh = reinterpret_cast<unsigned short*>(wb);
+      const int cpp = pl.cpc / 2;
+      const unsigned short* wsrc = reinterpret_cast<const unsigned short*>(w_off);
+      const int span8 = pl.cpc * g.K / 8, total = g.M * span8;
+      for (int base = tid; base < total; base += 2 * kThreads) {
+        uint4 v[2];
+        int mm[2], t0[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int idx = base + u * kThreads;
+          mm[u] = -1;
+          if (idx < total) {
+            const int m = idx / span8, q = idx - m * span8;
+            mm[u] = m;
+            t0[u] = 8 * q;
+            v[u] = *reinterpret_cast<const uint4*>(wsrc + ((long long)m * g.c_in + c_begin) * g.K + 8 * q);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          if (mm[u] < 0) continue;
+          const uint32_t vw[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          int cl = t0[u] / g.K, k = t0[u] - cl * g.K;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const unsigned short h = (unsigned short)((e & 1) ? (vw[e >> 1] >> 16) : (vw[e >> 1] & 0xffffu));
+            wh[((k * cpp + (cl >> 1)) * pl.mp + mm[u]) * 2 + (cl & 1)] = h;
+            if (++k == g.K) {
+              k = 0;
+              ++cl;
+            }
+          }
+        }
+      }
+      for (int idx = tid; idx < g.K * cpp * (pl.mp - g.M); idx += kThreads) {
+        const int row = idx / (pl.mp - g.M), m = g.M + idx - row * (pl.mp - g.M);
+        wb[row * pl.mp + m] = 0u;
+      }
+    } else if (kBf16) {
       uint32_t* wb = reinterpret_cast<uint32_t*>(smem + pl.off_w);  // [K][cpc/2][mp]
       const int cpp = pl.cpc / 2;
       const __nv_bfloat16* wsrc = reinterpret_cast<const __nv_bfloat16*>(w_off);
@@ -317,20 +362,27 @@ __global__ void __launch_bounds__(kThreads) k1_band_sample(SampleArgs a, Plan pl
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
     {
-      // four (m, px) items per round, their remote loads all in flight
+      // this CTA reduces its share of the (m, px) items (four per round, their
+      // remote loads all in flight) and writes each sum into every peer's
+      // offset array, so each partial is read once in the whole cluster
+      const int items = g.M * npx;
+      const int i_begin = (int)((long long)items * rank / pl.csize);
+      const int i_end = (int)((long long)items * (rank + 1) / pl.csize);
       band::Walk2 w;
-      w.init(tid, kThreads, npx);
-      while (w.a < g.M) {
+      w.init(i_begin + tid, kThreads, npx);
+      int idx = i_begin + tid;
+      while (idx < i_end) {
         int mm[4], pp[4];
         float v[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           mm[j] = -1;
           v[j] = 0.f;
-          if (w.a < g.M) {
+          if (idx < i_end) {
             mm[j] = w.a;
             pp[j] = w.b;
             w.next();
+            idx += kThreads;
           }
         }
         for (int r = 0; r < pl.csize; ++r) {
@@ -350,13 +402,13 @@ __global__ void __launch_bounds__(kThreads) k1_band_sample(SampleArgs a, Plan pl
             if (a.b_off) vv += a.b_off[m];
             const long long oi = ((long long)n * g.M + m) * g.howo + (long long)ho * g.wo + wo;
             if (a.off_add) vv += a.off_add[oi];
-            if (a.off_out && rank == 0) a.off_out[oi] = vv;
+            if (a.off_out) a.off_out[oi] = vv;
           }
-          offs[m * PS + px] = vv;
+          for (int r = 0; r < pl.csize; ++r) cluster.map_shared_rank(offs, r)[m * PS + px] = vv;
         }
       }
     }
-    cluster.sync();  // peers have finished reading this CTA's partials
+    cluster.sync();  // every CTA's offsets are complete; peers are done reading partials
   } else {
     __syncthreads();  // pixel table
     band::Walk2 w;
