@@ -37,16 +37,17 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 TRAFFIC = {
     # ncu --set full, res3 bf16, one launch each (profiles/<kernel>_res3_bf16.md,
     # profiles/tc_gemm_res3_bf16.md).  Writes mostly stay in the 129 MB L2.
-    ("res3_bf16", "k1_band_sample"): {"bytes": 2176256, "source": "9c5ad9459c81675a"},
-    ("res3_bf16", "k3_band_bwd"): {"bytes": 34691840 + 5888, "source": "ccb7bb3fdf278c8a"},
-    ("res3_bf16", "k4_offconv_bwd"): {"bytes": 5482752, "source": "1190cb609f794a95"},
-    ("res3_bf16", "gemm_fwd"): {"bytes": 14764800, "source": "38ef6860e950b566"},
-    ("res3_bf16", "gemm_gcol"): {"bytes": 2045184 + 106240, "source": "38ef6860e950b566"},
-    ("res3_bf16", "gemm_gw"): {"bytes": 16665600, "source": "38ef6860e950b566"},
+    ("res3_bf16", "k1_band_sample"): {"bytes": 2194176 + 256, "source": "f4ff7e59de4eecdc"},
+    ("res3_bf16", "k3_band_bwd"): {"bytes": 34715392 + 8192, "source": "062a6ec493dd8fee"},
+    ("res3_bf16", "k4_offconv_bwd"): {"bytes": 5468416, "source": "68a77d531657e67e"},
+    ("res3_bf16", "gemm_fwd"): {"bytes": 14764544, "source": "dabb998c5a83207d"},
+    ("res3_bf16", "gemm_gcol"): {"bytes": 1941248, "source": "dabb998c5a83207d"},
+    ("res3_bf16", "gemm_gw"): {"bytes": 16665600, "source": "dabb998c5a83207d"},
 }
 KERNEL_SOURCES = {
     "k1_band_sample": "k1_sample.cu", "k3_band_bwd": "k3_band_bwd.cu",
-    "k4_offconv_bwd": "k4_offconv_bwd.cu",
+    # bf16 workloads run the offset-convolution backward on tensor cores
+    "k4_offconv_bwd": "k4_offconv_bwd_tc.cu",
     "gemm_fwd": "gemm_tc.cu", "gemm_gcol": "gemm_tc.cu", "gemm_gw": "gemm_tc.cu",
 }
 
@@ -151,26 +152,51 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def cpu_baseline(wl, seconds):
-    """The oracle, as it stands, on image 0 of the workload (fwd + bwd),
-    repeated until `seconds` have passed (at least once)."""
-    import torch
-
+def oracle_sample(wl, rows=None):
+    """The oracle, as it stands, on image 0 of the workload (fwd + bwd in
+    fp64), optionally on its first `rows` input rows only (same per-pixel
+    work, for bounded samples).  Returns (run, flops per run, description)."""
     import oracle
     from deformable_convolution_gb300 import workloads as W
     d = W.generate(wl)
-    one = {k: (None if v is None else (v[:1] if k in ("x", "offset_add", "grad_y") else v))
-           for k, v in d.items()}
     p1 = wl.problem(1)
-    op = oracle.Problem(1, p1.c_in, p1.h, p1.w, p1.c_out, p1.kh, p1.kw, p1.stride, p1.pad,
+    h = p1.h if rows is None else max(1, min(p1.h, rows))
+    p1 = type(p1)(1, p1.c_in, h, p1.w, p1.c_out, p1.kh, p1.kw, p1.stride, p1.pad, p1.dil,
+                  p1.offset_groups, p1.dtype)
+    s = p1.shapes()
+    ho, wo = s["y"][2], s["y"][3]
+
+    def crop(k, v):
+        if v is None:
+            return None
+        if k == "x":
+            return v[:1, :, :h]
+        if k in ("offset_add", "grad_y"):
+            return v[:1, :, :ho, :wo]
+        return v
+    one = {k: crop(k, v) for k, v in d.items()}
+    op = oracle.Problem(1, p1.c_in, h, p1.w, p1.c_out, p1.kh, p1.kw, p1.stride, p1.pad,
                         p1.dil, p1.offset_groups)
-    f64 = lambda t: None if t is None else t.double().numpy()  # noqa: E731
+    f64 = lambda t: None if t is None else t.contiguous().double().numpy()  # noqa: E731
     args = [f64(one[k]) for k in ("x", "w_off", "b_off", "w", "offset_add")]
-    flops = 3 * W.conv_flops(p1)
+    gy = f64(one["grad_y"])
+
+    def run():
+        y, off = oracle.forward(op, *args)
+        oracle.backward(op, args[0], args[1], args[3], off, gy)
+    what = f"image 0 of {wl.name} (N=1 of {wl.n})" + (
+        f", input rows 0..{h - 1} of {wl.h}" if h < wl.h else "")
+    return run, 3 * W.conv_flops(p1), what
+
+
+def cpu_baseline(wl, seconds):
+    """The oracle on image 0 of the workload (fwd + bwd), repeated until
+    `seconds` have passed (at least once)."""
+    import oracle
+    run, flops, what = oracle_sample(wl)
     runs, t0 = 0, time.perf_counter()
     while True:
-        y, off = oracle.forward(op, *args)
-        oracle.backward(op, args[0], args[1], args[3], off, f64(one["grad_y"]))
+        run()
         runs += 1
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -178,39 +204,50 @@ def cpu_baseline(wl, seconds):
     per = el / runs
     return {"value": flops / per / 1e9, "unit": "GFLOP/s", "cores": oracle.num_threads(),
             "kind": "oracle",
-            "sample": f"image 0 of {wl.name} (N=1 of {wl.n}), fwd+bwd in fp64, {runs} run(s), "
-                      f"{per * 1e3:.0f} ms each", "ms_per_image": per * 1e3}
+            "sample": f"{what}, fwd+bwd in fp64, {runs} run(s), {per * 1e3:.0f} ms each",
+            "ms_per_image": per * 1e3}
+
+
+REFERENCE_BUDGET_S = 120.0  # whole --impl reference run (warm-up + timed steps)
 
 
 def run_reference(args, world, rank):
+    """The oracle as the reference arm: each step is a bounded sample of the
+    workload (image 0, cropped to the rows that keep the whole run within
+    REFERENCE_BUDGET_S seconds), timed on the host cores."""
+    import oracle
     from deformable_convolution_gb300 import workloads as W
     if rank != 0:
         return
     wl = W.WORKLOADS[args.workload]
-    p = wl.problem()
-    flops_full = 3 * W.conv_flops(p)
+    run, _, _ = oracle_sample(wl)
+    t0 = time.perf_counter()
+    run()
+    t_full = time.perf_counter() - t0
+    per_step = REFERENCE_BUDGET_S / max(1, args.steps + args.warmup)
+    rows = wl.h if t_full <= per_step else max(1, int(wl.h * per_step / t_full))
+    run, flops, what = oracle_sample(wl, rows)
     for _ in range(args.warmup):
-        cpu_baseline(wl, 0.0)
-    t = []
-    info = None
+        run()
+    t0 = time.perf_counter()
     for _ in range(args.steps):
-        info = cpu_baseline(wl, 0.0)
-        t.append(info["ms_per_image"])
-    ms_img = sum(t) / len(t)
-    gflops = info["value"]
+        run()
+    el = time.perf_counter() - t0
+    ms = el / max(1, args.steps) * 1e3
+    gflops = flops / (ms / 1e3) / 1e9
+    sample = f"{what}, fwd+bwd in fp64 per step"
     line = {"impl": "reference", "metric": METRIC, "value": gflops, "unit": "GFLOP/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms_img * wl.n, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, "n": wl.n, "c_in": wl.c_in, "c_out": wl.c_out,
                        "h": wl.h, "w": wl.w, "k": wl.k, "offset_groups": wl.groups,
-                       "step": "image 0 of the batch per step (oracle, host cores); "
-                               "ms_per_step extrapolated x N"},
-            "cpu_baseline": {"value": gflops, "unit": "GFLOP/s", "cores": info["cores"],
-                             "kind": "oracle", "sample": info["sample"]},
+                       "step": sample},
+            "cpu_baseline": {"value": gflops, "unit": "GFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
             "e2e": {"value": gflops, "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
-            "flops_per_step": flops_full}
+            "flops_per_step": flops}
     print(json.dumps(line), flush=True)
 
 
