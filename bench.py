@@ -360,6 +360,7 @@ def main():
         line["roofline"]["note"] = "dominant kernel of the step (longest per-launch time)"
         line["kernels"] = kernels
         line["sampling_stage"] = k1_roofline(p, t, dev, stream, flush, wl, args.roofline_iters)
+        line["unfused_ablation"] = unfused_ablation(p, t, dev, stream, flush, args.roofline_iters)
         line["e2e"] = e2e(p, d, dev, stream, flops_step, args.e2e_iters)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
@@ -508,6 +509,68 @@ def k1_roofline(p, t, dev, stream, flush, wl, iters=200):
             "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{src} (hbm_gbs, burst)",
             "traffic": traffic, "algorithmic_bytes": nbytes, "ms_per_launch": ms}
+
+
+def time_graph(launch, dev, stream, flush, iters):
+    """Average device time of `launch` captured in a CUDA graph and replayed
+    between L2 flushes (CUDA events on the launching stream)."""
+    import torch
+    with torch.cuda.stream(stream):
+        launch()
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        launch()
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            flush.fill_(3)
+            graph.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(iters)]
+        torch.cuda.synchronize(dev)
+        for a, b in ev:
+            flush.fill_(7)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+    torch.cuda.synchronize(dev)
+    return sum(a.elapsed_time(b) for a, b in ev) / iters
+
+
+def unfused_ablation(p, t, dev, stream, flush, iters=200):
+    """The pages' comparison, on this GPU: the fused stage (offset convolution
+    and interpolation in one kernel, offsets kept on chip) against the unfused
+    pipeline (offset convolution -> offsets in HBM -> interpolation), each
+    timed alone between L2 flushes.  Arithmetic intensity = the stage's flops
+    (offset convolution + 4-corner blends) / its algorithmic HBM bytes."""
+    import torch
+
+    from deformable_convolution_gb300 import binding as B
+    s = p.shapes()
+    col = torch.empty(s["col"], dtype=p.torch_dtype, device=dev)
+    off = torch.empty(s["offset"], dtype=torch.float32, device=dev)
+    add = t["offset_add"]
+    fused = time_graph(lambda: B.deform_conv_sample(p, t["x"], t["w_off"], t["b_off"], add, None,
+                                                    col, off), dev, stream, flush, iters)
+    k_off = time_graph(lambda: B.deform_conv_offsets(p, t["x"], t["w_off"], t["b_off"], add, off),
+                       dev, stream, flush, iters)
+    k_smp = time_graph(lambda: B.deform_conv_sample(p, t["x"], None, None, None, off, col),
+                       dev, stream, flush, iters)
+    elt = 2 if p.dtype == 1 else 4
+    P = p.n * p.ho * p.wo
+    kdim = p.c_in * p.kh * p.kw
+    x_b, w_b = p.n * p.c_in * p.h * p.w * elt, p.n_off * kdim * elt
+    off_b, col_b = p.n_off * P * 4, kdim * P * elt
+    add_b = off_b if add is not None else 0
+    flops = 2.0 * P * kdim * p.n_off + 8.0 * P * kdim  # offset conv + blends
+    bytes_fused = x_b + w_b + add_b + col_b + off_b
+    bytes_unfused = (x_b + w_b + add_b + off_b) + (x_b + off_b + col_b)
+    return {"fused_us": fused * 1e3, "unfused_offsets_us": k_off * 1e3,
+            "unfused_sampler_us": k_smp * 1e3, "unfused_us": (k_off + k_smp) * 1e3,
+            "speedup": (k_off + k_smp) / fused,
+            "ai_fused": flops / bytes_fused, "ai_unfused": flops / bytes_unfused,
+            "note": "fused: one K1 launch; unfused: offsets-only K1 then the sampler reading "
+                    "offsets from HBM; both write the offsets and the deformed map"}
 
 
 def e2e(p, d, dev, stream, flops_step, iters=20):

@@ -23,7 +23,7 @@ EXPORTED_SYMBOLS = (
     "dc_out_h", "dc_out_w", "deform_conv_workspace_size", "deform_conv_fwd",
     "deform_conv_bwd", "deform_conv_sample", "dc_status_string", "dc_build_info",
     "dc_launch_count", "deform_conv_fwd_noalloc", "dc_device_error", "dc_kernel_timing",
-    "dc_kernel_times",
+    "dc_kernel_times", "deform_conv_offsets",
 )
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
         L.deform_conv_bwd.restype = i
         L.deform_conv_sample.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.deform_conv_sample.restype = i
+        L.deform_conv_offsets.argtypes = [pp, vp, vp, vp, vp, vp, vp]
+        L.deform_conv_offsets.restype = i
         L.dc_status_string.argtypes = [i]
         L.dc_status_string.restype = ctypes.c_char_p
         L.dc_build_info.argtypes = []
@@ -268,6 +270,17 @@ def deform_conv_sample(p: Problem, x, w_off, b_off, offset_add, offset_in, col,
         _ptr(offset_out, "offset_out", s["offset"], f32, True),
         _ptr(slowpath_count, "slowpath_count", (1,), torch.int64, True),
         _stream(stream)), "deform_conv_sample")
+
+
+def deform_conv_offsets(p: Problem, x, w_off, b_off, offset_add, offset_out, stream=None):
+    s = p.shapes()
+    dt, f32 = p.torch_dtype, torch.float32
+    st = p.c_struct()
+    _check(lib().deform_conv_offsets(
+        ctypes.byref(st), _ptr(x, "x", s["x"], dt), _ptr(w_off, "w_off", s["w_off"], dt),
+        _ptr(b_off, "b_off", s["b_off"], f32, True),
+        _ptr(offset_add, "offset_add", s["offset"], f32, True),
+        _ptr(offset_out, "offset_out", s["offset"], f32), _stream(stream)), "deform_conv_offsets")
 
 
 # ---------------------------------------------------------------- conveniences

@@ -344,6 +344,30 @@ dc_status deform_conv_sample(const dc_problem* prob, const void* x, const void* 
   return cuda_status(timed("k1_band_sample", s, [&] { return launch_sample(sa, prob->dtype, s); }));
 }
 
+dc_status deform_conv_offsets(const dc_problem* prob, const void* x, const void* w_off,
+                              const float* b_off, const float* offset_add, float* offset_out,
+                              void* stream) {
+  Geom g;
+  int margin;
+  dc_status st = make_geom(prob, &g, &margin);
+  if (st != DC_OK) return st;
+  if (!x || !w_off || !offset_out) return DC_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, w_off, b_off, offset_add, offset_out};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return DC_ERR_UNSUPPORTED;
+  SampleArgs sa{};
+  sa.g = g;
+  sa.x = x;
+  sa.w_off = w_off;
+  sa.b_off = b_off;
+  sa.off_add = offset_add;
+  sa.col = nullptr;  // K1 stops after the offset convolution
+  sa.off_out = offset_out;
+  sa.margin = margin;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(timed("k1_offsets", s, [&] { return launch_sample(sa, prob->dtype, s); }));
+}
+
 const char* dc_status_string(dc_status status) {
   switch (status) {
     case DC_OK: return "DC_OK: success";

@@ -427,6 +427,7 @@ __global__ void __launch_bounds__(kThreads) k1_band_sample(SampleArgs a, Plan pl
   }
 
   pdl_release();  // the forward GEMM may set up while the sampling runs
+  if (!kReplay && col == nullptr) return;  // offset convolution only (no sampling)
 
   // ---------------------------------------------------------------- slow-path count
   if (a.slow_count && rank == 0) {

@@ -140,6 +140,22 @@ dc_status deform_conv_sample(const dc_problem* prob, const void* x, const void* 
                              const float* offset_in, void* col, float* offset_out,
                              unsigned long long* slowpath_count, void* stream);
 
+/* The offset convolution alone ("Following a deformable layer through DefT",
+ * Step 1 of 5: a small standard convolution over the input that predicts one
+ * (dy, dx) per tap and output pixel), written to HBM.  This is the first
+ * kernel of the unfused pipeline that the page contrasts with the fused one
+ * ("What people did before, and where it broke": offsets round-trip through
+ * memory before the interpolation reads them); deform_conv_sample with
+ * offset_in = these offsets is the second.  Same kernel as the fused stage,
+ * stopping before the interpolation.
+ *   x, w_off, b_off, offset_add  as in deform_conv_fwd
+ *   offset_out   [N, 2GK, Ho, Wo] float32, required
+ * Errors: DC_ERR_INVALID_ARG for a NULL x, w_off or offset_out,
+ * DC_ERR_UNSUPPORTED for a pointer that is not 16-byte aligned. */
+dc_status deform_conv_offsets(const dc_problem* prob, const void* x, const void* w_off,
+                              const float* b_off, const float* offset_add, float* offset_out,
+                              void* stream);
+
 /* Forward pass without a caller-provided workspace.  The paper has no
  * counterpart to this entry point; it exists for callers that cannot allocate
  * device memory -- loops that must not allocate once running, plug-ins whose

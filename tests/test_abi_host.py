@@ -115,3 +115,21 @@ def test_bwd_argument_checks_fail_before_any_launch():
     ptrs = [vp(0x10000 * (i + 1)) for i in range(11)]
     rc = B.lib().deform_conv_bwd(ctypes.byref(st), *ptrs, ctypes.c_size_t(need // 2), None)
     assert rc == B.DC_ERR_WORKSPACE
+
+
+def test_offsets_argument_checks_fail_before_any_launch():
+    p = problem()
+    st = p.c_struct()
+    vp = ctypes.c_void_p
+    good = [0x10000 * (i + 1) for i in range(5)]  # x w_off b_off add offset_out
+
+    def call(ptrs):
+        return B.lib().deform_conv_offsets(ctypes.byref(st), *[vp(v) if v else None for v in ptrs],
+                                           None)
+    for missing in (0, 1, 4):  # x, w_off and offset_out are required
+        bad = list(good)
+        bad[missing] = 0
+        assert call(bad) == B.DC_ERR_INVALID_ARG
+    bad = list(good)
+    bad[4] += 8
+    assert call(bad) == B.DC_ERR_UNSUPPORTED

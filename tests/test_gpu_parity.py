@@ -215,3 +215,28 @@ def test_backward_non_finite_gradient_propagates():
     # image 1 never sees the NaN: its gradient stays finite
     assert torch.isfinite(g["grad_x"][1]).all()
     assert B.device_error() == 0
+
+
+@pytest.mark.parametrize("dtype", [B.DC_F32, B.DC_BF16])
+def test_unfused_pipeline_matches_fused_stage(dtype):
+    """Offsets through HBM (deform_conv_offsets, then deform_conv_sample with
+    offset_in) give the fused stage's offsets and deformed map bit for bit,
+    and the offsets match the oracle."""
+    wl = W.WORKLOADS["res3_bf16" if dtype == B.DC_BF16 else "res3_f32"]
+    p = wl.problem()
+    d = {k: (None if v is None else v.cuda()) for k, v in W.generate(wl).items()}
+    s = p.shapes()
+    col_f = torch.empty(s["col"], dtype=p.torch_dtype, device="cuda")
+    off_f = torch.empty(s["offset"], dtype=torch.float32, device="cuda")
+    B.deform_conv_sample(p, d["x"], d["w_off"], d["b_off"], d["offset_add"], None, col_f, off_f)
+    off_u = torch.empty_like(off_f)
+    B.deform_conv_offsets(p, d["x"], d["w_off"], d["b_off"], d["offset_add"], off_u)
+    col_u = torch.empty_like(col_f)
+    B.deform_conv_sample(p, d["x"], None, None, None, off_u, col_u)
+    torch.cuda.synchronize()
+    assert torch.equal(off_u, off_f)
+    assert torch.equal(col_u.view(torch.int16) if dtype == B.DC_BF16 else col_u,
+                       col_f.view(torch.int16) if dtype == B.DC_BF16 else col_f)
+    cpu = {k: (None if v is None else v.cpu()) for k, v in d.items()}
+    _, off_ref = oracle_forward(p, cpu)
+    assert rel_err(f64(off_u), off_ref) <= TOL[dtype]
