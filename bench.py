@@ -361,6 +361,7 @@ def main():
         line["kernels"] = kernels
         line["sampling_stage"] = k1_roofline(p, t, dev, stream, flush, wl, args.roofline_iters)
         line["unfused_ablation"] = unfused_ablation(p, t, dev, stream, flush, args.roofline_iters)
+        line["margin"] = margin_report(p, t, dev)
         line["e2e"] = e2e(p, d, dev, stream, flops_step, args.e2e_iters)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
@@ -571,6 +572,26 @@ def unfused_ablation(p, t, dev, stream, flush, iters=200):
             "ai_fused": flops / bytes_fused, "ai_unfused": flops / bytes_unfused,
             "note": "fused: one K1 launch; unfused: offsets-only K1 then the sampler reading "
                     "offsets from HBM; both write the offsets and the deformed map"}
+
+
+def margin_report(p, t, dev):
+    """Slow-path fraction of the timed configuration's margin, measured by the
+    forward's own counter, and the margin the offset statistics suggest for at
+    most 1 % slow taps."""
+    import torch
+
+    from deformable_convolution_gb300 import binding as B
+    cnt = torch.zeros(1, dtype=torch.int64, device=dev)
+    y, off = B.forward(p, t["x"], t["w_off"], t["b_off"], t["w"], t["offset_add"],
+                       slowpath_count=cnt)
+    hist = torch.zeros(B.MARGIN_BINS, dtype=torch.int64, device=dev)
+    B.deform_conv_margin_histogram(p, off, hist)
+    torch.cuda.synchronize(dev)
+    h = [int(v) for v in hist.cpu().tolist()]
+    total = sum(h)
+    return {"halo_margin": p.halo_margin if p.halo_margin >= 0 else 3,
+            "slow_fraction": int(cnt.item()) / max(1, total),
+            "suggested_for_1pct": B.dc_suggest_margin(p, h, 0.01, True), "taps": total}
 
 
 def e2e(p, d, dev, stream, flops_step, iters=20):

@@ -23,8 +23,9 @@ EXPORTED_SYMBOLS = (
     "dc_out_h", "dc_out_w", "deform_conv_workspace_size", "deform_conv_fwd",
     "deform_conv_bwd", "deform_conv_sample", "dc_status_string", "dc_build_info",
     "dc_launch_count", "deform_conv_fwd_noalloc", "dc_device_error", "dc_kernel_timing",
-    "dc_kernel_times", "deform_conv_offsets",
+    "dc_kernel_times", "deform_conv_offsets", "deform_conv_margin_histogram", "dc_suggest_margin",
 )
+MARGIN_BINS = 64
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -64,6 +65,10 @@ def lib() -> ctypes.CDLL:
         L.deform_conv_sample.restype = i
         L.deform_conv_offsets.argtypes = [pp, vp, vp, vp, vp, vp, vp]
         L.deform_conv_offsets.restype = i
+        L.deform_conv_margin_histogram.argtypes = [pp, vp, vp, vp]
+        L.deform_conv_margin_histogram.restype = i
+        L.dc_suggest_margin.argtypes = [pp, ctypes.POINTER(ctypes.c_ulonglong), ctypes.c_double, i]
+        L.dc_suggest_margin.restype = i
         L.dc_status_string.argtypes = [i]
         L.dc_status_string.restype = ctypes.c_char_p
         L.dc_build_info.argtypes = []
@@ -281,6 +286,22 @@ def deform_conv_offsets(p: Problem, x, w_off, b_off, offset_add, offset_out, str
         _ptr(b_off, "b_off", s["b_off"], f32, True),
         _ptr(offset_add, "offset_add", s["offset"], f32, True),
         _ptr(offset_out, "offset_out", s["offset"], f32), _stream(stream)), "deform_conv_offsets")
+
+
+def deform_conv_margin_histogram(p: Problem, offset, hist, stream=None):
+    st = p.c_struct()
+    _check(lib().deform_conv_margin_histogram(
+        ctypes.byref(st), _ptr(offset, "offset", p.shapes()["offset"], torch.float32),
+        _ptr(hist, "hist", (MARGIN_BINS,), torch.int64), _stream(stream)),
+        "deform_conv_margin_histogram")
+
+
+def dc_suggest_margin(p: Problem, hist_host, max_slow_fraction: float, for_backward: bool) -> int:
+    """hist_host: MARGIN_BINS counts on the host (any integer sequence)."""
+    arr = (ctypes.c_ulonglong * MARGIN_BINS)(*[int(v) for v in hist_host])
+    st = p.c_struct()
+    return int(lib().dc_suggest_margin(ctypes.byref(st), arr, float(max_slow_fraction),
+                                       int(bool(for_backward))))
 
 
 # ---------------------------------------------------------------- conveniences

@@ -368,6 +368,46 @@ dc_status deform_conv_offsets(const dc_problem* prob, const void* x, const void*
   return cuda_status(timed("k1_offsets", s, [&] { return launch_sample(sa, prob->dtype, s); }));
 }
 
+dc_status deform_conv_margin_histogram(const dc_problem* prob, const float* offset,
+                                       unsigned long long* hist, void* stream) {
+  Geom g;
+  int margin;
+  dc_status st = make_geom(prob, &g, &margin);
+  if (st != DC_OK) return st;
+  if (!offset || !hist) return DC_ERR_INVALID_ARG;
+  int R, TW;
+  sample_band(g, prob->dtype, margin, &R, &TW);
+  return cuda_status(
+      launch_margin_histogram(offset, g, R, TW, hist, static_cast<cudaStream_t>(stream)));
+}
+
+int dc_suggest_margin(const dc_problem* prob, const unsigned long long* hist,
+                      double max_slow_fraction, int for_backward) {
+  if (!prob || !hist || !(max_slow_fraction >= 0.0 && max_slow_fraction <= 1.0)) return -1;
+  dc_problem q = *prob;
+  q.halo_margin = 0;
+  Geom g;
+  int m0;
+  if (make_geom(&q, &g, &m0) != DC_OK) return -1;
+  unsigned long long total = 0;
+  for (int b = 0; b < DC_MARGIN_BINS; ++b) total += hist[b];
+  // smallest m with (taps needing more than m) <= fraction * total
+  int m = DC_MARGIN_BINS - 1;
+  unsigned long long above = 0;
+  for (int b = DC_MARGIN_BINS - 1; b >= 1; --b) {
+    above += hist[b];  // taps needing b or more
+    if ((double)above > max_slow_fraction * (double)total) break;
+    m = b - 1;
+  }
+  if (m > kMaxMargin) m = kMaxMargin;
+  auto fits = [&](int mm) {
+    if (sample_smem_bytes(g, q.dtype, mm) > kMaxSmem) return false;
+    return !for_backward || bwd_smem_bytes(g, q.dtype, mm) <= kMaxSmem;
+  };
+  while (m > 0 && !fits(m)) --m;
+  return m;
+}
+
 const char* dc_status_string(dc_status status) {
   switch (status) {
     case DC_OK: return "DC_OK: success";

@@ -107,6 +107,8 @@ struct SampleArgs {
 };
 cudaError_t launch_sample(const SampleArgs& a, dc_dtype dt, cudaStream_t s);
 size_t sample_smem_bytes(const Geom& g, dc_dtype dt, int margin);
+// band (output rows R x columns TW) the fused stage tiles with at this margin
+void sample_band(const Geom& g, dc_dtype dt, int margin, int* R, int* TW);
 
 // Buffers a kernel zeroes as a side job (up to six float arrays); CTA `part`
 // of `nparts` clears its share of each, float4 where aligned.
@@ -191,6 +193,9 @@ struct OffconvBwdArgs {
 };
 cudaError_t launch_offconv_bwd(const OffconvBwdArgs& a, dc_dtype dt, cudaStream_t s);
 size_t offconv_bwd_smem_bytes(const Geom& g, dc_dtype dt);
+// histogram of the margin each sampling tap needs (DC_MARGIN_BINS bins)
+cudaError_t launch_margin_histogram(const float* offset, const Geom& g, int R, int TW,
+                                    unsigned long long* hist, cudaStream_t s);
 // tensor-core variant (bf16, few offset channels), chosen by launch_offconv_bwd
 bool offconv_bwd_tc_supported(const Geom& g, dc_dtype dt);
 size_t offconv_bwd_tc_smem_bytes(const Geom& g);

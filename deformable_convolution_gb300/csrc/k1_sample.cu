@@ -580,6 +580,12 @@ size_t sample_smem_bytes(const Geom& g, dc_dtype dt, int margin) {
   return make_plan(g, dt, margin, false).smem;
 }
 
+void sample_band(const Geom& g, dc_dtype dt, int margin, int* R, int* TW) {
+  const Plan p = make_plan(g, dt, margin, false);
+  *R = p.R;
+  *TW = p.TW;
+}
+
 cudaError_t launch_sample(const SampleArgs& a, dc_dtype dt, cudaStream_t s) {
   const bool replay = a.off_in != nullptr;
   const Plan pl = make_plan(a.g, dt, a.margin, replay);

@@ -156,6 +156,37 @@ dc_status deform_conv_offsets(const dc_problem* prob, const void* x, const void*
                               const float* b_off, const float* offset_add, float* offset_out,
                               void* stream);
 
+/* Margin statistics ("Why it works" / "The idea" on the explainer page: each
+ * tile is padded by just enough margin for the offsets that occur, measured
+ * from their distribution).  From the offsets a forward call returned, counts
+ * for every sampling tap (image, offset group, tap, output pixel) the margin
+ * in whole pixels its band's staged window needs to serve it on chip: how far
+ * the two rows and two columns it reads pass the edges of the band's
+ * receptive field, for the bands the fused stage uses with prob's current
+ * halo_margin.  Taps that sample entirely outside the image count as 0;
+ * needs of DC_MARGIN_BINS - 1 or more (and NaN positions) go to the last bin.
+ * With the same band shape, the taps of the bins above a margin m are exactly
+ * those the forward pass reads from global memory (its slowpath_count).
+ *   offset  [N, 2GK, Ho, Wo] float32 device pointer, required
+ *   hist    DC_MARGIN_BINS unsigned 64-bit device counters, required,
+ *           overwritten (cleared on the stream, then accumulated)
+ * Asynchronous on `stream`; allocates nothing.  Errors: DC_ERR_INVALID_ARG
+ * for NULL pointers or an invalid problem. */
+#define DC_MARGIN_BINS 64
+dc_status deform_conv_margin_histogram(const dc_problem* prob, const float* offset,
+                                       unsigned long long* hist, void* stream);
+
+/* Host helper: the smallest halo_margin m whose slow-path fraction, by the
+ * histogram (a HOST copy of deform_conv_margin_histogram's output), is at most
+ * max_slow_fraction: the taps in bins above m over all taps.  The result is
+ * lowered to the largest margin this build can stage for `prob` (forward, and
+ * backward too when for_backward != 0).  A margin large enough to make the
+ * fused stage pick smaller bands changes the shape the histogram assumed;
+ * measuring again at the new margin closes the loop.  Returns -1 for an
+ * invalid problem, histogram or fraction (outside [0, 1]). */
+int dc_suggest_margin(const dc_problem* prob, const unsigned long long* hist,
+                      double max_slow_fraction, int for_backward);
+
 /* Forward pass without a caller-provided workspace.  The paper has no
  * counterpart to this entry point; it exists for callers that cannot allocate
  * device memory -- loops that must not allocate once running, plug-ins whose

@@ -133,3 +133,37 @@ def test_offsets_argument_checks_fail_before_any_launch():
     bad = list(good)
     bad[4] += 8
     assert call(bad) == B.DC_ERR_UNSUPPORTED
+
+
+def _hist(**bins):
+    h = [0] * B.MARGIN_BINS
+    for k, v in bins.items():
+        h[int(k[1:])] = v
+    return h
+
+
+def test_suggest_margin_from_histogram():
+    p = problem()
+    # every tap needs 2 pixels: margin 2, whatever the allowed fraction
+    assert B.dc_suggest_margin(p, _hist(b2=1000), 0.0, False) == 2
+    assert B.dc_suggest_margin(p, _hist(b2=1000), 0.5, False) == 2
+    # 10 % of the taps need 5: allowed at 10 %, not at 5 %
+    h = _hist(b1=900, b5=100)
+    assert B.dc_suggest_margin(p, h, 0.10, False) == 1
+    assert B.dc_suggest_margin(p, h, 0.05, False) == 5
+    assert B.dc_suggest_margin(p, _hist(), 0.0, False) == 0  # no taps at all
+    assert B.dc_suggest_margin(p, h, -0.1, False) == -1
+    assert B.dc_suggest_margin(p, h, 1.5, False) == -1
+    assert B.dc_suggest_margin(problem(n=0), h, 0.1, False) == -1
+
+
+def test_suggested_margin_is_one_the_build_can_stage():
+    # a wide layer with a far-out tail: the ideal margin (62) does not fit in
+    # shared memory, so the helper lowers it to the largest one that does
+    p = problem(n=1, c_in=256, h=56, w=56, c_out=256, dtype=B.DC_BF16)
+    m = B.dc_suggest_margin(p, _hist(b1=10, b62=10), 0.0, True)
+    assert 0 <= m < 62
+    ok = B.Problem(1, 256, 56, 56, 256, dtype=B.DC_BF16, halo_margin=m)
+    assert ws_size(ok, True)[0] == B.DC_OK
+    too_big = B.Problem(1, 256, 56, 56, 256, dtype=B.DC_BF16, halo_margin=m + 1)
+    assert ws_size(too_big, True)[0] != B.DC_OK or ws_size(too_big, False)[0] != B.DC_OK

@@ -240,3 +240,62 @@ def test_unfused_pipeline_matches_fused_stage(dtype):
     cpu = {k: (None if v is None else v.cpu()) for k, v in d.items()}
     _, off_ref = oracle_forward(p, cpu)
     assert rel_err(f64(off_u), off_ref) <= TOL[dtype]
+
+
+def _margin_need_reference(p, off, R, TW):
+    """Per-tap margin need recomputed on the host from the offsets (float32
+    positions, as the kernels form them) for bands of R rows x TW columns."""
+    o = off.cpu().numpy().astype(np.float32)
+    n, m2, ho, wo = o.shape
+    K = p.kh * p.kw
+    G = m2 // (2 * K)
+    dy = o[:, 0::2].reshape(n, G, K, ho, wo)
+    dx = o[:, 1::2].reshape(n, G, K, ho, wo)
+    k = np.arange(K)
+    i, j = k // p.kw, k % p.kw
+    by = (np.arange(ho)[None, :] * p.stride[0] - p.pad[0] + i[:, None] * p.dil[0]).astype(np.float32)
+    bx = (np.arange(wo)[None, :] * p.stride[1] - p.pad[1] + j[:, None] * p.dil[1]).astype(np.float32)
+    py = by[None, None, :, :, None] + dy
+    px = bx[None, None, :, None, :] + dx
+    inside = (py >= -1) & (py < p.h) & (px >= -1) & (px < p.w)
+    # receptive field of each pixel's band
+    ylo = (np.arange(ho) // R * R * p.stride[0] - p.pad[0])[None, None, None, :, None]
+    xlo = (np.arange(wo) // TW * TW * p.stride[1] - p.pad[1])[None, None, None, None, :]
+    rows = (R - 1) * p.stride[0] + (p.kh - 1) * p.dil[0] + 1
+    cols = (TW - 1) * p.stride[1] + (p.kw - 1) * p.dil[1] + 1
+
+    def beyond(pos, lo, extent):
+        c = np.floor(pos)
+        return np.minimum(np.maximum(0, np.maximum(lo - c, c + 2 - (lo + extent))),
+                          B.MARGIN_BINS - 1)
+    b = np.where(inside, np.maximum(beyond(py, ylo, rows), beyond(px, xlo, cols)), 0)
+    return np.bincount(b.astype(np.int64).ravel(), minlength=B.MARGIN_BINS)
+
+
+def test_margin_histogram_and_suggested_margin_bound_the_slow_path():
+    wl = W.WORKLOADS["res3_bf16"]
+    p = wl.problem()
+    d = W.generate(wl)
+    _, off, _ = gpu_forward(p, d)
+    hist = torch.zeros(B.MARGIN_BINS, dtype=torch.int64, device="cuda")
+    B.deform_conv_margin_histogram(p, off, hist)
+    torch.cuda.synchronize()
+    h = hist.cpu().numpy()
+    # the fused stage tiles this 28 x 28 layer with bands of 4 full rows
+    # (112 of its 128-pixel budget)
+    assert np.array_equal(h, _margin_need_reference(p, off, 4, 28))
+    total = int(h.sum())
+    assert total == p.n * p.offset_groups * p.kh * p.kw * off.shape[2] * off.shape[3]
+    # at the default margin (3) exactly the taps above bin 3 took the slow path
+    _, _, slow3 = gpu_forward(p, d)
+    assert slow3 == int(h[4:].sum())
+    for frac in (0.0, 0.01, 0.2):
+        m = B.dc_suggest_margin(p, h.tolist(), frac, True)
+        assert m >= 0
+        pm = B.Problem(p.n, p.c_in, p.h, p.w, p.c_out, p.kh, p.kw, p.stride, p.pad, p.dil,
+                       p.offset_groups, p.dtype, m)
+        _, _, slow = gpu_forward(pm, d)
+        bound = int(h[m + 1:].sum())  # taps needing more than m
+        assert slow <= bound <= frac * total, (frac, m, slow, bound)
+        if frac == 0.01:
+            check_layer(pm, d)
