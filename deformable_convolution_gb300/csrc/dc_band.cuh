@@ -33,19 +33,11 @@ __host__ inline int pad_plane(int v) {
   return p;
 }
 
-// Band of at most `px` output pixels: full-width rows when the output is at
-// most `px` wide, else `px`-wide row segments.
-__host__ inline Shape make_shape(const Geom& g, int margin, int px) {
+// Tile of R output rows x TW output columns and its staged input window.
+__host__ inline Shape shape_rt(const Geom& g, int margin, int R, int TW) {
   Shape s{};
-  if (g.wo <= px) {
-    s.TW = g.wo;
-    s.R = px / g.wo;
-    if (s.R > g.ho) s.R = g.ho;
-    if (s.R < 1) s.R = 1;
-  } else {
-    s.TW = px;
-    s.R = 1;
-  }
+  s.TW = TW;
+  s.R = R;
   s.npx = s.R * s.TW;
   s.tiles_w = (int)ceil_div_ll(g.wo, s.TW);
   s.tiles_h = (int)ceil_div_ll(g.ho, s.R);
@@ -55,6 +47,43 @@ __host__ inline Shape make_shape(const Geom& g, int margin, int px) {
   s.cols = s.in_cols + 2 * margin;
   s.plane = pad_plane(s.rows * s.cols);
   return s;
+}
+
+// Per-shape cost model for the tile of at most `px` output pixels (the
+// page's tiling by output spatial dimensions, "The idea", with tile sizes left
+// open there).  Candidates: full-width rows (TW = Wo when Wo <= px) and 2-D
+// tiles of TW = 8, 16, ... columns.  Each is scored by the input positions all
+// tiles stage -- receptive field plus margin, the work of staging, clearing
+// and flushing the windows -- plus a fixed cost per tile (tables, weights,
+// barriers); full-width rows get a bonus for the contiguous row runs the
+// vector paths use, 8-column tiles a penalty for their half-sector writes of
+// the deformed map, and ties go to the wider tile.  Wide, dilated layers thus
+// get square-ish tiles instead of one-row bands whose window is mostly halo.
+constexpr double kTileFixedPositions = 512.0;
+constexpr double kFullWidthBonus = 0.85;
+constexpr double kNarrowPenalty = 1.15;
+
+__host__ inline Shape make_shape(const Geom& g, int margin, int px) {
+  Shape best{};
+  double best_cost = 0.0;
+  auto consider = [&](int TW) {
+    int R = px / TW;
+    if (R < 1) return;
+    if (R > g.ho) R = g.ho;
+    const Shape s = shape_rt(g, margin, R, TW);
+    double cost = (double)s.tiles_w * s.tiles_h * ((double)s.rows * s.cols + kTileFixedPositions);
+    if (TW == g.wo) cost *= kFullWidthBonus;
+    else if (TW < 16) cost *= kNarrowPenalty;
+    if (best.npx == 0 || cost <= best_cost) {
+      best = s;
+      best_cost = cost;
+    }
+  };
+  if (g.wo <= px) consider(g.wo);
+  for (int tw = 8; tw <= px; tw *= 2)
+    if (tw < g.wo) consider(tw);
+  if (best.npx == 0) consider(px < g.wo ? px : g.wo);
+  return best;
 }
 
 // Per (pixel, tap, group) sampling state.
