@@ -43,6 +43,7 @@ struct Plan {
   int cpc, csize;  // channels per CTA, number of channel slices
   int rows, cols, plane;
   int qcap;  // capacity of the deferred slow-tap queue
+  int ml;    // offset channels staged per CTA (2K per offset group of its slice)
   size_t off_halo, off_gx, off_offs, off_part, off_tab, off_q, smem;
 };
 
@@ -72,21 +73,20 @@ __host__ Plan make_plan(const Geom& g, dc_dtype dt, int margin) {
     at += (size_t)(bf16 ? cpc / 2 : cpc) * p.plane * 4;
     p.off_gx = at;
     at += (size_t)cpc * p.plane * 4;
+    int ngroups = 1;  // most offset groups any channel slice touches
+    for (int r = 0; r * cpc < g.c_in; ++r) {
+      const int lo = r * cpc, hi = (r + 1) * cpc < g.c_in ? (r + 1) * cpc : g.c_in;
+      const int ng = (hi - 1) / g.cg - lo / g.cg + 1;
+      if (ng > ngroups) ngroups = ng;
+    }
+    p.ml = 2 * g.K * ngroups;  // offset channels a CTA reads: its own groups only
     p.off_offs = at;
-    at += (size_t)g.M * p.ps * 4;
+    at += (size_t)p.ml * p.ps * 4;
     p.off_part = at;
-    at += (size_t)g.M * p.ps * 4;
+    at += (size_t)p.ml * p.ps * 4;
     p.off_tab = at;  // pixel table [ps] + tap offsets [K]
     at += (size_t)(p.ps + g.K) * 4;
-    {
-      int ngroups = 1;  // most offset groups any channel slice touches
-      for (int r = 0; r * cpc < g.c_in; ++r) {
-        const int lo = r * cpc, hi = (r + 1) * cpc < g.c_in ? (r + 1) * cpc : g.c_in;
-        const int ng = (hi - 1) / g.cg - lo / g.cg + 1;
-        if (ng > ngroups) ngroups = ng;
-      }
-      p.qcap = p.npx * g.K * (ngroups < 4 ? ngroups : 4);
-    }
+    p.qcap = p.npx * g.K * (ngroups < 4 ? ngroups : 4);
     p.off_q = at;  // queue counter + entries (overflow is handled in place)
     at += (size_t)(1 + p.qcap) * 4;
     p.smem = at;
@@ -247,8 +247,12 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
 
   uint32_t* xw = reinterpret_cast<uint32_t*>(smem + pl.off_halo);
   float* gxs = reinterpret_cast<float*>(smem + pl.off_gx);     // [cpc][PL] grad_x window
-  float* offs = reinterpret_cast<float*>(smem + pl.off_offs);  // [M][PS] offsets
-  float* part = reinterpret_cast<float*>(smem + pl.off_part);  // [M][PS]
+  // offsets and partial offset gradient of this slice's offset groups only:
+  // local row 2 * ((gg - g_begin) * K + k) (+1 for dx)
+  float* offs = reinterpret_cast<float*>(smem + pl.off_offs);  // [ml][PS]
+  float* part = reinterpret_cast<float*>(smem + pl.off_part);  // [ml][PS]
+  const int ml = 2 * g.K * ((c_end - 1) / g.cg - g_begin + 1);
+  const int m_base = 2 * g.K * g_begin;  // global offset channel of local row 0
   int* pix = reinterpret_cast<int*>(smem + pl.off_tab);        // (row << 16 | col) in band
   int* tapoff = pix + PS;                                      // window offset of tap k
   int* nslow = reinterpret_cast<int*>(smem + pl.off_q);        // deferred slow taps
@@ -262,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
   }
   band::stage_window<T>(x, g, img, c_begin, pl.cpc, ylo, xlo, pl.rows, pl.cols, PL, xw);
   for (int idx = tid; idx < pl.cpc * PL; idx += kThreads) gxs[idx] = 0.f;
-  for (int idx = tid; idx < M * PS; idx += kThreads) part[idx] = 0.f;
+  for (int idx = tid; idx < ml * PS; idx += kThreads) part[idx] = 0.f;
   if (tid == 0) {
     *nslow = 0;
     s_gmax = 0;
@@ -271,13 +275,13 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
   {
     band::Walk2 w;
     w.init(tid, kThreads, npx);
-    while (w.a < M) {
+    while (w.a < ml) {
       const int m = w.a, px = w.b;
       const int e = pix[px];
       const int ho = ho0 + (e >> 16), wo = wo0 + (e & 0xffff);
       float v = 0.f;
       if (ho < g.ho && wo < g.wo)
-        v = a.off[((long long)n * M + m) * g.howo + (long long)ho * g.wo + wo];
+        v = a.off[((long long)n * M + m_base + m) * g.howo + (long long)ho * g.wo + wo];
       offs[m * PS + px] = v;
       w.next();
     }
@@ -346,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
       int c = c_begin;
       for (int gg = g_begin; c < c_end; ++gg) {
         const int run_end = min(c_end, (gg + 1) * g.cg);
-        const Tap t = make_tap(by + offs[(2 * (gg * g.K + k)) * PS + px],
-                               bx + offs[(2 * (gg * g.K + k) + 1) * PS + px], g, ylo, xlo,
+        const Tap t = make_tap(by + offs[(2 * ((gg - g_begin) * g.K + k)) * PS + px],
+                               bx + offs[(2 * ((gg - g_begin) * g.K + k) + 1) * PS + px], g, ylo, xlo,
                                pl.rows, pl.cols);
         const int sbase = (t.y0 - ylo) * pl.cols + (t.x0 - xlo);
         const float hy = 1.0f - t.ly, hx = 1.0f - t.lx;
@@ -398,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
                                    cp, cstride, gxp, t.ly, t.lx, w00, w01, w10, w11, sdy, sdx);
           c = run_end;
         }
-        part[(2 * (gg * g.K + k)) * PS + px] = sdy;
-        part[(2 * (gg * g.K + k) + 1) * PS + px] = sdx;
+        part[(2 * ((gg - g_begin) * g.K + k)) * PS + px] = sdy;
+        part[(2 * ((gg - g_begin) * g.K + k) + 1) * PS + px] = sdx;
       }
     }
   }
@@ -421,8 +425,8 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
       const int e = pix[px];
       const int ho = ho0 + (e >> 16), wo = wo0 + (e & 0xffff);
       const int i = k / g.kw, j = k - i * g.kw;
-      const Tap t = make_tap((float)(ho * g.sh - g.ph + i * g.dh) + offs[(2 * (gg * g.K + k)) * PS + px],
-                             (float)(wo * g.sw - g.pw + j * g.dw) + offs[(2 * (gg * g.K + k) + 1) * PS + px],
+      const Tap t = make_tap((float)(ho * g.sh - g.ph + i * g.dh) + offs[(2 * ((gg - g_begin) * g.K + k)) * PS + px],
+                             (float)(wo * g.sw - g.pw + j * g.dw) + offs[(2 * ((gg - g_begin) * g.K + k) + 1) * PS + px],
                              g, ylo, xlo, pl.rows, pl.cols);
       const long long qo = (long long)ho * g.wo + wo;
       const float gc = __ldg(a.gcol + (long long)k * a.gcol_layout.row + (long long)n * a.gcol_layout.img +
@@ -436,8 +440,8 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
       gadd(gp, g, t.y0, t.x0 + 1, hy * t.lx * gc);
       gadd(gp, g, t.y0 + 1, t.x0, t.ly * hx * gc);
       gadd(gp, g, t.y0 + 1, t.x0 + 1, t.ly * t.lx * gc);
-      atomicAdd(part + (2 * (gg * g.K + k)) * PS + px, gc * (hx * (v10 - v00) + t.lx * (v11 - v01)));
-      atomicAdd(part + (2 * (gg * g.K + k) + 1) * PS + px, gc * (hy * (v01 - v00) + t.ly * (v11 - v10)));
+      atomicAdd(part + (2 * ((gg - g_begin) * g.K + k)) * PS + px, gc * (hx * (v10 - v00) + t.lx * (v11 - v01)));
+      atomicAdd(part + (2 * ((gg - g_begin) * g.K + k) + 1) * PS + px, gc * (hy * (v01 - v00) + t.ly * (v11 - v10)));
       if (col)
         col[(long long)k * a.col_layout.row + (long long)n * a.col_layout.img + qo + (long long)c * cstride] =
             from_f<T>(blend4(t.ly, t.lx, v00, v01, v10, v11));
@@ -456,19 +460,19 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
     if (vec) {
       band::Walk2 w;
       w.init(tid, kThreads, nvalid / 4);
-      while (w.a < M) {
+      while (w.a < ml) {
         const int m = w.a, p4 = w.b;
         w.next();
         const float4 v = *reinterpret_cast<const float4*>(part + m * PS + 4 * p4);
         if (v.x == 0.f && v.y == 0.f && v.z == 0.f && v.w == 0.f) continue;
-        atomicAdd(reinterpret_cast<float4*>(a.goff + ((long long)n * M + m) * g.howo +
+        atomicAdd(reinterpret_cast<float4*>(a.goff + ((long long)n * M + m_base + m) * g.howo +
                                             (long long)ho0 * g.wo + 4 * p4),
                   v);
       }
     } else {
       band::Walk2 w;
       w.init(tid, kThreads, npx);
-      while (w.a < M) {
+      while (w.a < ml) {
         const int m = w.a, px = w.b;
         w.next();
         const float v = part[m * PS + px];
@@ -476,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
         const int e = pix[px];
         const int ho = ho0 + (e >> 16), wo = wo0 + (e & 0xffff);
         if (ho < g.ho && wo < g.wo)
-          atomicAdd(a.goff + ((long long)n * M + m) * g.howo + (long long)ho * g.wo + wo, v);
+          atomicAdd(a.goff + ((long long)n * M + m_base + m) * g.howo + (long long)ho * g.wo + wo, v);
       }
     }
   }
