@@ -400,6 +400,8 @@ def kernel_costs(p, has_add):
         "gemm_fwd": ("tensor", gemm), "gemm_gcol": ("tensor", gemm), "gemm_gw": ("tensor", gemm),
         "k3_band_bwd": ("hbm", k3),
         "k4_offconv_bwd": ("hbm", k4),
+        # per-image grad_w_off partials of the tensor-core K4, summed
+        "gw_off_reduce": ("hbm", (p.n + 1) * p.n_off * kdim * 4),
     }
 
 

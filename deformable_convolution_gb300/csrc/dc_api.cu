@@ -126,7 +126,7 @@ dc_status make_geom(const dc_problem* p, Geom* g, int* margin) {
 // to a multiple of 8 elements so that every row starts 16-byte aligned.
 struct Plan {
   ColLayout col, gcol;
-  size_t col_off, gcol_off, off_off, gmax_off, total;
+  size_t col_off, gcol_off, off_off, gmax_off, gwo_img_off, total;
   int gmax_tx, gmax_ty;
 };
 
@@ -149,6 +149,11 @@ Plan make_plan(const Geom& g, dc_dtype dt, int backward) {
   pl.gmax_tx = (int)ceil_div_ll(g.howo, 128);
   pl.gmax_ty = (int)ceil_div_ll(g.kdim, 128);
   pl.gmax_off = backward ? take((size_t)g.n * pl.gmax_tx * pl.gmax_ty * 4 * sizeof(float)) : 0;
+  // per-image grad_w_off partials of the tensor-core offset-conv backward
+  // (one image's bands add into one copy: far fewer atomics per address)
+  pl.gwo_img_off = backward && offconv_bwd_tc_supported(g, dt)
+                       ? take((size_t)g.n * g.M * g.kdim * sizeof(float))
+                       : 0;
   pl.total = at;
   return pl;
 }
@@ -274,6 +279,9 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
   ga.zero.n[3] = grad_b_off ? g.M : 0;
   ga.zero.p[4] = goff;
   ga.zero.n[4] = (long long)g.n * g.M * g.howo;
+  float* gwo_img = pl.gwo_img_off ? reinterpret_cast<float*>(wsb + pl.gwo_img_off) : nullptr;
+  ga.zero.p[5] = gwo_img;
+  ga.zero.n[5] = gwo_img ? (long long)g.n * g.M * g.kdim : 0;
   // the tensor-core GCOL GEMM also reports max |gcol| per tile, from which K3
   // scales its fixed-point grad_x accumulation
   const bool tc_gcol = prob->dtype == DC_BF16 && tc_gemm_supported(g);
@@ -308,11 +316,16 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
   oa.gx = grad_x;
   oa.gw_off = grad_w_off;
   oa.gb_off = grad_b_off;
+  oa.gw_off_img = gwo_img;
   st = cuda_status(timed("k4_offconv_bwd", s, [&] { return launch_offconv_bwd(oa, prob->dtype, s); }));
   if (st != DC_OK) return st;
 
   // main weight gradient from the replayed map
-  return cuda_status(timed("gemm_gw", s, [&] { return launch_gemm_gw(ga, prob->dtype, s); }));
+  st = cuda_status(timed("gemm_gw", s, [&] { return launch_gemm_gw(ga, prob->dtype, s); }));
+  if (st != DC_OK || !gwo_img) return st;
+
+  // grad_w_off from K4's per-image partials
+  return cuda_status(timed("gw_off_reduce", s, [&] { return launch_gw_off_reduce(oa, s); }));
 }
 
 dc_status deform_conv_sample(const dc_problem* prob, const void* x, const void* w_off,

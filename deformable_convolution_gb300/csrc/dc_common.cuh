@@ -190,6 +190,9 @@ struct OffconvBwdArgs {
   float* gx;
   float* gw_off;
   float* gb_off;  // may be null
+  // tensor-core kernel: per-image partial sums of grad_w_off [n][M][C_in][K]
+  // (cleared by GCOL), reduced into gw_off by launch_gw_off_reduce
+  float* gw_off_img;
 };
 cudaError_t launch_offconv_bwd(const OffconvBwdArgs& a, dc_dtype dt, cudaStream_t s);
 size_t offconv_bwd_smem_bytes(const Geom& g, dc_dtype dt);
@@ -200,5 +203,7 @@ cudaError_t launch_margin_histogram(const float* offset, const Geom& g, int R, i
 bool offconv_bwd_tc_supported(const Geom& g, dc_dtype dt);
 size_t offconv_bwd_tc_smem_bytes(const Geom& g);
 cudaError_t launch_offconv_bwd_tc(const OffconvBwdArgs& a, cudaStream_t s);
+// gw_off = sum over images of gw_off_img (launched after the grad_W GEMM)
+cudaError_t launch_gw_off_reduce(const OffconvBwdArgs& a, cudaStream_t s);
 
 }  // namespace dc

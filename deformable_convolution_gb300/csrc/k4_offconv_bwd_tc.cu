@@ -80,14 +80,13 @@ __host__ TcPlan make_tc_plan(const Geom& g, int px) {
   return p;
 }
 
-// Largest band that keeps three CTAs per SM, else two, else the smallest.
+// Largest tile that fits two CTAs per SM (fewer, larger tiles: less staging
+// halo and fewer grad_w_off partial sums), else the smallest.
 __host__ TcPlan pick_tc_plan(const Geom& g) {
-  const size_t budgets[2] = {72 * 1024, 110 * 1024};
-  for (size_t budget : budgets)
-    for (int px = band::kBandPx; px >= 32; px /= 2) {
-      const TcPlan p = make_tc_plan(g, px);
-      if (p.smem <= budget) return p;
-    }
+  for (int px = band::kBandPx; px >= 32; px /= 2) {
+    const TcPlan p = make_tc_plan(g, px);
+    if (p.smem <= 110 * 1024) return p;
+  }
   return make_tc_plan(g, 32);
 }
 
@@ -133,6 +132,9 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
   const int gid = lane >> 2, tig = lane & 3;
   const int M = g.M, K = g.K;
   const long long img = (long long)n * g.c_in * g.hw;
+  // grad_w_off partial sums: this image's copy (reduced after the grad_W GEMM)
+  // when given, else grad_w_off itself
+  float* gwo = a.gw_off_img ? a.gw_off_img + (long long)n * M * g.c_in * K : a.gw_off;
 
   uint32_t* xp = reinterpret_cast<uint32_t*>(smem + pl.off_xp);      // [kCpc][xplane]
   uint32_t* ga = reinterpret_cast<uint32_t*>(smem + pl.off_ga);      // [mp8][sa]
@@ -378,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
             const int cl = gid + (h >> 1) * 8;
             const int m = (mt0 + t) * 8 + 2 * tig + (h & 1);
             if (cl < ncur && m < M)
-              atomicAdd(a.gw_off + ((long long)m * g.c_in + c_begin + cl) * K + k, acc[t][h]);
+              atomicAdd(gwo + ((long long)m * g.c_in + c_begin + cl) * K + k, acc[t][h]);
           }
         }
       }
@@ -462,7 +464,73 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
   }
 }
 
+// grad_w_off[e] = sum over images of the per-image partials; one thread per
+// element, the image loop strided by M * C_in * K
+__global__ void __launch_bounds__(kThreads) gw_off_reduce(const float* __restrict__ img_part,
+                                                          float* __restrict__ gw_off, int nimg,
+                                                          long long count) {
+  pdl_wait();  // the partials are complete once K4 (and the GEMM after it) finished
+  if ((count & 3) == 0 && (reinterpret_cast<uintptr_t>(img_part) & 15) == 0 &&
+      (reinterpret_cast<uintptr_t>(gw_off) & 15) == 0) {
+    // float4 columns, eight images' loads in flight per thread
+    const long long c4 = count / 4;
+    const float4* src = reinterpret_cast<const float4*>(img_part);
+    for (long long e = blockIdx.x * (long long)kThreads + threadIdx.x; e < c4;
+         e += (long long)gridDim.x * kThreads) {
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+      int n = 0;
+      for (; n + 8 <= nimg; n += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = src[(long long)(n + u) * c4 + e];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          s.x += v[u].x;
+          s.y += v[u].y;
+          s.z += v[u].z;
+          s.w += v[u].w;
+        }
+      }
+      for (; n < nimg; ++n) {
+        const float4 v = src[(long long)n * c4 + e];
+        s.x += v.x;
+        s.y += v.y;
+        s.z += v.z;
+        s.w += v.w;
+      }
+      reinterpret_cast<float4*>(gw_off)[e] = s;
+    }
+    return;
+  }
+  for (long long e = blockIdx.x * (long long)kThreads + threadIdx.x; e < count;
+       e += (long long)gridDim.x * kThreads) {
+    float s = 0.f;
+    for (int n = 0; n < nimg; ++n) s += img_part[(long long)n * count + e];
+    gw_off[e] = s;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_gw_off_reduce(const OffconvBwdArgs& a, cudaStream_t s) {
+  const long long count = (long long)a.g.M * a.g.kdim;
+  long long blocks = (count / 4 + kThreads - 1) / kThreads;
+  if (blocks > 152 * 4) blocks = 152 * 4;
+  if (blocks < 1) blocks = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gw_off_reduce, (const float*)a.gw_off_img, a.gw_off,
+                                     a.g.n, count);
+  note_launches(1);
+  return e;
+}
 
 bool offconv_bwd_tc_supported(const Geom& g, dc_dtype dt) { return dt == DC_BF16 && g.M <= kMaxM; }
 
