@@ -532,7 +532,8 @@ cudaError_t launch_gemm_gw_tc(const GemmArgs& ga, cudaStream_t s) {
   a.kb_total = a.qblocks * g.n;
   a.out = ga.gw;
   const long long tiles = ceil_div_ll(g.kdim, 128) * ceil_div_ll(g.c_out, kBM);
-  long long splits = ceil_div_ll(2 * 148, tiles);
+  // about one CTA per SM: more splits only add float4 atomics on grad_W
+  long long splits = ceil_div_ll(152, tiles);
   if (splits > a.kb_total) splits = a.kb_total;
   if (splits < 1) splits = 1;
   a.kb_per_split = (int)ceil_div_ll(a.kb_total, splits);
