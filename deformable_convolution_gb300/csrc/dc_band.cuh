@@ -15,7 +15,7 @@
 namespace dc {
 namespace band {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;  // block size of K3 and K4 (the helpers take any)
 constexpr int kBandPx = 128;  // largest band; smaller ones are tried when shared memory is short
 constexpr int kMaxCluster = 8;
 
@@ -197,7 +197,7 @@ __device__ __forceinline__ void stage_window_quads(const __nv_bfloat16* __restri
   const int nq = q_hi - q_lo + 1;
   const int units = cpc / 2;
   Walk3 w;
-  w.init(threadIdx.x, kThreads, rows, nq);
+  w.init(threadIdx.x, blockDim.x, rows, nq);
   while (w.a < units) {
     uint2 v0[kBatch], v1[kBatch];
     int uu[kBatch], rr[kBatch], qq[kBatch];
@@ -250,7 +250,7 @@ __device__ __forceinline__ void stage_window(const T* __restrict__ x, const Geom
   constexpr int kBatch = 16;
   const int units = kPairs ? cpc / 2 : cpc;
   Walk3 w;
-  w.init(threadIdx.x, kThreads, rows, cols);
+  w.init(threadIdx.x, blockDim.x, rows, cols);
   while (w.a < units) {
     uint32_t v[kBatch];
     int at[kBatch];
@@ -285,7 +285,7 @@ __device__ __forceinline__ void stage_window(const T* __restrict__ x, const Geom
 // Per-band table of output pixels: packs (row in band, column in band) into
 // one int so inner loops need no division by the band width.
 __device__ __forceinline__ void fill_pixel_table(int* tab, int npx, int TW) {
-  for (int px = threadIdx.x; px < npx; px += kThreads) {
+  for (int px = threadIdx.x; px < npx; px += blockDim.x) {
     const int r = px / TW;
     tab[px] = (r << 16) | (px - r * TW);
   }

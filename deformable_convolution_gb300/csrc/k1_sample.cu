@@ -35,7 +35,7 @@ namespace cg = cooperative_groups;
 namespace dc {
 namespace {
 
-using band::kThreads;
+constexpr int kThreads = 384;  // block size of K1 (12 warps: two CTAs per SM hide more latency)
 using band::Tap;
 using band::gload;
 using band::make_tap;
@@ -141,7 +141,7 @@ __device__ __forceinline__ float sample_global(const T* plane, const Geom& g, co
 }
 
 template <typename T, bool kReplay>
-__global__ void __launch_bounds__(kThreads) k1_band_sample(SampleArgs a, Plan pl) {
+__global__ void __launch_bounds__(kThreads, 2) k1_band_sample(SampleArgs a, Plan pl) {
   extern __shared__ __align__(16) unsigned char smem[];
   constexpr bool kBf16 = sizeof(T) == 2;
   const Geom g = a.g;
