@@ -320,9 +320,17 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
   st = cuda_status(timed("k4_offconv_bwd", s, [&] { return launch_offconv_bwd(oa, prob->dtype, s); }));
   if (st != DC_OK) return st;
 
-  // main weight gradient from the replayed map
+  // main weight gradient from the replayed map; the tensor-core GEMM also sums
+  // K4's per-image grad_w_off partials once K4 is done (its CTAs wait for K4
+  // before exiting anyway), else a small kernel does
+  const bool gw_reduces = gwo_img && tc_gcol && (g.M * g.kdim) % 4 == 0;
+  if (gw_reduces) {
+    ga.gwo_img = gwo_img;
+    ga.gw_off = grad_w_off;
+    ga.gwo_count = (long long)g.M * g.kdim;
+  }
   st = cuda_status(timed("gemm_gw", s, [&] { return launch_gemm_gw(ga, prob->dtype, s); }));
-  if (st != DC_OK || !gwo_img) return st;
+  if (st != DC_OK || !gwo_img || gw_reduces) return st;
 
   // grad_w_off from K4's per-image partials
   return cuda_status(timed("gw_off_reduce", s, [&] { return launch_gw_off_reduce(oa, s); }));

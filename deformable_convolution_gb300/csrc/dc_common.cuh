@@ -147,6 +147,11 @@ struct GemmArgs {
   float* gw;          // [c_out][kdim] fp32, accumulated with atomics (backward)
   ZeroArgs zero;      // GCOL kernels clear these (the backward's atomic targets)
   float* gmax;        // tensor-core GCOL: max |gcol| per 128 x 128 tile (4 floats each), or null
+  // tensor-core GW: after K4, gw_off = sum over images of gwo_img (count
+  // floats per image); null = nothing to reduce
+  const float* gwo_img;
+  float* gw_off;
+  long long gwo_count;
 };
 // Tensor-core (tcgen05, bf16) versions; need tc_gemm_supported(g).
 bool tc_gemm_supported(const Geom& g);

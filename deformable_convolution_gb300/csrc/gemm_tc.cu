@@ -44,6 +44,10 @@ struct TcArgs {
   long long out_row, out_img;  // GCOL: gcol pitches (elements)
   ZeroArgs zero;               // GCOL: the backward's atomic targets, cleared by warps 0-3
   float* gmax;                 // GCOL: max |gcol| of each tile, one float per epilogue warp
+  const float* gwo_img;        // GW: per-image grad_w_off partials to sum after K4 (or null)
+  float* gw_off;
+  long long gwo_count;         // floats per image
+  int gwo_nimg;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -374,7 +378,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"((uint32_t)C::kTmemCols)
                  : "memory");
-  if (KIND == GW) pdl_wait();  // completes no earlier than K4
+  if (KIND == GW) {
+    pdl_wait();  // completes no earlier than K4
+    if (a.gwo_img) {
+      // K4 is complete: sum its per-image grad_w_off partials, float4 columns
+      // spread over all CTAs of this grid (both buffers are 16-byte aligned
+      // and the count is a multiple of 4: checked on the host)
+      const long long c4 = a.gwo_count / 4;
+      const long long nthreads = (long long)gridDim.x * gridDim.y * gridDim.z * kThreads;
+      const long long me =
+          ((long long)blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z)) *
+              kThreads + threadIdx.x;
+      const float4* src = reinterpret_cast<const float4*>(a.gwo_img);
+      for (long long e = me; e < c4; e += nthreads) {
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int n = 0; n < a.gwo_nimg; ++n) {
+          const float4 v = src[(long long)n * c4 + e];
+          s.x += v.x;
+          s.y += v.y;
+          s.z += v.z;
+          s.w += v.w;
+        }
+        reinterpret_cast<float4*>(a.gw_off)[e] = s;
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -524,6 +552,15 @@ cudaError_t launch_gemm_gw_tc(const GemmArgs& ga, cudaStream_t s) {
   if (!gy_map(&A, ga.gy, g, 128)) return cudaErrorInvalidValue;
   if (!col_map(&B, ga.col, g, ga.col_layout, 128)) return cudaErrorInvalidValue;
   TcArgs a{};
+  if (ga.gwo_img) {
+    if ((ga.gwo_count & 3) || (reinterpret_cast<uintptr_t>(ga.gwo_img) & 15) ||
+        (reinterpret_cast<uintptr_t>(ga.gw_off) & 15))
+      return cudaErrorInvalidValue;
+    a.gwo_img = ga.gwo_img;
+    a.gw_off = ga.gw_off;
+    a.gwo_count = ga.gwo_count;
+    a.gwo_nimg = g.n;
+  }
   a.c_out = g.c_out;
   a.kdim = g.kdim;
   a.howo = (int)g.howo;
