@@ -22,6 +22,8 @@
 // skips the rest of its work, frees its tensor memory and returns.
 #include <cuda.h>
 
+#include <cooperative_groups.h>
+
 #include "dc_common.cuh"
 
 namespace dc {
@@ -40,6 +42,7 @@ struct TcArgs {
   int kb_total;          // k-blocks of the whole reduction
   int kb_per_split;      // GW: k-blocks per CTA along blockIdx.z
   int qblocks;           // GW: k-blocks per image (ceil(howo / 64))
+  int fwd_split;         // FWD: 2 = the k-blocks are split over a 2-CTA cluster along y
   void* out;
   long long out_row, out_img;  // GCOL: gcol pitches (elements)
   ZeroArgs zero;               // GCOL: the backward's atomic targets, cleared by warps 0-3
@@ -100,6 +103,29 @@ __device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, uint64
       "{%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+
+// Row m of y (bf16), columns n_first .. n_first + 31, from 32 fp32 values.
+__device__ __forceinline__ void store_y_row(__nv_bfloat16* dst, const uint32_t* r, int n_first,
+                                            int howo) {
+  if (n_first + 32 <= howo) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      uint4 pk;
+      uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[v * 8 + 2 * e]),
+                                                  __uint_as_float(r[v * 8 + 2 * e + 1]));
+        pw[e] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+      *reinterpret_cast<uint4*>(dst + v * 8) = pk;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (n_first + j < howo) dst[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+  }
 }
 
 // TMA store of a shared-memory box (bulk-group completion).
@@ -173,7 +199,8 @@ struct Cfg {
   static constexpr int kStage = kABytes + kBBytes;
   // GCOL reduces over C_out only (a few k-blocks): two stages, so that three
   // CTAs fit on an SM; the long reductions keep a deeper ring.
-  static constexpr int kStages = KIND == GCOL ? 2 : (BN >= 128 ? 4 : 6);
+  // GCOL has two k-blocks; four stages let two FWD CTAs share an SM
+  static constexpr int kStages = KIND == GCOL ? 2 : 4;
   static constexpr int kTmemCols = BN < 32 ? 32 : BN;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256;
   static constexpr int kAMn = KIND == GCOL ? 1 : 0;
@@ -194,13 +221,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * BN;
+  // FWD split over a 2-CTA cluster: rank 0 takes the first half of the
+  // k-blocks, rank 1 the second; rank 1 hands its fp32 tile to rank 0 through
+  // distributed shared memory and rank 0 writes y
+  const bool split = KIND == FWD && a.fwd_split == 2;
+  const int rank = split ? (int)(blockIdx.y & 1) : 0;
+  const int m0 = (split ? (int)(blockIdx.y >> 1) : (int)blockIdx.y) * kBM, n0 = blockIdx.x * BN;
   const int z = blockIdx.z;
   int kb_begin = 0, kb_end = a.kb_total;
   if (KIND == GW) {
     kb_begin = z * a.kb_per_split;
     kb_end = min(a.kb_total, kb_begin + a.kb_per_split);
   }
+  if (split) {
+    const int half = (a.kb_total + 1) / 2;
+    kb_begin = rank ? half : 0;
+    kb_end = rank ? a.kb_total : half;
+  }
+  bool ok = true;  // epilogue warps: the MMAs completed (no wait expired)
   const int nkb = kb_end > kb_begin ? kb_end - kb_begin : 0;
 
   if (warp == 0) {
@@ -290,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long part = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
       zero_share(a.zero, part, nparts, threadIdx.x, 128);
     }
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0));
+    ok = __all_sync(0xffffffffu, mbar_wait(done, 0));
     tc_fence_after();
     pdl_release();
     const int row = warp * 32 + lane;
@@ -305,28 +343,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tbase + c * 32, r);
       if (!ok || nkb == 0) continue;
       const int n_first = n0 + c * 32;
-      if (KIND == FWD) {
-        if (m >= a.c_out) continue;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
-                             ((long long)z * a.c_out + m) * a.howo + n_first;
-        if (n_first + 32 <= a.howo) {
+      if (KIND == FWD && split) {
+        // rank 1: its partial tile to its own shared memory, column-major
+        // (lanes write consecutive words); rank 0 combines after the cluster
+        // barrier below
+        if (rank == 1) {
+          float* part = reinterpret_cast<float*>(smem);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 pk;
-            uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[v * 8 + 2 * e]),
-                                                        __uint_as_float(r[v * 8 + 2 * e + 1]));
-              pw[e] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-            *reinterpret_cast<uint4*>(dst + v * 8) = pk;
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (n_first + j < a.howo) dst[j] = __float2bfloat16_rn(__uint_as_float(r[j]));
+          for (int j = 0; j < 32; ++j) part[(c * 32 + j) * kBM + row] = __uint_as_float(r[j]);
         }
+      } else if (KIND == FWD) {
+        if (m >= a.c_out) continue;
+        store_y_row(static_cast<__nv_bfloat16*>(a.out) + ((long long)z * a.c_out + m) * a.howo + n_first,
+                    r, n_first, a.howo);
       } else if (KIND == GCOL) {
         // this warp's 32 rows x 32 columns go through shared memory (the
         // operand stages are free once `done` fired) in the 128-byte swizzled
@@ -371,6 +400,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       const long long tile = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * z);
       if (lane == 0) a.gmax[tile * 4 + warp] = __uint_as_float(amax);
     }
+  }
+  if (KIND == FWD && split) {
+    // every thread of both CTAs: rank 1's partial is in its shared memory
+    cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
+    cluster.sync();
+    if (rank == 0 && warp < 4) {
+      const float* peer = cluster.map_shared_rank(reinterpret_cast<float*>(smem), 1);
+      const int row = warp * 32 + lane;
+      const int m = m0 + row;
+      const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
+      const bool peer_ok = nkb > 0 && a.kb_total > (a.kb_total + 1) / 2;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tbase + c * 32, r);
+        if (!ok) continue;
+        if (peer_ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            r[j] = __float_as_uint(__uint_as_float(r[j]) + peer[(c * 32 + j) * kBM + row]);
+        }
+        const int n_first = n0 + c * 32;
+        if (m < a.c_out)
+          store_y_row(static_cast<__nv_bfloat16*>(a.out) + ((long long)z * a.c_out + m) * a.howo + n_first,
+                      r, n_first, a.howo);
+      }
+    }
+    cluster.sync();  // rank 0 is done reading rank 1's shared memory
   }
   tc_fence_before();
   __syncthreads();
@@ -441,7 +498,7 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 
 template <int KIND, int BN>
 cudaError_t launch(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Cm,
-                   const TcArgs& a, dim3 grid, cudaStream_t s) {
+                   const TcArgs& a, dim3 grid, cudaStream_t s, int cluster_y = 1) {
   using C = Cfg<KIND, BN>;
   auto k = tc_gemm<KIND, BN>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
@@ -451,13 +508,24 @@ cudaError_t launch(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  int nattr = 0;
   // the forward GEMM follows K1 and the weight-gradient GEMM follows K4 in the
   // same call: both may start their prologue early
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  if (KIND != GCOL) {
+    attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+    ++nattr;
+  }
+  if (cluster_y > 1) {
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = 1;
+    attr[nattr].val.clusterDim.y = (unsigned)cluster_y;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = KIND == GCOL ? 0 : 1;
+  cfg.numAttrs = nattr;
   e = cudaLaunchKernelEx(&cfg, k, A, B, Cm, a);
   note_launches(1);
   return e;
@@ -521,8 +589,14 @@ cudaError_t launch_gemm_fwd_tc(const GemmArgs& ga, cudaStream_t s) {
   a.kb_total = (int)ceil_div_ll(g.kdim, kBK);
   a.out = ga.y;
   const int bn = pick_fwd_bn(g);
-  dim3 grid((unsigned)ceil_div_ll(g.howo, bn), (unsigned)ceil_div_ll(g.c_out, kBM), (unsigned)g.n);
-  return bn == 128 ? launch<FWD, 128>(A, B, A, a, grid, s) : launch<FWD, 64>(A, B, A, a, grid, s);
+  const long long tiles = ceil_div_ll(g.howo, bn) * ceil_div_ll(g.c_out, kBM) * g.n;
+  // fewer output tiles than SMs and a long reduction: split the k-blocks over
+  // a 2-CTA cluster (measured: a gain from 36 k-blocks, a loss at 18)
+  a.fwd_split = (bn == 64 && tiles < 152 && a.kb_total >= 24) ? 2 : 1;
+  dim3 grid((unsigned)ceil_div_ll(g.howo, bn), (unsigned)(ceil_div_ll(g.c_out, kBM) * a.fwd_split),
+            (unsigned)g.n);
+  return bn == 128 ? launch<FWD, 128>(A, B, A, a, grid, s)
+                   : launch<FWD, 64>(A, B, A, a, grid, s, a.fwd_split);
 }
 
 cudaError_t launch_gemm_gcol_tc(const GemmArgs& ga, cudaStream_t s) {
