@@ -37,12 +37,12 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 TRAFFIC = {
     # ncu --set full, res3 bf16, one launch each (profiles/<kernel>_res3_bf16.md,
     # profiles/tc_gemm_res3_bf16.md).  Writes mostly stay in the 129 MB L2.
-    ("res3_bf16", "k1_band_sample"): {"bytes": 2194176 + 256, "source": "f4ff7e59de4eecdc"},
-    ("res3_bf16", "k3_band_bwd"): {"bytes": 34715392 + 8192, "source": "062a6ec493dd8fee"},
-    ("res3_bf16", "k4_offconv_bwd"): {"bytes": 5468416, "source": "68a77d531657e67e"},
-    ("res3_bf16", "gemm_fwd"): {"bytes": 14764544, "source": "dabb998c5a83207d"},
-    ("res3_bf16", "gemm_gcol"): {"bytes": 1941248, "source": "dabb998c5a83207d"},
-    ("res3_bf16", "gemm_gw"): {"bytes": 16665600, "source": "dabb998c5a83207d"},
+    ("res3_bf16", "k1_band_sample"): {"bytes": 2192384 + 512, "source": "048294db81b141f0"},
+    ("res3_bf16", "k3_band_bwd"): {"bytes": 34712576 + 7168, "source": "15194933f3c16819"},
+    ("res3_bf16", "k4_offconv_bwd"): {"bytes": 6049024, "source": "78b457f998f30ead"},
+    ("res3_bf16", "gemm_fwd"): {"bytes": 14772224, "source": "4627777b2563466e"},
+    ("res3_bf16", "gemm_gcol"): {"bytes": 1940992 + 6144, "source": "4627777b2563466e"},
+    ("res3_bf16", "gemm_gw"): {"bytes": 17334528, "source": "4627777b2563466e"},
 }
 KERNEL_SOURCES = {
     "k1_band_sample": "k1_sample.cu", "k3_band_bwd": "k3_band_bwd.cu",

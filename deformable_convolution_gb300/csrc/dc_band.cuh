@@ -70,6 +70,7 @@ __host__ inline Shape make_shape(const Geom& g, int margin, int px) {
     int R = px / TW;
     if (R < 1) return;
     if (R > g.ho) R = g.ho;
+    R = (int)ceil_div_ll(g.ho, ceil_div_ll(g.ho, R));  // same tile count, rows balanced
     const Shape s = shape_rt(g, margin, R, TW);
     double cost = (double)s.tiles_w * s.tiles_h * ((double)s.rows * s.cols + kTileFixedPositions);
     if (TW == g.wo) cost *= kFullWidthBonus;
