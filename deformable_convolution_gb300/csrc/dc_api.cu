@@ -144,7 +144,10 @@ Plan make_plan(const Geom& g, dc_dtype dt, int backward) {
   };
   pl.col_off = take((size_t)g.kdim * pl.col.row * elt_size(dt));
   pl.off_off = take((size_t)g.n * g.M * g.howo * sizeof(float));
-  pl.gcol_off = backward ? take((size_t)g.kdim * pl.gcol.row * sizeof(float)) : 0;
+  // gcol: bf16 from the tensor-core GEMM (K3 then scales it into fixed point),
+  // fp32 from the CUDA-core GEMM
+  const size_t gcol_elt = dt == DC_BF16 && tc_gemm_supported(g) ? 2 : sizeof(float);
+  pl.gcol_off = backward ? take((size_t)g.kdim * pl.gcol.row * gcol_elt) : 0;
   // per-tile max |gcol| written by the tensor-core GCOL GEMM (128 x 128 tiles)
   pl.gmax_tx = (int)ceil_div_ll(g.howo, 128);
   pl.gmax_ty = (int)ceil_div_ll(g.kdim, 128);
@@ -265,7 +268,7 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
   ga.col = wsb + pl.col_off;
   ga.col_layout = pl.col;
   ga.gy = grad_y;
-  ga.gcol = reinterpret_cast<float*>(wsb + pl.gcol_off);
+  ga.gcol = wsb + pl.gcol_off;
   ga.gcol_layout = pl.gcol;
   ga.gw = grad_w;
   // the GCOL launch also clears the buffers later kernels accumulate into

@@ -142,7 +142,7 @@ struct GemmArgs {
   ColLayout col_layout;
   const void* gy;     // [n][c_out][howo], dtype
   void* y;            // [n][c_out][howo], dtype (forward)
-  float* gcol;        // column-layout gradient, fp32 (backward)
+  void* gcol;         // column-layout gradient: bf16 from the tensor-core GEMM, else fp32
   ColLayout gcol_layout;
   float* gw;          // [c_out][kdim] fp32, accumulated with atomics (backward)
   ZeroArgs zero;      // GCOL kernels clear these (the backward's atomic targets)
@@ -169,7 +169,7 @@ struct BwdArgs {
   Geom g;
   const void* x;
   const float* off;
-  const float* gcol;
+  const void* gcol;  // bf16 when gmax is given (tensor-core GCOL), else fp32
   ColLayout gcol_layout;
   void* col;  // may be null: deformed map not written
   ColLayout col_layout;

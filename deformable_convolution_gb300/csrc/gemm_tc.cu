@@ -357,26 +357,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         store_y_row(static_cast<__nv_bfloat16*>(a.out) + ((long long)z * a.c_out + m) * a.howo + n_first,
                     r, n_first, a.howo);
       } else if (KIND == GCOL) {
-        // this warp's 32 rows x 32 columns go through shared memory (the
-        // operand stages are free once `done` fired) in the 128-byte swizzled
-        // layout of the store map, then out with one TMA store; rows and
-        // columns beyond the tensor are clipped by the TMA unit
+        // gcol leaves as bf16: this warp's 32 rows x 64 columns go through
+        // shared memory (the operand stages are free once `done` fired) in the
+        // 128-byte swizzled layout of the store map, one TMA store per two
+        // 32-column chunks; rows and columns beyond the tensor are clipped by
+        // the TMA unit.  The magnitude bound is taken before rounding.
         if (m < a.kdim) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (n_first + j < a.howo) amax = max(amax, r[j] & 0x7fffffffu);
         }
-        unsigned char* buf = smem + (warp * (BN / 32) + c) * 4096;
+        unsigned char* buf = smem + (warp * (BN / 64) + (c >> 1)) * 4096;
 #pragma unroll
-        for (int v = 0; v < 8; ++v)
-          *reinterpret_cast<float4*>(buf + lane * 128 + ((v ^ (lane & 7)) << 4)) =
-              make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                          __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0 && m0 + warp * 32 < a.kdim && n_first < a.howo) {
-          tma_store_3d(&tmC, buf, n_first, z, m0 + warp * 32);
-          tma_store_commit();
+        for (int v = 0; v < 4; ++v) {
+          uint4 pk;
+          uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[v * 8 + 2 * e]),
+                                                      __uint_as_float(r[v * 8 + 2 * e + 1]));
+            pw[e] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+          const int piece = (c & 1) * 4 + v;  // 16-byte piece of the 128-byte row
+          *reinterpret_cast<uint4*>(buf + lane * 128 + ((piece ^ (lane & 7)) << 4)) = pk;
+        }
+        if (c & 1) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          const int box_n = n0 + (c >> 1) * 64;
+          if (lane == 0 && m0 + warp * 32 < a.kdim && box_n < a.howo) {
+            tma_store_3d(&tmC, buf, box_n, z, m0 + warp * 32);
+            tma_store_commit();
+          }
         }
       } else {
         if (m >= a.c_out) continue;
@@ -540,13 +552,13 @@ bool col_map(CUtensorMap* m, const void* col, const Geom& g, const ColLayout& L,
 }
 
 // grad_y as a 3-D tensor {pixel, channel, image}
-// gcol (fp32) as the store target of the GCOL epilogue: boxes of 32 pixels x
+// gcol (bf16) as the store target of the GCOL epilogue: boxes of 64 pixels x
 // 32 rows of one image
-bool gcol_map(CUtensorMap* m, const float* gcol, const Geom& g, const ColLayout& L) {
+bool gcol_map(CUtensorMap* m, const void* gcol, const Geom& g, const ColLayout& L) {
   const cuuint64_t dims[3] = {(cuuint64_t)g.howo, (cuuint64_t)g.n, (cuuint64_t)g.kdim};
-  const cuuint64_t strides[2] = {(cuuint64_t)L.img * 4, (cuuint64_t)L.row * 4};
-  const cuuint32_t box[3] = {32, 1, 32};
-  return make_map(m, gcol, 3, dims, strides, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+  const cuuint64_t strides[2] = {(cuuint64_t)L.img * 2, (cuuint64_t)L.row * 2};
+  const cuuint32_t box[3] = {64, 1, 32};
+  return make_map(m, gcol, 3, dims, strides, box);
 }
 
 bool gy_map(CUtensorMap* m, const void* gy, const Geom& g, cuuint32_t box_ch) {

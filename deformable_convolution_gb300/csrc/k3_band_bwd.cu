@@ -25,6 +25,8 @@
 // the window are queued and processed by all lanes together from global
 // memory.  The window is flushed to grad_x with float atomics (neighbouring
 // bands' windows overlap).
+#include <type_traits>
+
 #include "dc_band.cuh"
 
 namespace dc {
@@ -102,6 +104,14 @@ __device__ __forceinline__ void gadd(float* plane, const Geom& g, int y, int x, 
 
 __device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
 
+// gcol is bf16 when it comes from the tensor-core GEMM (the fixed-point
+// path), fp32 otherwise
+template <bool kFixed>
+using GcolT = typename std::conditional<kFixed, __nv_bfloat16, float>::type;
+
+__device__ __forceinline__ float ldg_f(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float ldg_f(const __nv_bfloat16* p) { return __bfloat162float(__ldg(p)); }
+
 // round(ws * gc) as an int, for |ws * gc| < 2^22: adding 1.5 * 2^23 puts the
 // rounded integer in the low mantissa bits (one rounding, to nearest even)
 __device__ __forceinline__ int to_fixed(float ws, float gc) {
@@ -118,7 +128,7 @@ __device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w 
 template <typename T, bool kFixed>
 __device__ __forceinline__ void band_bwd_run(const uint32_t* __restrict__ xw, int PL, int cols,
                                              int sbase, int cl0, int count,
-                                             const float* __restrict__ gp, long long gstride,
+                                             const GcolT<kFixed>* __restrict__ gp, long long gstride,
                                              T* cp, long long cstride, float* gxp, float ly,
                                              float lx, float w00, float w01, float w10, float w11,
                                              float& sdy, float& sdx) {
@@ -150,7 +160,7 @@ __device__ __forceinline__ void band_bwd_run(const uint32_t* __restrict__ xw, in
     const uint32_t* xs = xw + sbase;
     if (cl0 & 1) {  // odd start: high half of a pair word
       const uint32_t* wp = xs + (cl0 >> 1) * PL;
-      const float gc = __ldg(gp);
+      const float gc = ldg_f(gp);
       one(gc, hi_bf16(wp[0]), hi_bf16(wp[1]), hi_bf16(wp[cols]), hi_bf16(wp[cols + 1]), 0);
       scatter(gc, 0);
       ch = 1;
@@ -166,8 +176,8 @@ __device__ __forceinline__ void band_bwd_run(const uint32_t* __restrict__ xw, in
         a01[u] = wp[1];
         a10[u] = wp[cols];
         a11[u] = wp[cols + 1];
-        g0[u] = __ldg(gp + (long long)(ch + 2 * u) * gstride);
-        g1[u] = __ldg(gp + (long long)(ch + 2 * u + 1) * gstride);
+        g0[u] = ldg_f(gp + (long long)(ch + 2 * u) * gstride);
+        g1[u] = ldg_f(gp + (long long)(ch + 2 * u + 1) * gstride);
       }
 #pragma unroll
       for (int u = 0; u < kPairs; ++u) {
@@ -183,7 +193,7 @@ __device__ __forceinline__ void band_bwd_run(const uint32_t* __restrict__ xw, in
     for (; ch < count; ++ch) {
       const int cl = cl0 + ch;
       const uint32_t* wp = xs + (cl >> 1) * PL;
-      const float gc = __ldg(gp + (long long)ch * gstride);
+      const float gc = ldg_f(gp + (long long)ch * gstride);
       if (cl & 1)
         one(gc, hi_bf16(wp[0]), hi_bf16(wp[1]), hi_bf16(wp[cols]), hi_bf16(wp[cols + 1]), ch);
       else
@@ -202,7 +212,7 @@ __device__ __forceinline__ void band_bwd_run(const uint32_t* __restrict__ xw, in
         v01[u] = wp[1];
         v10[u] = wp[cols];
         v11[u] = wp[cols + 1];
-        gc[u] = __ldg(gp + (long long)(ch + u) * gstride);
+        gc[u] = ldg_f(gp + (long long)(ch + u) * gstride);
       }
 #pragma unroll
       for (int u = 0; u < kB; ++u) one(gc[u], v00[u], v01[u], v10[u], v11[u], ch + u);
@@ -211,7 +221,7 @@ __device__ __forceinline__ void band_bwd_run(const uint32_t* __restrict__ xw, in
     }
     for (; ch < count; ++ch) {
       const float* wp = xs + ch * PL;
-      const float gc = __ldg(gp + (long long)ch * gstride);
+      const float gc = ldg_f(gp + (long long)ch * gstride);
       one(gc, wp[0], wp[1], wp[cols], wp[cols + 1], ch);
       scatter(gc, ch);
     }
@@ -345,7 +355,8 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
       const float by = (float)(ho * g.sh - g.ph + i * g.dh);
       const float bx = (float)(wo * g.sw - g.pw + j * g.dw);
       const long long qo = (long long)ho * g.wo + wo;
-      const float* grow = a.gcol + (long long)k * a.gcol_layout.row + (long long)n * a.gcol_layout.img + qo;
+      const GcolT<kFixed>* grow = static_cast<const GcolT<kFixed>*>(a.gcol) +
+                                  (long long)k * a.gcol_layout.row + (long long)n * a.gcol_layout.img + qo;
       T* crow = col ? col + (long long)k * a.col_layout.row + (long long)n * a.col_layout.img + qo : nullptr;
       int c = c_begin;
       for (int gg = g_begin; c < c_end; ++gg) {
@@ -374,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
         if (c < run_end && !t.fast) {
           // queue full: this out-of-window tap is handled here, from global memory
           for (; c < run_end; ++c) {
-            const float gc = __ldg(grow + (long long)c * gstride);
+            const float gc = ldg_f(grow + (long long)c * gstride);
             const T* xp = x + img + (long long)c * g.hw;
             const float v00 = gload(xp, g, t.y0, t.x0), v01 = gload(xp, g, t.y0, t.x0 + 1);
             const float v10 = gload(xp, g, t.y0 + 1, t.x0), v11 = gload(xp, g, t.y0 + 1, t.x0 + 1);
@@ -390,10 +401,10 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
         }
         if (c < run_end) {
           // on-chip tap: gcol, corners, blend, offset-gradient terms, scatter
-          const float* gp = grow + (long long)c * gstride;
+          const GcolT<kFixed>* gp = grow + (long long)c * gstride;
           T* cp = crow ? crow + (long long)c * cstride : nullptr;
           float* gxp = gxs + (c - c_begin) * PL + sbase;
-          if (kFixed)
+          if constexpr (kFixed)
             band_bwd_run<T, true>(xw, PL, pl.cols, sbase, c - c_begin, run_end - c, gp, gstride, cp,
                                   cstride, gxp, t.ly, t.lx, w00 * fscale, w01 * fscale,
                                   w10 * fscale, w11 * fscale, sdy, sdx);
@@ -429,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
                              (float)(wo * g.sw - g.pw + j * g.dw) + offs[(2 * ((gg - g_begin) * g.K + k) + 1) * PS + px],
                              g, ylo, xlo, pl.rows, pl.cols);
       const long long qo = (long long)ho * g.wo + wo;
-      const float gc = __ldg(a.gcol + (long long)k * a.gcol_layout.row + (long long)n * a.gcol_layout.img +
+      const float gc = ldg_f(static_cast<const GcolT<kFixed>*>(a.gcol) + (long long)k * a.gcol_layout.row + (long long)n * a.gcol_layout.img +
                              qo + (long long)c * gstride);
       const T* xp = x + img + (long long)c * g.hw;
       const float v00 = gload(xp, g, t.y0, t.x0), v01 = gload(xp, g, t.y0, t.x0 + 1);
