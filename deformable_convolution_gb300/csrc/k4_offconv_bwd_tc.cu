@@ -171,8 +171,37 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
   // gb's last row stays zero: window positions that no pixel's tap reaches
   for (int j = tid; j < pl.mp16 / 2; j += kThreads) gb[pl.pxp * pl.sb + j] = 0u;
   // input window of the slice as pixel-pair words (x[q], x[q + column stride]),
-  // zero outside the image and beyond c_in
-  {
+  // zero outside the image and beyond c_in.  Unit stride with image rows of
+  // whole 8-byte quads: a task reads the 4-pixel quad and the next one (for
+  // the fifth value) and writes up to four words.
+  const bool xquad = g.sw == 1 && (g.w & 3) == 0 && (reinterpret_cast<uintptr_t>(x) & 7) == 0;
+  if (xquad) {
+    const int q_lo = (xlo >= 0 ? xlo : xlo - 3) / 4;
+    const int q_hi = (xlo + pl.cols - 1 >= 0 ? xlo + pl.cols - 1 : xlo + pl.cols - 4) / 4;
+    const int nqd = q_hi - q_lo + 1;
+    band::Walk3 w;
+    w.init(tid, kThreads, pl.rows, nqd);
+    while (w.a < kCpc) {
+      const int cl = w.a, r = w.b, x0 = 4 * (q_lo + w.c);
+      w.next();
+      const int c = c_begin + cl, yy = ylo + r;
+      uint2 cur = make_uint2(0u, 0u);
+      uint32_t nxt = 0u;
+      if (c < g.c_in && yy >= 0 && yy < g.h) {
+        const __nv_bfloat16* row = x + img + (long long)c * g.hw + (long long)yy * g.w;
+        if (x0 >= 0 && x0 < g.w) cur = *reinterpret_cast<const uint2*>(row + x0);
+        if (x0 + 4 >= 0 && x0 + 4 < g.w) nxt = *reinterpret_cast<const uint32_t*>(row + x0 + 4);
+      }
+      const uint32_t wv[4] = {cur.x, __byte_perm(cur.x, cur.y, 0x5432), cur.y,
+                              __byte_perm(cur.y, nxt, 0x5432)};
+      uint32_t* dst = xp + cl * pl.xplane + r * pl.cols;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int q = x0 + i - xlo;
+        if (q >= 0 && q < pl.cols) dst[q] = wv[i];
+      }
+    }
+  } else {
     constexpr int kB = 8;
     const int total = kCpc * pl.npos;
     band::Walk3 w;
@@ -200,8 +229,32 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
         if (at[u] >= 0) xp[at[u]] = v[u];
     }
   }
-  // w_off^T as [(k, c)][offset-channel pair] words, zero for m >= M or c >= c_in
-  {
+  // w_off^T as [(k, c)][offset-channel pair] words, zero for m >= M or c >= c_in.
+  // A full slice with aligned rows reads each offset channel's contiguous run
+  // w_off[m][c_begin ..][*] as uint4 and scatters the halves.
+  const bool wvec = c_begin + kCpc <= g.c_in && ((g.c_in * K) & 7) == 0 &&
+                    (reinterpret_cast<uintptr_t>(w_off) & 15) == 0;
+  if (wvec) {
+    for (int idx = tid; idx < K * kCpc * pl.sw; idx += kThreads) wa[idx] = 0u;
+    __syncthreads();
+    unsigned short* wh = reinterpret_cast<unsigned short*>(wa);
+    const int span8 = kCpc * K / 8, total = M * span8;
+    for (int idx = tid; idx < total; idx += kThreads) {
+      const int m = idx / span8, q = idx - m * span8;
+      const uint4 v = *reinterpret_cast<const uint4*>(w_off + ((long long)m * g.c_in + c_begin) * K + 8 * q);
+      const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+      int cl = (8 * q) / K, k = 8 * q - cl * K;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        wh[((k * kCpc + cl) * pl.sw) * 2 + m] =
+            (unsigned short)((e & 1) ? (vw[e >> 1] >> 16) : (vw[e >> 1] & 0xffffu));
+        if (++k == K) {
+          k = 0;
+          ++cl;
+        }
+      }
+    }
+  } else {
     constexpr int kB = 4;
     const int wpr = pl.mp16 / 2;  // words per row
     const int total = K * kCpc * wpr;
