@@ -261,8 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // The forward GEMM reads the column K1 writes; GCOL is the first kernel of
-  // the backward call (launched without early start, so the wait is a no-op).
+  // The forward GEMM reads the column K1 writes; GCOL, the first kernel of
+  // the backward call, waits for whatever precedes it on the stream.
   // The weight-gradient GEMM follows K4 but reads nothing K4 writes: it starts
   // only once every K4 block has passed its own wait on K3 (which replays the
   // column it reads, after GCOL cleared grad_w), so it runs beside K4 and
@@ -522,13 +522,12 @@ cudaError_t launch(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   int nattr = 0;
-  // the forward GEMM follows K1 and the weight-gradient GEMM follows K4 in the
-  // same call: both may start their prologue early
-  if (KIND != GCOL) {
-    attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[nattr].val.programmaticStreamSerializationAllowed = 1;
-    ++nattr;
-  }
+  // every GEMM may start its prologue (barriers, tensor memory) while its
+  // predecessor finishes: FWD and GCOL wait for it before touching global
+  // memory, GW (which reads nothing K4 writes) before it exits
+  attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+  ++nattr;
   if (cluster_y > 1) {
     attr[nattr].id = cudaLaunchAttributeClusterDimension;
     attr[nattr].val.clusterDim.x = 1;

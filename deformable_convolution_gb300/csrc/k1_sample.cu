@@ -171,6 +171,9 @@ __global__ void __launch_bounds__(kThreads, 2) k1_band_sample(SampleArgs a, Plan
   int* nslow = reinterpret_cast<int*>(smem + pl.off_q);            // deferred slow taps
   int* slowq = nslow + 1;
   if (tid == 0) *nslow = 0;
+  // x, the weights and offset_add may come from the previous kernel on the
+  // stream, and the column and offsets it may still be reading are rewritten
+  pdl_wait();
 
   band::fill_pixel_table(pix, npx, pl.TW);
   for (int k = tid; k < g.K; k += kThreads) {
@@ -558,14 +561,19 @@ cudaError_t launch_t(const SampleArgs& a, const Plan& pl, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   unsigned nattr = 0;
+  // early start behind whatever precedes on the stream: the kernel waits for
+  // it before its first global-memory access
+  attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+  ++nattr;
   if (!kReplay) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)pl.csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    nattr = 1;
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = (unsigned)pl.csize;
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
   }
   cfg.attrs = attr;
   cfg.numAttrs = nattr;
