@@ -402,6 +402,9 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
   const int qunits = (qtiles + kQGroup - 1) / kQGroup;
   const int mtiles8 = pl.mp8 / 8;
   const int ksteps = pl.pxp / 16;
+  // the pixels 2j, 2j + 1 of every pair share a band row (and are one column
+  // stride apart) when the tile is one row or an even number of columns wide
+  const bool pairs_in_row = pl.R == 1 || (pl.TW & 1) == 0;
   for (int unit = warp; unit < K + qunits; unit += kWarps) {
     if (unit < K) {
       // ---- weight part, tap k: rows = 16 channels, columns = offset channels
@@ -414,7 +417,20 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
         float acc[kMChunk][4];
 #pragma unroll
         for (int t = 0; t < kMChunk; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-        for (int ks = 0; ks < ksteps; ++ks) {
+        // k-steps whose 16 pixels all exist and whose pairs never straddle
+        // a band row read each fragment register with one plain load
+        const int ks_full = pairs_in_row ? pl.npx / 16 : 0;
+        for (int ks = 0; ks < ks_full; ++ks) {
+          const int x0 = pair[ks * 8 + tig].x + tap, x1 = pair[ks * 8 + tig + 4].x + tap;
+          const uint32_t a0 = p0[x0], a1 = p1[x0], a2 = p0[x1], a3 = p1[x1];
+#pragma unroll
+          for (int t = 0; t < kMChunk; ++t) {
+            if (mt0 + t >= mtiles8) break;
+            const uint32_t* b = ga + ((mt0 + t) * 8 + gid) * pl.sa + ks * 8 + tig;
+            mma16816(acc[t], a0, a1, a2, a3, b[0], b[4]);
+          }
+        }
+        for (int ks = ks_full; ks < ksteps; ++ks) {
           const int2 e0 = pair[ks * 8 + tig], e1 = pair[ks * 8 + tig + 4];
           const uint32_t a0 = x_pair(p0, e0, tap, g.sw), a1 = x_pair(p1, e0, tap, g.sw);
           const uint32_t a2 = x_pair(p0, e1, tap, g.sw), a3 = x_pair(p1, e1, tap, g.sw);
