@@ -283,8 +283,9 @@ def main():
     def step():
         B.deform_conv_fwd(p, t["x"], t["w_off"], t["b_off"], t["w"], t["offset_add"], y, off,
                           None, ws)
+        # the backward takes the deformed map the forward left in `ws`
         B.deform_conv_bwd(p, t["x"], t["w_off"], t["w"], off, t["grad_y"], gx, gwo, gbo, gw,
-                          goff, ws)
+                          goff, ws, after_fwd=True)
 
     launches_before = B.launch_count()
     with torch.cuda.stream(stream):
@@ -347,7 +348,9 @@ def main():
                            f" + {wl.outlier_p:.0%} outliers at +-{wl.outlier_px} px"
                            if wl.outlier_p else ""),
                        "l2": "flushed (256 MiB write) before every timed step",
-                       "graph": graph is not None, "parallelism": f"replicas x{world}"},
+                       "graph": graph is not None, "parallelism": f"replicas x{world}",
+                       "backward": "deform_conv_bwd_after_fwd (reuses the forward's deformed "
+                                   "map from the shared workspace)"},
             "flops_per_step": flops_step, "wall_s_timed_region": wall,
             "gpu_launches": launches_per_step * args.steps, "clocks": clocks}
 
@@ -624,7 +627,8 @@ def e2e(p, d, dev, stream, flops_step, iters=20):
         B.deform_conv_fwd(p, devt["x"], devt["w_off"], devt["b_off"], devt["w"],
                           devt["offset_add"], outs["y"], outs["off"], None, ws)
         B.deform_conv_bwd(p, devt["x"], devt["w_off"], devt["w"], outs["off"], devt["grad_y"],
-                          outs["gx"], outs["gwo"], outs["gbo"], outs["gw"], outs["goff"], ws)
+                          outs["gx"], outs["gwo"], outs["gbo"], outs["gw"], outs["goff"], ws,
+                          after_fwd=True)
         for k, v in outs.items():
             hout[k].copy_(v, non_blocking=True)
 

@@ -24,6 +24,7 @@ EXPORTED_SYMBOLS = (
     "deform_conv_bwd", "deform_conv_sample", "dc_status_string", "dc_build_info",
     "dc_launch_count", "deform_conv_fwd_noalloc", "dc_device_error", "dc_kernel_timing",
     "dc_kernel_times", "deform_conv_offsets", "deform_conv_margin_histogram", "dc_suggest_margin",
+    "deform_conv_bwd_after_fwd",
 )
 MARGIN_BINS = 64
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -61,6 +62,8 @@ def lib() -> ctypes.CDLL:
         L.deform_conv_fwd.restype = i
         L.deform_conv_bwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.deform_conv_bwd.restype = i
+        L.deform_conv_bwd_after_fwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.deform_conv_bwd_after_fwd.restype = i
         L.deform_conv_sample.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.deform_conv_sample.restype = i
         L.deform_conv_offsets.argtypes = [pp, vp, vp, vp, vp, vp, vp]
@@ -244,12 +247,15 @@ def deform_conv_fwd_noalloc(p: Problem, x, w_off, b_off, w, offset_add, y, offse
 
 
 def deform_conv_bwd(p: Problem, x, w_off, w, offset, grad_y, grad_x, grad_w_off, grad_b_off,
-                    grad_w, grad_offset=None, ws=None, stream=None):
+                    grad_w, grad_offset=None, ws=None, stream=None, after_fwd=False):
+    """after_fwd: `ws` still holds the deformed map of the deform_conv_fwd call
+    for these inputs (deform_conv_bwd_after_fwd); the map is not replayed."""
     s = p.shapes()
     dt, f32 = p.torch_dtype, torch.float32
     st = p.c_struct()
     ws_ptr = _ptr(ws, "ws", dtype=torch.uint8)
-    _check(lib().deform_conv_bwd(
+    fn = lib().deform_conv_bwd_after_fwd if after_fwd else lib().deform_conv_bwd
+    _check(fn(
         ctypes.byref(st), _ptr(x, "x", s["x"], dt), _ptr(w_off, "w_off", s["w_off"], dt),
         _ptr(w, "w", s["w"], dt), _ptr(offset, "offset", s["offset"], f32),
         _ptr(grad_y, "grad_y", s["y"], dt), _ptr(grad_x, "grad_x", s["x"], f32),

@@ -170,6 +170,115 @@ dc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DC_OK : DC_ERR_
 
 using namespace dc;
 
+namespace dc {
+namespace {
+
+// The backward pass; with reuse_map the deformed map the forward pass left in
+// the workspace feeds the weight-gradient GEMM and K3 does not replay it.
+dc_status backward(const dc_problem* prob, const void* x, const void* w_off, const void* w,
+                   const float* offset, const void* grad_y, float* grad_x, float* grad_w_off,
+                   float* grad_b_off, float* grad_w, float* grad_offset, void* ws,
+                   size_t ws_bytes, void* stream, bool reuse_map) {
+  Geom g;
+  int margin;
+  dc_status st = make_geom(prob, &g, &margin);
+  if (st != DC_OK) return st;
+  if (!x || !w_off || !w || !offset || !grad_y || !grad_x || !grad_w_off || !grad_w)
+    return DC_ERR_INVALID_ARG;
+  if (bwd_smem_bytes(g, prob->dtype, margin) > kMaxSmem ||
+      offconv_bwd_smem_bytes(g, prob->dtype) > kMaxSmem)
+    return DC_ERR_UNSUPPORTED;
+  const void* ptrs[] = {x, w_off, w, offset, grad_y, grad_x, grad_w_off, grad_b_off, grad_w,
+                        grad_offset, ws};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return DC_ERR_UNSUPPORTED;
+  const Plan pl = make_plan(g, prob->dtype, 1);
+  if (!ws || ws_bytes < pl.total) return DC_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* wsb = static_cast<char*>(ws);
+  float* goff = grad_offset ? grad_offset : reinterpret_cast<float*>(wsb + pl.off_off);
+
+  // gradient of the deformed map: gcol = w^T grad_y
+  GemmArgs ga{};
+  ga.g = g;
+  ga.w = w;
+  ga.col = wsb + pl.col_off;
+  ga.col_layout = pl.col;
+  ga.gy = grad_y;
+  ga.gcol = wsb + pl.gcol_off;
+  ga.gcol_layout = pl.gcol;
+  ga.gw = grad_w;
+  // the GCOL launch also clears the buffers later kernels accumulate into
+  ga.zero.p[0] = grad_x;
+  ga.zero.n[0] = (long long)g.n * g.c_in * g.hw;
+  ga.zero.p[1] = grad_w;
+  ga.zero.n[1] = (long long)g.c_out * g.kdim;
+  ga.zero.p[2] = grad_w_off;
+  ga.zero.n[2] = (long long)g.M * g.kdim;
+  ga.zero.p[3] = grad_b_off;
+  ga.zero.n[3] = grad_b_off ? g.M : 0;
+  ga.zero.p[4] = goff;
+  ga.zero.n[4] = (long long)g.n * g.M * g.howo;
+  float* gwo_img = pl.gwo_img_off ? reinterpret_cast<float*>(wsb + pl.gwo_img_off) : nullptr;
+  ga.zero.p[5] = gwo_img;
+  ga.zero.n[5] = gwo_img ? (long long)g.n * g.M * g.kdim : 0;
+  // the tensor-core GCOL GEMM also reports max |gcol| per tile, from which K3
+  // scales its fixed-point grad_x accumulation
+  const bool tc_gcol = prob->dtype == DC_BF16 && tc_gemm_supported(g);
+  ga.gmax = tc_gcol ? reinterpret_cast<float*>(wsb + pl.gmax_off) : nullptr;
+  st = cuda_status(timed("gemm_gcol", s, [&] { return launch_gemm_gcol(ga, prob->dtype, s); }));
+  if (st != DC_OK) return st;
+
+  // sampling backward; replays the deformed map for grad_w
+  BwdArgs ba{};
+  ba.g = g;
+  ba.x = x;
+  ba.off = offset;
+  ba.gcol = ga.gcol;
+  ba.gcol_layout = pl.gcol;
+  ba.col = reuse_map ? nullptr : wsb + pl.col_off;
+  ba.col_layout = pl.col;
+  ba.gx = grad_x;
+  ba.goff = goff;
+  ba.margin = margin;
+  ba.gmax = ga.gmax;
+  ba.gmax_tx = pl.gmax_tx;
+  ba.gmax_ty = pl.gmax_ty;
+  st = cuda_status(timed("k3_band_bwd", s, [&] { return launch_band_bwd(ba, prob->dtype, s); }));
+  if (st != DC_OK) return st;
+
+  // offset-convolution backward on the completed offset gradient
+  OffconvBwdArgs oa{};
+  oa.g = g;
+  oa.x = x;
+  oa.w_off = w_off;
+  oa.goff = goff;
+  oa.gx = grad_x;
+  oa.gw_off = grad_w_off;
+  oa.gb_off = grad_b_off;
+  oa.gw_off_img = gwo_img;
+  st = cuda_status(timed("k4_offconv_bwd", s, [&] { return launch_offconv_bwd(oa, prob->dtype, s); }));
+  if (st != DC_OK) return st;
+
+  // main weight gradient from the replayed map; the tensor-core GEMM also sums
+  // K4's per-image grad_w_off partials once K4 is done (its CTAs wait for K4
+  // before exiting anyway), else a small kernel does
+  const bool gw_reduces = gwo_img && tc_gcol && (g.M * g.kdim) % 4 == 0;
+  if (gw_reduces) {
+    ga.gwo_img = gwo_img;
+    ga.gw_off = grad_w_off;
+    ga.gwo_count = (long long)g.M * g.kdim;
+  }
+  st = cuda_status(timed("gemm_gw", s, [&] { return launch_gemm_gw(ga, prob->dtype, s); }));
+  if (st != DC_OK || !gwo_img || gw_reduces) return st;
+
+  // grad_w_off from K4's per-image partials
+  return cuda_status(timed("gw_off_reduce", s, [&] { return launch_gw_off_reduce(oa, s); }));
+}
+
+}  // namespace
+}  // namespace dc
+
 extern "C" {
 
 int dc_out_h(const dc_problem* prob) {
@@ -242,101 +351,17 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
                           const float* offset, const void* grad_y, float* grad_x,
                           float* grad_w_off, float* grad_b_off, float* grad_w,
                           float* grad_offset, void* ws, size_t ws_bytes, void* stream) {
-  Geom g;
-  int margin;
-  dc_status st = make_geom(prob, &g, &margin);
-  if (st != DC_OK) return st;
-  if (!x || !w_off || !w || !offset || !grad_y || !grad_x || !grad_w_off || !grad_w)
-    return DC_ERR_INVALID_ARG;
-  if (bwd_smem_bytes(g, prob->dtype, margin) > kMaxSmem ||
-      offconv_bwd_smem_bytes(g, prob->dtype) > kMaxSmem)
-    return DC_ERR_UNSUPPORTED;
-  const void* ptrs[] = {x, w_off, w, offset, grad_y, grad_x, grad_w_off, grad_b_off, grad_w,
-                        grad_offset, ws};
-  for (const void* p : ptrs)
-    if (p && !aligned16(p)) return DC_ERR_UNSUPPORTED;
-  const Plan pl = make_plan(g, prob->dtype, 1);
-  if (!ws || ws_bytes < pl.total) return DC_ERR_WORKSPACE;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  char* wsb = static_cast<char*>(ws);
-  float* goff = grad_offset ? grad_offset : reinterpret_cast<float*>(wsb + pl.off_off);
+  return dc::backward(prob, x, w_off, w, offset, grad_y, grad_x, grad_w_off, grad_b_off, grad_w,
+                      grad_offset, ws, ws_bytes, stream, false);
+}
 
-  // gradient of the deformed map: gcol = w^T grad_y
-  GemmArgs ga{};
-  ga.g = g;
-  ga.w = w;
-  ga.col = wsb + pl.col_off;
-  ga.col_layout = pl.col;
-  ga.gy = grad_y;
-  ga.gcol = wsb + pl.gcol_off;
-  ga.gcol_layout = pl.gcol;
-  ga.gw = grad_w;
-  // the GCOL launch also clears the buffers later kernels accumulate into
-  ga.zero.p[0] = grad_x;
-  ga.zero.n[0] = (long long)g.n * g.c_in * g.hw;
-  ga.zero.p[1] = grad_w;
-  ga.zero.n[1] = (long long)g.c_out * g.kdim;
-  ga.zero.p[2] = grad_w_off;
-  ga.zero.n[2] = (long long)g.M * g.kdim;
-  ga.zero.p[3] = grad_b_off;
-  ga.zero.n[3] = grad_b_off ? g.M : 0;
-  ga.zero.p[4] = goff;
-  ga.zero.n[4] = (long long)g.n * g.M * g.howo;
-  float* gwo_img = pl.gwo_img_off ? reinterpret_cast<float*>(wsb + pl.gwo_img_off) : nullptr;
-  ga.zero.p[5] = gwo_img;
-  ga.zero.n[5] = gwo_img ? (long long)g.n * g.M * g.kdim : 0;
-  // the tensor-core GCOL GEMM also reports max |gcol| per tile, from which K3
-  // scales its fixed-point grad_x accumulation
-  const bool tc_gcol = prob->dtype == DC_BF16 && tc_gemm_supported(g);
-  ga.gmax = tc_gcol ? reinterpret_cast<float*>(wsb + pl.gmax_off) : nullptr;
-  st = cuda_status(timed("gemm_gcol", s, [&] { return launch_gemm_gcol(ga, prob->dtype, s); }));
-  if (st != DC_OK) return st;
-
-  // sampling backward; replays the deformed map for grad_w
-  BwdArgs ba{};
-  ba.g = g;
-  ba.x = x;
-  ba.off = offset;
-  ba.gcol = ga.gcol;
-  ba.gcol_layout = pl.gcol;
-  ba.col = wsb + pl.col_off;
-  ba.col_layout = pl.col;
-  ba.gx = grad_x;
-  ba.goff = goff;
-  ba.margin = margin;
-  ba.gmax = ga.gmax;
-  ba.gmax_tx = pl.gmax_tx;
-  ba.gmax_ty = pl.gmax_ty;
-  st = cuda_status(timed("k3_band_bwd", s, [&] { return launch_band_bwd(ba, prob->dtype, s); }));
-  if (st != DC_OK) return st;
-
-  // offset-convolution backward on the completed offset gradient
-  OffconvBwdArgs oa{};
-  oa.g = g;
-  oa.x = x;
-  oa.w_off = w_off;
-  oa.goff = goff;
-  oa.gx = grad_x;
-  oa.gw_off = grad_w_off;
-  oa.gb_off = grad_b_off;
-  oa.gw_off_img = gwo_img;
-  st = cuda_status(timed("k4_offconv_bwd", s, [&] { return launch_offconv_bwd(oa, prob->dtype, s); }));
-  if (st != DC_OK) return st;
-
-  // main weight gradient from the replayed map; the tensor-core GEMM also sums
-  // K4's per-image grad_w_off partials once K4 is done (its CTAs wait for K4
-  // before exiting anyway), else a small kernel does
-  const bool gw_reduces = gwo_img && tc_gcol && (g.M * g.kdim) % 4 == 0;
-  if (gw_reduces) {
-    ga.gwo_img = gwo_img;
-    ga.gw_off = grad_w_off;
-    ga.gwo_count = (long long)g.M * g.kdim;
-  }
-  st = cuda_status(timed("gemm_gw", s, [&] { return launch_gemm_gw(ga, prob->dtype, s); }));
-  if (st != DC_OK || !gwo_img || gw_reduces) return st;
-
-  // grad_w_off from K4's per-image partials
-  return cuda_status(timed("gw_off_reduce", s, [&] { return launch_gw_off_reduce(oa, s); }));
+dc_status deform_conv_bwd_after_fwd(const dc_problem* prob, const void* x, const void* w_off,
+                                    const void* w, const float* offset, const void* grad_y,
+                                    float* grad_x, float* grad_w_off, float* grad_b_off,
+                                    float* grad_w, float* grad_offset, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  return dc::backward(prob, x, w_off, w, offset, grad_y, grad_x, grad_w_off, grad_b_off, grad_w,
+                      grad_offset, ws, ws_bytes, stream, true);
 }
 
 dc_status deform_conv_sample(const dc_problem* prob, const void* x, const void* w_off,

@@ -126,6 +126,20 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
                           float* grad_w, float* grad_offset, void* ws, size_t ws_bytes,
                           void* stream);
 
+/* The backward pass when the workspace still holds the forward pass's
+ * deformed map ("What people did before, and where it broke": the unrolled
+ * map the interpolation materialises): the weight-gradient GEMM reads that map
+ * and the sampling backward does not replay it.  Arguments as in
+ * deform_conv_bwd; `ws` must be the workspace the deform_conv_fwd call for
+ * these x, w_off and offsets used (any halo_margin), not rewritten since --
+ * a training step that keeps its forward workspace until the backward.  The
+ * library cannot check this: a stale map gives a wrong grad_w only. */
+dc_status deform_conv_bwd_after_fwd(const dc_problem* prob, const void* x, const void* w_off,
+                                    const void* w, const float* offset, const void* grad_y,
+                                    float* grad_x, float* grad_w_off, float* grad_b_off,
+                                    float* grad_w, float* grad_offset, void* ws, size_t ws_bytes,
+                                    void* stream);
+
 /* The fused offset-convolution + bilinear-interpolation stage alone ("This
  * paper's idea": the kernel whose arithmetic intensity the fusion raises),
  * returning the deformed feature map ("What people did before, and where it

@@ -299,3 +299,40 @@ def test_margin_histogram_and_suggested_margin_bound_the_slow_path():
         assert slow <= bound <= frac * total, (frac, m, slow, bound)
         if frac == 0.01:
             check_layer(pm, d)
+
+
+def test_backward_after_forward_reuses_the_map():
+    """deform_conv_bwd_after_fwd takes the deformed map the forward call left
+    in the workspace: its gradients match the oracle and the replaying
+    backward's.  Two backward runs agree only to bf16 level on grad_x and
+    grad_w_off: the offset gradient is summed over channel slices with float
+    atomics (order-dependent in the last bit) and then rounded to bf16 for the
+    offset-convolution backward's tensor-core contractions."""
+    wl = W.WORKLOADS["res3_bf16"]
+    p = wl.problem()
+    d = {k: (None if v is None else v.cuda()) for k, v in W.generate(wl).items()}
+    s = p.shapes()
+    ws = B.workspace(p, True, "cuda")
+    y = torch.empty(s["y"], dtype=p.torch_dtype, device="cuda")
+    off = torch.empty(s["offset"], dtype=torch.float32, device="cuda")
+    B.deform_conv_fwd(p, d["x"], d["w_off"], d["b_off"], d["w"], d["offset_add"], y, off, None, ws)
+
+    def bwd(after):
+        out = {k: torch.empty(s[sh], dtype=torch.float32, device="cuda") for k, sh in
+               (("grad_x", "x"), ("grad_w_off", "w_off"), ("grad_b_off", "b_off"), ("grad_w", "w"),
+                ("grad_offset", "offset"))}
+        B.deform_conv_bwd(p, d["x"], d["w_off"], d["w"], off, d["grad_y"], out["grad_x"],
+                          out["grad_w_off"], out["grad_b_off"], out["grad_w"], out["grad_offset"],
+                          ws, after_fwd=after)
+        torch.cuda.synchronize()
+        return out
+    reused = bwd(True)
+    replayed = bwd(False)
+    for k in ("grad_offset", "grad_w", "grad_b_off"):
+        assert rel_err(f64(reused[k]), f64(replayed[k])) <= 1e-5, k
+    for k in ("grad_x", "grad_w_off"):
+        assert rel_err(f64(reused[k]), f64(replayed[k])) <= 5e-3, k
+    cpu = {k: (None if v is None else v.cpu()) for k, v in d.items()}
+    ref = oracle_backward(p, cpu, off.cpu().double().numpy())
+    for k in ("grad_x", "grad_w", "grad_w_off", "grad_b_off", "grad_offset"):
+        assert rel_err(f64(reused[k]), ref[k]) <= TOL[p.dtype], k
