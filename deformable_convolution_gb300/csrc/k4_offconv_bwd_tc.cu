@@ -99,6 +99,19 @@ __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uin
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Four 8x8 b16 matrices from shared memory; lane l gives the 16-byte row
+// (l & 7) of matrix l >> 3.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -456,20 +469,27 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
     } else {
       // ---- input part: rows = 16 channels, columns = window positions,
       // reduction over (tap, offset channel); the pixel each position reads
-      // through tap k is found on the fly.  Two accumulator chains (even and
-      // odd offset-channel blocks) halve the dependent mma sequence.
+      // through tap k is found on the fly.  Fragments come from ldmatrix: one
+      // x4 load gives the A fragment, another the B fragments of two position
+      // tiles (each lane addresses one 16-byte row: lane & 7 picks the row,
+      // lane >> 3 the matrix).  Two accumulator chains (even and odd
+      // offset-channel blocks) halve the dependent mma sequence.
       const int nt0 = (unit - K) * kQGroup;
-      int qr[kQGroup], qc[kQGroup];
+      // this lane's ldmatrix row of the B matrices: position tile 2 * tp + (lane >> 4)
+      int lqr[kQGroup / 2], lqc[kQGroup / 2];
 #pragma unroll
-      for (int t = 0; t < kQGroup; ++t) {
-        const int q = (nt0 + t) * 8 + gid;
-        qr[t] = -(1 << 20);  // no pixel
-        qc[t] = 0;
+      for (int tp = 0; tp < kQGroup / 2; ++tp) {
+        const int q = (nt0 + 2 * tp + (lane >> 4)) * 8 + (lane & 7);
+        lqr[tp] = -(1 << 20);  // no pixel
+        lqc[tp] = 0;
         if (q < pl.npos) {
-          qr[t] = q / pl.cols;
-          qc[t] = q - qr[t] * pl.cols;
+          lqr[tp] = q / pl.cols;
+          lqc[tp] = q - lqr[tp] * pl.cols;
         }
       }
+      const uint32_t gb_lane = smem_addr(gb) + ((lane >> 3) & 1) * 16;
+      const uint32_t wa_lane =
+          smem_addr(wa) + ((lane & 7) + ((lane >> 3) & 1) * 8) * pl.sw * 4 + (lane >> 4) * 16;
       const int nmc = pl.mp16 / 16;
       float acc[2][kQGroup][4];
 #pragma unroll
@@ -478,10 +498,10 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
         for (int t = 0; t < kQGroup; ++t) acc[s][t][0] = acc[s][t][1] = acc[s][t][2] = acc[s][t][3] = 0.f;
       for (int i = 0, k = 0; i < g.kh; ++i) {
         for (int j = 0; j < g.kw; ++j, ++k) {
-          int prow[kQGroup];
+          uint32_t brow[kQGroup / 2];
 #pragma unroll
-          for (int t = 0; t < kQGroup; ++t) {
-            const int r = qr[t] - i * g.dh, c = qc[t] - j * g.dw;
+          for (int tp = 0; tp < kQGroup / 2; ++tp) {
+            const int r = lqr[tp] - i * g.dh, c = lqc[tp] - j * g.dw;
             int px = pl.pxp;
             if (unit_stride) {
               if (r >= 0 && r < pl.R && c >= 0 && c < pl.TW) px = r * pl.TW + c;
@@ -489,18 +509,20 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
                        c / g.sw < pl.TW) {
               px = (r / g.sh) * pl.TW + c / g.sw;
             }
-            prow[t] = px * pl.sb;
+            brow[tp] = gb_lane + px * pl.sb * 4;
           }
-          const uint32_t* ar = wa + (k * kCpc + gid) * pl.sw + tig;
+          const uint32_t arow = wa_lane + k * kCpc * pl.sw * 4;
 #pragma unroll
           for (int mc = 0; mc < kMaxM / 16; ++mc) {
             if (mc >= nmc) break;
-            const uint32_t a0 = ar[mc * 8], a2 = ar[mc * 8 + 4];
-            const uint32_t a1 = ar[8 * pl.sw + mc * 8], a3 = ar[8 * pl.sw + mc * 8 + 4];
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(arow + mc * 32, a0, a1, a2, a3);
 #pragma unroll
-            for (int t = 0; t < kQGroup; ++t) {
-              const uint32_t* b = gb + prow[t] + mc * 8 + tig;
-              mma16816(acc[mc & 1][t], a0, a1, a2, a3, b[0], b[4]);
+            for (int tp = 0; tp < kQGroup / 2; ++tp) {
+              uint32_t b0, b1, b2, b3;
+              ldsm_x4(brow[tp] + mc * 32, b0, b1, b2, b3);
+              mma16816(acc[mc & 1][2 * tp], a0, a1, a2, a3, b0, b1);
+              mma16816(acc[mc & 1][2 * tp + 1], a0, a1, a2, a3, b2, b3);
             }
           }
         }
@@ -514,13 +536,10 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
         if (nt0 + t >= qtiles) break;
 #pragma unroll
         for (int hc = 0; hc < 2; ++hc) {
-          // window position of accumulator column 2 * tig + hc: the lane whose
-          // gid is that column computed its (row, column) above
-          const int src = (2 * tig + hc) * 4;
-          const int qrow = __shfl_sync(0xffffffffu, qr[t], src);
-          const int qcol = __shfl_sync(0xffffffffu, qc[t], src);
+          // window position of accumulator column 2 * tig + hc
           const int q = (nt0 + t) * 8 + 2 * tig + hc;
           if (q >= pl.npos) continue;
+          const int qrow = q / pl.cols, qcol = q - qrow * pl.cols;
           const int yy = ylo + qrow, xx = xlo + qcol;
           if (yy < 0 || yy >= g.h || xx < 0 || xx >= g.w) continue;
           float* dst = a.gx + img + (long long)c_begin * g.hw + (long long)yy * g.w + xx;
