@@ -37,12 +37,12 @@ FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 TRAFFIC = {
     # ncu --set full, res3 bf16, one launch each (profiles/<kernel>_res3_bf16.md,
     # profiles/tc_gemm_res3_bf16.md).  Writes mostly stay in the 129 MB L2.
-    ("res3_bf16", "k1_band_sample"): {"bytes": 2192384 + 512, "source": "048294db81b141f0"},
-    ("res3_bf16", "k3_band_bwd"): {"bytes": 34712576 + 7168, "source": "15194933f3c16819"},
-    ("res3_bf16", "k4_offconv_bwd"): {"bytes": 6049024, "source": "78b457f998f30ead"},
-    ("res3_bf16", "gemm_fwd"): {"bytes": 14772224, "source": "4627777b2563466e"},
-    ("res3_bf16", "gemm_gcol"): {"bytes": 1940992 + 6144, "source": "4627777b2563466e"},
-    ("res3_bf16", "gemm_gw"): {"bytes": 17334528, "source": "4627777b2563466e"},
+    ("res3_bf16", "k1_band_sample"): {"bytes": 2192896 + 256, "source": "8492705966c2d40d"},
+    ("res3_bf16", "k3_band_bwd"): {"bytes": 20261888, "source": "25e9bbf1e45d51e8"},
+    ("res3_bf16", "k4_offconv_bwd"): {"bytes": 6055680, "source": "762f9488fd022f59"},
+    ("res3_bf16", "gemm_fwd"): {"bytes": 14771968, "source": "61925501d85a5c24"},
+    ("res3_bf16", "gemm_gcol"): {"bytes": 1941248, "source": "61925501d85a5c24"},
+    ("res3_bf16", "gemm_gw"): {"bytes": 17334528, "source": "61925501d85a5c24"},
 }
 KERNEL_SOURCES = {
     "k1_band_sample": "k1_sample.cu", "k3_band_bwd": "k3_band_bwd.cu",
@@ -393,8 +393,11 @@ def kernel_costs(p, has_add):
     off_b = p.n_off * P * 4
     gemm = 2.0 * p.c_out * kdim * P
     gx_b = p.n * p.c_in * p.h * p.w * 4
-    k3 = (x_b + off_b + kdim * P * 4       # read x, offsets, gcol
-          + gx_b + off_b + kdim * P * elt)  # write grad_x, grad_offset, replayed map
+    # gcol is bf16 from the tensor-core GEMM (bf16 problems), fp32 otherwise; the
+    # step's backward reuses the forward's deformed map, so K3 writes no map
+    gcol_elt = 2 if p.dtype == 1 else 4
+    k3 = (x_b + off_b + kdim * P * gcol_elt  # read x, offsets, gcol
+          + gx_b + off_b)                     # write grad_x, grad_offset
     k4 = (x_b + off_b + p.n_off * kdim * elt  # read x, grad_offset, w_off
           + 2 * gx_b                          # add into grad_x (read + write)
           + p.n_off * (kdim + 1) * 4)         # write grad_w_off, grad_b_off
