@@ -131,11 +131,14 @@ __device__ __forceinline__ void band_bwd_run(const uint32_t* __restrict__ xw, in
                                              const GcolT<kFixed>* __restrict__ gp, long long gstride,
                                              T* cp, long long cstride, float* gxp, float ly,
                                              float lx, float w00, float w01, float w10, float w11,
-                                             float& sdy, float& sdx) {
-  const float hy = 1.0f - ly, hx = 1.0f - lx;
+                                             float& sA, float& sB, float& sC) {
+  // offset-gradient terms as three sums over the run's channels, combined
+  // once per tap by the caller: sA = sum gc (v10 - v00), sB = sum gc (v11 - v01),
+  // sC = sum gc (v01 - v00); the fourth difference v11 - v10 is b + c - a
   auto one = [&](float gc, float v00, float v01, float v10, float v11, int ch) {
-    sdy = __fmaf_rn(gc, hx * (v10 - v00) + lx * (v11 - v01), sdy);
-    sdx = __fmaf_rn(gc, hy * (v01 - v00) + ly * (v11 - v10), sdx);
+    sA = __fmaf_rn(gc, v10 - v00, sA);
+    sB = __fmaf_rn(gc, v11 - v01, sB);
+    sC = __fmaf_rn(gc, v01 - v00, sC);
     if (cp) cp[(long long)ch * cstride] = from_f<T>(blend4(ly, lx, v00, v01, v10, v11));
   };
   auto scatter = [&](float gc, int ch) {
@@ -368,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
         const float hy = 1.0f - t.ly, hx = 1.0f - t.lx;
         const float w00 = hy * hx, w01 = hy * t.lx, w10 = t.ly * hx, w11 = t.ly * t.lx;
         float sdy = 0.f, sdx = 0.f;
+        float sA = 0.f, sB = 0.f, sC = 0.f;  // on-chip run sums (see band_bwd_run)
         if (t.inside && !t.fast) {
           // out-of-window tap: queued for the cooperative pass below, so that
           // this warp does not wait on global memory for one lane
@@ -407,12 +411,15 @@ __global__ void __launch_bounds__(kThreads, 3) k3_band_bwd(BwdArgs a, Plan pl) {
           if constexpr (kFixed)
             band_bwd_run<T, true>(xw, PL, pl.cols, sbase, c - c_begin, run_end - c, gp, gstride, cp,
                                   cstride, gxp, t.ly, t.lx, w00 * fscale, w01 * fscale,
-                                  w10 * fscale, w11 * fscale, sdy, sdx);
+                                  w10 * fscale, w11 * fscale, sA, sB, sC);
           else
             band_bwd_run<T, false>(xw, PL, pl.cols, sbase, c - c_begin, run_end - c, gp, gstride,
-                                   cp, cstride, gxp, t.ly, t.lx, w00, w01, w10, w11, sdy, sdx);
+                                   cp, cstride, gxp, t.ly, t.lx, w00, w01, w10, w11, sA, sB, sC);
           c = run_end;
         }
+        // dy term: hx (v10 - v00) + lx (v11 - v01); dx term: hy (v01 - v00) + ly (v11 - v10)
+        sdy += hx * sA + t.lx * sB;
+        sdx += hy * sC + t.ly * (sB + sC - sA);
         part[(2 * ((gg - g_begin) * g.K + k)) * PS + px] = sdy;
         part[(2 * ((gg - g_begin) * g.K + k) + 1) * PS + px] = sdx;
       }
