@@ -167,3 +167,17 @@ def test_suggested_margin_is_one_the_build_can_stage():
     assert ws_size(ok, True)[0] == B.DC_OK
     too_big = B.Problem(1, 256, 56, 56, 256, dtype=B.DC_BF16, halo_margin=m + 1)
     assert ws_size(too_big, True)[0] != B.DC_OK or ws_size(too_big, False)[0] != B.DC_OK
+
+
+def test_bwd_after_fwd_argument_checks_fail_before_any_launch():
+    p = problem()
+    _, need = ws_size(p, True)
+    st = p.c_struct()
+    vp = ctypes.c_void_p
+    ptrs = [vp(0x10000 * (i + 1)) for i in range(11)]
+    ptrs[4] = None  # grad_y missing
+    rc = B.lib().deform_conv_bwd_after_fwd(ctypes.byref(st), *ptrs, ctypes.c_size_t(need), None)
+    assert rc == B.DC_ERR_INVALID_ARG
+    ptrs = [vp(0x10000 * (i + 1)) for i in range(11)]
+    rc = B.lib().deform_conv_bwd_after_fwd(ctypes.byref(st), *ptrs, ctypes.c_size_t(need - 1), None)
+    assert rc == B.DC_ERR_WORKSPACE
