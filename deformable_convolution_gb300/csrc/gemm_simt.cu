@@ -28,6 +28,7 @@ struct StridedGemm {
   long long c_z, c_m, c_n;
   int atomic;  // 1: atomically add fp32 into C, 0: store
   ZeroArgs zero;  // buffers this launch clears as a side job (GCOL)
+  int ksplit;     // K ranges per batch entry along blockIdx.z (needs atomic when > 1)
 };
 
 template <typename TA, typename TB, typename TC>
@@ -35,8 +36,13 @@ __global__ void __launch_bounds__(kThreads)
     gemm_simt_kernel(StridedGemm p, const TA* __restrict__ A, const TB* __restrict__ B, TC* C) {
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
-  const int z = blockIdx.z;
+  const int ks = p.ksplit > 1 ? p.ksplit : 1;
+  const int z = blockIdx.z / ks;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  // this CTA's K range (whole BK blocks)
+  const int kchunk = (int)ceil_div_ll(ceil_div_ll(p.K, ks), BK) * BK;
+  const int k_begin = (int)(blockIdx.z % ks) * kchunk;
+  const int k_end = min(p.K, k_begin + kchunk);
   {
     const long long nparts = (long long)gridDim.x * gridDim.y * gridDim.z;
     const long long part = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
@@ -52,20 +58,20 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
 
-  for (int k0 = 0; k0 < p.K; k0 += BK) {
+  for (int k0 = k_begin; k0 < k_end; k0 += BK) {
     // stage A tile (BM x BK) and B tile (BK x BN); lanes run along whichever
     // index is contiguous in memory
     for (int idx = tid; idx < BM * BK; idx += kThreads) {
       int mm, kk;
       if (p.a_m == 1) { mm = idx % BM; kk = idx / BM; } else { kk = idx % BK; mm = idx / BK; }
       const int m = m0 + mm, k = k0 + kk;
-      As[kk][mm] = (m < p.M && k < p.K) ? ld_f(Az + m * p.a_m + k * p.a_k) : 0.0f;
+      As[kk][mm] = (m < p.M && k < k_end) ? ld_f(Az + m * p.a_m + k * p.a_k) : 0.0f;
     }
     for (int idx = tid; idx < BK * BN; idx += kThreads) {
       int nn, kk;
       if (p.b_n == 1) { nn = idx % BN; kk = idx / BN; } else { kk = idx % BK; nn = idx / BK; }
       const int nidx = n0 + nn, k = k0 + kk;
-      Bs[kk][nn] = (nidx < p.N && k < p.K) ? ld_f(Bz + k * p.b_k + nidx * p.b_n) : 0.0f;
+      Bs[kk][nn] = (nidx < p.N && k < k_end) ? ld_f(Bz + k * p.b_k + nidx * p.b_n) : 0.0f;
     }
     __syncthreads();
 #pragma unroll
@@ -104,7 +110,8 @@ template <typename TA, typename TB, typename TC>
 cudaError_t run(const StridedGemm& p, int batch, const void* A, const void* B, void* C,
                 cudaStream_t s) {
   if (p.M <= 0 || p.N <= 0 || batch <= 0) return cudaSuccess;
-  dim3 grid((unsigned)ceil_div_ll(p.N, BN), (unsigned)ceil_div_ll(p.M, BM), (unsigned)batch);
+  const int ks = p.ksplit > 1 ? p.ksplit : 1;
+  dim3 grid((unsigned)ceil_div_ll(p.N, BN), (unsigned)ceil_div_ll(p.M, BM), (unsigned)(batch * ks));
   gemm_simt_kernel<TA, TB, TC><<<grid, kThreads, 0, s>>>(
       p, static_cast<const TA*>(A), static_cast<const TB*>(B), static_cast<TC*>(C));
   note_launches(1);
@@ -150,6 +157,16 @@ cudaError_t launch_gemm_gw_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s) 
   p.b_z = a.col_layout.img; p.b_k = 1; p.b_n = a.col_layout.row;
   p.c_z = 0; p.c_m = g.kdim; p.c_n = 1;
   p.atomic = 1;
+  // split the pixel reduction until about two CTAs per SM run (at least 128
+  // pixels per CTA): small problems would otherwise leave most SMs idle
+  {
+    const long long tiles = ceil_div_ll(p.N, BN) * ceil_div_ll(p.M, BM) * g.n;
+    long long ks = ceil_div_ll(304, tiles);
+    const long long kmax = p.K / 128 > 1 ? p.K / 128 : 1;
+    if (ks > kmax) ks = kmax;
+    if (ks < 1) ks = 1;
+    p.ksplit = (int)ks;
+  }
   if (dt == DC_BF16)
     return run<__nv_bfloat16, __nv_bfloat16, float>(p, g.n, a.gy, a.col, a.gw, s);
   return run<float, float, float>(p, g.n, a.gy, a.col, a.gw, s);
