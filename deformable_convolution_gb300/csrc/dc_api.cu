@@ -153,9 +153,10 @@ Plan make_plan(const Geom& g, dc_dtype dt, int backward) {
   pl.gmax_ty = (int)ceil_div_ll(g.kdim, 128);
   pl.gmax_off = backward ? take((size_t)g.n * pl.gmax_tx * pl.gmax_ty * 4 * sizeof(float)) : 0;
   // per-image grad_w_off partials of the tensor-core offset-conv backward
-  // (one image's bands add into one copy: far fewer atomics per address)
+  // (one image's bands add into one copy: far fewer atomics per address), in
+  // the kernel's accumulator order
   pl.gwo_img_off = backward && offconv_bwd_tc_supported(g, dt)
-                       ? take((size_t)g.n * g.M * g.kdim * sizeof(float))
+                       ? take((size_t)g.n * gwo_frag_count(g.M, g.c_in, g.K) * sizeof(float))
                        : 0;
   pl.total = at;
   return pl;
@@ -221,7 +222,7 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
   ga.zero.n[4] = (long long)g.n * g.M * g.howo;
   float* gwo_img = pl.gwo_img_off ? reinterpret_cast<float*>(wsb + pl.gwo_img_off) : nullptr;
   ga.zero.p[5] = gwo_img;
-  ga.zero.n[5] = gwo_img ? (long long)g.n * g.M * g.kdim : 0;
+  ga.zero.n[5] = gwo_img ? (long long)g.n * gwo_frag_count(g.M, g.c_in, g.K) : 0;
   // the tensor-core GCOL GEMM also reports max |gcol| per tile, from which K3
   // scales its fixed-point grad_x accumulation
   const bool tc_gcol = prob->dtype == DC_BF16 && tc_gemm_supported(g);
@@ -263,11 +264,11 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
   // main weight gradient from the replayed map; the tensor-core GEMM also sums
   // K4's per-image grad_w_off partials once K4 is done (its CTAs wait for K4
   // before exiting anyway), else a small kernel does
-  const bool gw_reduces = gwo_img && tc_gcol && (g.M * g.kdim) % 4 == 0;
+  const bool gw_reduces = gwo_img && tc_gcol;
   if (gw_reduces) {
     ga.gwo_img = gwo_img;
     ga.gw_off = grad_w_off;
-    ga.gwo_count = (long long)g.M * g.kdim;
+    ga.gwo_count = gwo_frag_count(g.M, g.c_in, g.K);
   }
   st = cuda_status(timed("gemm_gw", s, [&] { return launch_gemm_gw(ga, prob->dtype, s); }));
   if (st != DC_OK || !gwo_img || gw_reduces) return st;

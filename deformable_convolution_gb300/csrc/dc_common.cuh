@@ -148,7 +148,7 @@ struct GemmArgs {
   ZeroArgs zero;      // GCOL kernels clear these (the backward's atomic targets)
   float* gmax;        // tensor-core GCOL: max |gcol| per 128 x 128 tile (4 floats each), or null
   // tensor-core GW: after K4, gw_off = sum over images of gwo_img (count
-  // floats per image); null = nothing to reduce
+  // floats per image, in the order of gwo_frag_dest); null = nothing to reduce
   const float* gwo_img;
   float* gw_off;
   long long gwo_count;
@@ -195,10 +195,41 @@ struct OffconvBwdArgs {
   float* gx;
   float* gw_off;
   float* gb_off;  // may be null
-  // tensor-core kernel: per-image partial sums of grad_w_off [n][M][C_in][K]
-  // (cleared by GCOL), reduced into gw_off by launch_gw_off_reduce
+  // tensor-core kernel: per-image partial sums of grad_w_off, gwo_frag_count
+  // floats per image in the order below (cleared by GCOL), reduced into gw_off
+  // by the grad_W GEMM's tail or launch_gw_off_reduce
   float* gw_off_img;
 };
+
+// The tensor-core K4 adds its grad_w_off partials in the order of its mma
+// accumulators, [channel slice of 16][tap][offset-channel tile of 8][lane][4],
+// so that a warp's partial of one tile is 512 contiguous bytes (one 16-byte
+// atomic per lane) instead of 32 scattered floats per instruction.
+constexpr int kGwoSlice = 16;
+
+__host__ __device__ inline long long gwo_frag_count(int M, int c_in, int K) {
+  return (long long)((c_in + kGwoSlice - 1) / kGwoSlice) * K * ((M + 7) / 8) * 128;
+}
+
+// grad_w_off [M][C_in][K] indices of the four elements 4 * e4 .. 4 * e4 + 3
+// of that order (one lane's accumulator tile); -1 for the padding (offset
+// channel >= M or input channel >= C_in).  Accumulator element h of lane l
+// holds row (l >> 2) + 8 * (h >> 1) (the channel within the slice) and column
+// 2 * (l & 3) + (h & 1) (the offset channel within the tile).  32-bit index
+// arithmetic: one image's partials are far below 2^31 floats.
+__host__ __device__ inline void gwo_frag_dest4(int e4, int M, int c_in, int K, long long d[4]) {
+  const int lane = e4 & 31, r = e4 >> 5;
+  const int mtiles = (M + 7) / 8;
+  const int sk = r / mtiles, mt = r - sk * mtiles;
+  const int slice = sk / K, k = sk - slice * K;
+  const int m0 = mt * 8 + 2 * (lane & 3);
+  const int c0 = slice * kGwoSlice + (lane >> 2);
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const int m = m0 + (h & 1), c = c0 + 8 * (h >> 1);
+    d[h] = (m < M && c < c_in) ? ((long long)m * c_in + c) * K + k : -1;
+  }
+}
 cudaError_t launch_offconv_bwd(const OffconvBwdArgs& a, dc_dtype dt, cudaStream_t s);
 size_t offconv_bwd_smem_bytes(const Geom& g, dc_dtype dt);
 // histogram of the margin each sampling tap needs (DC_MARGIN_BINS bins)

@@ -50,7 +50,7 @@ struct TcArgs {
   const float* gwo_img;        // GW: per-image grad_w_off partials to sum after K4 (or null)
   float* gw_off;
   long long gwo_count;         // floats per image
-  int gwo_nimg;
+  int gwo_nimg, gwo_m, gwo_cin, gwo_k;  // images; M, C_in, K of the partials' order
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -450,9 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (KIND == GW) {
     pdl_wait();  // completes no earlier than K4
     if (a.gwo_img) {
-      // K4 is complete: sum its per-image grad_w_off partials, float4 columns
-      // spread over all CTAs of this grid (both buffers are 16-byte aligned
-      // and the count is a multiple of 4: checked on the host)
+      // K4 is complete: sum its per-image grad_w_off partials, float4 runs of
+      // K4's accumulator order spread over all CTAs of this grid, each element
+      // stored to its place in grad_w_off (the buffer is 16-byte aligned and
+      // the count a multiple of 4: checked on the host)
       const long long c4 = a.gwo_count / 4;
       const long long nthreads = (long long)gridDim.x * gridDim.y * gridDim.z * kThreads;
       const long long me =
@@ -460,15 +461,26 @@ __global__ void __launch_bounds__(kThreads, 1)
               kThreads + threadIdx.x;
       const float4* src = reinterpret_cast<const float4*>(a.gwo_img);
       for (long long e = me; e < c4; e += nthreads) {
-        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int n = 0; n < a.gwo_nimg; ++n) {
-          const float4 v = src[(long long)n * c4 + e];
-          s.x += v.x;
-          s.y += v.y;
-          s.z += v.z;
-          s.w += v.w;
+        // eight images' loads in flight per thread
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int n0 = 0; n0 < a.gwo_nimg; n0 += 8) {
+          float4 v[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            v[u] = n0 + u < a.gwo_nimg ? src[(long long)(n0 + u) * c4 + e] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            s[0] += v[u].x;
+            s[1] += v[u].y;
+            s[2] += v[u].z;
+            s[3] += v[u].w;
+          }
         }
-        reinterpret_cast<float4*>(a.gw_off)[e] = s;
+        long long d[4];
+        gwo_frag_dest4((int)e, a.gwo_m, a.gwo_cin, a.gwo_k, d);
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+          if (d[h] >= 0) a.gw_off[d[h]] = s[h];
       }
     }
   }
@@ -638,13 +650,15 @@ cudaError_t launch_gemm_gw_tc(const GemmArgs& ga, cudaStream_t s) {
   if (!col_map(&B, ga.col, g, ga.col_layout, 128)) return cudaErrorInvalidValue;
   TcArgs a{};
   if (ga.gwo_img) {
-    if ((ga.gwo_count & 3) || (reinterpret_cast<uintptr_t>(ga.gwo_img) & 15) ||
-        (reinterpret_cast<uintptr_t>(ga.gw_off) & 15))
+    if ((ga.gwo_count & 3) || (reinterpret_cast<uintptr_t>(ga.gwo_img) & 15))
       return cudaErrorInvalidValue;
     a.gwo_img = ga.gwo_img;
     a.gw_off = ga.gw_off;
     a.gwo_count = ga.gwo_count;
     a.gwo_nimg = g.n;
+    a.gwo_m = g.M;
+    a.gwo_cin = g.c_in;
+    a.gwo_k = g.K;
   }
   a.c_out = g.c_out;
   a.kdim = g.kdim;

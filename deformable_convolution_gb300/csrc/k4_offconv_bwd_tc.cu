@@ -28,7 +28,7 @@ namespace dc {
 namespace {
 
 using band::kThreads;
-constexpr int kCpc = 16;  // channels per CTA: one mma row tile
+constexpr int kCpc = kGwoSlice;  // channels per CTA: one mma row tile
 constexpr int kMaxM = 80;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMChunk = 5;  // offset-channel n-tiles per pass of the weight part
@@ -36,7 +36,7 @@ constexpr int kQGroup = 4;  // window-position n-tiles per unit of the input par
 
 struct TcPlan {
   int R, TW, tiles_w, tiles_h, npx, nslices;
-  int rows, cols, npos, nq;  // window (receptive field), positions, rounded to 8
+  int rows, cols, npos, nq;  // window (receptive field + 1 column, even), positions, rounded to 8
   int xplane;                // words per channel plane of the pair-packed window
   int pxp, mp8, mp16;        // pixels to 16, offset channels to 8 and 16
   int sa, sb, sw;            // word strides of ga [m][px/2], gb [px][m/2], wa [(k,c)][m/2]
@@ -53,8 +53,11 @@ __host__ TcPlan make_tc_plan(const Geom& g, int px) {
   p.tiles_h = sh.tiles_h;
   p.nslices = (g.c_in + kCpc - 1) / kCpc;
   p.rows = sh.rows;
-  p.cols = sh.cols;
-  p.npos = sh.rows * sh.cols;
+  // one more column, rounded to even: the window starts at an even image
+  // column, so the two window positions of an accumulator pair are two
+  // adjacent, 8-byte aligned grad_x elements
+  p.cols = (sh.cols + 2) & ~1;
+  p.npos = p.rows * p.cols;
   p.nq = (p.npos + 7) / 8 * 8;
   p.xplane = band::pad_plane(p.npos);
   p.pxp = (p.npx + 15) / 16 * 16;
@@ -140,14 +143,17 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
   const int n = blockIdx.z;
   const int c_begin = slice * kCpc;
   const int ncur = min(g.c_in, c_begin + kCpc) - c_begin;
-  const int ylo = ho0 * g.sh - g.ph, xlo = wo0 * g.sw - g.pw;
+  const int ylo = ho0 * g.sh - g.ph;
+  // window column 0 is image column xlo (even); the receptive field starts xs later
+  const int xs = (wo0 * g.sw - g.pw) & 1, xlo = wo0 * g.sw - g.pw - xs;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int M = g.M, K = g.K;
   const long long img = (long long)n * g.c_in * g.hw;
-  // grad_w_off partial sums: this image's copy (reduced after the grad_W GEMM)
-  // when given, else grad_w_off itself
-  float* gwo = a.gw_off_img ? a.gw_off_img + (long long)n * M * g.c_in * K : a.gw_off;
+  // grad_w_off partial sums: this image's copy in accumulator order (reduced
+  // after K4) when given, else grad_w_off itself
+  const bool gwo_frag = a.gw_off_img != nullptr;
+  float* gwo = gwo_frag ? a.gw_off_img + (long long)n * gwo_frag_count(M, g.c_in, K) : a.gw_off;
 
   uint32_t* xp = reinterpret_cast<uint32_t*>(smem + pl.off_xp);      // [kCpc][xplane]
   uint32_t* ga = reinterpret_cast<uint32_t*>(smem + pl.off_ga);      // [mp8][sa]
@@ -163,10 +169,10 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
     const int p = 2 * j;
     if (p < pl.npx) {
       const int r = p / pl.TW, c = p - r * pl.TW;
-      e.x = r * g.sh * pl.cols + c * g.sw;
+      e.x = r * g.sh * pl.cols + c * g.sw + xs;
       if (p + 1 < pl.npx) {
         const int r1 = (p + 1) / pl.TW, c1 = p + 1 - r1 * pl.TW;
-        e.y = r1 * g.sh * pl.cols + c1 * g.sw;
+        e.y = r1 * g.sh * pl.cols + c1 * g.sw + xs;
       }
     }
     pair[j] = e;
@@ -418,6 +424,8 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
   // the pixels 2j, 2j + 1 of every pair share a band row (and are one column
   // stride apart) when the tile is one row or an even number of columns wide
   const bool pairs_in_row = pl.R == 1 || (pl.TW & 1) == 0;
+  // grad_x element pairs are 8-byte aligned when image rows have even length
+  const bool gx_pairs = (g.w & 1) == 0 && (reinterpret_cast<uintptr_t>(a.gx) & 7) == 0;
   for (int unit = warp; unit < K + qunits; unit += kWarps) {
     if (unit < K) {
       // ---- weight part, tap k: rows = 16 channels, columns = offset channels
@@ -457,6 +465,15 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
 #pragma unroll
         for (int t = 0; t < kMChunk; ++t) {
           if (mt0 + t >= mtiles8) break;
+          if (gwo_frag) {
+            // the accumulator tile as one 16-byte atomic per lane (lanes whose
+            // four elements are all padding hold zeros and skip it)
+            if (gid < ncur && (mt0 + t) * 8 + 2 * tig < M)
+              atomicAdd(reinterpret_cast<float4*>(gwo + ((long long)(slice * K + k) * mtiles8 + mt0 + t) * 128 +
+                                                  lane * 4),
+                        make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]));
+            continue;
+          }
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
             const int cl = gid + (h >> 1) * 8;
@@ -484,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
         lqc[tp] = 0;
         if (q < pl.npos) {
           lqr[tp] = q / pl.cols;
-          lqc[tp] = q - lqr[tp] * pl.cols;
+          lqc[tp] = q - lqr[tp] * pl.cols - xs;
         }
       }
       const uint32_t gb_lane = smem_addr(gb) + ((lane >> 3) & 1) * 16;
@@ -534,74 +551,82 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
 #pragma unroll
       for (int t = 0; t < kQGroup; ++t) {
         if (nt0 + t >= qtiles) break;
+        // window positions q0 = 8 * tile + 2 * tig and q0 + 1 of accumulator
+        // columns 2 * tig, 2 * tig + 1: one window row (cols and npos are even)
+        const int q0 = (nt0 + t) * 8 + 2 * tig;
+        if (q0 >= pl.npos) continue;
+        const int qrow = q0 / pl.cols, qcol = q0 - qrow * pl.cols;
+        const int yy = ylo + qrow, xx = xlo + qcol;
+        if (yy < 0 || yy >= g.h) continue;
+        float* dst = a.gx + img + (long long)c_begin * g.hw + (long long)yy * g.w + xx;
+        if (gx_pairs) {
+          // xx is even and the image width even: both columns lie in the image
+          // or both outside; one 8-byte atomic per channel
+          if (xx < 0 || xx >= g.w) continue;
+          if (gid < ncur && (acc[0][t][0] != 0.f || acc[0][t][1] != 0.f))
+            atomicAdd(reinterpret_cast<float2*>(dst + (long long)gid * g.hw),
+                      make_float2(acc[0][t][0], acc[0][t][1]));
+          if (gid + 8 < ncur && (acc[0][t][2] != 0.f || acc[0][t][3] != 0.f))
+            atomicAdd(reinterpret_cast<float2*>(dst + (long long)(gid + 8) * g.hw),
+                      make_float2(acc[0][t][2], acc[0][t][3]));
+          continue;
+        }
 #pragma unroll
         for (int hc = 0; hc < 2; ++hc) {
-          // window position of accumulator column 2 * tig + hc
-          const int q = (nt0 + t) * 8 + 2 * tig + hc;
-          if (q >= pl.npos) continue;
-          const int qrow = q / pl.cols, qcol = q - qrow * pl.cols;
-          const int yy = ylo + qrow, xx = xlo + qcol;
-          if (yy < 0 || yy >= g.h || xx < 0 || xx >= g.w) continue;
-          float* dst = a.gx + img + (long long)c_begin * g.hw + (long long)yy * g.w + xx;
-          if (gid < ncur && acc[0][t][hc] != 0.f) atomicAdd(dst + (long long)gid * g.hw, acc[0][t][hc]);
+          if (xx + hc < 0 || xx + hc >= g.w) continue;
+          if (gid < ncur && acc[0][t][hc] != 0.f) atomicAdd(dst + hc + (long long)gid * g.hw, acc[0][t][hc]);
           if (gid + 8 < ncur && acc[0][t][2 + hc] != 0.f)
-            atomicAdd(dst + (long long)(gid + 8) * g.hw, acc[0][t][2 + hc]);
+            atomicAdd(dst + hc + (long long)(gid + 8) * g.hw, acc[0][t][2 + hc]);
         }
       }
     }
   }
 }
 
-// grad_w_off[e] = sum over images of the per-image partials; one thread per
-// element, the image loop strided by M * C_in * K
+// grad_w_off = sum over images of the per-image partials (in K4's accumulator
+// order): one thread per float4 of that order, eight images' loads in flight,
+// each element stored to its place in grad_w_off
 __global__ void __launch_bounds__(kThreads) gw_off_reduce(const float* __restrict__ img_part,
                                                           float* __restrict__ gw_off, int nimg,
-                                                          long long count) {
+                                                          long long count, int M, int c_in, int K) {
   pdl_wait();  // the partials are complete once K4 (and the GEMM after it) finished
-  if ((count & 3) == 0 && (reinterpret_cast<uintptr_t>(img_part) & 15) == 0 &&
-      (reinterpret_cast<uintptr_t>(gw_off) & 15) == 0) {
-    // float4 columns, eight images' loads in flight per thread
-    const long long c4 = count / 4;
-    const float4* src = reinterpret_cast<const float4*>(img_part);
-    for (long long e = blockIdx.x * (long long)kThreads + threadIdx.x; e < c4;
-         e += (long long)gridDim.x * kThreads) {
-      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-      int n = 0;
-      for (; n + 8 <= nimg; n += 8) {
-        float4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) v[u] = src[(long long)(n + u) * c4 + e];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          s.x += v[u].x;
-          s.y += v[u].y;
-          s.z += v[u].z;
-          s.w += v[u].w;
-        }
-      }
-      for (; n < nimg; ++n) {
-        const float4 v = src[(long long)n * c4 + e];
-        s.x += v.x;
-        s.y += v.y;
-        s.z += v.z;
-        s.w += v.w;
-      }
-      reinterpret_cast<float4*>(gw_off)[e] = s;
-    }
-    return;
-  }
-  for (long long e = blockIdx.x * (long long)kThreads + threadIdx.x; e < count;
+  const long long c4 = count / 4;
+  const float4* src = reinterpret_cast<const float4*>(img_part);
+  for (long long e = blockIdx.x * (long long)kThreads + threadIdx.x; e < c4;
        e += (long long)gridDim.x * kThreads) {
-    float s = 0.f;
-    for (int n = 0; n < nimg; ++n) s += img_part[(long long)n * count + e];
-    gw_off[e] = s;
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    int n = 0;
+    for (; n + 8 <= nimg; n += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = src[(long long)(n + u) * c4 + e];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        s[0] += v[u].x;
+        s[1] += v[u].y;
+        s[2] += v[u].z;
+        s[3] += v[u].w;
+      }
+    }
+    for (; n < nimg; ++n) {
+      const float4 v = src[(long long)n * c4 + e];
+      s[0] += v.x;
+      s[1] += v.y;
+      s[2] += v.z;
+      s[3] += v.w;
+    }
+    long long d[4];
+    gwo_frag_dest4((int)e, M, c_in, K, d);
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      if (d[h] >= 0) gw_off[d[h]] = s[h];
   }
 }
 
 }  // namespace
 
 cudaError_t launch_gw_off_reduce(const OffconvBwdArgs& a, cudaStream_t s) {
-  const long long count = (long long)a.g.M * a.g.kdim;
+  const long long count = gwo_frag_count(a.g.M, a.g.c_in, a.g.K);
   long long blocks = (count / 4 + kThreads - 1) / kThreads;
   if (blocks > 152 * 4) blocks = 152 * 4;
   if (blocks < 1) blocks = 1;
@@ -615,7 +640,7 @@ cudaError_t launch_gw_off_reduce(const OffconvBwdArgs& a, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, gw_off_reduce, (const float*)a.gw_off_img, a.gw_off,
-                                     a.g.n, count);
+                                     a.g.n, count, a.g.M, a.g.c_in, a.g.K);
   note_launches(1);
   return e;
 }
