@@ -134,6 +134,7 @@ __device__ __forceinline__ uint32_t x_pair(const uint32_t* plane, int2 e, int ta
 
 __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs a, TcPlan pl) {
   extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int s_next_unit;  // work units handed out after each warp's first
   const Geom g = a.g;
   const __nv_bfloat16* __restrict__ x = static_cast<const __nv_bfloat16*>(a.x);
   const unsigned short* __restrict__ w_off = static_cast<const unsigned short*>(a.w_off);
@@ -187,6 +188,7 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
     }
     gpos[px] = v;
   }
+  if (tid == 0) s_next_unit = 0;
   // gb's last row stays zero: window positions that no pixel's tap reaches
   for (int j = tid; j < pl.mp16 / 2; j += kThreads) gb[pl.pxp * pl.sb + j] = 0u;
   // input window of the slice as pixel-pair words (x[q], x[q + column stride]),
@@ -322,15 +324,25 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
       const int o = gpos[px];
       return (m < M && o >= 0) ? gsrc[(long long)m * g.howo + o] : 0.f;
     };
-    // full-width band with 16-byte aligned rows: the band's pixels are one
-    // contiguous run of each goff plane, read as float4; a warp covers 8
-    // offset-channel pairs x 4 pixel quads (conflicts on the packed stores stay
-    // two-way)
+    // pixel quads read as float4; a warp covers 8 offset-channel pairs x 4
+    // pixel quads (conflicts on the packed stores stay two-way).  Full-width
+    // band with 16-byte aligned rows: the band's pixels are one contiguous run
+    // of each goff plane.  Tile rows of whole quads (TW and Wo multiples of 4):
+    // a quad is four pixels of one tile row, all inside or all outside the
+    // output.
     const int nvalid = (min(ho0 + pl.R, g.ho) - ho0) * g.wo;
-    const bool vec = pl.TW == g.wo && (g.howo & 3) == 0 && ((ho0 * g.wo) & 3) == 0 &&
-                     (nvalid & 3) == 0 && (reinterpret_cast<uintptr_t>(a.goff) & 15) == 0;
+    const bool aligned = (reinterpret_cast<uintptr_t>(a.goff) & 15) == 0;
+    const bool run = pl.TW == g.wo && (g.howo & 3) == 0 && ((ho0 * g.wo) & 3) == 0 &&
+                     (nvalid & 3) == 0 && aligned;
+    const bool quads = !run && (pl.TW & 3) == 0 && (g.wo & 3) == 0 && aligned;
+    const bool vec = run || quads;
+    // goff plane offset of the tile's pixel quad p4, -1 outside the output
+    auto quad_at = [&](int p4) -> int {
+      if (run) return 4 * p4 < nvalid ? ho0 * g.wo + 4 * p4 : -1;
+      const int r = (4 * p4) / pl.TW, c = 4 * p4 - r * pl.TW;
+      return (4 * p4 < pl.npx && ho0 + r < g.ho && wo0 + c < g.wo) ? (ho0 + r) * g.wo + wo0 + c : -1;
+    };
     if (vec) {
-      const float* band0 = gsrc + (long long)ho0 * g.wo;
       const int pblocks = pl.pxp / 16, nblk = (pl.mp16 / 16) * pblocks;
       for (int blk0 = warp; blk0 < nblk; blk0 += 2 * kWarps) {
         float4 f[2][2];
@@ -342,11 +354,12 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
           jj[u] = jb * 8 + (lane >> 2);
           pq[u] = pb * 4 + (lane & 3);
           f[u][0] = f[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (blk < nblk && 4 * pq[u] < nvalid) {
+          const int o = blk < nblk ? quad_at(pq[u]) : -1;
+          if (o >= 0) {
             if (2 * jj[u] < M)
-              f[u][0] = *reinterpret_cast<const float4*>(band0 + (long long)(2 * jj[u]) * g.howo + 4 * pq[u]);
+              f[u][0] = *reinterpret_cast<const float4*>(gsrc + (long long)(2 * jj[u]) * g.howo + o);
             if (2 * jj[u] + 1 < M)
-              f[u][1] = *reinterpret_cast<const float4*>(band0 + (long long)(2 * jj[u] + 1) * g.howo + 4 * pq[u]);
+              f[u][1] = *reinterpret_cast<const float4*>(gsrc + (long long)(2 * jj[u] + 1) * g.howo + o);
           }
         }
 #pragma unroll
@@ -414,8 +427,10 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
   __syncthreads();
 
   // ---------------------------------------------------------------- both contractions
-  // work units, round robin over the warps: K weight-part units (one tap each)
-  // then the input part in groups of kQGroup position tiles
+  // work units: the input part in groups of kQGroup position tiles (the
+  // larger units, first) and K weight-part units (one tap each); each warp
+  // takes its first unit by index and every further one from a shared
+  // counter, so warps that drew small units take more of them
   const int qtiles = pl.nq / 8;
   const bool unit_stride = g.sh == 1 && g.sw == 1;
   const int qunits = (qtiles + kQGroup - 1) / kQGroup;
@@ -426,7 +441,13 @@ __global__ void __launch_bounds__(kThreads, 3) k4_offconv_bwd_tc(OffconvBwdArgs 
   const bool pairs_in_row = pl.R == 1 || (pl.TW & 1) == 0;
   // grad_x element pairs are 8-byte aligned when image rows have even length
   const bool gx_pairs = (g.w & 1) == 0 && (reinterpret_cast<uintptr_t>(a.gx) & 7) == 0;
-  for (int unit = warp; unit < K + qunits; unit += kWarps) {
+  auto next_seq = [&]() {
+    int v = 0;
+    if (lane == 0) v = atomicAdd(&s_next_unit, 1);
+    return __shfl_sync(0xffffffffu, v, 0) + kWarps;
+  };
+  for (int seq = warp; seq < K + qunits; seq = next_seq()) {
+    const int unit = seq < qunits ? K + seq : seq - qunits;
     if (unit < K) {
       // ---- weight part, tap k: rows = 16 channels, columns = offset channels
       const int k = unit;
