@@ -604,7 +604,12 @@ def margin_report(p, t, dev):
 
 def e2e(p, d, dev, stream, flops_step, iters=20):
     """Same metric through the ABI with host buffers: every step copies its
-    inputs from pinned host memory and reads the outputs back."""
+    inputs from pinned host memory and reads all outputs back.  The step is
+    one CUDA graph over two streams: grad_y's upload and the read-back of the
+    forward's outputs (y, offsets) run on a copy stream beside the compute,
+    the forward's inputs go up before the forward and the gradients come
+    back after the backward.  Each replay is a whole step: every copy of
+    every step happens inside the timed region."""
     import torch
 
     from deformable_convolution_gb300 import binding as B
@@ -622,32 +627,68 @@ def e2e(p, d, dev, stream, flops_step, iters=20):
     ws = B.workspace(p, True, dev)
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = sum(v.numel() * v.element_size() for v in hout.values())
+    cs = torch.cuda.Stream(device=dev)
+    e_gy = torch.cuda.Event()
+    e_fwd = torch.cuda.Event()
 
     def one():
+        # fork: the copy stream uploads grad_y while the forward runs
+        cs.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cs):
+            devt["grad_y"].copy_(host["grad_y"], non_blocking=True)
+            e_gy.record(cs)
         for k, v in host.items():
-            if v is not None:
+            if v is not None and k != "grad_y":
                 devt[k].copy_(v, non_blocking=True)
         B.deform_conv_fwd(p, devt["x"], devt["w_off"], devt["b_off"], devt["w"],
                           devt["offset_add"], outs["y"], outs["off"], None, ws)
+        e_fwd.record(torch.cuda.current_stream(dev))
+        # the forward's outputs come back while the backward runs (both only read them)
+        cs.wait_event(e_fwd)
+        with torch.cuda.stream(cs):
+            for k in ("y", "off"):
+                hout[k].copy_(outs[k], non_blocking=True)
+        torch.cuda.current_stream(dev).wait_event(e_gy)
         B.deform_conv_bwd(p, devt["x"], devt["w_off"], devt["w"], outs["off"], devt["grad_y"],
                           outs["gx"], outs["gwo"], outs["gbo"], outs["gw"], outs["goff"], ws,
                           after_fwd=True)
-        for k, v in outs.items():
-            hout[k].copy_(v, non_blocking=True)
+        for k in ("gx", "gwo", "gbo", "gw", "goff"):
+            hout[k].copy_(outs[k], non_blocking=True)
+        # join
+        torch.cuda.current_stream(dev).wait_stream(cs)
 
     with torch.cuda.stream(stream):
         for _ in range(3):
             one()
+    torch.cuda.synchronize(dev)
+    step = one
+    how = "CUDA graph per step"
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            one()
+        torch.cuda.synchronize(dev)
+        step = graph.replay
+    except RuntimeError as e:  # capture refused: the same two-stream step, launched eagerly
+        torch.cuda.synchronize(dev)
+        how = f"eager launches (graph capture failed: {str(e).splitlines()[0][:120]})"
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
         torch.cuda.synchronize(dev)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for _ in range(iters):
-            one()
+            step()
         b.record(stream)
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / iters
+    # the read-back is complete: the last step's y on the host equals the device copy
+    assert torch.equal(hout["y"], outs["y"].cpu()), "e2e read-back mismatch"
     return {"value": flops_step / (ms / 1e3) / 1e9, "unit": "GFLOP/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "method": how + ": forward inputs up, forward, backward, gradients back on the compute "
+                            "stream; grad_y up and y/offsets back on a copy stream beside it"}
 
 
 if __name__ == "__main__":
