@@ -364,6 +364,9 @@ def main():
         line["kernels"] = kernels
         line["sampling_stage"] = k1_roofline(p, t, dev, stream, flush, wl, args.roofline_iters)
         line["unfused_ablation"] = unfused_ablation(p, t, dev, stream, flush, args.roofline_iters)
+        sga = sampled_gemm_ablation(p, t, dev, stream, flush, args.roofline_iters)
+        if sga is not None:
+            line["sampled_gemm_ablation"] = sga
         line["margin"] = margin_report(p, t, dev)
         line["e2e"] = e2e(p, d, dev, stream, flops_step, args.e2e_iters)
         if not args.no_cpu_baseline:
@@ -580,6 +583,39 @@ def unfused_ablation(p, t, dev, stream, flush, iters=200):
             "ai_fused": flops / bytes_fused, "ai_unfused": flops / bytes_unfused,
             "note": "fused: one K1 launch; unfused: offsets-only K1 then the sampler reading "
                     "offsets from HBM; both write the offsets and the deformed map"}
+
+
+def sampled_gemm_ablation(p, t, dev, stream, flush, iters=200):
+    """The forward pass two ways, each timed alone between L2 flushes: the
+    library's path (fused offset convolution + interpolation writing the
+    deformed map, then the tensor-core GEMM reading it) against the sampled-
+    operand GEMM (offsets-only K1, then one kernel that samples each map tile
+    into shared memory as the GEMM's B operand: the map never reaches memory).
+    The explainer page argues for the first (the GEMM stays a separate, tuned
+    kernel); the second removes the map's write and read."""
+    import torch
+
+    from deformable_convolution_gb300 import binding as B
+    if p.dtype != 1:
+        return None
+    s = p.shapes()
+    y = torch.empty(s["y"], dtype=p.torch_dtype, device=dev)
+    off = torch.empty(s["offset"], dtype=torch.float32, device=dev)
+    ws = B.workspace(p, False, dev)
+    add = t["offset_add"]
+    two = time_graph(lambda: B.deform_conv_fwd(p, t["x"], t["w_off"], t["b_off"], t["w"], add, y,
+                                               off, None, ws), dev, stream, flush, iters)
+    one = time_graph(lambda: B.deform_conv_fwd_sampled_gemm(p, t["x"], t["w_off"], t["b_off"],
+                                                            t["w"], add, y, off),
+                     dev, stream, flush, iters)
+    P = p.n * p.ho * p.wo
+    kdim = p.c_in * p.kh * p.kw
+    col_b = kdim * P * 2
+    return {"map_in_hbm_us": two * 1e3, "sampled_operand_us": one * 1e3, "speedup": two / one,
+            "map_bytes_avoided": 2 * col_b,
+            "note": "map_in_hbm: K1 (offset conv + sampling, map to memory) + tensor-core GEMM; "
+                    "sampled_operand: offsets-only K1 + one GEMM whose sampling warps write each "
+                    "64x64 map tile into its shared-memory B operand"}
 
 
 def margin_report(p, t, dev):

@@ -24,7 +24,7 @@ EXPORTED_SYMBOLS = (
     "deform_conv_bwd", "deform_conv_sample", "dc_status_string", "dc_build_info",
     "dc_launch_count", "deform_conv_fwd_noalloc", "dc_device_error", "dc_kernel_timing",
     "dc_kernel_times", "deform_conv_offsets", "deform_conv_margin_histogram", "dc_suggest_margin",
-    "deform_conv_bwd_after_fwd",
+    "deform_conv_bwd_after_fwd", "deform_conv_fwd_sampled_gemm",
 )
 MARGIN_BINS = 64
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
         L.deform_conv_sample.restype = i
         L.deform_conv_offsets.argtypes = [pp, vp, vp, vp, vp, vp, vp]
         L.deform_conv_offsets.restype = i
+        L.deform_conv_fwd_sampled_gemm.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.deform_conv_fwd_sampled_gemm.restype = i
         L.deform_conv_margin_histogram.argtypes = [pp, vp, vp, vp]
         L.deform_conv_margin_histogram.restype = i
         L.dc_suggest_margin.argtypes = [pp, ctypes.POINTER(ctypes.c_ulonglong), ctypes.c_double, i]
@@ -292,6 +294,19 @@ def deform_conv_offsets(p: Problem, x, w_off, b_off, offset_add, offset_out, str
         _ptr(b_off, "b_off", s["b_off"], f32, True),
         _ptr(offset_add, "offset_add", s["offset"], f32, True),
         _ptr(offset_out, "offset_out", s["offset"], f32), _stream(stream)), "deform_conv_offsets")
+
+
+def deform_conv_fwd_sampled_gemm(p: Problem, x, w_off, b_off, w, offset_add, y, offset_out,
+                                 stream=None):
+    s = p.shapes()
+    dt, f32 = p.torch_dtype, torch.float32
+    st = p.c_struct()
+    _check(lib().deform_conv_fwd_sampled_gemm(
+        ctypes.byref(st), _ptr(x, "x", s["x"], dt), _ptr(w_off, "w_off", s["w_off"], dt),
+        _ptr(b_off, "b_off", s["b_off"], f32, True), _ptr(w, "w", s["w"], dt),
+        _ptr(offset_add, "offset_add", s["offset"], f32, True), _ptr(y, "y", s["y"], dt),
+        _ptr(offset_out, "offset_out", s["offset"], f32), _stream(stream)),
+        "deform_conv_fwd_sampled_gemm")
 
 
 def deform_conv_margin_histogram(p: Problem, offset, hist, stream=None):

@@ -418,6 +418,36 @@ dc_status deform_conv_offsets(const dc_problem* prob, const void* x, const void*
   return cuda_status(timed("k1_offsets", s, [&] { return launch_sample(sa, prob->dtype, s); }));
 }
 
+dc_status deform_conv_fwd_sampled_gemm(const dc_problem* prob, const void* x, const void* w_off,
+                                       const float* b_off, const void* w,
+                                       const float* offset_add, void* y, float* offset_out,
+                                       void* stream) {
+  Geom g;
+  int margin;
+  dc_status st = make_geom(prob, &g, &margin);
+  if (st != DC_OK) return st;
+  if (!x || !w_off || !w || !y || !offset_out) return DC_ERR_INVALID_ARG;
+  if (prob->dtype != DC_BF16 || !fwd_sampled_supported(g)) return DC_ERR_UNSUPPORTED;
+  const void* ptrs[] = {x, w_off, b_off, w, offset_add, y, offset_out};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return DC_ERR_UNSUPPORTED;
+  SampleArgs sa{};
+  sa.g = g;
+  sa.x = x;
+  sa.w_off = w_off;
+  sa.b_off = b_off;
+  sa.off_add = offset_add;
+  sa.col = nullptr;  // K1 stops after the offset convolution
+  sa.off_out = offset_out;
+  sa.margin = margin;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = cuda_status(timed("k1_offsets", s, [&] { return launch_sample(sa, prob->dtype, s); }));
+  if (st != DC_OK) return st;
+  return cuda_status(timed("gemm_fwd_sampled", s, [&] {
+    return launch_fwd_sampled_tc(g, x, w, offset_out, y, s);
+  }));
+}
+
 dc_status deform_conv_margin_histogram(const dc_problem* prob, const float* offset,
                                        unsigned long long* hist, void* stream) {
   Geom g;

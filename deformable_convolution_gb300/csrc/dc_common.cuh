@@ -158,6 +158,11 @@ bool tc_gemm_supported(const Geom& g);
 cudaError_t launch_gemm_fwd_tc(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_gcol_tc(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_gw_tc(const GemmArgs& a, cudaStream_t s);
+// Forward GEMM with its B operand sampled in shared memory from x and the
+// offsets (bf16, tensor cores; no column buffer): y = w * map(x, off).
+bool fwd_sampled_supported(const Geom& g);
+cudaError_t launch_fwd_sampled_tc(const Geom& g, const void* x, const void* w, const float* off,
+                                  void* y, cudaStream_t s);
 // CUDA-core (fp32 arithmetic) versions, any layout pitch.
 cudaError_t launch_gemm_fwd_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
 cudaError_t launch_gemm_gcol_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s);

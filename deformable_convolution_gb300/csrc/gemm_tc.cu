@@ -68,6 +68,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -486,6 +490,236 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- sampled forward GEMM
+// The forward main convolution with its B operand -- the deformed map --
+// produced in shared memory by sampling warps instead of read from a column
+// buffer in HBM: the three operators of "The argument in one glance" in fewer
+// kernels, the fusion the explainer page argues against because the GEMM
+// stops being a library call ("Why it fell short", "This paper's idea"), built
+// here as a measured alternative.  One CTA computes a 128 x 64 tile of y.  Per
+// 64-row k-block, warp 4 loads the weight tile with TMA, the ten sampling
+// warps (0-3 and 6-11) write the 64 x 64 bf16 map tile in the 128-byte
+// swizzled MN-major layout a TMA load of the column would have produced, and
+// warp 5 issues the MMAs; warps 0-3 then drain the accumulator.  The samples
+// use the offsets the offset convolution wrote (staged once per CTA) and read
+// x's four corners from global memory with the fused stage's arithmetic, so
+// the map values and the MMA sequence are those of the two-kernel path.
+constexpr int kFsThreads = 384;
+constexpr int kFsSampleWarps = 10;
+constexpr int kFsStages = 4;
+constexpr int kFsBN = 64;
+
+struct FsArgs {
+  Geom g;
+  const __nv_bfloat16* x;
+  const float* off;  // [n][M][howo]
+  __nv_bfloat16* y;  // [n][c_out][howo]
+  int kb_total;
+};
+
+__host__ __device__ inline size_t fs_smem_bytes(int M) {
+  return 1024 + (size_t)kFsStages * Cfg<FWD, kFsBN>::kStage + (size_t)M * kFsBN * 4 +
+         (size_t)kFsBN * 8 + 256;
+}
+
+__device__ __forceinline__ float corner(const __nv_bfloat16* plane, const Geom& g, int y, int x) {
+  return (y >= 0 && y < g.h && x >= 0 && x < g.w) ? __bfloat162float(plane[(long long)y * g.w + x])
+                                                  : 0.0f;
+}
+
+__global__ void __launch_bounds__(kFsThreads, 1)
+    tc_fwd_sampled(const __grid_constant__ CUtensorMap tmA, FsArgs a) {
+  using C = Cfg<FWD, kFsBN>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const Geom g = a.g;
+  float* offs = reinterpret_cast<float*>(smem + kFsStages * C::kStage);  // [M][64]
+  int2* base = reinterpret_cast<int2*>(offs + (size_t)g.M * kFsBN);      // tap-0 row, column per pixel
+  uint64_t* full = reinterpret_cast<uint64_t*>(base + kFsBN);
+  uint64_t* empty = full + kFsStages;
+  uint64_t* done = empty + kFsStages;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kFsBN, n = blockIdx.z;
+  const int nkb = a.kb_total;
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_holder)),
+                 "r"((uint32_t)C::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (threadIdx.x == 32) {
+    for (int s = 0; s < kFsStages; ++s) {
+      mbar_init(&full[s], 1 + kFsSampleWarps);  // the TMA's expect_tx + one per sampling warp
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  pdl_wait();  // the offsets come from the offset convolution just before
+  for (int idx = threadIdx.x; idx < g.M * kFsBN; idx += kFsThreads) {
+    const int m = idx / kFsBN, p = idx - m * kFsBN;
+    offs[idx] = n0 + p < g.howo ? a.off[((long long)n * g.M + m) * g.howo + n0 + p] : 0.f;
+  }
+  for (int p = threadIdx.x; p < kFsBN; p += kFsThreads) {
+    const int q = n0 + p, ho = q / g.wo, wo = q - ho * g.wo;
+    base[p] = make_int2(ho * g.sh - g.ph, wo * g.sw - g.pw);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_release();
+  const uint32_t tmem = *tmem_holder;
+  bool ok = true;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer (weights)
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % kFsStages;
+        if (i >= kFsStages && !mbar_wait(&empty[s], ((i / kFsStages) - 1) & 1)) break;
+        mbar_expect_tx(&full[s], C::kABytes);
+        tma_2d(smem + s * C::kStage, &tmA, &full[s], i * kBK, m0);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = idesc_bf16(kFsBN, 0, 1);
+      for (int i = 0; i < nkb; ++i) {
+        const int s = i % kFsStages;
+        if (!mbar_wait(&full[s], (i / kFsStages) & 1)) break;
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + s * C::kStage);
+        const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          umma(tmem, sdesc(sa + kk * 32, 16, 1024), sdesc(sb + kk * 2048, 8192, 1024), idesc,
+               (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&empty[s]);
+      }
+      umma_commit(done);
+    }
+  } else {
+    // -------------------------------------------------------------- sampling warps
+    // The block's 64 k rows are (channel, tap) pairs in the weights' order
+    // k = c * K + tap.  A warp takes a (tap, 32-pixel half) item: lane l owns
+    // pixel l (+ 32), computes that tap's sampling point once per offset
+    // group and blends it for every channel of the block that has a row for
+    // the tap, storing each value at its place in the row's swizzled 16-byte
+    // chunks.  The corner loads of one instruction fall on neighbouring pixels.
+    constexpr int kH = kFsBN / 32;
+    const int sw = warp < 4 ? warp : warp - 2;
+    const __nv_bfloat16* ximg = a.x + (long long)n * g.c_in * g.hw;
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % kFsStages;
+      if (i >= kFsStages) {
+        const bool w_ok = mbar_wait(&empty[s], ((i / kFsStages) - 1) & 1);
+        if (!__all_sync(0xffffffffu, w_ok)) {
+          ok = false;
+          break;
+        }
+      }
+      unsigned char* sb = smem + s * C::kStage + C::kABytes;
+      const int k_first = i * kBK;
+      const int k_last = min(g.kdim, k_first + kBK) - 1;
+      for (int item = sw; item < g.K * kH; item += kFsSampleWarps) {
+        const int tap = item / kH, h = item - tap * kH;
+        const int p = lane + 32 * h;
+        const int ti = tap / g.kw, tj = tap - ti * g.kw;
+        const bool px_ok = n0 + p < g.howo;
+        const int2 b = base[p];
+        // channels whose row c * K + tap lies in [k_first, k_last], in runs
+        // of one offset group (one sampling point) and chunks of eight whose
+        // corner loads are all issued before the first blend
+        const int c_lo = (k_first - tap + g.K - 1) / g.K;  // k_first - tap >= -(K - 1)
+        const int c_hi = (k_last - tap) >= 0 ? (k_last - tap) / g.K : -1;
+        int c = c_lo < 0 ? 0 : c_lo;
+        while (c <= c_hi) {
+          const int gg = c / g.cg;
+          const int c_end = min(c_hi, (gg + 1) * g.cg - 1);
+          bool inside = false;
+          float ly = 0.f, lx = 0.f;
+          int y0 = 0, x0 = 0;
+          if (px_ok) {
+            const float py = (float)(b.x + ti * g.dh) + offs[(2 * (gg * g.K + tap)) * kFsBN + p];
+            const float px = (float)(b.y + tj * g.dw) + offs[(2 * (gg * g.K + tap) + 1) * kFsBN + p];
+            inside = touches_image(py, px, g.h, g.w);
+            if (inside) {
+              const float fy = floorf(py), fx = floorf(px);
+              y0 = (int)fy;
+              x0 = (int)fx;
+              ly = py - fy;
+              lx = px - fx;
+            }
+          }
+          for (int c8 = c; c8 <= c_end; c8 += 8) {
+            float cv[8][4];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              cv[u][0] = cv[u][1] = cv[u][2] = cv[u][3] = 0.f;
+              if (inside && c8 + u <= c_end) {
+                const __nv_bfloat16* plane = ximg + (long long)(c8 + u) * g.hw;
+                cv[u][0] = corner(plane, g, y0, x0);
+                cv[u][1] = corner(plane, g, y0, x0 + 1);
+                cv[u][2] = corner(plane, g, y0 + 1, x0);
+                cv[u][3] = corner(plane, g, y0 + 1, x0 + 1);
+              }
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              if (c8 + u > c_end) break;
+              const float v = inside ? blend4(ly, lx, cv[u][0], cv[u][1], cv[u][2], cv[u][3]) : 0.f;
+              const int kl = (c8 + u) * g.K + tap - k_first;
+              *reinterpret_cast<unsigned short*>(sb + kl * 128 + (((p >> 3) ^ (kl & 7)) << 4) + (p & 7) * 2) =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(v));
+            }
+          }
+          c = c_end + 1;
+        }
+      }
+      // rows past the reduction (last block): zeros
+      for (int kl = k_last - k_first + 1 + sw; kl < kBK; kl += kFsSampleWarps)
+#pragma unroll
+        for (int h = 0; h < kH; ++h) {
+          const int p = lane + 32 * h;
+          *reinterpret_cast<unsigned short*>(sb + kl * 128 + (((p >> 3) ^ (kl & 7)) << 4) + (p & 7) * 2) = 0;
+        }
+      // the tile is read by the tensor cores (async proxy)
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[s]);
+    }
+    if (warp < 4) {
+      // ------------------------------------------------------------ epilogue
+      ok = __all_sync(0xffffffffu, ok && mbar_wait(done, 0));
+      tc_fence_after();
+      const int row = warp * 32 + lane;
+      const int m = m0 + row;
+      const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < kFsBN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tbase + c * 32, r);
+        if (!ok || nkb == 0 || m >= g.c_out) continue;
+        const int n_first = n0 + c * 32;
+        store_y_row(a.y + ((long long)n * g.c_out + m) * g.howo + n_first, r, n_first, (int)g.howo);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"((uint32_t)C::kTmemCols)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -676,6 +910,38 @@ cudaError_t launch_gemm_gw_tc(const GemmArgs& ga, cudaStream_t s) {
   splits = ceil_div_ll(a.kb_total, a.kb_per_split);
   dim3 grid((unsigned)ceil_div_ll(g.kdim, 128), (unsigned)ceil_div_ll(g.c_out, kBM), (unsigned)splits);
   return launch<GW, 128>(A, B, A, a, grid, s);
+}
+
+bool fwd_sampled_supported(const Geom& g) {
+  return tc_gemm_supported(g) && fs_smem_bytes(g.M) <= 227 * 1024;
+}
+
+cudaError_t launch_fwd_sampled_tc(const Geom& g, const void* x, const void* w, const float* off,
+                                  void* y, cudaStream_t s) {
+  CUtensorMap A;
+  if (!w_map(&A, w, g, 64, 128)) return cudaErrorInvalidValue;
+  FsArgs a{};
+  a.g = g;
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.off = off;
+  a.y = static_cast<__nv_bfloat16*>(y);
+  a.kb_total = (int)ceil_div_ll(g.kdim, kBK);
+  const size_t smem = fs_smem_bytes(g.M);
+  cudaError_t e = cudaFuncSetAttribute(tc_fwd_sampled, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ceil_div_ll(g.howo, kFsBN), (unsigned)ceil_div_ll(g.c_out, kBM), (unsigned)g.n);
+  cfg.blockDim = dim3(kFsThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, tc_fwd_sampled, A, a);
+  note_launches(1);
+  return e;
 }
 
 }  // namespace dc

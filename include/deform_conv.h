@@ -170,6 +170,27 @@ dc_status deform_conv_offsets(const dc_problem* prob, const void* x, const void*
                               const float* b_off, const float* offset_add, float* offset_out,
                               void* stream);
 
+/* The forward pass with the deformed map never written to memory: the
+ * offset convolution (as deform_conv_offsets, offsets to offset_out), then one
+ * tensor-core kernel that samples each 64 x 64 tile of the map from x and the
+ * offsets straight into shared memory as the main GEMM's B operand and
+ * multiplies it by w.  This is the fusion of interpolation and main
+ * convolution that the explainer page argues against ("This paper's idea":
+ * the main convolution should stay a separate, library-grade GEMM), provided
+ * to measure that trade-off.  Same sampling arithmetic and MMA order as
+ * deform_conv_fwd for the same offsets.
+ *   x, w_off, b_off, w, offset_add, y, offset_out  as in deform_conv_fwd
+ *     (y, offset_out required)
+ * No workspace.  Asynchronous on `stream`.  Errors: DC_ERR_INVALID_ARG for a
+ * NULL x, w_off, w, y or offset_out or an invalid problem;
+ * DC_ERR_UNSUPPORTED unless the problem is bf16 with C_in*Kh*Kw and Ho*Wo
+ * multiples of 8 (the tensor-core GEMM's alignment) or for a pointer that is
+ * not 16-byte aligned. */
+dc_status deform_conv_fwd_sampled_gemm(const dc_problem* prob, const void* x, const void* w_off,
+                                       const float* b_off, const void* w,
+                                       const float* offset_add, void* y, float* offset_out,
+                                       void* stream);
+
 /* Margin statistics ("Why it works" / "The idea" on the explainer page: each
  * tile is padded by just enough margin for the offsets that occur, measured
  * from their distribution).  From the offsets a forward call returned, counts

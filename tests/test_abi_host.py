@@ -135,6 +135,27 @@ def test_offsets_argument_checks_fail_before_any_launch():
     assert call(bad) == B.DC_ERR_UNSUPPORTED
 
 
+def test_sampled_gemm_forward_argument_checks_fail_before_any_launch():
+    vp = ctypes.c_void_p
+    good = [0x10000 * (i + 1) for i in range(7)]  # x w_off b_off w add y offset_out
+
+    def call(p, ptrs):
+        st = p.c_struct()
+        return B.lib().deform_conv_fwd_sampled_gemm(ctypes.byref(st),
+                                                    *[vp(v) if v else None for v in ptrs], None)
+    pb = B.Problem(2, 16, 8, 8, 16, 3, 3, 1, 1, 1, 1, B.DC_BF16)
+    for missing in (0, 1, 3, 5, 6):  # x, w_off, w, y and offset_out are required
+        bad = list(good)
+        bad[missing] = 0
+        assert call(pb, bad) == B.DC_ERR_INVALID_ARG
+    bad = list(good)
+    bad[6] += 8
+    assert call(pb, bad) == B.DC_ERR_UNSUPPORTED
+    # tensor-core path only: bf16, C_in*Kh*Kw and Ho*Wo multiples of 8
+    assert call(B.Problem(2, 16, 8, 8, 16, 3, 3, 1, 1, 1, 1, B.DC_F32), good) == B.DC_ERR_UNSUPPORTED
+    assert call(B.Problem(2, 16, 7, 7, 16, 3, 3, 1, 1, 1, 1, B.DC_BF16), good) == B.DC_ERR_UNSUPPORTED
+
+
 def _hist(**bins):
     h = [0] * B.MARGIN_BINS
     for k, v in bins.items():

@@ -336,3 +336,63 @@ def test_backward_after_forward_reuses_the_map():
     ref = oracle_backward(p, cpu, off.cpu().double().numpy())
     for k in ("grad_x", "grad_w", "grad_w_off", "grad_b_off", "grad_offset"):
         assert rel_err(f64(reused[k]), ref[k]) <= TOL[p.dtype], k
+
+
+# The forward pass with the deformed map sampled straight into the GEMM's
+# shared-memory operand (no column buffer): bf16, C_in*Kh*Kw and Ho*Wo
+# multiples of 8.  Geometries: offset groups, stride + dilation, a partial
+# last k-block and pixel tile with two output-channel tiles.
+SAMPLED_GEOMETRIES = [
+    (2, 16, 12, 10, 24, 3, 3, 1, 1, 1, 2),
+    (1, 8, 17, 16, 8, 3, 3, 2, 2, 2, 1),
+    (1, 40, 20, 20, 136, 3, 3, 1, 1, 1, 1),
+]
+
+
+def sampled_forward(p, d):
+    dd = {k: (None if v is None else v.cuda()) for k, v in d.items()}
+    s = p.shapes()
+    y = torch.empty(s["y"], dtype=p.torch_dtype, device="cuda")
+    off = torch.empty(s["offset"], dtype=torch.float32, device="cuda")
+    B.deform_conv_fwd_sampled_gemm(p, dd["x"], dd["w_off"], dd["b_off"], dd["w"], dd["offset_add"],
+                                   y, off)
+    torch.cuda.synchronize()
+    return y, off
+
+
+@pytest.mark.parametrize("geom", SAMPLED_GEOMETRIES)
+def test_sampled_gemm_forward_matches_oracle_and_two_kernel_path(geom):
+    n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups = geom
+    p = B.Problem(n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups, B.DC_BF16)
+    d = random_inputs(p, 300 + h * w + c_in)
+    y, off = sampled_forward(p, d)
+    y_ref, off_ref = oracle_forward(p, d)
+    assert rel_err(f64(y), y_ref) <= TOL[B.DC_BF16]
+    assert rel_err(f64(off), off_ref) <= TOL[B.DC_BF16]
+    y2, off2, _ = gpu_forward(p, d)
+    assert torch.equal(off, off2)
+    # same deformed-map values; the GEMMs may differ in tile width, so the
+    # bf16 outputs agree up to a rounding of the fp32 sums
+    assert rel_err(f64(y), f64(y2)) <= 1e-2
+
+
+def test_sampled_gemm_forward_equals_two_kernel_forward_bitwise_res3():
+    """res3 bf16: the two-kernel forward uses the same 128 x 64 tiles and
+    k-block order, so the sampled-operand GEMM reproduces y bit for bit."""
+    wl = W.WORKLOADS["res3_bf16"]
+    p = wl.problem()
+    d = W.generate(wl)
+    y, off = sampled_forward(p, d)
+    y2, off2, _ = gpu_forward(p, d)
+    assert torch.equal(off, off2)
+    assert torch.equal(y, y2)
+
+
+def test_sampled_gemm_forward_early_layer_full_batch():
+    wl = W.WORKLOADS["early_bf16"]
+    p = wl.problem()
+    d = W.generate(wl)
+    y, off = sampled_forward(p, d)
+    y2, off2, _ = gpu_forward(p, d)
+    assert torch.equal(off, off2)
+    assert rel_err(f64(y), f64(y2)) <= 1e-2
