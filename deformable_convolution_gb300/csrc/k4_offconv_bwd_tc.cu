@@ -83,14 +83,26 @@ __host__ TcPlan make_tc_plan(const Geom& g, int px) {
   return p;
 }
 
-// Largest tile that fits two CTAs per SM (fewer, larger tiles: less staging
-// halo and fewer grad_w_off partial sums), else the smallest.
+// The largest tile (up to 256 pixels) that fits two CTAs per SM and still
+// gives the grid at least two CTAs per SM of the GPU's 152: larger tiles stage
+// less halo and add fewer grad_w_off partials, but a grid below two CTAs per
+// SM leaves K4's tail, which runs after the sampling backward, on few SMs
+// (measured: res3 103.8 us per step with 448 CTAs of 112 pixels against
+// 107.3 us with 256 CTAs of 196 pixels; the 56 x 56 stack layer 667 ->
+// 639 us with 224- instead of 112-pixel tiles).  Problems too small for that
+// take the smallest tile that fits (the most CTAs).
 __host__ TcPlan pick_tc_plan(const Geom& g) {
-  for (int px = band::kBandPx; px >= 32; px /= 2) {
+  constexpr int kMinGrid = 2 * 152;
+  TcPlan fallback{};
+  bool have = false;
+  for (int px = 2 * band::kBandPx; px >= 32; px /= 2) {
     const TcPlan p = make_tc_plan(g, px);
-    if (p.smem <= 110 * 1024) return p;
+    if (p.smem > 110 * 1024) continue;
+    if ((long long)p.nslices * p.tiles_w * p.tiles_h * g.n >= kMinGrid) return p;
+    fallback = p;
+    have = true;
   }
-  return make_tc_plan(g, 32);
+  return have ? fallback : make_tc_plan(g, 32);
 }
 
 __device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
