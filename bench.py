@@ -39,7 +39,7 @@ TRAFFIC = {
     # profiles/tc_gemm_res3_bf16.md).  Writes mostly stay in the 129 MB L2.
     ("res3_bf16", "k1_band_sample"): {"bytes": 2193408, "source": "8492705966c2d40d"},
     ("res3_bf16", "k3_band_bwd"): {"bytes": 20262400, "source": "1a9b981b39ec521e"},
-    ("res3_bf16", "k4_offconv_bwd"): {"bytes": 6218752, "source": "02ed034d68493cf3"},
+    ("res3_bf16", "k4_offconv_bwd"): {"bytes": 6218752, "source": "b3d2877a101e5de4"},
     ("res3_bf16", "gemm_fwd"): {"bytes": 14771968, "source": "f657fe41ae0cab4d"},
     ("res3_bf16", "gemm_gcol"): {"bytes": 1941248, "source": "f657fe41ae0cab4d"},
     ("res3_bf16", "gemm_gw"): {"bytes": 17554944, "source": "f657fe41ae0cab4d"},

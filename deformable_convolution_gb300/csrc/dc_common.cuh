@@ -148,7 +148,7 @@ struct GemmArgs {
   ZeroArgs zero;      // GCOL kernels clear these (the backward's atomic targets)
   float* gmax;        // tensor-core GCOL: max |gcol| per 128 x 128 tile (4 floats each), or null
   // tensor-core GW: after K4, gw_off = sum over images of gwo_img (count
-  // floats per image, in the order of gwo_frag_dest); null = nothing to reduce
+  // floats per image, in the order of gwo_frag_dest4); null = nothing to reduce
   const float* gwo_img;
   float* gw_off;
   long long gwo_count;

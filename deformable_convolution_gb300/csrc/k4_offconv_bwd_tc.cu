@@ -16,12 +16,15 @@
 // Both parts are dense mma.sync m16n8k16 contractions (bf16 operands, fp32
 // accumulation).  The input part is written as a gather over window positions
 // (the im2col of goff), so every grad_x element of the window is produced once
-// in registers and added to global memory with one atomic: there is no shared
-// grad_x window and no shared-memory atomic.  Every fragment register is one
-// 32-bit shared load: goff is packed twice (pixel pairs [m][px/2], offset-
-// channel pairs [px][m/2]), w_off^T as [(k,c)][m/2], and the input window as
-// pixel-pair words (x[q], x[q + stride]) so that the two pixels a register
-// holds are one word whenever they lie in the same band row.
+// in registers and added to global memory by one atomic (an 8-byte atomic for
+// two adjacent elements when image rows have even length): there is no shared
+// grad_x window and no shared-memory atomic.  The weight part's partial sums go
+// to a per-image copy laid out in the accumulators' own order (one 16-byte
+// atomic per lane and tile), summed over images after K4.  Every fragment
+// register is one 32-bit shared load: goff is packed twice (pixel pairs
+// [m][px/2], offset-channel pairs [px][m/2]), w_off^T as [(k,c)][m/2], and the
+// input window as pixel-pair words (x[q], x[q + stride]) so that the two
+// pixels a register holds are one word whenever they lie in the same band row.
 #include "dc_band.cuh"
 
 namespace dc {
