@@ -16,6 +16,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -638,31 +639,58 @@ def margin_report(p, t, dev):
             "suggested_for_1pct": B.dc_suggest_margin(p, h, 0.01, True), "taps": total}
 
 
+def _packed(specs, device, pinned):
+    """One buffer holding several tensors (256-byte aligned views), so that a
+    group of them moves between host and device in one copy."""
+    import torch
+    at, place = 0, {}
+    for name, shape, dt in specs:
+        nbytes = math.prod(shape) * torch.empty((), dtype=dt).element_size()
+        at = (at + 255) // 256 * 256
+        place[name] = (at, nbytes, shape, dt)
+        at += nbytes
+    buf = torch.empty(max(at, 1), dtype=torch.uint8, device=device, pin_memory=pinned)
+    views = {n: buf[o:o + nb].view(dt).view(shape) for n, (o, nb, shape, dt) in place.items()}
+    return buf, views
+
+
 def e2e(p, d, dev, stream, flops_step, iters=20):
     """Same metric through the ABI with host buffers: every step copies its
     inputs from pinned host memory and reads all outputs back.  The step is
     one CUDA graph over two streams: grad_y's upload and the read-back of the
     forward's outputs (y, offsets) run on a copy stream beside the compute,
     the forward's inputs go up before the forward and the gradients come
-    back after the backward.  Each replay is a whole step: every copy of
-    every step happens inside the timed region."""
+    back after the backward.  Each group of tensors lives in one packed
+    buffer on both sides, so each group is one copy.  Each replay is a whole
+    step: every copy of every step happens inside the timed region."""
     import torch
 
     from deformable_convolution_gb300 import binding as B
-    host = {k: (None if v is None else v.pin_memory()) for k, v in d.items()}
-    devt = {k: (None if v is None else torch.empty_like(v, device=dev)) for k, v in d.items()}
     s = p.shapes()
-    outs = dict(y=torch.empty(s["y"], dtype=p.torch_dtype, device=dev),
-                off=torch.empty(s["offset"], dtype=torch.float32, device=dev),
-                gx=torch.empty(s["x"], dtype=torch.float32, device=dev),
-                gwo=torch.empty(s["w_off"], dtype=torch.float32, device=dev),
-                gbo=torch.empty(s["b_off"], dtype=torch.float32, device=dev),
-                gw=torch.empty(s["w"], dtype=torch.float32, device=dev),
-                goff=torch.empty(s["offset"], dtype=torch.float32, device=dev))
-    hout = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in outs.items()}
+    f32, dt = torch.float32, p.torch_dtype
+    fwd_in = [(k, tuple(v.shape), v.dtype) for k, v in d.items() if v is not None and k != "grad_y"]
+    groups = {
+        "in": fwd_in,
+        "gy": [("grad_y", tuple(d["grad_y"].shape), d["grad_y"].dtype)],
+        "fwd_out": [("y", tuple(s["y"]), dt), ("off", tuple(s["offset"]), f32)],
+        "bwd_out": [("gx", tuple(s["x"]), f32), ("gwo", tuple(s["w_off"]), f32),
+                    ("gbo", tuple(s["b_off"]), f32), ("gw", tuple(s["w"]), f32),
+                    ("goff", tuple(s["offset"]), f32)],
+    }
+    hbuf, dbuf, hv, dv = {}, {}, {}, {}
+    for gname, specs in groups.items():
+        hbuf[gname], h = _packed(specs, "cpu", True)
+        dbuf[gname], g = _packed(specs, dev, False)
+        hv.update(h)
+        dv.update(g)
+    for k, v in d.items():
+        if v is not None:
+            hv[k].copy_(v)
+    devt = {k: (dv[k] if v is not None else None) for k, v in d.items()}
+    outs = {k: dv[k] for k in ("y", "off", "gx", "gwo", "gbo", "gw", "goff")}
     ws = B.workspace(p, True, dev)
-    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
-    d2h = sum(v.numel() * v.element_size() for v in hout.values())
+    h2d = sum(v.numel() * v.element_size() for v in d.values() if v is not None)
+    d2h = sum(v.numel() * v.element_size() for v in outs.values())
     cs = torch.cuda.Stream(device=dev)
     e_gy = torch.cuda.Event()
     e_fwd = torch.cuda.Event()
@@ -671,25 +699,21 @@ def e2e(p, d, dev, stream, flops_step, iters=20):
         # fork: the copy stream uploads grad_y while the forward runs
         cs.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(cs):
-            devt["grad_y"].copy_(host["grad_y"], non_blocking=True)
+            dbuf["gy"].copy_(hbuf["gy"], non_blocking=True)
             e_gy.record(cs)
-        for k, v in host.items():
-            if v is not None and k != "grad_y":
-                devt[k].copy_(v, non_blocking=True)
+        dbuf["in"].copy_(hbuf["in"], non_blocking=True)
         B.deform_conv_fwd(p, devt["x"], devt["w_off"], devt["b_off"], devt["w"],
                           devt["offset_add"], outs["y"], outs["off"], None, ws)
         e_fwd.record(torch.cuda.current_stream(dev))
         # the forward's outputs come back while the backward runs (both only read them)
         cs.wait_event(e_fwd)
         with torch.cuda.stream(cs):
-            for k in ("y", "off"):
-                hout[k].copy_(outs[k], non_blocking=True)
+            hbuf["fwd_out"].copy_(dbuf["fwd_out"], non_blocking=True)
         torch.cuda.current_stream(dev).wait_event(e_gy)
         B.deform_conv_bwd(p, devt["x"], devt["w_off"], devt["w"], outs["off"], devt["grad_y"],
                           outs["gx"], outs["gwo"], outs["gbo"], outs["gw"], outs["goff"], ws,
                           after_fwd=True)
-        for k in ("gx", "gwo", "gbo", "gw", "goff"):
-            hout[k].copy_(outs[k], non_blocking=True)
+        hbuf["bwd_out"].copy_(dbuf["bwd_out"], non_blocking=True)
         # join
         torch.cuda.current_stream(dev).wait_stream(cs)
 
@@ -719,12 +743,15 @@ def e2e(p, d, dev, stream, flops_step, iters=20):
         b.record(stream)
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / iters
-    # the read-back is complete: the last step's y on the host equals the device copy
-    assert torch.equal(hout["y"], outs["y"].cpu()), "e2e read-back mismatch"
+    # the read-back is complete: the last step's y and grad_x on the host equal
+    # the device copies
+    assert torch.equal(hv["y"], outs["y"].cpu()), "e2e read-back mismatch"
+    assert torch.equal(hv["gx"], outs["gx"].cpu()), "e2e read-back mismatch"
     return {"value": flops_step / (ms / 1e3) / 1e9, "unit": "GFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "method": how + ": forward inputs up, forward, backward, gradients back on the compute "
-                            "stream; grad_y up and y/offsets back on a copy stream beside it"}
+            "method": how + ": forward inputs up (one packed copy), forward, backward, gradients "
+                            "back (one packed copy) on the compute stream; grad_y up and y/offsets "
+                            "back on a copy stream beside it"}
 
 
 if __name__ == "__main__":
