@@ -408,3 +408,102 @@ def test_cell_is_decided_on_the_float32_coordinate():
     # the sample itself is continuous across the line
     col = oracle.column(p, x, off)
     assert abs(col[0, 0, 0, 3, 1] - x[0, 0, 4, 1]) < 1e-7
+
+
+# ---------------------------------------------------------------- offset convolution (Step 1 of 5)
+
+OFFSET_GEOMETRIES = GEOMETRIES + [
+    # kh != kw with per-axis stride, padding and dilation, several offset groups
+    (2, 6, 7, 9, 2, 2, 3, (2, 1), (1, 0), (1, 2), 2),
+    (1, 8, 6, 5, 2, 3, 2, 1, (2, 1), (2, 1), 4),
+]
+
+
+def torch_conv_bias(p, x, w, b):
+    return F.conv2d(x, w, b, stride=(p.stride_h, p.stride_w), padding=(p.pad_h, p.pad_w),
+                    dilation=(p.dil_h, p.dil_w))
+
+
+@pytest.mark.parametrize("g", OFFSET_GEOMETRIES)
+def test_offset_convolution_equals_torch_conv(g):
+    """Step 1 of 5 ("Following a deformable layer through DefT"): the offsets
+    are a standard convolution of the input, with the main convolution's
+    kernel size, stride, padding and dilation and a bias (reading C1), plus
+    offset_add.  Nonzero random w_off, compared with torch's fp64 conv2d."""
+    p = make_problem(g)
+    x, w_off, b_off, w, _ = rand_inputs(p, 21, w_off_std=1.0)
+    add = np.random.default_rng(22).standard_normal((p.n, p.n_off, p.ho, p.wo))
+    got = oracle.offsets(p, x, w_off, b_off, add)
+    ref = torch_conv_bias(p, torch.from_numpy(x), torch.from_numpy(w_off),
+                          torch.from_numpy(b_off)).numpy() + add
+    assert got.shape == ref.shape
+    assert rel_err(got, ref) < 1e-12
+    _, off = oracle.forward(p, x, w_off, b_off, w, add)
+    assert np.array_equal(off, got)
+
+
+@pytest.mark.parametrize("g", OFFSET_GEOMETRIES)
+def test_offset_convolution_backward_equals_conv_autograd(g):
+    """The offset convolution's part of the backward -- grad_w_off, grad_b_off
+    and its term of grad_x -- is torch autograd of the same fp64 conv2d,
+    driven by the oracle's offset gradient.  The sampling term of grad_x is
+    removed by a second run at the same offsets with w_off = 0 (the offset
+    gradient depends only on the offsets, so it is identical)."""
+    p = make_problem(g)
+    x, w_off, b_off, w, gy = rand_inputs(p, 23, w_off_std=0.3)
+    _, off = oracle.forward(p, x, w_off, b_off, w)
+    full = oracle.backward(p, x, w_off, w, off, gy)
+    samp = oracle.backward(p, x, np.zeros_like(w_off), w, off, gy)
+    assert np.array_equal(full["grad_offset"], samp["grad_offset"])
+    xt = torch.from_numpy(x).requires_grad_()
+    wt = torch.from_numpy(w_off).requires_grad_()
+    bt = torch.from_numpy(b_off).requires_grad_()
+    o = torch_conv_bias(p, xt, wt, bt)
+    (o * torch.from_numpy(full["grad_offset"])).sum().backward()
+    assert rel_err(full["grad_w_off"], wt.grad.numpy()) < 1e-12
+    assert rel_err(full["grad_b_off"], bt.grad.numpy()) < 1e-12
+    assert rel_err(full["grad_x"] - samp["grad_x"], xt.grad.numpy()) < 1e-10
+
+
+# ---------------------------------------------------------------- channel -> offset group
+
+GROUP_GEOMETRIES = [
+    # n, c_in, h, w, c_out, kh, kw, stride, pad, dil, groups -- every group has Cg > 1
+    (2, 8, 6, 7, 3, 3, 3, 1, 1, 1, 2),
+    (1, 8, 7, 6, 2, 3, 3, 2, 1, 1, 4),
+    (2, 6, 5, 6, 2, 2, 3, 1, (1, 0), (1, 2), 3),
+]
+
+
+@pytest.mark.parametrize("g", GROUP_GEOMETRIES)
+def test_offset_groups_split_the_channels_into_contiguous_blocks(g):
+    """Offset group q serves input channels [q*Cg, (q+1)*Cg) (reading C3).
+    The main convolution is linear over input channels, so with a distinct
+    random offset field per group the layer is the sum, over q, of a
+    one-group layer on channel block q that samples at group q's offsets; the
+    gradients of x, of w and of the offsets are the blocks' gradients side by
+    side.  The one-group runs never evaluate the channel-to-group index."""
+    p = make_problem(g)
+    G, Cg, K = p.groups, p.c_in // p.groups, p.kh * p.kw
+    rng = np.random.default_rng(24)
+    x = rng.standard_normal((p.n, p.c_in, p.h, p.w))
+    w = rng.standard_normal((p.c_out, p.c_in, p.kh, p.kw))
+    gy = rng.standard_normal((p.n, p.c_out, p.ho, p.wo))
+    add = rng.standard_normal((p.n, p.n_off, p.ho, p.wo)) * 1.5
+    y, off = oracle.forward(p, x, np.zeros((p.n_off, p.c_in, p.kh, p.kw)), None, w, add)
+    full = oracle.backward(p, x, np.zeros((p.n_off, p.c_in, p.kh, p.kw)), w, off, gy)
+    y_sum = np.zeros_like(y)
+    for q in range(G):
+        blk = slice(q * Cg, (q + 1) * Cg)
+        om = slice(2 * q * K, 2 * (q + 1) * K)
+        p1 = oracle.Problem(p.n, Cg, p.h, p.w, p.c_out, p.kh, p.kw,
+                            (p.stride_h, p.stride_w), (p.pad_h, p.pad_w),
+                            (p.dil_h, p.dil_w), 1)
+        zero_w = np.zeros((2 * K, Cg, p.kh, p.kw))
+        yq, offq = oracle.forward(p1, x[:, blk], zero_w, None, w[:, blk], add[:, om])
+        bq = oracle.backward(p1, x[:, blk], zero_w, w[:, blk], offq, gy)
+        y_sum += yq
+        assert rel_err(full["grad_x"][:, blk], bq["grad_x"]) < 1e-12
+        assert rel_err(full["grad_w"][:, blk], bq["grad_w"]) < 1e-12
+        assert rel_err(full["grad_offset"][:, om], bq["grad_offset"]) < 1e-12
+    assert rel_err(y, y_sum) < 1e-12
