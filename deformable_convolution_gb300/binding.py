@@ -24,7 +24,7 @@ EXPORTED_SYMBOLS = (
     "deform_conv_bwd", "deform_conv_sample", "dc_status_string", "dc_build_info",
     "dc_launch_count", "deform_conv_fwd_noalloc", "dc_device_error", "dc_kernel_timing",
     "dc_kernel_times", "deform_conv_offsets", "deform_conv_margin_histogram", "dc_suggest_margin",
-    "deform_conv_bwd_after_fwd", "deform_conv_fwd_sampled_gemm",
+    "deform_conv_bwd_after_fwd", "deform_conv_fwd_sampled_gemm", "dc_relu_fwd", "dc_relu_bwd",
 )
 MARGIN_BINS = 64
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -86,6 +86,10 @@ def lib() -> ctypes.CDLL:
         L.dc_kernel_times.restype = i
         L.dc_device_error.argtypes = [i]
         L.dc_device_error.restype = i
+        L.dc_relu_fwd.argtypes = [vp, vp, sz, i, vp]
+        L.dc_relu_fwd.restype = i
+        L.dc_relu_bwd.argtypes = [vp, vp, vp, sz, i, vp]
+        L.dc_relu_bwd.restype = i
         L.dc_launch_count.argtypes = []
         L.dc_launch_count.restype = ctypes.c_ulonglong
         _configured = True
@@ -323,6 +327,30 @@ def dc_suggest_margin(p: Problem, hist_host, max_slow_fraction: float, for_backw
     st = p.c_struct()
     return int(lib().dc_suggest_margin(ctypes.byref(st), arr, float(max_slow_fraction),
                                        int(bool(for_backward))))
+
+
+def _dc_dtype(t):
+    for k, v in _TORCH_DTYPE.items():
+        if t.dtype == v:
+            return k
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def dc_relu_fwd(y, out, stream=None):
+    """out = max(y, 0) (float32 or bfloat16 tensors of one shape; out may be y)."""
+    if out.shape != y.shape or out.dtype != y.dtype:
+        raise ValueError("y and out must have the same shape and dtype")
+    _check(lib().dc_relu_fwd(_ptr(y, "y"), _ptr(out, "out"), ctypes.c_size_t(y.numel()),
+                             _dc_dtype(y), _stream(stream)), "dc_relu_fwd")
+
+
+def dc_relu_bwd(act, grad_out, grad_in, stream=None):
+    """grad_in = grad_out where act > 0 else 0, in act's dtype; grad_out float32."""
+    if grad_out.shape != act.shape or grad_in.shape != act.shape or grad_in.dtype != act.dtype:
+        raise ValueError("act, grad_out and grad_in must have one shape; grad_in act's dtype")
+    _check(lib().dc_relu_bwd(_ptr(act, "act"), _ptr(grad_out, "grad_out", dtype=torch.float32),
+                             _ptr(grad_in, "grad_in"), ctypes.c_size_t(act.numel()),
+                             _dc_dtype(act), _stream(stream)), "dc_relu_bwd")
 
 
 # ---------------------------------------------------------------- conveniences

@@ -34,7 +34,7 @@ struct TimedLaunch {
   cudaEvent_t a, b;
 };
 std::mutex g_timing_mu;
-bool g_timing = false;
+std::atomic<bool> g_timing{false};  // read without the lock on every launch
 TimedLaunch g_timed[kMaxTimed];
 int g_ntimed = 0;
 int g_nevents = 0;  // event pairs created so far (reused across calls)
@@ -42,9 +42,9 @@ int g_nevents = 0;  // event pairs created so far (reused across calls)
 template <typename F>
 cudaError_t timed(const char* name, cudaStream_t s, F&& launch) {
   int slot = -1;
-  if (g_timing) {
+  if (g_timing.load(std::memory_order_relaxed)) {
     std::lock_guard<std::mutex> lock(g_timing_mu);
-    if (g_ntimed < kMaxTimed) {
+    if (g_timing.load(std::memory_order_relaxed) && g_ntimed < kMaxTimed) {
       slot = g_ntimed++;
       if (slot >= g_nevents) {
         if (cudaEventCreate(&g_timed[slot].a) != cudaSuccess ||
@@ -488,6 +488,29 @@ int dc_suggest_margin(const dc_problem* prob, const unsigned long long* hist,
   return m;
 }
 
+dc_status dc_relu_fwd(const void* y, void* out, size_t count, dc_dtype dtype, void* stream) {
+  if (dtype != DC_F32 && dtype != DC_BF16) return DC_ERR_INVALID_ARG;
+  if (count == 0) return DC_OK;
+  if (!y || !out) return DC_ERR_INVALID_ARG;
+  if (!aligned16(y) || !aligned16(out)) return DC_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(timed("relu_fwd", s, [&] {
+    return launch_relu_fwd(y, out, (long long)count, dtype, s);
+  }));
+}
+
+dc_status dc_relu_bwd(const void* act, const float* grad_out, void* grad_in, size_t count,
+                      dc_dtype dtype, void* stream) {
+  if (dtype != DC_F32 && dtype != DC_BF16) return DC_ERR_INVALID_ARG;
+  if (count == 0) return DC_OK;
+  if (!act || !grad_out || !grad_in) return DC_ERR_INVALID_ARG;
+  if (!aligned16(act) || !aligned16(grad_out) || !aligned16(grad_in)) return DC_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return cuda_status(timed("relu_bwd", s, [&] {
+    return launch_relu_bwd(act, grad_out, grad_in, (long long)count, dtype, s);
+  }));
+}
+
 const char* dc_status_string(dc_status status) {
   switch (status) {
     case DC_OK: return "DC_OK: success";
@@ -502,7 +525,7 @@ const char* dc_status_string(dc_status status) {
 
 void dc_kernel_timing(int enable) {
   std::lock_guard<std::mutex> lock(g_timing_mu);
-  g_timing = enable != 0;
+  g_timing.store(enable != 0, std::memory_order_relaxed);
   g_ntimed = 0;
 }
 

@@ -247,4 +247,10 @@ cudaError_t launch_offconv_bwd_tc(const OffconvBwdArgs& a, cudaStream_t s);
 // gw_off = sum over images of gw_off_img (launched after the grad_W GEMM)
 cudaError_t launch_gw_off_reduce(const OffconvBwdArgs& a, cudaStream_t s);
 
+// ReLU between stacked layers: out = max(y, 0); gin = gout where act > 0
+// (rounded to the dtype), else 0.  16-byte aligned pointers.
+cudaError_t launch_relu_fwd(const void* y, void* out, long long count, dc_dtype dt, cudaStream_t s);
+cudaError_t launch_relu_bwd(const void* act, const float* gout, void* gin, long long count,
+                            dc_dtype dt, cudaStream_t s);
+
 }  // namespace dc

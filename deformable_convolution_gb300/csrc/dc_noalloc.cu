@@ -11,21 +11,16 @@
 //
 // The array is a file-scope __device__ object, so every GPU that loads the
 // library holds DC_NOALLOC_SCRATCH_BYTES of it until the process exits.  Host
-// code cannot use its name as a device address; the address is looked up with
-// cudaGetSymbolAddress once per device, with that device current, on the
-// first call made on that device.
-#include <mutex>
-
+// code cannot use its name as a device address; every call looks the address
+// up with cudaGetSymbolAddress on the current device (a host-side query that
+// allocates nothing).  Nothing is cached, so a device reset or another
+// context on the device, which can place the array elsewhere, never leaves a
+// stale address behind.
 #include "dc_common.cuh"
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 static __device__ __align__(256) unsigned char g_noalloc_scratch[DC_NOALLOC_SCRATCH_BYTES];
-
-std::mutex g_noalloc_mu;
-void* g_noalloc_addr[kMaxDevices] = {};
 
 }  // namespace
 
@@ -39,20 +34,10 @@ extern "C" dc_status deform_conv_fwd_noalloc(const dc_problem* prob, const void*
   const dc_status st = deform_conv_workspace_size(prob, 0, &need);
   if (st != DC_OK) return st;
   if (need > (size_t)DC_NOALLOC_SCRATCH_BYTES) return DC_ERR_WORKSPACE;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DC_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return DC_ERR_UNSUPPORTED;
+  // the array's address on the current device, looked up on every call
   void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
-      void* addr = nullptr;
-      if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || !addr)
-        return DC_ERR_CUDA;
-      g_noalloc_addr[dev] = addr;
-    }
-    scratch = g_noalloc_addr[dev];
-  }
+  if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess || !scratch)
+    return DC_ERR_CUDA;
   // Nothing in the forward workspace has to start at zero: every byte the
   // kernels read there was written earlier in the same call.
   return deform_conv_fwd(prob, x, w_off, b_off, w, offset_add, y, offset_out, slowpath_count,

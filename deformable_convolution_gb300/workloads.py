@@ -15,12 +15,20 @@ Recipe (one ``torch.Generator(seed)`` on the CPU, draws in this order):
      offset convolution's output has standard deviation ~sigma at interior
      pixels; b_off = -E[x] * sum_{c,i,j} w_off[m, c, i, j] removes the mean a
      non-centred input gives (zero for centred x);
-  3. w ~ N(0, 1 / (Kh * Kw * C_in));
+  3. w ~ N(0, gain / (Kh * Kw * C_in)), gain 1 (gain 2 for the training
+     stack: He initialisation, which keeps a ReLU network's activations at
+     the scale of its input from layer to layer);
   4. offset_add: each element independently, with probability
      ``outlier_p``, is +-``outlier_px`` (uniform sign), else 0;
   5. grad_y ~ N(0, 1).
 bf16 workloads round x, w_off and w to bf16 (round to nearest even) once;
 both sides of every comparison receive the same rounded values.
+
+Stacks of layers (``generate_stack``): layer 0 is ``generate(wl)``; layer l
+draws its w_off, b_off and w by the same recipe from seed ``wl.seed + 1000 *
+l``.  The offset weights of every layer are scaled for a post-ReLU N(0, 1)
+input, the distribution a He-initialised layer's ReLU output keeps
+approximately; grad_y at the stack's output is layer 0's draw.
 """
 from __future__ import annotations
 
@@ -51,6 +59,7 @@ class Workload:
     outlier_p: float = 0.0
     outlier_px: float = 0.0
     layers: int = 1
+    w_gain: float = 1.0         # variance gain of the main weights
     seed: int = 0
 
     def problem(self, n=None, halo_margin=-1) -> Problem:
@@ -78,8 +87,9 @@ WORKLOADS = {
     "early_bf16": Workload("early_bf16", 16, 64, 64, 112, 112, pad=2, dil=2, groups=4,
                            dtype=DC_BF16, sigma=1.5, seed=3),
     # one layer of the 4-layer training stack: N8 C256->256 56x56, offsets ~N(0, 1)
+    # (the whole stack: 4 such layers with ReLU between them, He-initialised)
     "stack_bf16": Workload("stack_bf16", 8, 256, 256, 56, 56, dtype=DC_BF16, relu_x=True,
-                           layers=4, seed=4),
+                           layers=4, w_gain=2.0, seed=4),
 }
 
 
@@ -100,7 +110,7 @@ def generate(wl: Workload, n=None, seed=None):
         mean, var = 0.0, 1.0 / 3.0
     s = wl.sigma / math.sqrt(wl.c_in * K * var)
     w_off = torch.randn(p.shapes()["w_off"], generator=gen) * s
-    w = torch.randn(p.shapes()["w"], generator=gen) / math.sqrt(K * wl.c_in)
+    w = torch.randn(p.shapes()["w"], generator=gen) * math.sqrt(wl.w_gain / (K * wl.c_in))
     tdt = p.torch_dtype
     x, w_off, w = x.to(tdt), w_off.to(tdt), w.to(tdt)
     b_off = (-mean * w_off.float().sum(dim=(1, 2, 3))).contiguous()
@@ -112,6 +122,22 @@ def generate(wl: Workload, n=None, seed=None):
         offset_add = (hit.float() * sign * wl.outlier_px).contiguous()
     grad_y = torch.randn(p.shapes()["y"], generator=gen).to(tdt)
     return dict(x=x, w_off=w_off, b_off=b_off, w=w, offset_add=offset_add, grad_y=grad_y)
+
+
+def generate_stack(wl: Workload, n=None):
+    """Inputs of a stack of ``wl.layers`` layers with ReLU between them:
+    (x of layer 0, [dict(w_off, b_off, w) per layer], grad_y at the output).
+    Every layer has C_in = C_out and keeps the spatial size, so that a layer's
+    output is the next layer's input."""
+    p = wl.problem(n)
+    if p.c_in != p.c_out or (p.ho, p.wo) != (p.h, p.w):
+        raise ValueError("a stack needs layers that keep the channel count and size")
+    first = generate(wl, n)
+    layers = [{k: first[k] for k in ("w_off", "b_off", "w")}]
+    for l in range(1, wl.layers):
+        d = generate(wl, 1, seed=wl.seed + 1000 * l)
+        layers.append({k: d[k] for k in ("w_off", "b_off", "w")})
+    return first["x"], layers, first["grad_y"]
 
 
 def conv_flops(p: Problem) -> float:

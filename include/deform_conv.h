@@ -233,9 +233,10 @@ int dc_suggest_margin(const dc_problem* prob, const unsigned long long* hist,
  *     Problems whose forward workspace (deform_conv_workspace_size(prob, 0))
  *     exceeds it are rejected with DC_ERR_WORKSPACE before anything runs.
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *   - The first call on each device looks up the array's device address on
- *     that device (cudaGetSymbolAddress); make that first call before any
- *     stream capture.
+ *   - Every call looks up the array's address on the current device
+ *     (cudaGetSymbolAddress, a host-side query that allocates nothing; the
+ *     first one on a device may load this library's module there): make the
+ *     first call on each device before any stream capture.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; nothing there needs to start at zero.  Calls whose work
  *     overlaps on the GPU (other streams, other host threads) race on the
@@ -245,6 +246,26 @@ dc_status deform_conv_fwd_noalloc(const dc_problem* prob, const void* x, const v
                                   const float* b_off, const void* w, const float* offset_add,
                                   void* y, float* offset_out,
                                   unsigned long long* slowpath_count, void* stream);
+
+/* ReLU between stacked deformable layers.  The explainer page's networks
+ * stack deformable layers throughout a ResNet ("What people did before, and
+ * where it broke": adding deformable layers; "Why it works / Fixing the
+ * slowest stage lifts the whole layer": training a fully deformable ResNet),
+ * whose convolutions are separated by ReLU activations; a training step over
+ * such a stack needs the activation and its gradient between layers.
+ *   dc_relu_fwd: out[i] = y[i] <= 0 ? 0 : y[i] (NaN stays NaN).  y and out are
+ *     `count` elements of `dtype`; out may equal y (in place).
+ *   dc_relu_bwd: grad_in[i] = act[i] > 0 ? grad_out[i] : 0, rounded to dtype
+ *     (nearest even).  act is the activation's OUTPUT (`dtype`, positive
+ *     exactly where its input was; NaN gives a zero gradient), grad_out float32
+ *     (the next layer's grad_x),
+ *     grad_in `dtype` (the previous layer's grad_y).
+ * Device pointers, 16-byte aligned (else DC_ERR_UNSUPPORTED); NULL or a bad
+ * dtype gives DC_ERR_INVALID_ARG; count 0 does nothing.  Asynchronous on
+ * `stream`; allocates nothing. */
+dc_status dc_relu_fwd(const void* y, void* out, size_t count, dc_dtype dtype, void* stream);
+dc_status dc_relu_bwd(const void* act, const float* grad_out, void* grad_in, size_t count,
+                      dc_dtype dtype, void* stream);
 
 /* Static description of a status code. */
 const char* dc_status_string(dc_status status);
@@ -266,7 +287,10 @@ dc_status dc_device_error(int clear);
  * while a stream is being captured into a CUDA graph.  dc_kernel_times waits
  * for the recorded launches, writes up to `capacity` (static name, duration in
  * ms) pairs in launch order (-1 for a launch that could not be timed), returns
- * how many it wrote and clears the record.  names or ms may be NULL. */
+ * how many it wrote and clears the record.  names or ms may be NULL.
+ * The record is process-wide (shared by every host thread and device): it is
+ * the one piece of state this library keeps across calls, outside the
+ * no-state rule above, and exists only while timing is enabled. */
 void dc_kernel_timing(int enable);
 int dc_kernel_times(const char** names, float* ms, int capacity);
 

@@ -23,6 +23,10 @@ Deformable Convolution Operations on GPUs":
 * ``bilinear`` / ``bilinear_closed_form`` / ``bilinear_grad`` -- the single
   sample, as the four-corner blend and, independently, as the tent-kernel sum
   over every pixel.
+* ``relu`` / ``relu_grad`` -- the activation between stacked layers of the
+  networks the page trains ("What people did before, and where it broke":
+  deformable layers throughout a ResNet) and its derivative, elementwise in
+  numpy.
 """
 from __future__ import annotations
 
@@ -249,3 +253,16 @@ def bilinear_grad(plane, py, px):
     _load().orc_bilinear_grad(_ptr(plane), plane.shape[0], plane.shape[1],
                               float(py), float(px), ctypes.byref(dy), ctypes.byref(dx))
     return float(dy.value), float(dx.value)
+
+
+def relu(y):
+    """max(y, 0) elementwise; NaN stays NaN (it is not <= 0)."""
+    y = np.asarray(y, dtype=np.float64)
+    return np.where(y <= 0.0, 0.0, y)
+
+
+def relu_grad(act, g):
+    """Gradient through the activation given its OUTPUT act: g where act > 0,
+    else 0 (act > 0 exactly where the input was > 0)."""
+    act = np.asarray(act, dtype=np.float64)
+    return np.where(act > 0.0, np.asarray(g, dtype=np.float64), 0.0)

@@ -1,0 +1,138 @@
+"""GPU parity of the training stack: deformable layers with ReLU between them
+(the networks the explainer page "DefT: Boosting Scalability of Deformable
+Convolution Operations on GPUs" trains: deformable layers throughout a ResNet,
+"What people did before, and where it broke" and "Why it works / Fixing the
+slowest stage lifts the whole layer").
+
+The oracle runs the stack layer by layer in fp64 on image 0; each activation
+and each gradient between layers is stored in the layers' dtype (bf16) on both
+sides, so the oracle rounds it the same way (to float32, then to bf16,
+nearest even).  The CUDA path is compared layer by layer at the oracle's
+inputs (forward, backward at the oracle's float32 offsets, and the ReLU
+kernels bit for bit), then as a chain through the stack runner on the
+one-image slice and at full batch (forward output of image 0, and the top
+layer's weight gradient, which depends on no offset gradient)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deformable_convolution_gb300 import binding as B
+from deformable_convolution_gb300 import stack as S
+from deformable_convolution_gb300 import workloads as W
+
+from parity import TOL, f64, oracle_problem, rel_err
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+
+def to_bf16_via_f32(a):
+    """fp64 -> float32 -> bf16 (nearest even at each step), back as fp64."""
+    return torch.from_numpy(np.asarray(a, dtype=np.float64)).float().to(torch.bfloat16).double().numpy()
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("count", [1, 7, 8, 4099, 1 << 20])
+def test_relu_kernels_match_the_definition(dtype, count):
+    gen = torch.Generator().manual_seed(count)
+    y = (torch.randn(count, generator=gen) * 3).to(dtype)
+    special = torch.tensor([0.0, -0.0, float("nan"), float("inf"), -float("inf"), 1e-30, -1e-30],
+                           dtype=dtype)
+    y[:min(count, special.numel())] = special[:min(count, special.numel())]
+    g = torch.randn(count, generator=gen)
+    yd, gd = y.cuda(), g.cuda()
+    out = torch.empty_like(yd)
+    B.dc_relu_fwd(yd, out)
+    gin = torch.empty_like(yd)
+    B.dc_relu_bwd(out, gd, gin)
+    inplace = yd.clone()
+    B.dc_relu_fwd(inplace, inplace)
+    torch.cuda.synchronize()
+    want = torch.from_numpy(oracle.relu(y.double().numpy())).to(dtype)
+    bits = torch.int16 if dtype == torch.bfloat16 else torch.int32
+    nan = torch.isnan(want)
+    for got in (out.cpu(), inplace.cpu()):
+        # NaN stays NaN (the hardware may return its canonical NaN); every
+        # other element bit for bit, +0 for the zeros
+        assert torch.equal(torch.isnan(got), nan)
+        assert torch.equal(got.view(bits)[~nan], want.view(bits)[~nan])
+    gwant = torch.from_numpy(oracle.relu_grad(want.double().numpy(), g.double().numpy()))
+    gwant = gwant.float().to(dtype)
+    assert torch.equal(gin.cpu().view(bits), gwant.view(bits))
+
+
+def oracle_stack(p1, x0, layers, gy, backward=True):
+    """The stack in fp64 on one image: per layer the oracle's forward, ReLU,
+    storage rounding; then (unless backward is False) the backward from the
+    top at each layer's float32 offsets, the gradient through the ReLU stored
+    rounded as well."""
+    op = oracle_problem(p1)
+    L = len(layers)
+    xs, ys, offs = [f64(x0)], [], []
+    for l, q in enumerate(layers):
+        y, off = oracle.forward(op, xs[l], f64(q["w_off"]), f64(q["b_off"]), f64(q["w"]))
+        ys.append(y)
+        offs.append(off.astype(np.float32).astype(np.float64))
+        if l + 1 < L:
+            xs.append(to_bf16_via_f32(oracle.relu(y)))
+    gys = [None] * (L - 1) + [f64(gy)]
+    grads = [None] * L
+    for l in reversed(range(L) if backward else []):
+        q = layers[l]
+        grads[l] = oracle.backward(op, xs[l], f64(q["w_off"]), f64(q["w"]), offs[l], gys[l])
+        if l > 0:
+            gx32 = grads[l]["grad_x"].astype(np.float32).astype(np.float64)
+            gys[l - 1] = to_bf16_via_f32(oracle.relu_grad(xs[l], gx32))
+    return xs, ys, offs, gys, grads
+
+
+def test_stack_layer_by_layer_and_chained_on_one_image():
+    wl = W.WORKLOADS["stack_bf16"]
+    x0, layers, gy = W.generate_stack(wl)
+    p1 = wl.problem(1)
+    x0, gy = x0[:1].contiguous(), gy[:1].contiguous()
+    xs, ys, offs, gys, grads = oracle_stack(p1, x0, layers, gy)
+    tol = TOL[p1.dtype]
+    dt = p1.torch_dtype
+    bf = lambda a: torch.from_numpy(a).to(dt).cuda()  # noqa: E731  (values already bf16)
+    dev_layers = [{k: v.cuda() for k, v in q.items()} for q in layers]
+    for l, q in enumerate(dev_layers):
+        y, off = B.forward(p1, bf(xs[l]), q["w_off"], q["b_off"], q["w"])
+        g = B.backward(p1, bf(xs[l]), q["w_off"], q["w"],
+                       torch.from_numpy(offs[l]).float().cuda(), bf(gys[l]))
+        torch.cuda.synchronize()
+        assert rel_err(f64(y), ys[l]) <= tol, l
+        assert rel_err(f64(off), offs[l]) <= tol, l
+        for k in ("grad_x", "grad_w", "grad_w_off", "grad_b_off", "grad_offset"):
+            assert rel_err(f64(g[k]), grads[l][k]) <= tol, (l, k)
+        if l + 1 < len(layers):
+            act = torch.empty(p1.shapes()["x"], dtype=dt, device="cuda")
+            B.dc_relu_fwd(bf(to_bf16_via_f32(ys[l])), act)
+            torch.cuda.synchronize()
+            assert np.array_equal(f64(act), xs[l + 1]), l
+        if l > 0:
+            gin = torch.empty(p1.shapes()["y"], dtype=dt, device="cuda")
+            B.dc_relu_bwd(bf(xs[l]), torch.from_numpy(grads[l]["grad_x"]).float().cuda(), gin)
+            torch.cuda.synchronize()
+            assert np.array_equal(f64(gin), gys[l - 1]), l
+    # the chain through the stack runner, on the same image
+    st = S.Stack(p1, dev_layers, "cuda")
+    st.step(x0.cuda(), gy.cuda())
+    torch.cuda.synchronize()
+    assert rel_err(f64(st.y[-1]), ys[-1]) <= tol
+    assert rel_err(f64(st.grads[-1]["grad_w"]), grads[-1]["grad_w"]) <= tol
+
+
+def test_stack_full_batch_matches_the_oracle_on_image_0():
+    wl = W.WORKLOADS["stack_bf16"]
+    x0, layers, gy = W.generate_stack(wl)
+    p = wl.problem()
+    st = S.Stack(p, [{k: v.cuda() for k, v in q.items()} for q in layers], "cuda")
+    st.step(x0.cuda(), gy.cuda())
+    torch.cuda.synchronize()
+    p1 = wl.problem(1)
+    _, ys, _, _, _ = oracle_stack(p1, x0[:1].contiguous(), layers, gy[:1].contiguous(),
+                                  backward=False)
+    assert rel_err(f64(st.y[-1][:1]), ys[-1]) <= TOL[p.dtype]
+    assert B.device_error() == 0

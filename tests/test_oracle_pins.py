@@ -507,3 +507,18 @@ def test_offset_groups_split_the_channels_into_contiguous_blocks(g):
         assert rel_err(full["grad_w"][:, blk], bq["grad_w"]) < 1e-12
         assert rel_err(full["grad_offset"][:, om], bq["grad_offset"]) < 1e-12
     assert rel_err(y, y_sum) < 1e-12
+
+
+# ---------------------------------------------------------------- activation between layers
+
+
+def test_relu_and_its_gradient_by_hand():
+    """Values worked by hand: negatives and both zeros go to +0, positives
+    pass, NaN passes; the gradient flows only where the output is positive."""
+    y = np.array([-2.5, -0.0, 0.0, 1e-30, 3.0, np.nan, -np.inf, np.inf])
+    r = oracle.relu(y)
+    assert r[:5].tolist() == [0.0, 0.0, 0.0, 1e-30, 3.0]
+    assert np.isnan(r[5]) and r[6] == 0.0 and r[7] == np.inf
+    assert not np.signbit(r[1])
+    g = np.array([1.0, 2.0, 3.0, 4.0, 5.0, 6.0, 7.0, 8.0])
+    assert oracle.relu_grad(r, g).tolist() == [0.0, 0.0, 0.0, 4.0, 5.0, 0.0, 0.0, 8.0]
