@@ -77,6 +77,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--roofline-iters", type=int, default=200)
     ap.add_argument("--e2e-iters", type=int, default=20)
+    ap.add_argument("--only", choices=["stage", "offsets", "replay", "step"],
+                    help="profiling runs: launch only the sampling stage (fused, offsets only, or "
+                         "sampling at given offsets) or the whole step, warm-up + steps times on "
+                         "layer 0's inputs, eagerly, and print the device time per call")
     return ap.parse_args()
 
 
@@ -284,6 +288,9 @@ def main():
     dev = torch.device("cuda", local)
     wl = W.WORKLOADS[args.workload]
     stacked = wl.layers > 1 and not args.single_layer
+    if args.only:
+        run_only(args, wl, stacked, dev)
+        return
     job = StackJob(wl, dev) if stacked else LayerJob(wl, dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
@@ -329,6 +336,42 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def run_only(args, wl, stacked, dev):
+    """A short eager run of one piece of the path, for profilers: the sampling
+    stage three ways (deform_conv_sample fused, deform_conv_offsets, or
+    deform_conv_sample at offsets given) on layer 0's inputs, or the whole
+    step."""
+    import torch
+
+    from deformable_convolution_gb300 import binding as B
+    job = StackJob(wl, dev) if stacked else LayerJob(wl, dev)
+    p, t = job.p, job.t
+    s = p.shapes()
+    col = torch.empty(B.col_shape(p), dtype=p.torch_dtype, device=dev)
+    off = torch.empty(s["offset"], dtype=torch.float32, device=dev)
+    ws = B.workspace(p, False, dev)
+    B.deform_conv_offsets(p, t["x"], t["w_off"], t["b_off"], t["offset_add"], off, ws=ws)
+    launch = {
+        "stage": lambda: B.deform_conv_sample(p, t["x"], t["w_off"], t["b_off"], t["offset_add"],
+                                              None, col, off, ws=ws),
+        "offsets": lambda: B.deform_conv_offsets(p, t["x"], t["w_off"], t["b_off"],
+                                                 t["offset_add"], off, ws=ws),
+        "replay": lambda: B.deform_conv_sample(p, t["x"], None, None, None, off, col, ws=ws),
+        "step": job.step,
+    }[args.only]
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        launch()
+    b.record()
+    torch.cuda.synchronize(dev)
+    print(json.dumps({"only": args.only, "workload": wl.name, "stacked": stacked,
+                      "ms_per_call": a.elapsed_time(b) / max(1, args.steps)}), flush=True)
 
 
 def job_config(wl, stacked):
@@ -631,11 +674,13 @@ def k1_roofline(p, t, dev, stream, flush, wl, iters=200):
     import torch
 
     from deformable_convolution_gb300 import binding as B
-    col = torch.empty(p.shapes()["col"], dtype=p.torch_dtype, device=dev)
+    col = torch.empty(B.col_shape(p), dtype=p.torch_dtype, device=dev)
     off = torch.empty(p.shapes()["offset"], dtype=torch.float32, device=dev)
+    ws = B.workspace(p, False, dev)
 
     def launch():
-        B.deform_conv_sample(p, t["x"], t["w_off"], t["b_off"], t["offset_add"], None, col, off)
+        B.deform_conv_sample(p, t["x"], t["w_off"], t["b_off"], t["offset_add"], None, col, off,
+                             ws=ws)
 
     with torch.cuda.stream(stream):
         launch()
@@ -705,14 +750,15 @@ def unfused_ablation(p, t, dev, stream, flush, iters=200):
 
     from deformable_convolution_gb300 import binding as B
     s = p.shapes()
-    col = torch.empty(s["col"], dtype=p.torch_dtype, device=dev)
+    col = torch.empty(B.col_shape(p), dtype=p.torch_dtype, device=dev)
     off = torch.empty(s["offset"], dtype=torch.float32, device=dev)
+    ws = B.workspace(p, False, dev)
     add = t["offset_add"]
     fused = time_graph(lambda: B.deform_conv_sample(p, t["x"], t["w_off"], t["b_off"], add, None,
-                                                    col, off), dev, stream, flush, iters)
-    k_off = time_graph(lambda: B.deform_conv_offsets(p, t["x"], t["w_off"], t["b_off"], add, off),
-                       dev, stream, flush, iters)
-    k_smp = time_graph(lambda: B.deform_conv_sample(p, t["x"], None, None, None, off, col),
+                                                    col, off, ws=ws), dev, stream, flush, iters)
+    k_off = time_graph(lambda: B.deform_conv_offsets(p, t["x"], t["w_off"], t["b_off"], add, off,
+                                                     ws=ws), dev, stream, flush, iters)
+    k_smp = time_graph(lambda: B.deform_conv_sample(p, t["x"], None, None, None, off, col, ws=ws),
                        dev, stream, flush, iters)
     elt = 2 if p.dtype == 1 else 4
     P = p.n * p.ho * p.wo

@@ -25,7 +25,9 @@ EXPORTED_SYMBOLS = (
     "dc_launch_count", "deform_conv_fwd_noalloc", "dc_device_error", "dc_kernel_timing",
     "dc_kernel_times", "deform_conv_offsets", "deform_conv_margin_histogram", "dc_suggest_margin",
     "deform_conv_bwd_after_fwd", "deform_conv_fwd_sampled_gemm", "dc_relu_fwd", "dc_relu_bwd",
+    "dc_col_layout", "dc_sample_tile",
 )
+DC_COL_PLANE_MAJOR, DC_COL_PIXEL_MAJOR = 0, 1
 MARGIN_BINS = 64
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
@@ -64,9 +66,13 @@ def lib() -> ctypes.CDLL:
         L.deform_conv_bwd.restype = i
         L.deform_conv_bwd_after_fwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.deform_conv_bwd_after_fwd.restype = i
-        L.deform_conv_sample.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.deform_conv_sample.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.deform_conv_sample.restype = i
-        L.deform_conv_offsets.argtypes = [pp, vp, vp, vp, vp, vp, vp]
+        L.dc_col_layout.argtypes = [pp]
+        L.dc_col_layout.restype = i
+        L.dc_sample_tile.argtypes = [pp, ctypes.POINTER(i), ctypes.POINTER(i)]
+        L.dc_sample_tile.restype = i
+        L.deform_conv_offsets.argtypes = [pp, vp, vp, vp, vp, vp, vp, sz, vp]
         L.deform_conv_offsets.restype = i
         L.deform_conv_fwd_sampled_gemm.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp]
         L.deform_conv_fwd_sampled_gemm.restype = i
@@ -181,6 +187,9 @@ class Problem:
                     y=(self.n, self.c_out, self.ho, self.wo),
                     col=(self.c_in * self.kh * self.kw, self.n, self.ho * self.wo))
 
+    # (the deformed map's shape depends on the path the library takes for the
+    # problem: binding.col_shape)
+
 
 def _ptr(t, name, shape=None, dtype=None, optional=False):
     if t is None:
@@ -272,32 +281,65 @@ def deform_conv_bwd(p: Problem, x, w_off, w, offset, grad_y, grad_x, grad_w_off,
         ws_ptr, ctypes.c_size_t(ws.numel()), _stream(stream)), "deform_conv_bwd")
 
 
+def col_layout(p: Problem) -> int:
+    """DC_COL_PLANE_MAJOR or DC_COL_PIXEL_MAJOR (the deformed map's layout)."""
+    st = p.c_struct()
+    v = int(lib().dc_col_layout(ctypes.byref(st)))
+    if v < 0:
+        raise DcError(DC_ERR_INVALID_ARG, "dc_col_layout")
+    return v
+
+
+def col_shape(p: Problem):
+    """Shape of the deformed map in the problem's layout."""
+    if col_layout(p) == DC_COL_PIXEL_MAJOR:
+        return (p.n, p.ho * p.wo, p.kh * p.kw, p.c_in)
+    return (p.c_in * p.kh * p.kw, p.n, p.ho * p.wo)
+
+
+def sample_tile(p: Problem):
+    """(tile_h, tile_w): the output tile the sampling stage stages a window for."""
+    st = p.c_struct()
+    th, tw = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().dc_sample_tile(ctypes.byref(st), ctypes.byref(th), ctypes.byref(tw)),
+           "dc_sample_tile")
+    return th.value, tw.value
+
+
 def deform_conv_sample(p: Problem, x, w_off, b_off, offset_add, offset_in, col,
-                       offset_out=None, slowpath_count=None, stream=None):
+                       offset_out=None, slowpath_count=None, ws=None, stream=None):
     s = p.shapes()
     dt, f32 = p.torch_dtype, torch.float32
     st = p.c_struct()
+    if ws is None:
+        ws = workspace(p, False, x.device)
     _check(lib().deform_conv_sample(
         ctypes.byref(st), _ptr(x, "x", s["x"], dt),
         _ptr(w_off, "w_off", s["w_off"], dt, True),
         _ptr(b_off, "b_off", s["b_off"], f32, True),
         _ptr(offset_add, "offset_add", s["offset"], f32, True),
         _ptr(offset_in, "offset_in", s["offset"], f32, True),
-        _ptr(col, "col", s["col"], dt),
+        _ptr(col, "col", col_shape(p), dt),
         _ptr(offset_out, "offset_out", s["offset"], f32, True),
         _ptr(slowpath_count, "slowpath_count", (1,), torch.int64, True),
+        _ptr(ws, "ws", dtype=torch.uint8), ctypes.c_size_t(ws.numel()),
         _stream(stream)), "deform_conv_sample")
 
 
-def deform_conv_offsets(p: Problem, x, w_off, b_off, offset_add, offset_out, stream=None):
+def deform_conv_offsets(p: Problem, x, w_off, b_off, offset_add, offset_out, ws=None,
+                        stream=None):
     s = p.shapes()
     dt, f32 = p.torch_dtype, torch.float32
     st = p.c_struct()
+    if ws is None:
+        ws = workspace(p, False, x.device)
     _check(lib().deform_conv_offsets(
         ctypes.byref(st), _ptr(x, "x", s["x"], dt), _ptr(w_off, "w_off", s["w_off"], dt),
         _ptr(b_off, "b_off", s["b_off"], f32, True),
         _ptr(offset_add, "offset_add", s["offset"], f32, True),
-        _ptr(offset_out, "offset_out", s["offset"], f32), _stream(stream)), "deform_conv_offsets")
+        _ptr(offset_out, "offset_out", s["offset"], f32),
+        _ptr(ws, "ws", dtype=torch.uint8), ctypes.c_size_t(ws.numel()),
+        _stream(stream)), "deform_conv_offsets")
 
 
 def deform_conv_fwd_sampled_gemm(p: Problem, x, w_off, b_off, w, offset_add, y, offset_out,

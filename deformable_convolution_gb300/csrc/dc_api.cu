@@ -118,20 +118,26 @@ dc_status make_geom(const dc_problem* p, Geom* g, int* margin) {
     return DC_ERR_UNSUPPORTED;
   *margin = p->halo_margin < 0 ? kDefaultMargin : p->halo_margin;
   if (*margin > kMaxMargin) return DC_ERR_UNSUPPORTED;
-  if (sample_smem_bytes(*g, p->dtype, *margin) > kMaxSmem) return DC_ERR_UNSUPPORTED;
+  if (!cl_supported(*g, p->dtype, *margin) && sample_smem_bytes(*g, p->dtype, *margin) > kMaxSmem)
+    return DC_ERR_UNSUPPORTED;
   return DC_OK;
 }
 
 // Workspace carve-up.  The column buffer keeps each image's pixel run padded
 // to a multiple of 8 elements so that every row starts 16-byte aligned.
+// The channels-last path (bf16, see cl_supported) adds x's NHWC copy, the
+// permuted main weights and the fragment-ordered offset weights, and keeps
+// the deformed map pixel-major (col[n][pixel][tap][channel], no padding).
 struct Plan {
+  bool cl;
   ColLayout col, gcol;
-  size_t col_off, gcol_off, off_off, gmax_off, gwo_img_off, total;
+  size_t col_off, gcol_off, off_off, gmax_off, gwo_img_off, xc_off, wp_off, wfrag_off, total;
   int gmax_tx, gmax_ty;
 };
 
-Plan make_plan(const Geom& g, dc_dtype dt, int backward) {
+Plan make_plan(const Geom& g, dc_dtype dt, int backward, int margin) {
   Plan pl{};
+  pl.cl = cl_supported(g, dt, margin);
   const long long pitch = round_up(g.howo, 8);
   pl.col.img = pitch;
   pl.col.row = pitch * g.n;
@@ -144,6 +150,11 @@ Plan make_plan(const Geom& g, dc_dtype dt, int backward) {
   };
   pl.col_off = take((size_t)g.kdim * pl.col.row * elt_size(dt));
   pl.off_off = take((size_t)g.n * g.M * g.howo * sizeof(float));
+  if (pl.cl) {
+    pl.xc_off = take((size_t)g.n * g.hw * g.c_in * 2);
+    pl.wp_off = take((size_t)g.c_out * g.kdim * 2);
+    pl.wfrag_off = take(cl_wfrag_bytes(g));
+  }
   // gcol: bf16 from the tensor-core GEMM (K3 then scales it into fixed point),
   // fp32 from the CUDA-core GEMM
   const size_t gcol_elt = dt == DC_BF16 && tc_gemm_supported(g) ? 2 : sizeof(float);
@@ -166,6 +177,41 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 dc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DC_OK : DC_ERR_CUDA; }
 
+}  // namespace
+
+namespace {
+// The channels-last sampling stage: x to NHWC; in one launch the main weights
+// permuted (when `w` is given) and w_off in mma fragment order (unless in
+// replay mode); then K1 over the staged windows.
+dc_status cl_stage(const Geom& g, int margin, const Plan& pl, char* wsb, const void* x,
+                   const void* w_off, const void* w, const float* b_off, const float* off_add,
+                   const float* off_in, void* col, float* off_out, unsigned long long* slow,
+                   cudaStream_t s) {
+  dc_status st = cuda_status(timed("cl_prep_x", s, [&] {
+    return launch_cl_prep_x(x, wsb + pl.xc_off, g, s);
+  }));
+  if (st != DC_OK) return st;
+  if (!off_in || w) {
+    st = cuda_status(timed("cl_prep_weights", s, [&] {
+      return launch_cl_prep_weights(w, wsb + pl.wp_off, w_off, off_in ? nullptr : wsb + pl.wfrag_off,
+                                    g, margin, s);
+    }));
+    if (st != DC_OK) return st;
+  }
+  ClArgs ca{};
+  ca.g = g;
+  ca.xc = wsb + pl.xc_off;
+  ca.wfrag = wsb + pl.wfrag_off;
+  ca.b_off = off_in ? nullptr : b_off;
+  ca.off_add = off_in ? nullptr : off_add;
+  ca.off_in = off_in;
+  ca.col = col;
+  ca.off_out = off_out;
+  ca.slow_count = slow;
+  ca.margin = margin;
+  const char* name = col ? "k1_cl_sample" : "k1_cl_offsets";
+  return cuda_status(timed(name, s, [&] { return launch_cl_sample(ca, s); }));
+}
 }  // namespace
 }  // namespace dc
 
@@ -193,11 +239,18 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
                         grad_offset, ws};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return DC_ERR_UNSUPPORTED;
-  const Plan pl = make_plan(g, prob->dtype, 1);
+  const Plan pl = make_plan(g, prob->dtype, 1, margin);
   if (!ws || ws_bytes < pl.total) return DC_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* wsb = static_cast<char*>(ws);
   float* goff = grad_offset ? grad_offset : reinterpret_cast<float*>(wsb + pl.off_off);
+  if (pl.cl && !reuse_map) {
+    // the pixel-major map for the weight-gradient GEMM, sampled at the given
+    // offsets, and the permuted weights
+    st = cl_stage(g, margin, pl, wsb, x, w_off, w, nullptr, nullptr, offset, wsb + pl.col_off,
+                  nullptr, nullptr, s);
+    if (st != DC_OK) return st;
+  }
 
   // gradient of the deformed map: gcol = w^T grad_y
   GemmArgs ga{};
@@ -237,7 +290,7 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
   ba.off = offset;
   ba.gcol = ga.gcol;
   ba.gcol_layout = pl.gcol;
-  ba.col = reuse_map ? nullptr : wsb + pl.col_off;
+  ba.col = (reuse_map || pl.cl) ? nullptr : wsb + pl.col_off;
   ba.col_layout = pl.col;
   ba.gx = grad_x;
   ba.goff = goff;
@@ -270,7 +323,9 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
     ga.gw_off = grad_w_off;
     ga.gwo_count = gwo_frag_count(g.M, g.c_in, g.K);
   }
-  st = cuda_status(timed("gemm_gw", s, [&] { return launch_gemm_gw(ga, prob->dtype, s); }));
+  st = cuda_status(timed("gemm_gw", s, [&] {
+    return pl.cl ? launch_gemm_gw_cl(ga, s) : launch_gemm_gw(ga, prob->dtype, s);
+  }));
   if (st != DC_OK || !gwo_img || gw_reduces) return st;
 
   // grad_w_off from K4's per-image partials
@@ -303,7 +358,7 @@ dc_status deform_conv_workspace_size(const dc_problem* prob, int backward, size_
   if (backward && (bwd_smem_bytes(g, prob->dtype, margin) > kMaxSmem ||
                    offconv_bwd_smem_bytes(g, prob->dtype) > kMaxSmem))
     return DC_ERR_UNSUPPORTED;
-  *bytes = make_plan(g, prob->dtype, backward ? 1 : 0).total;
+  *bytes = make_plan(g, prob->dtype, backward ? 1 : 0, margin).total;
   return DC_OK;
 }
 
@@ -319,11 +374,22 @@ dc_status deform_conv_fwd(const dc_problem* prob, const void* x, const void* w_o
   const void* ptrs[] = {x, w_off, b_off, w, offset_add, y, offset_out, slowpath_count, ws};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return DC_ERR_UNSUPPORTED;
-  const Plan pl = make_plan(g, prob->dtype, 0);
+  const Plan pl = make_plan(g, prob->dtype, 0, margin);
   if (!ws || ws_bytes < pl.total) return DC_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* wsb = static_cast<char*>(ws);
 
+  if (pl.cl) {
+    st = cl_stage(g, margin, pl, wsb, x, w_off, w, b_off, offset_add, nullptr, wsb + pl.col_off,
+                  offset_out, slowpath_count, s);
+    if (st != DC_OK) return st;
+    GemmArgs ga{};
+    ga.g = g;
+    ga.w = wsb + pl.wp_off;
+    ga.col = wsb + pl.col_off;
+    ga.y = y;
+    return cuda_status(timed("gemm_fwd", s, [&] { return launch_gemm_fwd_cl(ga, s); }));
+  }
   SampleArgs sa{};
   sa.g = g;
   sa.x = x;
@@ -368,15 +434,20 @@ dc_status deform_conv_bwd_after_fwd(const dc_problem* prob, const void* x, const
 dc_status deform_conv_sample(const dc_problem* prob, const void* x, const void* w_off,
                              const float* b_off, const float* offset_add, const float* offset_in,
                              void* col, float* offset_out, unsigned long long* slowpath_count,
-                             void* stream) {
+                             void* ws, size_t ws_bytes, void* stream) {
   Geom g;
   int margin;
   dc_status st = make_geom(prob, &g, &margin);
   if (st != DC_OK) return st;
   if (!x || !col || (!offset_in && !w_off)) return DC_ERR_INVALID_ARG;
-  const void* ptrs[] = {x, w_off, b_off, offset_add, offset_in, col, offset_out, slowpath_count};
+  const void* ptrs[] = {x, w_off, b_off, offset_add, offset_in, col, offset_out, slowpath_count, ws};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return DC_ERR_UNSUPPORTED;
+  const Plan pl = make_plan(g, prob->dtype, 0, margin);
+  if (!ws || ws_bytes < pl.total) return DC_ERR_WORKSPACE;
+  if (pl.cl)
+    return cl_stage(g, margin, pl, static_cast<char*>(ws), x, w_off, nullptr, b_off, offset_add,
+                    offset_in, col, offset_out, slowpath_count, static_cast<cudaStream_t>(stream));
   SampleArgs sa{};
   sa.g = g;
   sa.x = x;
@@ -396,15 +467,20 @@ dc_status deform_conv_sample(const dc_problem* prob, const void* x, const void* 
 
 dc_status deform_conv_offsets(const dc_problem* prob, const void* x, const void* w_off,
                               const float* b_off, const float* offset_add, float* offset_out,
-                              void* stream) {
+                              void* ws, size_t ws_bytes, void* stream) {
   Geom g;
   int margin;
   dc_status st = make_geom(prob, &g, &margin);
   if (st != DC_OK) return st;
   if (!x || !w_off || !offset_out) return DC_ERR_INVALID_ARG;
-  const void* ptrs[] = {x, w_off, b_off, offset_add, offset_out};
+  const void* ptrs[] = {x, w_off, b_off, offset_add, offset_out, ws};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return DC_ERR_UNSUPPORTED;
+  const Plan pl = make_plan(g, prob->dtype, 0, margin);
+  if (!ws || ws_bytes < pl.total) return DC_ERR_WORKSPACE;
+  if (pl.cl)
+    return cl_stage(g, margin, pl, static_cast<char*>(ws), x, w_off, nullptr, b_off, offset_add,
+                    nullptr, nullptr, offset_out, nullptr, static_cast<cudaStream_t>(stream));
   SampleArgs sa{};
   sa.g = g;
   sa.x = x;
@@ -456,7 +532,10 @@ dc_status deform_conv_margin_histogram(const dc_problem* prob, const float* offs
   if (st != DC_OK) return st;
   if (!offset || !hist) return DC_ERR_INVALID_ARG;
   int R, TW;
-  sample_band(g, prob->dtype, margin, &R, &TW);
+  if (cl_supported(g, prob->dtype, margin))
+    cl_tile(g, margin, &R, &TW);
+  else
+    sample_band(g, prob->dtype, margin, &R, &TW);
   return cuda_status(
       launch_margin_histogram(offset, g, R, TW, hist, static_cast<cudaStream_t>(stream)));
 }
@@ -486,6 +565,26 @@ int dc_suggest_margin(const dc_problem* prob, const unsigned long long* hist,
   };
   while (m > 0 && !fits(m)) --m;
   return m;
+}
+
+int dc_col_layout(const dc_problem* prob) {
+  Geom g;
+  int margin;
+  if (make_geom(prob, &g, &margin) != DC_OK) return -1;
+  return cl_supported(g, prob->dtype, margin) ? DC_COL_PIXEL_MAJOR : DC_COL_PLANE_MAJOR;
+}
+
+dc_status dc_sample_tile(const dc_problem* prob, int* tile_h, int* tile_w) {
+  Geom g;
+  int margin;
+  const dc_status st = make_geom(prob, &g, &margin);
+  if (st != DC_OK) return st;
+  if (!tile_h || !tile_w) return DC_ERR_INVALID_ARG;
+  if (cl_supported(g, prob->dtype, margin))
+    cl_tile(g, margin, tile_h, tile_w);
+  else
+    sample_band(g, prob->dtype, margin, tile_h, tile_w);
+  return DC_OK;
 }
 
 dc_status dc_relu_fwd(const void* y, void* out, size_t count, dc_dtype dtype, void* stream) {

@@ -2,6 +2,7 @@
 // kernel launch entry points).  Nothing here is visible through the C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -158,6 +159,11 @@ bool tc_gemm_supported(const Geom& g);
 cudaError_t launch_gemm_fwd_tc(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_gcol_tc(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_gemm_gw_tc(const GemmArgs& a, cudaStream_t s);
+// The same on the pixel-major map (channels-last path): `w` is w'[o][tap][c],
+// `col` / `gcol` are col[n][pixel][tap][c]; GW writes grad_w[o][c][tap].
+cudaError_t launch_gemm_fwd_cl(const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_gcol_cl(const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_gw_cl(const GemmArgs& a, cudaStream_t s);
 // Forward GEMM with its B operand sampled in shared memory from x and the
 // offsets (bf16, tensor cores; no column buffer): y = w * map(x, off).
 bool fwd_sampled_supported(const Geom& g);
@@ -246,6 +252,38 @@ size_t offconv_bwd_tc_smem_bytes(const Geom& g);
 cudaError_t launch_offconv_bwd_tc(const OffconvBwdArgs& a, cudaStream_t s);
 // gw_off = sum over images of gw_off_img (launched after the grad_W GEMM)
 cudaError_t launch_gw_off_reduce(const OffconvBwdArgs& a, cudaStream_t s);
+
+// ---------------------------------------------------------------- channels-last path
+// bf16 problems with C_in % 64 == 0 (C_in <= 256), 8 | C_in / G, H*W % 8 == 0
+// and the tensor-core GEMMs' alignment run on x copied to NHWC and a
+// pixel-major deformed map col[n][pixel][tap][channel] (row = n*Ho*Wo + pixel,
+// kdim = K*C_in elements per row, tap-major); the main weights are permuted
+// to w'[o][tap][channel] to match.
+bool cl_supported(const Geom& g, dc_dtype dt, int margin);
+void cl_tile(const Geom& g, int margin, int* th, int* tw);  // output tile of the sampling stage
+size_t cl_wfrag_bytes(const Geom& g);  // w_off in mma B-fragment order
+struct ClArgs {
+  Geom g;
+  const void* xc;      // x, NHWC bf16
+  const void* wfrag;   // launch_cl_prep_woff's output (ignored in replay mode)
+  const float* b_off;
+  const float* off_add;
+  const float* off_in;  // non-null: sample these offsets (replay), no offset convolution
+  void* col;            // pixel-major deformed map, or null: offsets only
+  float* off_out;
+  unsigned long long* slow_count;
+  int margin;
+};
+cudaError_t launch_cl_prep_x(const void* x, void* xc, const Geom& g, cudaStream_t s);
+// w [o][c][tap] -> w' [o][tap][c] (w non-null), and w_off in mma B-fragment
+// order (frag non-null), in one launch
+cudaError_t launch_cl_prep_weights(const void* w, void* wp, const void* w_off, void* frag,
+                                   const Geom& g, int margin, cudaStream_t s);
+cudaError_t launch_cl_sample(const ClArgs& a, cudaStream_t s);
+unsigned int cl_read_error(int clear);
+bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const unsigned long long* dims,
+                    const unsigned long long* strides_bytes, const unsigned int* box,
+                    bool swizzle128);
 
 // ReLU between stacked layers: out = max(y, 0); gin = gout where act > 0
 // (rounded to the dtype), else 0.  16-byte aligned pointers.

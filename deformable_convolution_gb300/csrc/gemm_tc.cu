@@ -35,7 +35,20 @@ namespace {
 constexpr int kBM = 128, kBK = 64;
 constexpr int kThreads = 192;
 constexpr uint32_t kSpinLimit = 1u << 24;
-enum Kind { FWD = 0, GCOL = 1, GW = 2 };
+// FWD / GCOL / GW work on the plane-major deformed map col[c*K + tap][n][pixel];
+// FWDC / GCOLC / GWC on the pixel-major one, col[n][pixel][tap][channel], with
+// the main weights permuted to w'[o][tap][channel] (the channels-last path):
+//   FWDC   y[b][o][q]       = sum_r w'[o][r] * col[b][q][r]     A = w'  (K-major)
+//                                                               B = col (K-major)
+//   GCOLC  gcol[b][q][r]    = sum_o gy[b][o][q] * w'[o][r]      A = gy  (MN-major, M = pixels)
+//                                                               B = w'  (MN-major)
+//   GWC    gw[o][c][tap]   += sum_b,q gy[b][o][q] * col[b][q][r], r = tap*C + c
+//                                                               A = gy  (K-major)
+//                                                               B = col (MN-major)
+enum Kind { FWD = 0, GCOL = 1, GW = 2, FWDC = 3, GCOLC = 4, GWC = 5 };
+constexpr bool is_fwd(int k) { return k == FWD || k == FWDC; }
+constexpr bool is_gcol(int k) { return k == GCOL || k == GCOLC; }
+constexpr bool is_gw(int k) { return k == GW || k == GWC; }
 
 struct TcArgs {
   int c_out, kdim, howo, nimg;
@@ -51,6 +64,7 @@ struct TcArgs {
   float* gw_off;
   long long gwo_count;         // floats per image
   int gwo_nimg, gwo_m, gwo_cin, gwo_k;  // images; M, C_in, K of the partials' order
+  int cin, ktaps;              // GWC: C_in and taps, to map columns (tap, c) to grad_w[o][c][tap]
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -204,11 +218,11 @@ struct Cfg {
   // GCOL reduces over C_out only (a few k-blocks): two stages, so that three
   // CTAs fit on an SM; the long reductions keep a deeper ring.
   // GCOL has two k-blocks; four stages let two FWD CTAs share an SM
-  static constexpr int kStages = KIND == GCOL ? 2 : 4;
+  static constexpr int kStages = is_gcol(KIND) ? 2 : 4;
   static constexpr int kTmemCols = BN < 32 ? 32 : BN;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256;
-  static constexpr int kAMn = KIND == GCOL ? 1 : 0;
-  static constexpr int kBMn = KIND == GW ? 0 : 1;
+  static constexpr int kAMn = is_gcol(KIND) ? 1 : 0;
+  static constexpr int kBMn = (KIND == GW || KIND == FWDC) ? 0 : 1;
 };
 
 template <int KIND, int BN>
@@ -228,12 +242,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // FWD split over a 2-CTA cluster: rank 0 takes the first half of the
   // k-blocks, rank 1 the second; rank 1 hands its fp32 tile to rank 0 through
   // distributed shared memory and rank 0 writes y
-  const bool split = KIND == FWD && a.fwd_split == 2;
+  const bool split = is_fwd(KIND) && a.fwd_split == 2;
   const int rank = split ? (int)(blockIdx.y & 1) : 0;
   const int m0 = (split ? (int)(blockIdx.y >> 1) : (int)blockIdx.y) * kBM, n0 = blockIdx.x * BN;
   const int z = blockIdx.z;
   int kb_begin = 0, kb_end = a.kb_total;
-  if (KIND == GW) {
+  if (is_gw(KIND)) {
     kb_begin = z * a.kb_per_split;
     kb_end = min(a.kb_total, kb_begin + a.kb_per_split);
   }
@@ -271,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // only once every K4 block has passed its own wait on K3 (which replays the
   // column it reads, after GCOL cleared grad_w), so it runs beside K4 and
   // waits for K4 only before it exits.
-  if (KIND != GW) pdl_wait();
+  if (!is_gw(KIND)) pdl_wait();
 
   if (warp == 4) {
     if (lane == 0) {
@@ -287,6 +301,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_2d(sa, &tmA, &full[s], kb * kBK, m0);
 #pragma unroll
           for (int h = 0; h < BN / 64; ++h) tma_3d(sb + h * 8192, &tmB, &full[s], n0 + 64 * h, z, kb * kBK);
+        } else if (KIND == FWDC) {
+          // A: w' rows m0.., k-block kb; B: BN pixels of image z, k-block kb
+          tma_2d(sa, &tmA, &full[s], kb * kBK, m0);
+          tma_3d(sb, &tmB, &full[s], kb * kBK, n0, z);
+        } else if (KIND == GCOLC) {
+          // A: grad_y rows kb*64.. (output channels) x 128 pixels of image z,
+          // as two 64-pixel MN chunks; B: w' rows kb*64.. x BN columns
+          tma_3d(sa, &tmA, &full[s], m0, kb * kBK, z);
+          tma_3d(sa + 8192, &tmA, &full[s], m0 + 64, kb * kBK, z);
+#pragma unroll
+          for (int h = 0; h < BN / 64; ++h) tma_2d(sb + h * 8192, &tmB, &full[s], n0 + 64 * h, kb * kBK);
+        } else if (KIND == GWC) {
+          const int img = kb / a.qblocks, q0 = (kb - img * a.qblocks) * kBK;
+          tma_3d(sa, &tmA, &full[s], q0, m0, img);
+#pragma unroll
+          for (int h = 0; h < BN / 64; ++h) tma_3d(sb + h * 8192, &tmB, &full[s], n0 + 64 * h, q0, img);
         } else if (KIND == GCOL) {
           tma_2d(sa, &tmA, &full[s], m0, kb * kBK);
           tma_2d(sa + 8192, &tmA, &full[s], m0 + 64, kb * kBK);
@@ -325,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_release();
   } else {
     // -------------------------------------------------------------- epilogue (warps 0-3)
-    if (KIND == GCOL) {
+    if (is_gcol(KIND)) {
       // while the tensor cores work, clear this CTA's share of the buffers the
       // rest of the backward pass accumulates into with atomics
       const long long nparts = (long long)gridDim.x * gridDim.y * gridDim.z;
@@ -347,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tbase + c * 32, r);
       if (!ok || nkb == 0) continue;
       const int n_first = n0 + c * 32;
-      if (KIND == FWD && split) {
+      if (is_fwd(KIND) && split) {
         // rank 1: its partial tile to its own shared memory, column-major
         // (lanes write consecutive words); rank 0 combines after the cluster
         // barrier below
@@ -356,17 +386,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) part[(c * 32 + j) * kBM + row] = __uint_as_float(r[j]);
         }
-      } else if (KIND == FWD) {
+      } else if (is_fwd(KIND)) {
         if (m >= a.c_out) continue;
         store_y_row(static_cast<__nv_bfloat16*>(a.out) + ((long long)z * a.c_out + m) * a.howo + n_first,
                     r, n_first, a.howo);
-      } else if (KIND == GCOL) {
+      } else if (is_gcol(KIND)) {
         // gcol leaves as bf16: this warp's 32 rows x 64 columns go through
         // shared memory (the operand stages are free once `done` fired) in the
         // 128-byte swizzled layout of the store map, one TMA store per two
         // 32-column chunks; rows and columns beyond the tensor are clipped by
         // the TMA unit.  The magnitude bound is taken before rounding.
-        if (m < a.kdim) {
+        if (KIND == GCOL && m < a.kdim) {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             if (n_first + j < a.howo) amax = max(amax, r[j] & 0x7fffffffu);
@@ -389,9 +419,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
           const int box_n = n0 + (c >> 1) * 64;
-          if (lane == 0 && m0 + warp * 32 < a.kdim && box_n < a.howo) {
+          if (KIND == GCOL && lane == 0 && m0 + warp * 32 < a.kdim && box_n < a.howo) {
             tma_store_3d(&tmC, buf, box_n, z, m0 + warp * 32);
             tma_store_commit();
+          }
+          // pixel-major: rows are pixels, columns (tap, channel)
+          if (KIND == GCOLC && lane == 0 && m0 + warp * 32 < a.howo && box_n < a.kdim) {
+            tma_store_3d(&tmC, buf, box_n, m0 + warp * 32, z);
+            tma_store_commit();
+          }
+        }
+      } else if (KIND == GWC) {
+        if (m >= a.c_out) continue;
+        // column r = tap * C + c of w' is grad_w[m][c][tap]
+        float* dst = static_cast<float*>(a.out) + (long long)m * a.kdim;
+        int tap = n_first / a.cin, c = n_first - tap * a.cin;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (n_first + j < a.kdim) atomicAdd(dst + (long long)c * a.ktaps + tap, __uint_as_float(r[j]));
+          if (++c == a.cin) {
+            c = 0;
+            ++tap;
           }
         }
       } else {
@@ -410,14 +458,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (KIND == GCOL && lane == 0) tma_store_wait_all();  // gcol written before exit
+    if (is_gcol(KIND) && lane == 0) tma_store_wait_all();  // gcol written before exit
     if (KIND == GCOL && a.gmax) {
       for (int o = 16; o > 0; o >>= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
       const long long tile = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * z);
       if (lane == 0) a.gmax[tile * 4 + warp] = __uint_as_float(amax);
     }
   }
-  if (KIND == FWD && split) {
+  if (is_fwd(KIND) && split) {
     // every thread of both CTAs: rank 1's partial is in its shared memory
     cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
     cluster.sync();
@@ -451,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"((uint32_t)C::kTmemCols)
                  : "memory");
-  if (KIND == GW) {
+  if (is_gw(KIND)) {
     pdl_wait();  // completes no earlier than K4
     if (a.gwo_img) {
       // K4 is complete: sum its per-image grad_w_off partials, float4 runs of
@@ -912,6 +960,91 @@ cudaError_t launch_gemm_gw_tc(const GemmArgs& ga, cudaStream_t s) {
   return launch<GW, 128>(A, B, A, a, grid, s);
 }
 
+// pixel-major deformed map (or its gradient) as a 3-D tensor {(tap, channel), pixel, image}
+bool colc_map(CUtensorMap* m, const void* col, const Geom& g, cuuint32_t box_px,
+              cuuint32_t box_r = 64) {
+  const cuuint64_t dims[3] = {(cuuint64_t)g.kdim, (cuuint64_t)g.howo, (cuuint64_t)g.n};
+  const cuuint64_t strides[2] = {(cuuint64_t)g.kdim * 2, (cuuint64_t)g.howo * g.kdim * 2};
+  const cuuint32_t box[3] = {box_r, box_px, 1};
+  return make_map(m, col, 3, dims, strides, box);
+}
+
+cudaError_t launch_gemm_fwd_cl(const GemmArgs& ga, cudaStream_t s) {
+  const Geom& g = ga.g;
+  const int bn = pick_fwd_bn(g);
+  CUtensorMap A, B;
+  if (!w_map(&A, ga.w, g, 64, 128)) return cudaErrorInvalidValue;
+  if (!colc_map(&B, ga.col, g, (cuuint32_t)bn)) return cudaErrorInvalidValue;
+  TcArgs a{};
+  a.c_out = g.c_out;
+  a.kdim = g.kdim;
+  a.howo = (int)g.howo;
+  a.nimg = g.n;
+  a.kb_total = (int)ceil_div_ll(g.kdim, kBK);
+  a.out = ga.y;
+  const long long tiles = ceil_div_ll(g.howo, bn) * ceil_div_ll(g.c_out, kBM) * g.n;
+  a.fwd_split = (bn == 64 && tiles < 152 && a.kb_total >= 24) ? 2 : 1;
+  dim3 grid((unsigned)ceil_div_ll(g.howo, bn), (unsigned)(ceil_div_ll(g.c_out, kBM) * a.fwd_split),
+            (unsigned)g.n);
+  return bn == 128 ? launch<FWDC, 128>(A, B, A, a, grid, s)
+                   : launch<FWDC, 64>(A, B, A, a, grid, s, a.fwd_split);
+}
+
+cudaError_t launch_gemm_gcol_cl(const GemmArgs& ga, cudaStream_t s) {
+  const Geom& g = ga.g;
+  CUtensorMap A, B, Cm;
+  if (!gy_map(&A, ga.gy, g, 64)) return cudaErrorInvalidValue;
+  if (!w_map(&B, ga.w, g, 64, 64)) return cudaErrorInvalidValue;
+  if (!colc_map(&Cm, ga.gcol, g, 32)) return cudaErrorInvalidValue;
+  TcArgs a{};
+  a.c_out = g.c_out;
+  a.kdim = g.kdim;
+  a.howo = (int)g.howo;
+  a.nimg = g.n;
+  a.kb_total = (int)ceil_div_ll(g.c_out, kBK);
+  a.out = ga.gcol;
+  a.zero = ga.zero;
+  a.gmax = nullptr;
+  dim3 grid((unsigned)ceil_div_ll(g.kdim, 128), (unsigned)ceil_div_ll(g.howo, kBM), (unsigned)g.n);
+  return launch<GCOLC, 128>(A, B, Cm, a, grid, s);
+}
+
+cudaError_t launch_gemm_gw_cl(const GemmArgs& ga, cudaStream_t s) {
+  const Geom& g = ga.g;
+  CUtensorMap A, B;
+  if (!gy_map(&A, ga.gy, g, 128)) return cudaErrorInvalidValue;
+  if (!colc_map(&B, ga.col, g, 64)) return cudaErrorInvalidValue;
+  TcArgs a{};
+  if (ga.gwo_img) {
+    if ((ga.gwo_count & 3) || (reinterpret_cast<uintptr_t>(ga.gwo_img) & 15))
+      return cudaErrorInvalidValue;
+    a.gwo_img = ga.gwo_img;
+    a.gw_off = ga.gw_off;
+    a.gwo_count = ga.gwo_count;
+    a.gwo_nimg = g.n;
+    a.gwo_m = g.M;
+    a.gwo_cin = g.c_in;
+    a.gwo_k = g.K;
+  }
+  a.c_out = g.c_out;
+  a.kdim = g.kdim;
+  a.howo = (int)g.howo;
+  a.nimg = g.n;
+  a.cin = g.c_in;
+  a.ktaps = g.K;
+  a.qblocks = (int)ceil_div_ll(g.howo, kBK);
+  a.kb_total = a.qblocks * g.n;
+  a.out = ga.gw;
+  const long long tiles = ceil_div_ll(g.kdim, 128) * ceil_div_ll(g.c_out, kBM);
+  long long splits = ceil_div_ll(152, tiles);
+  if (splits > a.kb_total) splits = a.kb_total;
+  if (splits < 1) splits = 1;
+  a.kb_per_split = (int)ceil_div_ll(a.kb_total, splits);
+  splits = ceil_div_ll(a.kb_total, a.kb_per_split);
+  dim3 grid((unsigned)ceil_div_ll(g.kdim, 128), (unsigned)ceil_div_ll(g.c_out, kBM), (unsigned)splits);
+  return launch<GWC, 128>(A, B, A, a, grid, s);
+}
+
 bool fwd_sampled_supported(const Geom& g) {
   return tc_gemm_supported(g) && fs_smem_bytes(g.M) <= 227 * 1024;
 }
@@ -947,6 +1080,7 @@ cudaError_t launch_fwd_sampled_tc(const Geom& g, const void* x, const void* w, c
 }  // namespace dc
 
 // Reads (and optionally clears) the flag bounded device waits raise on expiry.
+// The channels-last kernels keep their own flag (cl_read_error: 2 = unreadable).
 extern "C" dc_status dc_device_error(int clear) {
   unsigned int v = 0;
   if (cudaMemcpyFromSymbol(&v, dc::g_dc_device_error, sizeof(v)) != cudaSuccess) return DC_ERR_CUDA;
@@ -955,5 +1089,7 @@ extern "C" dc_status dc_device_error(int clear) {
     if (cudaMemcpyToSymbol(dc::g_dc_device_error, &zero, sizeof(zero)) != cudaSuccess)
       return DC_ERR_CUDA;
   }
-  return v ? DC_ERR_TIMEOUT : DC_OK;
+  const unsigned int c = dc::cl_read_error(clear);
+  if (c == 2u) return DC_ERR_CUDA;
+  return (v || c) ? DC_ERR_TIMEOUT : DC_OK;
 }

@@ -140,19 +140,41 @@ dc_status deform_conv_bwd_after_fwd(const dc_problem* prob, const void* x, const
                                     float* grad_w, float* grad_offset, void* ws, size_t ws_bytes,
                                     void* stream);
 
+/* Layout of the deformed feature map for a problem (dc_col_layout):
+ *   DC_COL_PLANE_MAJOR  col[C_in*Kh*Kw][N][Ho*Wo]: row c*Kh*Kw + k holds channel
+ *                       c sampled at tap k for every output pixel;
+ *   DC_COL_PIXEL_MAJOR  col[N][Ho*Wo][Kh*Kw][C_in]: for each output pixel and
+ *                       tap, the C_in channels are contiguous.
+ * bf16 problems with C_in a multiple of 64 (at most 256), C_in / G a multiple
+ * of 8, H*W, C_in*Kh*Kw and Ho*Wo multiples of 8 take the channels-last path
+ * (pixel-major map, x staged from an NHWC copy); all others the plane-major
+ * one.  Returns -1 for an invalid problem. */
+#define DC_COL_PLANE_MAJOR 0
+#define DC_COL_PIXEL_MAJOR 1
+int dc_col_layout(const dc_problem* prob);
+
+/* Output tile (tile_h rows x tile_w columns of output pixels) over which the
+ * fused sampling stage stages its input window for this problem and margin
+ * (the window is the tile's receptive field plus halo_margin pixels per side).
+ * DC_ERR_INVALID_ARG for an invalid problem or NULL outputs. */
+dc_status dc_sample_tile(const dc_problem* prob, int* tile_h, int* tile_w);
+
 /* The fused offset-convolution + bilinear-interpolation stage alone ("This
  * paper's idea": the kernel whose arithmetic intensity the fusion raises),
  * returning the deformed feature map ("What people did before, and where it
  * broke": the unrolled map the interpolation materialises).
- *   col        [C_in*Kh*Kw, N, Ho*Wo] dtype, required; row c*Kh*Kw + k holds
- *              channel c sampled at tap k for every output pixel
+ *   col        dtype, required, C_in*Kh*Kw*N*Ho*Wo elements in the problem's
+ *              layout (dc_col_layout)
  *   offset_add, b_off, offset_out, slowpath_count as in deform_conv_fwd
+ *   ws, ws_bytes  workspace from deform_conv_workspace_size(prob, 0, ...)
+ *              (the channels-last path keeps x's NHWC copy there)
  * If `offset_in` is non-NULL the offset convolution is skipped and those
  * offsets [N, 2GK, Ho, Wo] are sampled instead (w_off and b_off are ignored). */
 dc_status deform_conv_sample(const dc_problem* prob, const void* x, const void* w_off,
                              const float* b_off, const float* offset_add,
                              const float* offset_in, void* col, float* offset_out,
-                             unsigned long long* slowpath_count, void* stream);
+                             unsigned long long* slowpath_count, void* ws, size_t ws_bytes,
+                             void* stream);
 
 /* The offset convolution alone ("Following a deformable layer through DefT",
  * Step 1 of 5: a small standard convolution over the input that predicts one
@@ -164,11 +186,13 @@ dc_status deform_conv_sample(const dc_problem* prob, const void* x, const void* 
  * stopping before the interpolation.
  *   x, w_off, b_off, offset_add  as in deform_conv_fwd
  *   offset_out   [N, 2GK, Ho, Wo] float32, required
+ *   ws, ws_bytes workspace from deform_conv_workspace_size(prob, 0, ...)
  * Errors: DC_ERR_INVALID_ARG for a NULL x, w_off or offset_out,
- * DC_ERR_UNSUPPORTED for a pointer that is not 16-byte aligned. */
+ * DC_ERR_UNSUPPORTED for a pointer that is not 16-byte aligned,
+ * DC_ERR_WORKSPACE for a missing or short workspace. */
 dc_status deform_conv_offsets(const dc_problem* prob, const void* x, const void* w_off,
                               const float* b_off, const float* offset_add, float* offset_out,
-                              void* stream);
+                              void* ws, size_t ws_bytes, void* stream);
 
 /* The forward pass with the deformed map never written to memory: the
  * offset convolution (as deform_conv_offsets, offsets to offset_out), then one

@@ -121,11 +121,12 @@ def test_offsets_argument_checks_fail_before_any_launch():
     p = problem()
     st = p.c_struct()
     vp = ctypes.c_void_p
-    good = [0x10000 * (i + 1) for i in range(5)]  # x w_off b_off add offset_out
+    good = [0x10000 * (i + 1) for i in range(6)]  # x w_off b_off add offset_out ws
+    _, need = ws_size(p, False)
 
-    def call(ptrs):
+    def call(ptrs, ws_bytes=need):
         return B.lib().deform_conv_offsets(ctypes.byref(st), *[vp(v) if v else None for v in ptrs],
-                                           None)
+                                           ctypes.c_size_t(ws_bytes), None)
     for missing in (0, 1, 4):  # x, w_off and offset_out are required
         bad = list(good)
         bad[missing] = 0
@@ -133,6 +134,10 @@ def test_offsets_argument_checks_fail_before_any_launch():
     bad = list(good)
     bad[4] += 8
     assert call(bad) == B.DC_ERR_UNSUPPORTED
+    bad = list(good)
+    bad[5] = 0
+    assert call(bad) == B.DC_ERR_WORKSPACE
+    assert call(good, need - 1) == B.DC_ERR_WORKSPACE
 
 
 def test_sampled_gemm_forward_argument_checks_fail_before_any_launch():
