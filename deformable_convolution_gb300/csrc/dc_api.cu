@@ -130,14 +130,17 @@ dc_status make_geom(const dc_problem* p, Geom* g, int* margin) {
 // the deformed map pixel-major (col[n][pixel][tap][channel], no padding).
 struct Plan {
   bool cl;
+  bool k3cl;  // channels-last sampling backward (pixel-major gcol, NHWC grad_x accumulator)
   ColLayout col, gcol;
-  size_t col_off, gcol_off, off_off, gmax_off, gwo_img_off, xc_off, wp_off, wfrag_off, total;
+  size_t col_off, gcol_off, off_off, gmax_off, gwo_img_off, xc_off, wp_off, wfrag_off, gxc_off,
+      total;
   int gmax_tx, gmax_ty;
 };
 
 Plan make_plan(const Geom& g, dc_dtype dt, int backward, int margin) {
   Plan pl{};
   pl.cl = cl_supported(g, dt, margin);
+  pl.k3cl = backward && pl.cl && k3cl_supported(g, dt, margin);
   const long long pitch = round_up(g.howo, 8);
   pl.col.img = pitch;
   pl.col.row = pitch * g.n;
@@ -166,6 +169,7 @@ Plan make_plan(const Geom& g, dc_dtype dt, int backward, int margin) {
   // per-image grad_w_off partials of the tensor-core offset-conv backward
   // (one image's bands add into one copy: far fewer atomics per address), in
   // the kernel's accumulator order
+  pl.gxc_off = pl.k3cl ? take((size_t)g.n * g.hw * g.c_in * sizeof(float)) : 0;
   pl.gwo_img_off = backward && offconv_bwd_tc_supported(g, dt)
                        ? take((size_t)g.n * gwo_frag_count(g.M, g.c_in, g.K) * sizeof(float))
                        : 0;
@@ -262,8 +266,12 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
   ga.gcol = wsb + pl.gcol_off;
   ga.gcol_layout = pl.gcol;
   ga.gw = grad_w;
-  // the GCOL launch also clears the buffers later kernels accumulate into
-  ga.zero.p[0] = grad_x;
+  // the GCOL launch also clears the buffers later kernels accumulate into (on
+  // the channels-last path grad_x's NHWC accumulator: grad_x is written whole
+  // from it)
+  float* gxc = pl.k3cl ? reinterpret_cast<float*>(wsb + pl.gxc_off) : nullptr;
+  if (pl.k3cl) ga.w = wsb + pl.wp_off;
+  ga.zero.p[0] = pl.k3cl ? gxc : grad_x;
   ga.zero.n[0] = (long long)g.n * g.c_in * g.hw;
   ga.zero.p[1] = grad_w;
   ga.zero.n[1] = (long long)g.c_out * g.kdim;
@@ -279,9 +287,29 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
   // the tensor-core GCOL GEMM also reports max |gcol| per tile, from which K3
   // scales its fixed-point grad_x accumulation
   const bool tc_gcol = prob->dtype == DC_BF16 && tc_gemm_supported(g);
-  ga.gmax = tc_gcol ? reinterpret_cast<float*>(wsb + pl.gmax_off) : nullptr;
-  st = cuda_status(timed("gemm_gcol", s, [&] { return launch_gemm_gcol(ga, prob->dtype, s); }));
+  ga.gmax = tc_gcol && !pl.k3cl ? reinterpret_cast<float*>(wsb + pl.gmax_off) : nullptr;
+  st = cuda_status(timed("gemm_gcol", s, [&] {
+    return pl.k3cl ? launch_gemm_gcol_cl(ga, s) : launch_gemm_gcol(ga, prob->dtype, s);
+  }));
   if (st != DC_OK) return st;
+  ga.w = w;
+
+  if (pl.k3cl) {
+    // sampling backward over the staged NHWC windows, then grad_x from the
+    // NHWC accumulator
+    K3ClArgs ka{};
+    ka.g = g;
+    ka.xc = wsb + pl.xc_off;
+    ka.off = offset;
+    ka.gcol = ga.gcol;
+    ka.gx_nhwc = gxc;
+    ka.goff = goff;
+    ka.margin = margin;
+    st = cuda_status(timed("k3_cl_bwd", s, [&] { return launch_k3cl(ka, s); }));
+    if (st != DC_OK) return st;
+    st = cuda_status(timed("gx_to_nchw", s, [&] { return launch_gx_to_nchw(gxc, grad_x, g, s); }));
+    if (st != DC_OK) return st;
+  }
 
   // sampling backward; replays the deformed map for grad_w
   BwdArgs ba{};
@@ -298,8 +326,10 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
   ba.gmax = ga.gmax;
   ba.gmax_tx = pl.gmax_tx;
   ba.gmax_ty = pl.gmax_ty;
-  st = cuda_status(timed("k3_band_bwd", s, [&] { return launch_band_bwd(ba, prob->dtype, s); }));
-  if (st != DC_OK) return st;
+  if (!pl.k3cl) {
+    st = cuda_status(timed("k3_band_bwd", s, [&] { return launch_band_bwd(ba, prob->dtype, s); }));
+    if (st != DC_OK) return st;
+  }
 
   // offset-convolution backward on the completed offset gradient
   OffconvBwdArgs oa{};

@@ -281,6 +281,22 @@ cudaError_t launch_cl_prep_weights(const void* w, void* wp, const void* w_off, v
                                    const Geom& g, int margin, cudaStream_t s);
 cudaError_t launch_cl_sample(const ClArgs& a, cudaStream_t s);
 unsigned int cl_read_error(int clear);
+// Backward of the sampling step on the channels-last path (one offset group):
+// grad_x accumulated into an NHWC float32 buffer, the offset gradient into
+// goff (both cleared beforehand); then launch_gx_to_nchw writes grad_x.
+bool k3cl_supported(const Geom& g, dc_dtype dt, int margin);
+struct K3ClArgs {
+  Geom g;
+  const void* xc;    // x, NHWC bf16
+  const float* off;  // offsets [n][M][Ho][Wo]
+  const void* gcol;  // pixel-major gradient of the deformed map, bf16
+  float* gx_nhwc;    // [n][H][W][C_in] float32
+  float* goff;
+  int margin;
+};
+cudaError_t launch_k3cl(const K3ClArgs& a, cudaStream_t s);
+cudaError_t launch_gx_to_nchw(const float* gx_nhwc, float* grad_x, const Geom& g, cudaStream_t s);
+unsigned int cl3_read_error(int clear);
 bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const unsigned long long* dims,
                     const unsigned long long* strides_bytes, const unsigned int* box,
                     bool swizzle128);

@@ -16,6 +16,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// The dynamic shared-memory array advanced to a 1024-byte boundary.  The
+// result is the array plus an integer, so the compiler still knows that it
+// points to shared memory (shared-space loads, stores and atomics instead of
+// generic ones).
+__device__ __forceinline__ unsigned char* align1024(unsigned char* smem_raw) {
+  const uint32_t raw = smem_u32(smem_raw);
+  return smem_raw + (((raw + 1023u) & ~1023u) - raw);
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
                : "memory");

@@ -419,8 +419,7 @@ template <int NT, int CPS, bool kReplay>
 __global__ void __launch_bounds__(kThreads, 1)
     k1_cl_sample(const __grid_constant__ CUtensorMap xmap, ClKArgs a, ClPlan pl) {
   extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem =
-      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* smem = px::align1024(smem_raw);
   const Geom g = a.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t stage_pitch = (uint32_t)pl.chunks * pl.chunk_pitch;

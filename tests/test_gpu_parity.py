@@ -435,3 +435,53 @@ def test_sampled_gemm_forward_early_layer_full_batch():
     y2, off2, _ = gpu_forward(p, d)
     assert rel_err(f64(off), f64(off2)) <= 1e-5
     assert rel_err(f64(y), f64(y2)) <= 1e-2
+
+
+# One offset group, bf16, C_in a multiple of 64: the backward runs the
+# channels-last sampling backward (pixel-major gcol from the tensor-core GEMM,
+# grad_x gathered per window position into an NHWC accumulator).  Geometries:
+# 64 / 128 / 256 channels (2, 4, 8 channels per lane), stride 2, dilation 2
+# with a ragged last row of tiles, a 3 x 4 filter; then margin 0 with wide
+# offsets, where most samples leave the window and take the global path.
+CL_BACKWARD_GEOMETRIES = [
+    (2, 64, 20, 24, 32, 3, 3, 1, 1, 1, 1),
+    (1, 128, 18, 32, 40, 3, 3, 2, 1, 1, 1),
+    (2, 256, 15, 16, 24, 3, 3, 1, 2, 2, 1),
+    (1, 64, 16, 24, 16, 3, 4, 1, 1, 1, 1),
+]
+
+
+def backward_kernels(p, d):
+    """Names of the kernels one backward call launches."""
+    dd = {k: (None if v is None else v.cuda()) for k, v in d.items()}
+    s = p.shapes()
+    ws = B.workspace(p, True, "cuda")
+    off = torch.zeros(s["offset"], dtype=torch.float32, device="cuda")
+    out = [torch.empty(s[sh], dtype=torch.float32, device="cuda")
+           for sh in ("x", "w_off", "b_off", "w", "offset")]
+    torch.cuda.synchronize()
+    B.kernel_timing(True)
+    B.deform_conv_bwd(p, dd["x"], dd["w_off"], dd["w"], off, dd["grad_y"], *out, ws)
+    names = [n for n, _ in B.kernel_times()]
+    B.kernel_timing(False)
+    return names
+
+
+@pytest.mark.parametrize("geom", CL_BACKWARD_GEOMETRIES)
+def test_channels_last_backward_matches_oracle(geom):
+    n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups = geom
+    p = B.Problem(n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups, B.DC_BF16)
+    assert B.col_layout(p) == B.DC_COL_PIXEL_MAJOR
+    d = random_inputs(p, 500 + h * w + c_in)
+    assert "k3_cl_bwd" in backward_kernels(p, d)
+    errs = check_layer(p, d)
+    print(geom, errs)
+
+
+def test_channels_last_backward_global_path_matches_oracle():
+    n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups = CL_BACKWARD_GEOMETRIES[0]
+    p = B.Problem(n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups, B.DC_BF16, 0)
+    d = random_inputs(p, 600, off_scale=4.0)
+    assert "k3_cl_bwd" in backward_kernels(p, d)
+    errs = check_layer(p, d)
+    print(errs)
