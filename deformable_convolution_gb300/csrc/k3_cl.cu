@@ -68,8 +68,8 @@ struct K3Plan {
   int csplit, cpc, chunks;  // CTAs per tile (independent), channels per CTA, 64-channel chunks
   int npx, items;           // pixels per tile; samples per tile (npx * K)
   uint32_t win_bytes, gc_bytes, chunk_pitch;
-  size_t off_stage, off_gc, off_tap, off_syx, off_ent, off_pst, off_cnt, off_D, off_slow, off_oin,
-      off_bar, smem;
+  size_t off_stage, off_gc, off_tap, off_syx, off_ent, off_pst, off_cnt, off_pix, off_itab, off_otab,
+      off_D, off_slow, off_oin, off_bar, smem;
   int grid;
 };
 
@@ -96,7 +96,7 @@ __host__ K3Plan k3_plan_for(const Geom& g, int margin, int TH, int TW, int cspli
   at += 2 * (size_t)p.chunks * p.chunk_pitch;
   p.off_gc = at;  // two gcol buffers [items][cpc]
   at += 2 * (((size_t)p.gc_bytes + 1023) / 1024 * 1024);
-  p.off_tap = at;  // [2][items] int4 {ly, lx, gcol row in the image, kind}
+  p.off_tap = at;  // [2][items] int4 {ly, lx, -, kind}
   at += 2 * (size_t)p.items * 16;
   p.off_syx = at;  // [2][items] int2 {y0, x0} of the upper-left corner
   at += 2 * (size_t)p.items * 8;
@@ -106,6 +106,13 @@ __host__ K3Plan k3_plan_for(const Geom& g, int margin, int TH, int TW, int cspli
   at += 2 * (size_t)(p.npos + 1) * 4;
   p.off_cnt = at;  // [npos + 1] bucket counts (P only)
   at += (size_t)(p.npos + 1) * 4;
+  p.off_pix = at;  // [npos] window position -> pixel offset from the window's corner, wy * W + wx
+  at += (size_t)p.npos * 4;
+  at = (at + 15) / 16 * 16;
+  p.off_itab = at;  // [items] int4 {row, column of the tap in the window w/o margin, pixel row | col << 16, k | p << 16}
+  at += (size_t)p.items * 16;
+  p.off_otab = at;  // [M * npx] int2 {offset-map element from the tile's first, pixel row | col << 16}
+  at += (size_t)g.M * p.npx * 8;
   p.off_D = at;  // [2][items * 4] D_j(s) (S only)
   at += 2 * (size_t)p.items * 4 * 4;
   p.off_slow = at;  // [2][items + 1] samples read from global memory (count first)
@@ -113,6 +120,7 @@ __host__ K3Plan k3_plan_for(const Geom& g, int margin, int TH, int TW, int cspli
   at = (at + 15) / 16 * 16;
   p.off_oin = at;  // [2][M][npx] the tile's offsets (prefetched a tile ahead)
   at += 2 * (size_t)g.M * p.npx * 4;
+
   at = (at + 7) / 8 * 8;
   p.off_bar = at;  // wfull[2], wempty[2], tfull[2], tempty[2]
   at += 8 * 8;
@@ -348,6 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   int4* tap0 = reinterpret_cast<int4*>(smem + pl.off_tap);
   int2* syx0 = reinterpret_cast<int2*>(smem + pl.off_syx);
   int2* ent0 = reinterpret_cast<int2*>(smem + pl.off_ent);
+  int* pixoff = reinterpret_cast<int*>(smem + pl.off_pix);
+  const int4* itab = reinterpret_cast<const int4*>(smem + pl.off_itab);
+  const int2* otab = reinterpret_cast<const int2*>(smem + pl.off_otab);
   int* pst0 = reinterpret_cast<int*>(smem + pl.off_pst);
   int* cnt = reinterpret_cast<int*>(smem + pl.off_cnt);
   float* D0 = reinterpret_cast<float*>(smem + pl.off_D);
@@ -383,6 +394,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     px::fence_mbar_init();
   }
+  // tile-independent index tables (no divisions in the per-tile loops)
+  for (int q = tid; q < npos; q += kThreads) {
+    const int wy = q / pl.cols;
+    pixoff[q] = wy * g.w + (q - wy * pl.cols);
+  }
+  for (int it = tid; it < items; it += kThreads) {
+    const int p = it / K, k = it - p * K;
+    const int pr = p / pl.TW, pc = p - pr * pl.TW;
+    const int ki = k / g.kw, kj = k - ki * g.kw;
+    reinterpret_cast<int4*>(smem + pl.off_itab)[it] =
+        make_int4(pr * g.sh + ki * g.dh, pc * g.sw + kj * g.dw, pr | (pc << 16), k | (p << 16));
+  }
+  for (int e = tid; e < M * pl.npx; e += kThreads) {
+    const int m = e / pl.npx, p = e - m * pl.npx;
+    const int pr = p / pl.TW, pc = p - pr * pl.TW;
+    reinterpret_cast<int2*>(smem + pl.off_otab)[e] =
+        make_int2((int)((long long)m * g.howo + (long long)pr * g.wo + pc), pr | (pc << 16));
+  }
   __syncthreads();
   // x's NHWC copy, the offsets and gcol come from earlier kernels on the stream
   pdl_wait();
@@ -401,11 +430,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (t >= pl.tiles) return;
       const TileXY tq = tile_xy(t, pl, g, a.margin);
       float* dsto = oin + (size_t)buf * M * pl.npx;
+      const float* first = a.off + (long long)tq.n * M * g.howo + (long long)tq.ho0 * g.wo + tq.wo0;
       for (int e = tid; e < M * pl.npx; e += kPThreads) {
-        const int m = e / pl.npx, p = e - m * pl.npx;
-        const int ho = tq.ho0 + p / pl.TW, wo = tq.wo0 + p % pl.TW;
-        if (ho < g.ho && wo < g.wo) {
-          const float* src = a.off + ((long long)tq.n * M + m) * g.howo + (long long)ho * g.wo + wo;
+        const int2 ot = otab[e];
+        if (tq.ho0 + (ot.y & 0xffff) < g.ho && tq.wo0 + (ot.y >> 16) < g.wo) {
+          const float* src = first + ot.x;
           asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(px::smem_u32(dsto + e)), "l"(src)
                        : "memory");
         } else {
@@ -441,16 +470,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) pr[u][j] = ~0u;
         if (it >= items) continue;
-        const int p = it / K, k = it - p * K;
-        const int ho = tx.ho0 + p / pl.TW, wo = tx.wo0 + p % pl.TW;
+        const int4 ie = itab[it];
+        const int k = ie.w & 0xffff, p = ie.w >> 16;
         int4 tp = make_int4(0, 0, 0, 3);  // kind 3: pixel outside the output
-        if (ho < g.ho && wo < g.wo) {
-          const int ki = k / g.kw, kj = k - ki * g.kw;
-          const float by = (float)(ho * g.sh - g.ph + ki * g.dh);
-          const float bx = (float)(wo * g.sw - g.pw + kj * g.dw);
+        if (tx.ho0 + (ie.z & 0xffff) < g.ho && tx.wo0 + (ie.z >> 16) < g.wo) {
+          const float by = (float)(tx.ho0 * g.sh - g.ph + ie.x);
+          const float bx = (float)(tx.wo0 * g.sw - g.pw + ie.y);
           const float pyf = by + offs[(2 * k) * pl.npx + p];
           const float pxf = bx + offs[(2 * k + 1) * pl.npx + p];
-          tp.z = (ho * g.wo + wo) * K + k;
           tp.w = 1;  // kind 1: no corner touches the image
           if (touches_image(pyf, pxf, g.h, g.w)) {
             const float fy = floorf(pyf), fx = floorf(pxf);
@@ -536,6 +563,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // lane l holds channels cbeg + l * CPL .. + CPL - 1
     const int sw = warp - kPWarps;
     const int cl = lane * CPL;
+    // lanes in groups of L = cpc / 8, eight channels each
+    constexpr int L = CPL * 4;
+    constexpr int G = 32 / L;  // groups per warp
+    const int gl = lane & (L - 1);
+    const int gid = sw * G + (lane / L);
+
     const uint32_t row_bytes = (uint32_t)pl.cpc * 2u;
     for (int i = 0, t = t0; t < pl.tiles; ++i, t += tstep) {
       const int s = i & 1;
@@ -553,7 +586,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const unsigned char* xsm0 = smem + pl.off_stage + (size_t)s * stage_pitch;
       const unsigned char* gsm0 = smem + pl.off_gc + (size_t)s * gc_pitch;
       const unsigned char* gsm = gsm0 + cl * 2;
-      float* gximg0 = a.gx + (long long)tx.n * g.hw * C + cbeg;
       float* gximg = a.gx + (long long)tx.n * g.hw * C + cbeg + cl;
       for (int e = tid - kPThreads; e < items * 4; e += kSThreads) Dt[e] = 0.f;
       s_sync();
@@ -566,82 +598,109 @@ __global__ void __launch_bounds__(kThreads, 1)
       // with x at that position are kept; one transposing butterfly per batch
       // sums them over the group.
       {
-        constexpr int L = CPL * 4;  // lanes per group: eight channels each
-        constexpr int G = 32 / L;   // groups per warp
         constexpr int NB = 8;
-        const int gl = lane & (L - 1);                  // lane in the group
-        const int gid = sw * G + (lane / L);            // group in the CTA
-        const uint32_t gbit = (uint32_t)gl * 16u;       // this lane's 16 bytes of a row
         const uint32_t xo = (uint32_t)(gl >> 3) * pl.chunk_pitch;
         const uint32_t xp = (uint32_t)(gl & 7) << 4;
         const int E = pst[npos];
         const int ngroups = kSWarps * G;
         const int ebeg = (int)((long long)E * gid / ngroups);
         const int eend = (int)((long long)E * (gid + 1) / ngroups);
-        const int maxlen = (E + ngroups - 1) / ngroups;
-        const uint32_t gs = px::smem_u32(gsm0) + gbit;
+        const int minlen = E / ngroups, maxlen = (E + ngroups - 1) / ngroups;
+        const uint32_t gs = px::smem_u32(gsm0) + (uint32_t)gl * 16u;
         const uint32_t xs = px::smem_u32(xsm0) + xo;
-        float* gxl = gximg0 + gl * 8;
+        float* gxrow = a.gx + (((long long)tx.n * g.h + tx.ylo) * g.w + tx.xlo) * C + cbeg;
         int cur = -1;
         float2 xv[4], acc[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) xv[c] = acc[c] = make_float2(0.f, 0.f);
-        for (int b = 0; b < maxlen; b += NB) {
-          float dp[NB];
+        // the group's gradient at `pos` into the NHWC buffer (vector float atomics)
+        auto flush = [&](int pos) {
+          red_add<8>(gxrow + (long long)pixoff[pos] * C + gl * 8, reinterpret_cast<const float*>(acc));
+        };
+        // the sample's gcol slice of a pair
+        auto row = [&](const int2 en) {
+          uint4 gw;
+          asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+              : "=r"(gw.x), "=r"(gw.y), "=r"(gw.z), "=r"(gw.w)
+              : "r"(gs + (uint32_t)((en.x & 0xffff) >> 2) * row_bytes));
+          return gw;
+        };
+        // one pair: its gradient at the current position, its partial dot product
+        auto pair = [&](const int2 en, const uint4 gw, bool valid, float& dpj) {
+          const int pos = (int)((uint32_t)en.x >> 16);
+          if (valid && pos != cur) {
+            if (cur >= 0) flush(cur);
+            cur = pos;
+            uint4 xw;
+            asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                : "=r"(xw.x), "=r"(xw.y), "=r"(xw.z), "=r"(xw.w)
+                : "r"(xs + (line_off((uint32_t)cur) ^ xp)));
+            xv[0] = bf2(xw.x);
+            xv[1] = bf2(xw.y);
+            xv[2] = bf2(xw.z);
+            xv[3] = bf2(xw.w);
 #pragma unroll
-          for (int j = 0; j < NB; ++j) {
-            const int e = ebeg + b + j;
-            const bool valid = e < eend;
-            int2 en = make_int2(0, 0);
-            if (valid) en = ent[e];
-            const int pos = (int)((uint32_t)en.x >> 16);
-            const int it = (en.x & 0xffff) >> 2;
-            uint4 gw = make_uint4(0u, 0u, 0u, 0u);
-            if (valid)
-              asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                  : "=r"(gw.x), "=r"(gw.y), "=r"(gw.z), "=r"(gw.w)
-                  : "r"(gs + (uint32_t)it * row_bytes));
-            if (valid && pos != cur) {
-              if (cur >= 0) {
-                const int wy = cur / pl.cols, wx = cur - wy * pl.cols;
-                red_add<8>(gxl + ((long long)(tx.ylo + wy) * g.w + (tx.xlo + wx)) * C,
-                           reinterpret_cast<const float*>(acc));
-              }
-              cur = pos;
-              uint4 xw;
-              asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                  : "=r"(xw.x), "=r"(xw.y), "=r"(xw.z), "=r"(xw.w)
-                  : "r"(xs + (line_off((uint32_t)cur) ^ xp)));
-              xv[0] = bf2(xw.x);
-              xv[1] = bf2(xw.y);
-              xv[2] = bf2(xw.z);
-              xv[3] = bf2(xw.w);
-#pragma unroll
-              for (int c = 0; c < 4; ++c) acc[c] = make_float2(0.f, 0.f);
-            }
-            const float w = valid ? __int_as_float(en.y) : 0.f;
-            const float2 w2 = make_float2(w, w);
-            const float2 g0 = bf2(gw.x), g1 = bf2(gw.y), g2 = bf2(gw.z), g3 = bf2(gw.w);
-            acc[0] = ffma2(w2, g0, acc[0]);
-            acc[1] = ffma2(w2, g1, acc[1]);
-            acc[2] = ffma2(w2, g2, acc[2]);
-            acc[3] = ffma2(w2, g3, acc[3]);
-            float2 d2 = ffma2(g0, xv[0], make_float2(0.f, 0.f));
-            d2 = ffma2(g1, xv[1], d2);
-            d2 = ffma2(g2, xv[2], d2);
-            d2 = ffma2(g3, xv[3], d2);
-            dp[j] = d2.x + d2.y;
+            for (int c = 0; c < 4; ++c) acc[c] = make_float2(0.f, 0.f);
           }
+          const float w = __int_as_float(en.y);
+          const float2 w2 = make_float2(w, w);
+          const float2 g0 = bf2(gw.x), g1 = bf2(gw.y), g2 = bf2(gw.z), g3 = bf2(gw.w);
+          acc[0] = ffma2(w2, g0, acc[0]);
+          acc[1] = ffma2(w2, g1, acc[1]);
+          acc[2] = ffma2(w2, g2, acc[2]);
+          acc[3] = ffma2(w2, g3, acc[3]);
+          float2 d2 = ffma2(g0, xv[0], make_float2(0.f, 0.f));
+          d2 = ffma2(g1, xv[1], d2);
+          d2 = ffma2(g2, xv[2], d2);
+          d2 = ffma2(g3, xv[3], d2);
+          dpj = d2.x + d2.y;
+        };
+        // the batch's dot products summed over the group, to the D table
+        auto finish = [&](float* dp, int b) {
           const float dsum = group_sum_transpose8<L>(dp, lane);
           constexpr int kSh = L == 8 ? 0 : (L == 16 ? 1 : 2);
           const int e = ebeg + b + (gl >> kSh);
           if ((gl & ((1 << kSh) - 1)) == 0 && e < eend) Dt[ent[e].x & 0xffff] = dsum;
+        };
+        // full batches (every group has NB pairs left), software-pipelined:
+        // the next batch's pairs load while this one computes; then one
+        // checked tail
+        const int fullb = minlen / NB * NB;
+        int2 enn[NB];
+        if (fullb > 0) {
+#pragma unroll
+          for (int j = 0; j < NB; ++j) enn[j] = ent[ebeg + j];
         }
-        if (cur >= 0) {
-          const int wy = cur / pl.cols, wx = cur - wy * pl.cols;
-          red_add<8>(gxl + ((long long)(tx.ylo + wy) * g.w + (tx.xlo + wx)) * C,
-                     reinterpret_cast<const float*>(acc));
+        for (int b = 0; b < fullb; b += NB) {
+          int2 en[NB];
+          uint4 gw[NB];
+#pragma unroll
+          for (int j = 0; j < NB; ++j) {
+            en[j] = enn[j];
+            gw[j] = row(en[j]);
+          }
+          if (b + NB < fullb) {
+#pragma unroll
+            for (int j = 0; j < NB; ++j) enn[j] = ent[ebeg + b + NB + j];
+          }
+          float dp[NB];
+#pragma unroll
+          for (int j = 0; j < NB; ++j) pair(en[j], gw[j], true, dp[j]);
+          finish(dp, b);
         }
+        if (fullb < maxlen) {
+          float dp[NB];
+#pragma unroll
+          for (int j = 0; j < NB; ++j) {
+            const int e = ebeg + fullb + j;
+            const bool valid = e < eend;
+            const int2 en = valid ? ent[e] : make_int2(0, 0);
+            const uint4 gw = valid ? row(en) : make_uint4(0u, 0u, 0u, 0u);
+            pair(en, gw, valid, dp[j]);
+          }
+          finish(dp, fullb);
+        }
+        if (cur >= 0) flush(cur);
       }
       // ---------------------------------------------- samples outside the window
       const int nslow = slow[0];
@@ -692,8 +751,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float d00 = Dt[it * 4], d01 = Dt[it * 4 + 1], d10 = Dt[it * 4 + 2], d11 = Dt[it * 4 + 3];
         const float gy = __fmaf_rn(1.0f - lx, d10 - d00, lx * (d11 - d01));
         const float gxo = __fmaf_rn(1.0f - ly, d01 - d00, ly * (d11 - d10));
-        const int p = it / K, k = it - p * K;
-        const long long pix = (long long)(tx.ho0 + p / pl.TW) * g.wo + (tx.wo0 + p % pl.TW);
+        const int4 ie = itab[it];
+        const int k = ie.w & 0xffff;
+        const long long pix = (long long)(tx.ho0 + (ie.z & 0xffff)) * g.wo + (tx.wo0 + (ie.z >> 16));
         atomicAdd(a.goff + ((long long)tx.n * M + 2 * k) * g.howo + pix, gy);
         atomicAdd(a.goff + ((long long)tx.n * M + 2 * k + 1) * g.howo + pix, gxo);
       }
@@ -766,6 +826,7 @@ int sm_count3() {
 
 bool k3cl_supported(const Geom& g, dc_dtype dt, int margin) {
   if (!cl_supported(g, dt, margin) || g.groups != 1) return false;
+  if ((long long)g.M * g.howo >= INT_MAX) return false;  // offset-map index table is 32-bit
   const int sms = sm_count3();
   if (sms <= 0) return false;
   return k3_make_plan(g, margin, sms).npx != 0;
