@@ -131,8 +131,9 @@ dc_status make_geom(const dc_problem* p, Geom* g, int* margin) {
 struct Plan {
   bool cl;
   bool k3cl;  // channels-last sampling backward (pixel-major gcol, NHWC grad_x accumulator)
+  bool k4cl;  // channels-last offset-convolution backward (writes grad_x from that accumulator)
   ColLayout col, gcol;
-  size_t col_off, gcol_off, off_off, gmax_off, gwo_img_off, xc_off, wp_off, wfrag_off, gxc_off,
+  size_t col_off, gcol_off, off_off, gmax_off, gwo_img_off, xc_off, wp_off, wfrag_off, gxc_off, k4part_off,
       total;
   int gmax_tx, gmax_ty;
 };
@@ -141,6 +142,7 @@ Plan make_plan(const Geom& g, dc_dtype dt, int backward, int margin) {
   Plan pl{};
   pl.cl = cl_supported(g, dt, margin);
   pl.k3cl = backward && pl.cl && k3cl_supported(g, dt, margin);
+  pl.k4cl = pl.k3cl && k4cl_supported(g);
   const long long pitch = round_up(g.howo, 8);
   pl.col.img = pitch;
   pl.col.row = pitch * g.n;
@@ -170,7 +172,8 @@ Plan make_plan(const Geom& g, dc_dtype dt, int backward, int margin) {
   // (one image's bands add into one copy: far fewer atomics per address), in
   // the kernel's accumulator order
   pl.gxc_off = pl.k3cl ? take((size_t)g.n * g.hw * g.c_in * sizeof(float)) : 0;
-  pl.gwo_img_off = backward && offconv_bwd_tc_supported(g, dt)
+  pl.k4part_off = pl.k4cl ? take(k4cl_part_bytes(g)) : 0;
+  pl.gwo_img_off = backward && !pl.k4cl && offconv_bwd_tc_supported(g, dt)
                        ? take((size_t)g.n * gwo_frag_count(g.M, g.c_in, g.K) * sizeof(float))
                        : 0;
   pl.total = at;
@@ -307,6 +310,29 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
     ka.margin = margin;
     st = cuda_status(timed("k3_cl_bwd", s, [&] { return launch_k3cl(ka, s); }));
     if (st != DC_OK) return st;
+    if (pl.k4cl) {
+      // offset-convolution backward: the weight part's chunk partials (it
+      // also lays out w_off for the input part), then grad_x (NCHW) written
+      // whole from the NHWC accumulator plus the input part; the partials
+      // are summed after the weight-gradient GEMM
+      K4ClArgs k4{};
+      k4.g = g;
+      k4.xc = wsb + pl.xc_off;
+      k4.w_off = w_off;
+      k4.goff = goff;
+      k4.gx_nhwc = gxc;
+      k4.grad_x = grad_x;
+      k4.grad_w_off = grad_w_off;
+      k4.grad_b_off = grad_b_off;
+      k4.part = reinterpret_cast<float*>(wsb + pl.k4part_off);
+      st = cuda_status(timed("k4cl_weight", s, [&] { return launch_k4cl_weight(k4, s); }));
+      if (st != DC_OK) return st;
+      st = cuda_status(timed("k4cl_input", s, [&] { return launch_k4cl_input(k4, s); }));
+      if (st != DC_OK) return st;
+      st = cuda_status(timed("gemm_gw", s, [&] { return launch_gemm_gw_cl(ga, s); }));
+      if (st != DC_OK) return st;
+      return cuda_status(timed("k4cl_reduce", s, [&] { return launch_k4cl_reduce(k4, s); }));
+    }
     st = cuda_status(timed("gx_to_nchw", s, [&] { return launch_gx_to_nchw(gxc, grad_x, g, s); }));
     if (st != DC_OK) return st;
   }

@@ -297,6 +297,28 @@ struct K3ClArgs {
 cudaError_t launch_k3cl(const K3ClArgs& a, cudaStream_t s);
 cudaError_t launch_gx_to_nchw(const float* gx_nhwc, float* grad_x, const Geom& g, cudaStream_t s);
 unsigned int cl3_read_error(int clear);
+// Backward of the offset convolution on the channels-last path (one offset
+// group, K <= 9 taps): the input part adds into the NHWC grad_x buffer's
+// values and writes grad_x (NCHW) whole; the weight part writes per-chunk
+// partial sums into `part` (k4cl_part_bytes), which the reduce kernel adds
+// into grad_w_off and grad_b_off (overwritten).
+bool k4cl_supported(const Geom& g);
+size_t k4cl_part_bytes(const Geom& g);
+struct K4ClArgs {
+  Geom g;
+  const void* xc;       // x, NHWC bf16
+  const void* w_off;    // [M][C_in][K] bf16
+  const float* goff;    // [n][M][Ho][Wo]
+  const float* gx_nhwc; // the sampling backward's grad_x, NHWC float32
+  float* grad_x;        // [n][C_in][H][W]
+  float* grad_w_off;    // [M][C_in][K]
+  float* grad_b_off;    // [M] or null
+  float* part;          // workspace, k4cl_part_bytes
+};
+cudaError_t launch_k4cl_input(const K4ClArgs& a, cudaStream_t s);
+cudaError_t launch_k4cl_weight(const K4ClArgs& a, cudaStream_t s);
+cudaError_t launch_k4cl_reduce(const K4ClArgs& a, cudaStream_t s);
+unsigned int k4cl_read_error(int clear);
 bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const unsigned long long* dims,
                     const unsigned long long* strides_bytes, const unsigned int* box,
                     bool swizzle128);

@@ -23,15 +23,16 @@
 //                (sample, corner) pair that lands in the window and in the
 //                image, bucketed by window position (counts and ranks from
 //                shared-memory atomics, a scan, a scatter);
-//   S warps (12) per tile: the bucketed pairs are split evenly over the
-//                warps, lanes over the CTA's channels (2, 4 or 8 each), and
-//                walked in batches of 16: per pair, the sample's gcol slice
-//                from shared memory, w * gcol accumulated in registers for the
-//                current position (added to a float32 NHWC buffer with
-//                vector float atomics when the position changes) and the
-//                lanes' partial dot products with x at that position, which
-//                one transposing butterfly per batch sums over the warp
-//                (D_j(s)); then per sample its offset gradient from its four
+//   S warps (12) per tile: lanes in groups of cpc / 8 (eight channels
+//                each); the bucketed pairs are split evenly over the groups
+//                and walked in batches of 8: per pair, the sample's gcol
+//                slice from shared memory, w * gcol accumulated in registers
+//                (packed fp32 FMAs) for the current position (added to a
+//                float32 NHWC buffer with vector float atomics when the
+//                position changes) and the lanes' partial dot products with x
+//                at that position, which one transposing butterfly per batch
+//                sums over the group (D_j(s)); then per sample its offset
+//                gradient from its four
 //                D_j, added with float atomics (the CTAs of a tile each hold
 //                a slice of the channels).  Samples whose corners leave the
 //                window read x from global memory and add their corners'
@@ -120,7 +121,6 @@ __host__ K3Plan k3_plan_for(const Geom& g, int margin, int TH, int TW, int cspli
   at = (at + 15) / 16 * 16;
   p.off_oin = at;  // [2][M][npx] the tile's offsets (prefetched a tile ahead)
   at += 2 * (size_t)g.M * p.npx * 4;
-
   at = (at + 7) / 8 * 8;
   p.off_bar = at;  // wfull[2], wempty[2], tfull[2], tempty[2]
   at += 8 * 8;
