@@ -65,6 +65,9 @@ struct TcArgs {
   long long gwo_count;         // floats per image
   int gwo_nimg, gwo_m, gwo_cin, gwo_k;  // images; M, C_in, K of the partials' order
   int cin, ktaps;              // GWC: C_in and taps, to map columns (tap, c) to grad_w[o][c][tap]
+  // the tile grid (x: column tiles, y: row tiles, z: images or splits); a
+  // persistent launch runs tiles blockIdx.x, + gridDim.x, ... of it
+  int vgx, vgy, vgz, persistent;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -210,54 +213,87 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-template <int KIND, int BN>
+// MH = 2: one CTA computes 256 rows of the output (two M = 128 halves, two
+// accumulators side by side in tensor memory) against one B tile, so the
+// large B operand (the deformed map) is read once instead of once per half.
+template <int KIND, int BN, int MH = 1>
 struct Cfg {
-  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kAHalf = kBM * kBK * 2;
+  static constexpr int kABytes = MH * kAHalf;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStage = kABytes + kBBytes;
   // GCOL reduces over C_out only (a few k-blocks): two stages, so that three
   // CTAs fit on an SM; the long reductions keep a deeper ring.
   // GCOL has two k-blocks; four stages let two FWD CTAs share an SM
   static constexpr int kStages = is_gcol(KIND) ? 2 : 4;
-  static constexpr int kTmemCols = BN < 32 ? 32 : BN;
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + 256;
+  // two accumulators (the epilogue of one tile overlaps the next tile's MMAs)
+  static constexpr int kTmemCols = 2 * MH * BN < 32 ? 32 : 2 * MH * BN;
+  // GCOL's bf16 store staging: 4 warps x BN/64 boxes of 32 x 64
+  static constexpr int kStg = is_gcol(KIND) ? 4 * (BN / 64) * 4096 : 0;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + kStg + 256;
   static constexpr int kAMn = is_gcol(KIND) ? 1 : 0;
   static constexpr int kBMn = (KIND == GW || KIND == FWDC) ? 0 : 1;
 };
 
-template <int KIND, int BN>
+template <int KIND, int BN, int MH = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, TcArgs a) {
-  using C = Cfg<KIND, BN>;
+  using C = Cfg<KIND, BN, MH>;
+  static_assert(MH == 1 || KIND == FWDC || KIND == GWC, "two M halves: forward and weight-gradient kinds");
+  constexpr uint32_t kAcc = MH * BN;  // tensor-memory columns of one accumulator
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStage);
+  unsigned char* stg = smem + C::kStages * C::kStage;  // GCOL store staging
+  uint64_t* full = reinterpret_cast<uint64_t*>(stg + C::kStg);
   uint64_t* empty = full + C::kStages;
-  uint64_t* done = empty + C::kStages;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* tfull = empty + C::kStages;  // accumulator b complete (MMA -> epilogue)
+  uint64_t* tempty = tfull + 2;          // accumulator b drained (epilogue -> MMA)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // FWD split over a 2-CTA cluster: rank 0 takes the first half of the
   // k-blocks, rank 1 the second; rank 1 hands its fp32 tile to rank 0 through
-  // distributed shared memory and rank 0 writes y
+  // distributed shared memory and rank 0 writes y (one tile per CTA)
   const bool split = is_fwd(KIND) && a.fwd_split == 2;
   const int rank = split ? (int)(blockIdx.y & 1) : 0;
-  const int m0 = (split ? (int)(blockIdx.y >> 1) : (int)blockIdx.y) * kBM, n0 = blockIdx.x * BN;
-  const int z = blockIdx.z;
-  int kb_begin = 0, kb_end = a.kb_total;
-  if (is_gw(KIND)) {
-    kb_begin = z * a.kb_per_split;
-    kb_end = min(a.kb_total, kb_begin + a.kb_per_split);
-  }
-  if (split) {
-    const int half = (a.kb_total + 1) / 2;
-    kb_begin = rank ? half : 0;
-    kb_end = rank ? a.kb_total : half;
-  }
-  bool ok = true;  // epilogue warps: the MMAs completed (no wait expired)
-  const int nkb = kb_end > kb_begin ? kb_end - kb_begin : 0;
+  const int ntiles =
+      a.persistent ? (a.vgx * a.vgy * a.vgz - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 1;
+  struct Tile {
+    int bx, by, m0, n0, z, kb_begin, nkb;
+  };
+  // this CTA's j-th tile
+  auto tile = [&](int j) {
+    Tile T;
+    if (a.persistent) {
+      const int t = (int)blockIdx.x + j * (int)gridDim.x;
+      T.bx = t % a.vgx;
+      const int r = t / a.vgx;
+      T.by = r % a.vgy;
+      T.z = r / a.vgy;
+    } else {
+      T.bx = blockIdx.x;
+      T.by = blockIdx.y;
+      T.z = blockIdx.z;
+    }
+    T.m0 = (split ? (T.by >> 1) : T.by) * kBM * MH;
+    T.n0 = T.bx * BN;
+    int kb_begin = 0, kb_end = a.kb_total;
+    if (is_gw(KIND)) {
+      kb_begin = T.z * a.kb_per_split;
+      kb_end = min(a.kb_total, kb_begin + a.kb_per_split);
+    }
+    if (split) {
+      const int half = (a.kb_total + 1) / 2;
+      kb_begin = rank ? half : 0;
+      kb_end = rank ? a.kb_total : half;
+    }
+    T.kb_begin = kb_begin;
+    T.nkb = kb_end > kb_begin ? kb_end - kb_begin : 0;
+    return T;
+  };
+  bool ok = true;  // no wait expired
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -271,7 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);  // one arrival per epilogue warp
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -290,42 +329,52 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 4) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % C::kStages;
-        if (i >= C::kStages && !mbar_wait(&empty[s], ((i / C::kStages) - 1) & 1)) break;
-        unsigned char* sa = smem + s * C::kStage;
-        unsigned char* sb = sa + C::kABytes;
-        mbar_expect_tx(&full[s], C::kStage);
-        const int kb = kb_begin + i;
-        if (KIND == FWD) {
-          tma_2d(sa, &tmA, &full[s], kb * kBK, m0);
+      int it = 0;  // k-blocks issued so far (all tiles): ring slot and phase
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const Tile T = tile(j);
+        const int m0 = T.m0, n0 = T.n0, z = T.z;
+        for (int i = 0; i < T.nkb; ++i, ++it) {
+          const int s = it % C::kStages;
+          if (it >= C::kStages && !mbar_wait(&empty[s], ((it / C::kStages) - 1) & 1)) {
+            ok = false;
+            break;
+          }
+          unsigned char* sa = smem + s * C::kStage;
+          unsigned char* sb = sa + C::kABytes;
+          mbar_expect_tx(&full[s], C::kStage);
+          const int kb = T.kb_begin + i;
+          if (KIND == FWD) {
+            tma_2d(sa, &tmA, &full[s], kb * kBK, m0);
 #pragma unroll
-          for (int h = 0; h < BN / 64; ++h) tma_3d(sb + h * 8192, &tmB, &full[s], n0 + 64 * h, z, kb * kBK);
-        } else if (KIND == FWDC) {
-          // A: w' rows m0.., k-block kb; B: BN pixels of image z, k-block kb
-          tma_2d(sa, &tmA, &full[s], kb * kBK, m0);
-          tma_3d(sb, &tmB, &full[s], kb * kBK, n0, z);
-        } else if (KIND == GCOLC) {
-          // A: grad_y rows kb*64.. (output channels) x 128 pixels of image z,
-          // as two 64-pixel MN chunks; B: w' rows kb*64.. x BN columns
-          tma_3d(sa, &tmA, &full[s], m0, kb * kBK, z);
-          tma_3d(sa + 8192, &tmA, &full[s], m0 + 64, kb * kBK, z);
+            for (int h = 0; h < BN / 64; ++h) tma_3d(sb + h * 8192, &tmB, &full[s], n0 + 64 * h, z, kb * kBK);
+          } else if (KIND == FWDC) {
+            // A: w' rows m0.. (and m0 + 128..), k-block kb; B: BN pixels of image z, k-block kb
+            tma_2d(sa, &tmA, &full[s], kb * kBK, m0);
+            if (MH == 2) tma_2d(sa + C::kAHalf, &tmA, &full[s], kb * kBK, m0 + kBM);
+            tma_3d(sb, &tmB, &full[s], kb * kBK, n0, z);
+          } else if (KIND == GCOLC) {
+            // A: grad_y rows kb*64.. (output channels) x 128 pixels of image z,
+            // as two 64-pixel MN chunks; B: w' rows kb*64.. x BN columns
+            tma_3d(sa, &tmA, &full[s], m0, kb * kBK, z);
+            tma_3d(sa + 8192, &tmA, &full[s], m0 + 64, kb * kBK, z);
 #pragma unroll
-          for (int h = 0; h < BN / 64; ++h) tma_2d(sb + h * 8192, &tmB, &full[s], n0 + 64 * h, kb * kBK);
-        } else if (KIND == GWC) {
-          const int img = kb / a.qblocks, q0 = (kb - img * a.qblocks) * kBK;
-          tma_3d(sa, &tmA, &full[s], q0, m0, img);
+            for (int h = 0; h < BN / 64; ++h) tma_2d(sb + h * 8192, &tmB, &full[s], n0 + 64 * h, kb * kBK);
+          } else if (KIND == GWC) {
+            const int img = kb / a.qblocks, q0 = (kb - img * a.qblocks) * kBK;
+            tma_3d(sa, &tmA, &full[s], q0, m0, img);
+            if (MH == 2) tma_3d(sa + C::kAHalf, &tmA, &full[s], q0, m0 + kBM, img);
 #pragma unroll
-          for (int h = 0; h < BN / 64; ++h) tma_3d(sb + h * 8192, &tmB, &full[s], n0 + 64 * h, q0, img);
-        } else if (KIND == GCOL) {
-          tma_2d(sa, &tmA, &full[s], m0, kb * kBK);
-          tma_2d(sa + 8192, &tmA, &full[s], m0 + 64, kb * kBK);
+            for (int h = 0; h < BN / 64; ++h) tma_3d(sb + h * 8192, &tmB, &full[s], n0 + 64 * h, q0, img);
+          } else if (KIND == GCOL) {
+            tma_2d(sa, &tmA, &full[s], m0, kb * kBK);
+            tma_2d(sa + 8192, &tmA, &full[s], m0 + 64, kb * kBK);
 #pragma unroll
-          for (int h = 0; h < BN / 64; ++h) tma_3d(sb + h * 8192, &tmB, &full[s], n0 + 64 * h, kb * kBK, z);
-        } else {
-          const int img = kb / a.qblocks, q0 = (kb - img * a.qblocks) * kBK;
-          tma_3d(sa, &tmA, &full[s], q0, m0, img);
-          tma_3d(sb, &tmB, &full[s], q0, img, n0);
+            for (int h = 0; h < BN / 64; ++h) tma_3d(sb + h * 8192, &tmB, &full[s], n0 + 64 * h, kb * kBK, z);
+          } else {
+            const int img = kb / a.qblocks, q0 = (kb - img * a.qblocks) * kBK;
+            tma_3d(sa, &tmA, &full[s], q0, m0, img);
+            tma_3d(sb, &tmB, &full[s], q0, img, n0);
+          }
         }
       }
     }
@@ -334,142 +383,181 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t idesc = idesc_bf16(BN, C::kAMn, C::kBMn);
-      for (int i = 0; i < nkb; ++i) {
-        const int s = i % C::kStages;
-        if (!mbar_wait(&full[s], (i / C::kStages) & 1)) break;
-        tc_fence_after();
-        const uint32_t sa = smem_u32(smem + s * C::kStage);
-        const uint32_t sb = sa + C::kABytes;
-#pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          // K-major: step 32 bytes inside the 128-byte swizzled row;
-          // MN-major: step 16 k-rows = two 1024-byte swizzle atoms
-          const uint64_t da = C::kAMn ? sdesc(sa + kk * 2048, 8192, 1024) : sdesc(sa + kk * 32, 16, 1024);
-          const uint64_t db = C::kBMn ? sdesc(sb + kk * 2048, 8192, 1024) : sdesc(sb + kk * 32, 16, 1024);
-          umma(tmem, da, db, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+      int it = 0;
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const Tile T = tile(j);
+        const int b = j & 1;
+        // accumulator b was drained by the epilogue (its use two tiles ago)
+        if (j >= 2 && !mbar_wait(&tempty[b], ((j >> 1) - 1) & 1)) {
+          ok = false;
+          break;
         }
-        umma_commit(&empty[s]);
+        tc_fence_after();
+        const uint32_t acc = tmem + (uint32_t)b * kAcc;
+        for (int i = 0; i < T.nkb; ++i, ++it) {
+          const int s = it % C::kStages;
+          if (!mbar_wait(&full[s], (it / C::kStages) & 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + s * C::kStage);
+          const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // K-major: step 32 bytes inside the 128-byte swizzled row;
+            // MN-major: step 16 k-rows = two 1024-byte swizzle atoms
+            const uint64_t db = C::kBMn ? sdesc(sb + kk * 2048, 8192, 1024) : sdesc(sb + kk * 32, 16, 1024);
+#pragma unroll
+            for (int h = 0; h < MH; ++h) {
+              const uint32_t sah = sa + h * C::kAHalf;
+              const uint64_t da = C::kAMn ? sdesc(sah + kk * 2048, 8192, 1024) : sdesc(sah + kk * 32, 16, 1024);
+              umma(acc + h * BN, da, db, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          umma_commit(&empty[s]);
+        }
+        umma_commit(&tfull[b]);  // arrives once the tile's MMAs are complete
       }
-      umma_commit(done);
     }
     pdl_release();
   } else {
     // -------------------------------------------------------------- epilogue (warps 0-3)
     if (is_gcol(KIND)) {
-      // while the tensor cores work, clear this CTA's share of the buffers the
-      // rest of the backward pass accumulates into with atomics
+      // before the first accumulator is ready, clear this CTA's share of the
+      // buffers the rest of the backward pass accumulates into with atomics
       const long long nparts = (long long)gridDim.x * gridDim.y * gridDim.z;
       const long long part = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * blockIdx.z);
       zero_share(a.zero, part, nparts, threadIdx.x, 128);
     }
-    ok = __all_sync(0xffffffffu, mbar_wait(done, 0));
-    tc_fence_after();
-    pdl_release();
     const int row = warp * 32 + lane;
-    const int m = m0 + row;
-    const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16);
-    // GCOL: bits of the largest |value| this thread stores; as integers the
-    // magnitudes order like the floats, and inf / NaN sort above every finite value
-    uint32_t amax = 0u;
+    for (int j = 0; j < ntiles; ++j) {
+      const Tile T = tile(j);
+      const int m0 = T.m0, n0 = T.n0, z = T.z, nkb = T.nkb;
+      const int b = j & 1;
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&tfull[b], (j >> 1) & 1));
+      if (!ok) break;
+      tc_fence_after();
+      if (is_gcol(KIND)) {
+        // the staging buffers' previous TMA stores have read them
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+        __syncwarp();
+      }
+      // GCOL: bits of the largest |value| this thread stores; as integers the
+      // magnitudes order like the floats, and inf / NaN sort above every finite value
+      uint32_t amax = 0u;
 #pragma unroll 1
-    for (int c = 0; c < BN / 32; ++c) {
-      uint32_t r[32];
-      tmem_ld32(tbase + c * 32, r);
-      if (!ok || nkb == 0) continue;
-      const int n_first = n0 + c * 32;
-      if (is_fwd(KIND) && split) {
-        // rank 1: its partial tile to its own shared memory, column-major
-        // (lanes write consecutive words); rank 0 combines after the cluster
-        // barrier below
-        if (rank == 1) {
-          float* part = reinterpret_cast<float*>(smem);
+      for (int hc = 0; hc < MH * (BN / 32); ++hc) {
+        // half h (rows m0 + 128 h ..) of the output, its column chunk c
+        const int h = hc / (BN / 32), c = hc - h * (BN / 32);
+        const int m = m0 + h * kBM + row;
+        const uint32_t tbase = tmem + (uint32_t)b * kAcc + (uint32_t)(h * BN) + ((uint32_t)(warp * 32) << 16);
+        uint32_t r[32];
+        tmem_ld32(tbase + c * 32, r);
+        if (nkb == 0) continue;
+        const int n_first = n0 + c * 32;
+        if (is_fwd(KIND) && split) {
+          // rank 1: its partial tile to its own shared memory, column-major
+          // (lanes write consecutive words); rank 0 combines after the cluster
+          // barrier below
+          if (rank == 1) {
+            float* part = reinterpret_cast<float*>(smem);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) part[(c * 32 + j) * kBM + row] = __uint_as_float(r[j]);
-        }
-      } else if (is_fwd(KIND)) {
-        if (m >= a.c_out) continue;
-        store_y_row(static_cast<__nv_bfloat16*>(a.out) + ((long long)z * a.c_out + m) * a.howo + n_first,
-                    r, n_first, a.howo);
-      } else if (is_gcol(KIND)) {
-        // gcol leaves as bf16: this warp's 32 rows x 64 columns go through
-        // shared memory (the operand stages are free once `done` fired) in the
-        // 128-byte swizzled layout of the store map, one TMA store per two
-        // 32-column chunks; rows and columns beyond the tensor are clipped by
-        // the TMA unit.  The magnitude bound is taken before rounding.
-        if (KIND == GCOL && m < a.kdim) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (n_first + j < a.howo) amax = max(amax, r[j] & 0x7fffffffu);
-        }
-        unsigned char* buf = smem + (warp * (BN / 64) + (c >> 1)) * 4096;
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint4 pk;
-          uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[v * 8 + 2 * e]),
-                                                      __uint_as_float(r[v * 8 + 2 * e + 1]));
-            pw[e] = *reinterpret_cast<uint32_t*>(&b2);
+            for (int jj = 0; jj < 32; ++jj) part[(c * 32 + jj) * kBM + row] = __uint_as_float(r[jj]);
           }
-          const int piece = (c & 1) * 4 + v;  // 16-byte piece of the 128-byte row
-          *reinterpret_cast<uint4*>(buf + lane * 128 + ((piece ^ (lane & 7)) << 4)) = pk;
-        }
-        if (c & 1) {
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          const int box_n = n0 + (c >> 1) * 64;
-          if (KIND == GCOL && lane == 0 && m0 + warp * 32 < a.kdim && box_n < a.howo) {
-            tma_store_3d(&tmC, buf, box_n, z, m0 + warp * 32);
-            tma_store_commit();
-          }
-          // pixel-major: rows are pixels, columns (tap, channel)
-          if (KIND == GCOLC && lane == 0 && m0 + warp * 32 < a.howo && box_n < a.kdim) {
-            tma_store_3d(&tmC, buf, box_n, m0 + warp * 32, z);
-            tma_store_commit();
-          }
-        }
-      } else if (KIND == GWC) {
-        if (m >= a.c_out) continue;
-        // column r = tap * C + c of w' is grad_w[m][c][tap]
-        float* dst = static_cast<float*>(a.out) + (long long)m * a.kdim;
-        int tap = n_first / a.cin, c = n_first - tap * a.cin;
+        } else if (is_fwd(KIND)) {
+          if (m >= a.c_out) continue;
+          store_y_row(static_cast<__nv_bfloat16*>(a.out) + ((long long)z * a.c_out + m) * a.howo + n_first,
+                      r, n_first, a.howo);
+        } else if (is_gcol(KIND)) {
+          // gcol leaves as bf16: this warp's 32 rows x 64 columns go through
+          // its staging buffer in the 128-byte swizzled layout of the store
+          // map, one TMA store per two 32-column chunks; rows and columns
+          // beyond the tensor are clipped by the TMA unit.  The magnitude
+          // bound is taken before rounding.
+          if (KIND == GCOL && m < a.kdim) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (n_first + j < a.kdim) atomicAdd(dst + (long long)c * a.ktaps + tap, __uint_as_float(r[j]));
-          if (++c == a.cin) {
-            c = 0;
-            ++tap;
+            for (int jj = 0; jj < 32; ++jj)
+              if (n_first + jj < a.howo) amax = max(amax, r[jj] & 0x7fffffffu);
           }
-        }
-      } else {
-        if (m >= a.c_out) continue;
-        float* dst = static_cast<float*>(a.out) + (long long)m * a.kdim + n_first;
-        if (n_first + 32 <= a.kdim) {
+          unsigned char* buf = stg + (warp * (BN / 64) + (c >> 1)) * 4096;
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            atomicAdd(reinterpret_cast<float4*>(dst + v * 4),
-                      make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                  __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+          for (int v = 0; v < 4; ++v) {
+            uint4 pk;
+            uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(r[v * 8 + 2 * e]),
+                                                        __uint_as_float(r[v * 8 + 2 * e + 1]));
+              pw[e] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+            const int piece = (c & 1) * 4 + v;  // 16-byte piece of the 128-byte row
+            *reinterpret_cast<uint4*>(buf + lane * 128 + ((piece ^ (lane & 7)) << 4)) = pk;
+          }
+          if (c & 1) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            const int box_n = n0 + (c >> 1) * 64;
+            if (KIND == GCOL && lane == 0 && m0 + warp * 32 < a.kdim && box_n < a.howo) {
+              tma_store_3d(&tmC, buf, box_n, z, m0 + warp * 32);
+              tma_store_commit();
+            }
+            // pixel-major: rows are pixels, columns (tap, channel)
+            if (KIND == GCOLC && lane == 0 && m0 + warp * 32 < a.howo && box_n < a.kdim) {
+              tma_store_3d(&tmC, buf, box_n, m0 + warp * 32, z);
+              tma_store_commit();
+            }
+          }
+        } else if (KIND == GWC) {
+          if (m >= a.c_out) continue;
+          // column r = tap * C + c of w' is grad_w[m][c][tap]
+          float* dst = static_cast<float*>(a.out) + (long long)m * a.kdim;
+          int tap = n_first / a.cin, cc = n_first - tap * a.cin;
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            if (n_first + jj < a.kdim) atomicAdd(dst + (long long)cc * a.ktaps + tap, __uint_as_float(r[jj]));
+            if (++cc == a.cin) {
+              cc = 0;
+              ++tap;
+            }
+          }
         } else {
+          if (m >= a.c_out) continue;
+          float* dst = static_cast<float*>(a.out) + (long long)m * a.kdim + n_first;
+          if (n_first + 32 <= a.kdim) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (n_first + j < a.kdim) atomicAdd(dst + j, __uint_as_float(r[j]));
+            for (int v = 0; v < 8; ++v)
+              atomicAdd(reinterpret_cast<float4*>(dst + v * 4),
+                        make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3])));
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+              if (n_first + jj < a.kdim) atomicAdd(dst + jj, __uint_as_float(r[jj]));
+          }
         }
+      }
+      // accumulator b is free for the tile after next (the split forward
+      // reads its only tile once more below; it has no next tile)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[b]);
+      if (KIND == GCOL && a.gmax) {
+        for (int o = 16; o > 0; o >>= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const long long t = T.bx + (long long)a.vgx * (T.by + (long long)a.vgy * z);
+        if (lane == 0) a.gmax[t * 4 + warp] = __uint_as_float(amax);
       }
     }
     if (is_gcol(KIND) && lane == 0) tma_store_wait_all();  // gcol written before exit
-    if (KIND == GCOL && a.gmax) {
-      for (int o = 16; o > 0; o >>= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-      const long long tile = blockIdx.x + (long long)gridDim.x * (blockIdx.y + (long long)gridDim.y * z);
-      if (lane == 0) a.gmax[tile * 4 + warp] = __uint_as_float(amax);
-    }
+    pdl_release();
   }
   if (is_fwd(KIND) && split) {
     // every thread of both CTAs: rank 1's partial is in its shared memory
     cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
     cluster.sync();
     if (rank == 0 && warp < 4) {
+      const Tile T = tile(0);
+      const int m0 = T.m0, n0 = T.n0, z = T.z, nkb = T.nkb;
       const float* peer = cluster.map_shared_rank(reinterpret_cast<float*>(smem), 1);
       const int row = warp * 32 + lane;
       const int m = m0 + row;
@@ -802,15 +890,34 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int KIND, int BN>
+int gemm_sm_count();
+
+// `grid` is the tile grid.  Without a cluster the launch is persistent: one
+// CTA per resident slot (shared and tensor memory bound it), each taking
+// tiles blockIdx.x, + gridDim.x, ... of the tile grid.
+template <int KIND, int BN, int MH = 1>
 cudaError_t launch(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Cm,
-                   const TcArgs& a, dim3 grid, cudaStream_t s, int cluster_y = 1) {
-  using C = Cfg<KIND, BN>;
-  auto k = tc_gemm<KIND, BN>;
+                   const TcArgs& args, dim3 grid, cudaStream_t s, int cluster_y = 1) {
+  using C = Cfg<KIND, BN, MH>;
+  auto k = tc_gemm<KIND, BN, MH>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
   if (e != cudaSuccess) return e;
+  TcArgs a = args;
+  a.vgx = (int)grid.x;
+  a.vgy = (int)grid.y;
+  a.vgz = (int)grid.z;
+  a.persistent = cluster_y == 1 ? 1 : 0;
+  dim3 g = grid;
+  if (a.persistent) {
+    const long long tiles = (long long)grid.x * grid.y * grid.z;
+    int per_sm = (int)((227 * 1024) / (C::kSmem + 1024));
+    if (per_sm > 512 / C::kTmemCols) per_sm = 512 / C::kTmemCols;
+    if (per_sm < 1) per_sm = 1;
+    const long long cap = (long long)per_sm * gemm_sm_count();
+    g = dim3((unsigned)(tiles < cap ? tiles : cap), 1, 1);
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
+  cfg.gridDim = g;
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = s;
@@ -867,6 +974,14 @@ bool w_map(CUtensorMap* m, const void* w, const Geom& g, cuuint32_t box0, cuuint
   const cuuint64_t strides[1] = {(cuuint64_t)g.kdim * 2};
   const cuuint32_t box[2] = {box0, box1};
   return make_map(m, w, 2, dims, strides, box);
+}
+
+int gemm_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return 152;
+  return sms;
 }
 
 int pick_fwd_bn(const Geom& g) {
@@ -982,6 +1097,13 @@ cudaError_t launch_gemm_fwd_cl(const GemmArgs& ga, cudaStream_t s) {
   a.nimg = g.n;
   a.kb_total = (int)ceil_div_ll(g.kdim, kBK);
   a.out = ga.y;
+  if (bn == 128 && g.c_out > kBM) {
+    // all output channels of a pixel tile in one CTA (two halves): the map is
+    // read once
+    a.fwd_split = 1;
+    dim3 grid((unsigned)ceil_div_ll(g.howo, bn), (unsigned)ceil_div_ll(g.c_out, 2 * kBM), (unsigned)g.n);
+    return launch<FWDC, 128, 2>(A, B, A, a, grid, s);
+  }
   const long long tiles = ceil_div_ll(g.howo, bn) * ceil_div_ll(g.c_out, kBM) * g.n;
   a.fwd_split = (bn == 64 && tiles < 152 && a.kb_total >= 24) ? 2 : 1;
   dim3 grid((unsigned)ceil_div_ll(g.howo, bn), (unsigned)(ceil_div_ll(g.c_out, kBM) * a.fwd_split),
@@ -1035,14 +1157,19 @@ cudaError_t launch_gemm_gw_cl(const GemmArgs& ga, cudaStream_t s) {
   a.qblocks = (int)ceil_div_ll(g.howo, kBK);
   a.kb_total = a.qblocks * g.n;
   a.out = ga.gw;
-  const long long tiles = ceil_div_ll(g.kdim, 128) * ceil_div_ll(g.c_out, kBM);
-  long long splits = ceil_div_ll(152, tiles);
+  // all output channels of a column tile in one CTA when C_out > 128 (two
+  // halves: the map is read once); the pixels split over CTAs so that the
+  // grid is one wave
+  const int mh = g.c_out > kBM ? 2 : 1;
+  const long long tiles = ceil_div_ll(g.kdim, 128) * ceil_div_ll(g.c_out, kBM * mh);
+  const int sms = gemm_sm_count();
+  long long splits = sms / tiles;
   if (splits > a.kb_total) splits = a.kb_total;
   if (splits < 1) splits = 1;
   a.kb_per_split = (int)ceil_div_ll(a.kb_total, splits);
   splits = ceil_div_ll(a.kb_total, a.kb_per_split);
-  dim3 grid((unsigned)ceil_div_ll(g.kdim, 128), (unsigned)ceil_div_ll(g.c_out, kBM), (unsigned)splits);
-  return launch<GWC, 128>(A, B, A, a, grid, s);
+  dim3 grid((unsigned)ceil_div_ll(g.kdim, 128), (unsigned)ceil_div_ll(g.c_out, kBM * mh), (unsigned)splits);
+  return mh == 2 ? launch<GWC, 128, 2>(A, B, A, a, grid, s) : launch<GWC, 128>(A, B, A, a, grid, s);
 }
 
 bool fwd_sampled_supported(const Geom& g) {
