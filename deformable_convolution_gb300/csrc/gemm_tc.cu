@@ -226,8 +226,11 @@ struct Cfg {
   // CTAs fit on an SM; the long reductions keep a deeper ring.
   // GCOL has two k-blocks; four stages let two FWD CTAs share an SM
   static constexpr int kStages = is_gcol(KIND) ? 2 : 4;
-  // two accumulators (the epilogue of one tile overlaps the next tile's MMAs)
-  static constexpr int kTmemCols = 2 * MH * BN < 32 ? 32 : 2 * MH * BN;
+  // tensor-memory columns of one half's accumulator: BN rounded up to a
+  // power of two; two accumulators (the epilogue of one tile overlaps the
+  // next tile's MMAs), allocated as a power of two
+  static constexpr int kHS = BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
+  static constexpr int kTmemCols = 2 * MH * kHS;
   // GCOL's bf16 store staging: 4 warps x BN/64 boxes of 32 x 64
   static constexpr int kStg = is_gcol(KIND) ? 4 * (BN / 64) * 4096 : 0;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + kStg + 256;
@@ -241,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const __grid_constant__ CUtensorMap tmC, TcArgs a) {
   using C = Cfg<KIND, BN, MH>;
   static_assert(MH == 1 || KIND == FWDC || KIND == GWC, "two M halves: forward and weight-gradient kinds");
-  constexpr uint32_t kAcc = MH * BN;  // tensor-memory columns of one accumulator
+  constexpr uint32_t kAcc = MH * C::kHS;  // tensor-memory columns of one accumulator
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -412,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h = 0; h < MH; ++h) {
               const uint32_t sah = sa + h * C::kAHalf;
               const uint64_t da = C::kAMn ? sdesc(sah + kk * 2048, 8192, 1024) : sdesc(sah + kk * 32, 16, 1024);
-              umma(acc + h * BN, da, db, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+              umma(acc + h * C::kHS, da, db, idesc, (i > 0 || kk > 0) ? 1u : 0u);
             }
           }
           umma_commit(&empty[s]);
@@ -451,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // half h (rows m0 + 128 h ..) of the output, its column chunk c
         const int h = hc / (BN / 32), c = hc - h * (BN / 32);
         const int m = m0 + h * kBM + row;
-        const uint32_t tbase = tmem + (uint32_t)b * kAcc + (uint32_t)(h * BN) + ((uint32_t)(warp * 32) << 16);
+        const uint32_t tbase = tmem + (uint32_t)b * kAcc + (uint32_t)(h * C::kHS) + ((uint32_t)(warp * 32) << 16);
         uint32_t r[32];
         tmem_ld32(tbase + c * 32, r);
         if (nkb == 0) continue;
@@ -1099,10 +1102,12 @@ cudaError_t launch_gemm_fwd_cl(const GemmArgs& ga, cudaStream_t s) {
   a.out = ga.y;
   if (bn == 128 && g.c_out > kBM) {
     // all output channels of a pixel tile in one CTA (two halves): the map is
-    // read once
+    // read once; 96-pixel tiles (more tiles than SMs by a finer grain)
+    CUtensorMap B96;
+    if (!colc_map(&B96, ga.col, g, 96)) return cudaErrorInvalidValue;
     a.fwd_split = 1;
-    dim3 grid((unsigned)ceil_div_ll(g.howo, bn), (unsigned)ceil_div_ll(g.c_out, 2 * kBM), (unsigned)g.n);
-    return launch<FWDC, 128, 2>(A, B, A, a, grid, s);
+    dim3 grid((unsigned)ceil_div_ll(g.howo, 96), (unsigned)ceil_div_ll(g.c_out, 2 * kBM), (unsigned)g.n);
+    return launch<FWDC, 96, 2>(A, B96, A, a, grid, s);
   }
   const long long tiles = ceil_div_ll(g.howo, bn) * ceil_div_ll(g.c_out, kBM) * g.n;
   a.fwd_split = (bn == 64 && tiles < 152 && a.kb_total >= 24) ? 2 : 1;
