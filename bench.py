@@ -55,6 +55,8 @@ TRAFFIC = {
 }
 KERNEL_SOURCES = {
     "k1_band_sample": "k1_sample.cu", "k3_band_bwd": "k3_band_bwd.cu",
+    "k1_cl_sample": "k1_cl.cu", "k3_cl_bwd": "k3_cl.cu", "k4cl_input": "k4_cl.cu",
+    "k4cl_weight": "k4_cl.cu",
     # bf16 workloads run the offset-convolution backward on tensor cores
     "k4_offconv_bwd": "k4_offconv_bwd_tc.cu",
     "gemm_fwd": "gemm_tc.cu", "gemm_gcol": "gemm_tc.cu", "gemm_gw": "gemm_tc.cu",
@@ -586,11 +588,28 @@ def kernel_costs(p, has_add):
     k4 = (x_b + off_b + p.n_off * kdim * elt  # read x, grad_offset, w_off
           + 2 * gx_b                          # add into grad_x (read + write)
           + p.n_off * (kdim + 1) * 4)         # write grad_w_off, grad_b_off
+    # channels-last path (bf16, C_in a multiple of 64): x copied to NHWC once
+    # per layer; the backward kernels read that copy
+    w_b = p.c_out * kdim * elt
+    woff_b = p.n_off * kdim * elt
+    k4cl_chunks = 152 // max(1, p.c_in // 64)
     return {
         "k1_band_sample": ("hbm", k1_bytes(p, has_add)),
+        "k1_cl_sample": ("hbm", k1_bytes(p, has_add)),
+        "k1_cl_offsets": ("hbm", x_b + woff_b + off_b * (2 if has_add else 1)),
+        "cl_prep_x": ("hbm", 2 * x_b),
+        "cl_prep_weights": ("hbm", 2 * w_b + 2 * woff_b),
         "gemm_fwd": ("tensor", gemm), "gemm_gcol": ("tensor", gemm), "gemm_gw": ("tensor", gemm),
         "k3_band_bwd": ("hbm", k3),
+        # read x (NHWC), offsets, gcol; grad_x into the NHWC float32 buffer, goff
+        "k3_cl_bwd": ("hbm", k3),
+        "gx_to_nchw": ("hbm", 2 * gx_b),
         "k4_offconv_bwd": ("hbm", k4),
+        # input part: read goff, w_off and the NHWC grad_x buffer, write grad_x
+        "k4cl_input": ("hbm", off_b + woff_b + 2 * gx_b),
+        # weight part: read x (NHWC) and goff, write the chunk partials
+        "k4cl_weight": ("hbm", x_b + off_b + k4cl_chunks * p.n_off * (kdim + 1) * 4),
+        "k4cl_reduce": ("hbm", (k4cl_chunks + 1) * p.n_off * (kdim + 1) * 4),
         # per-image grad_w_off partials of the tensor-core K4, summed
         "gw_off_reduce": ("hbm", (p.n + 1) * p.n_off * kdim * 4),
         # ReLU between stacked layers: read y, write the next input; read the
@@ -705,10 +724,13 @@ def k1_roofline(p, t, dev, stream, flush, wl, iters=200):
     nbytes = k1_bytes(p, t["offset_add"] is not None)
     peaks, src = measured_peaks()
     achieved = nbytes / (ms / 1e3) / 1e9
-    src_hash = source_hash(os.path.join(ROOT, "deformable_convolution_gb300", "csrc",
-                                        "k1_sample.cu"))
-    traffic = traffic_for(wl.name, "k1_band_sample")
-    return {"kernel": "k1_band_sample (offset conv + bilinear sampling)", "bound": "hbm",
+    cl = B.col_layout(p) == B.DC_COL_PIXEL_MAJOR
+    name = "k1_cl_sample" if cl else "k1_band_sample"
+    traffic = traffic_for(wl.name, name)
+    what = ("cl_prep_x (x to NHWC) + cl_prep_weights + k1_cl_sample (offset conv + bilinear "
+            "sampling), one deform_conv_sample call" if cl
+            else "k1_band_sample (offset conv + bilinear sampling)")
+    return {"kernel": what, "bound": "hbm",
             "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{src} (hbm_gbs, burst)",
             "traffic": traffic, "algorithmic_bytes": nbytes, "ms_per_launch": ms}

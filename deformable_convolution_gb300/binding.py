@@ -25,7 +25,7 @@ EXPORTED_SYMBOLS = (
     "dc_launch_count", "deform_conv_fwd_noalloc", "dc_device_error", "dc_kernel_timing",
     "dc_kernel_times", "deform_conv_offsets", "deform_conv_margin_histogram", "dc_suggest_margin",
     "deform_conv_bwd_after_fwd", "deform_conv_fwd_sampled_gemm", "dc_relu_fwd", "dc_relu_bwd",
-    "dc_col_layout", "dc_sample_tile",
+    "dc_col_layout", "dc_sample_tile", "dc_selftest_wait_timeout", "dc_test_fail_launches",
 )
 DC_COL_PLANE_MAJOR, DC_COL_PIXEL_MAJOR = 0, 1
 MARGIN_BINS = 64
@@ -92,6 +92,10 @@ def lib() -> ctypes.CDLL:
         L.dc_kernel_times.restype = i
         L.dc_device_error.argtypes = [i]
         L.dc_device_error.restype = i
+        L.dc_selftest_wait_timeout.argtypes = [ctypes.c_uint, vp]
+        L.dc_selftest_wait_timeout.restype = i
+        L.dc_test_fail_launches.argtypes = [i]
+        L.dc_test_fail_launches.restype = i
         L.dc_relu_fwd.argtypes = [vp, vp, sz, i, vp]
         L.dc_relu_fwd.restype = i
         L.dc_relu_bwd.argtypes = [vp, vp, vp, sz, i, vp]
@@ -113,6 +117,18 @@ def build_info() -> str:
 def device_error(clear: bool = False) -> int:
     """DC_ERR_TIMEOUT if a bounded device wait expired (synchronises)."""
     return int(lib().dc_device_error(1 if clear else 0))
+
+
+def selftest_wait_timeout(spins: int, stream=None) -> int:
+    """Test hook: a kernel whose bounded wait on an mbarrier nothing arrives on
+    expires after `spins` polls (the next device_error() is DC_ERR_TIMEOUT)."""
+    return int(lib().dc_selftest_wait_timeout(spins, _stream(stream)))
+
+
+def test_fail_launches(count: int) -> int:
+    """Test hook: the next `count` launches of the layer entry points fail
+    with DC_ERR_CUDA without being made (0 cancels)."""
+    return int(lib().dc_test_fail_launches(count))
 
 
 def kernel_timing(enable: bool) -> None:

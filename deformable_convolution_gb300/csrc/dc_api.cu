@@ -39,8 +39,14 @@ TimedLaunch g_timed[kMaxTimed];
 int g_ntimed = 0;
 int g_nevents = 0;  // event pairs created so far (reused across calls)
 
+// Test hook (dc_test_fail_launches): launches still to fail without being made.
+std::atomic<int> g_fail_launches{0};
+
 template <typename F>
 cudaError_t timed(const char* name, cudaStream_t s, F&& launch) {
+  if (g_fail_launches.load(std::memory_order_relaxed) > 0 &&
+      g_fail_launches.fetch_sub(1, std::memory_order_relaxed) > 0)
+    return cudaErrorLaunchFailure;  // injected: nothing is enqueued
   int slot = -1;
   if (g_timing.load(std::memory_order_relaxed)) {
     std::lock_guard<std::mutex> lock(g_timing_mu);
@@ -392,6 +398,12 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
 }  // namespace dc
 
 extern "C" {
+
+dc_status dc_test_fail_launches(int count) {
+  if (count < 0) return DC_ERR_INVALID_ARG;
+  g_fail_launches.store(count, std::memory_order_relaxed);
+  return DC_OK;
+}
 
 int dc_out_h(const dc_problem* prob) {
   Geom g;

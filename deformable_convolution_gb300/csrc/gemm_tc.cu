@@ -1211,6 +1211,30 @@ cudaError_t launch_fwd_sampled_tc(const Geom& g, const void* x, const void* w, c
 
 }  // namespace dc
 
+namespace dc {
+namespace {
+// One thread waits, for at most `spins` polls, on an mbarrier that nothing
+// arrives on; on expiry it raises the flag as every bounded wait of the
+// library does.  No copy or tensor-memory allocation is outstanding.
+__global__ void selftest_wait_kernel(unsigned int spins) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  for (unsigned int i = 0; i < spins; ++i)
+    if (mbar_try_wait(&bar, 0)) return;
+  atomicOr(&g_dc_device_error, 1u);
+}
+}  // namespace
+}  // namespace dc
+
+extern "C" dc_status dc_selftest_wait_timeout(unsigned int spins, void* stream) {
+  if (spins == 0 || spins > (1u << 20)) return DC_ERR_INVALID_ARG;
+  dc::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(spins);
+  dc::note_launches(1);
+  return cudaGetLastError() == cudaSuccess ? DC_OK : DC_ERR_CUDA;
+}
+
 // Reads (and optionally clears) the flag bounded device waits raise on expiry.
 // The channels-last kernels keep their own flags (cl_read_error, cl3_read_error,
 // k4cl_read_error: 2 = unreadable).

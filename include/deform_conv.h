@@ -304,6 +304,26 @@ const char* dc_build_info(void);
  * rest of its work: its outputs are not valid. */
 dc_status dc_device_error(int clear);
 
+/* Test hooks for the failure paths (no counterpart on the explainer page;
+ * they exist so that tests can drive the error reporting without a fault).
+ *
+ * dc_selftest_wait_timeout enqueues on `stream` (a cudaStream_t, NULL = the
+ * default stream) one kernel whose single thread polls, at most `spins`
+ * times (1 .. 2^20), an mbarrier that nothing arrives on, then raises the
+ * device error flag exactly as an expired wait of the layer's kernels does:
+ * the next dc_device_error reports DC_ERR_TIMEOUT.  The kernel holds no
+ * copies and no tensor memory, so the expiry leaves the context usable.
+ * Returns DC_ERR_INVALID_ARG for spins out of range, DC_ERR_CUDA if the
+ * launch fails.
+ *
+ * dc_test_fail_launches(n): the next n kernel launches of the layer entry
+ * points (deform_conv_fwd, _bwd, _sample, _offsets and their variants) are
+ * not made and the call returns DC_ERR_CUDA, as for a failed launch; n = 0
+ * cancels.  Process-wide, like the timing record below; DC_ERR_INVALID_ARG
+ * for n < 0. */
+dc_status dc_selftest_wait_timeout(unsigned int spins, void* stream);
+dc_status dc_test_fail_launches(int count);
+
 /* Kernel timing (tracing).  dc_kernel_timing(1) starts recording: every
  * kernel (and the backward pass's group of memsets) enqueued by the calls that
  * follow is bracketed by two CUDA events on its stream, up to 256 launches;

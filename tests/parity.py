@@ -32,6 +32,19 @@ def rel_err(got, ref):
     return float(np.max(np.abs(got - ref)) / scale)
 
 
+def elementwise_err(got, ref, tol):
+    """Largest violation ratio of the per-element bound
+    |got - ref| <= tol * (|ref| + max|ref| / 4): relative for large elements,
+    a quarter of the tensor-wide bound for small ones (<= 1 passes)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    scale = np.max(np.abs(ref)) if ref.size else 0.0
+    if scale == 0.0:
+        return 0.0 if not got.size or np.max(np.abs(got)) == 0.0 else float("inf")
+    bound = tol * (np.abs(ref) + 0.25 * scale)
+    return float(np.max(np.abs(got - ref) / bound))
+
+
 def to_dev(d):
     return {k: (None if v is None else v.cuda()) for k, v in d.items()}
 
@@ -81,4 +94,12 @@ def check_layer(p, d, tol=None, margin=None, check_bwd=True):
             errs[k] = rel_err(f64(g[k]), ref[k])
     bad = {k: v for k, v in errs.items() if not v <= tol}
     assert not bad, f"parity failed (tol {tol}): {errs}"
+    # and element by element: small outputs may not hide large relative errors
+    # behind the tensor's maximum
+    elem = {"y": elementwise_err(f64(y), y_ref, tol)}
+    if check_bwd:
+        for k in ("grad_x", "grad_w", "grad_w_off", "grad_b_off", "grad_offset"):
+            elem[k] = elementwise_err(f64(g[k]), ref[k], tol)
+    bad = {k: v for k, v in elem.items() if not v <= 1.0}
+    assert not bad, f"elementwise parity failed (tol {tol}): {elem}"
     return errs

@@ -98,6 +98,27 @@ def test_edge_geometries(geom, dtype):
     check_layer(p, random_inputs(p, 100 + h * w + c_in))
 
 
+# One offset group per input channel (8 to 16 of them) with margin 0: every
+# channel slice of the fused stage and of the sampling backward holds more than
+# four offset groups, many of whose taps leave the window, so the deferred
+# slow-tap queue (sized for at most four groups per slice) overflows and is
+# drained in place.  (Wider many-group problems exceed the shared memory of
+# the plane-major kernels and are refused as unsupported.)
+@pytest.mark.parametrize("dtype,c_in", [(B.DC_F32, 8), (B.DC_F32, 12), (B.DC_BF16, 8),
+                                         (B.DC_BF16, 16)])
+def test_slow_tap_queue_overflow(dtype, c_in):
+    p = B.Problem(2, c_in, 14, 18, 8, 3, 3, 1, 1, 1, c_in, dtype, 0)
+    d = random_inputs(p, 900 + c_in, off_scale=3.0)
+    cnt = torch.zeros(1, dtype=torch.int64, device="cuda")
+    dd = {k: v.cuda() for k, v in d.items()}
+    B.forward(p, dd["x"], dd["w_off"], dd["b_off"], dd["w"], dd["offset_add"], slowpath_count=cnt)
+    torch.cuda.synchronize()
+    taps = p.n * c_in * p.kh * p.kw * p.ho * p.wo
+    assert int(cnt.item()) > taps // 4  # many taps take the global path
+    errs = check_layer(p, d)
+    print(c_in, errs)
+
+
 @pytest.mark.parametrize("dtype,c_in,layout", [
     (B.DC_F32, 16, B.DC_COL_PLANE_MAJOR), (B.DC_BF16, 16, B.DC_COL_PLANE_MAJOR),
     (B.DC_BF16, 64, B.DC_COL_PIXEL_MAJOR)])

@@ -522,3 +522,19 @@ def test_relu_and_its_gradient_by_hand():
     assert not np.signbit(r[1])
     g = np.array([1.0, 2.0, 3.0, 4.0, 5.0, 6.0, 7.0, 8.0])
     assert oracle.relu_grad(r, g).tolist() == [0.0, 0.0, 0.0, 4.0, 5.0, 0.0, 0.0, 8.0]
+
+
+def test_elementwise_parity_bound_catches_what_the_tensor_bound_misses():
+    """The parity helper's per-element bound: an error in a small element that
+    the max-normalised measure lets through is caught; exact and relative
+    errors within the bound pass."""
+    from parity import elementwise_err, rel_err
+    ref = np.array([1000.0, 1.0, -3.0])
+    got = ref.copy()
+    got[1] += 6.0  # 0.6 % of the tensor's maximum, 600 % of the element
+    assert rel_err(got, ref) <= 2e-2
+    assert elementwise_err(got, ref, 2e-2) > 1.0
+    assert elementwise_err(ref, ref, 2e-2) == 0.0
+    ok = ref * (1 + 1e-2)  # 1 % relative everywhere
+    assert elementwise_err(ok, ref, 2e-2) <= 1.0
+    assert elementwise_err(np.zeros(3), np.zeros(3), 2e-2) == 0.0
