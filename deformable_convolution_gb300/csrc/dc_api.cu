@@ -140,6 +140,7 @@ struct Plan {
   bool k4cl;  // channels-last offset-convolution backward (writes grad_x from that accumulator)
   ColLayout col, gcol;
   size_t col_off, gcol_off, off_off, gmax_off, gwo_img_off, xc_off, wp_off, wfrag_off, gxc_off, k4part_off,
+      gwp_off,
       total;
   int gmax_tx, gmax_ty;
 };
@@ -179,6 +180,8 @@ Plan make_plan(const Geom& g, dc_dtype dt, int backward, int margin) {
   // the kernel's accumulator order
   pl.gxc_off = pl.k3cl ? take((size_t)g.n * g.hw * g.c_in * sizeof(float)) : 0;
   pl.k4part_off = pl.k4cl ? take(k4cl_part_bytes(g)) : 0;
+  // grad_w in w' order, permuted by the offset-convolution backward's reduce
+  pl.gwp_off = pl.k4cl ? take((size_t)g.c_out * g.kdim * sizeof(float)) : 0;
   pl.gwo_img_off = backward && !pl.k4cl && offconv_bwd_tc_supported(g, dt)
                        ? take((size_t)g.n * gwo_frag_count(g.M, g.c_in, g.K) * sizeof(float))
                        : 0;
@@ -282,7 +285,8 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
   if (pl.k3cl) ga.w = wsb + pl.wp_off;
   ga.zero.p[0] = pl.k3cl ? gxc : grad_x;
   ga.zero.n[0] = (long long)g.n * g.c_in * g.hw;
-  ga.zero.p[1] = grad_w;
+  float* gw_perm = pl.k4cl ? reinterpret_cast<float*>(wsb + pl.gwp_off) : nullptr;
+  ga.zero.p[1] = pl.k4cl ? gw_perm : grad_w;
   ga.zero.n[1] = (long long)g.c_out * g.kdim;
   ga.zero.p[2] = grad_w_off;
   ga.zero.n[2] = (long long)g.M * g.kdim;
@@ -331,10 +335,14 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
       k4.grad_w_off = grad_w_off;
       k4.grad_b_off = grad_b_off;
       k4.part = reinterpret_cast<float*>(wsb + pl.k4part_off);
+      k4.gw_perm = gw_perm;
+      k4.grad_w = grad_w;
+      k4.c_out = g.c_out;
       st = cuda_status(timed("k4cl_weight", s, [&] { return launch_k4cl_weight(k4, s); }));
       if (st != DC_OK) return st;
       st = cuda_status(timed("k4cl_input", s, [&] { return launch_k4cl_input(k4, s); }));
       if (st != DC_OK) return st;
+      ga.gw_perm = gw_perm;
       st = cuda_status(timed("gemm_gw", s, [&] { return launch_gemm_gw_cl(ga, s); }));
       if (st != DC_OK) return st;
       return cuda_status(timed("k4cl_reduce", s, [&] { return launch_k4cl_reduce(k4, s); }));

@@ -146,6 +146,8 @@ struct GemmArgs {
   void* gcol;         // column-layout gradient: bf16 from the tensor-core GEMM, else fp32
   ColLayout gcol_layout;
   float* gw;          // [c_out][kdim] fp32, accumulated with atomics (backward)
+  float* gw_perm;     // channels-last GW: when given, the gradient is added in w' order
+                      // ([c_out][tap][c], float4 atomics) here instead of into gw
   ZeroArgs zero;      // GCOL kernels clear these (the backward's atomic targets)
   float* gmax;        // tensor-core GCOL: max |gcol| per 128 x 128 tile (4 floats each), or null
   // tensor-core GW: after K4, gw_off = sum over images of gwo_img (count
@@ -314,6 +316,9 @@ struct K4ClArgs {
   float* grad_w_off;    // [M][C_in][K]
   float* grad_b_off;    // [M] or null
   float* part;          // workspace, k4cl_part_bytes
+  const float* gw_perm; // grad_w in w' order [C_out][K][C_in] (the GEMM's), or null
+  float* grad_w;        // [C_out][C_in][K], written from gw_perm by the reduce kernel
+  int c_out;
 };
 cudaError_t launch_k4cl_input(const K4ClArgs& a, cudaStream_t s);
 cudaError_t launch_k4cl_weight(const K4ClArgs& a, cudaStream_t s);

@@ -64,7 +64,8 @@ struct TcArgs {
   float* gw_off;
   long long gwo_count;         // floats per image
   int gwo_nimg, gwo_m, gwo_cin, gwo_k;  // images; M, C_in, K of the partials' order
-  int cin, ktaps;              // GWC: C_in and taps, to map columns (tap, c) to grad_w[o][c][tap]
+  int cin, ktaps;              // GWC: C_in and taps, to map columns (tap, c) to grad_w[o][c][tap];
+                               // cin = 0: add in w' order ([o][tap][c], float4 atomics)
   // the tile grid (x: column tiles, y: row tiles, z: images or splits); a
   // persistent launch runs tiles blockIdx.x, + gridDim.x, ... of it
   int vgx, vgy, vgz, persistent;
@@ -511,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_store_commit();
             }
           }
-        } else if (KIND == GWC) {
+        } else if (KIND == GWC && a.cin > 0) {
           if (m >= a.c_out) continue;
           // column r = tap * C + c of w' is grad_w[m][c][tap]
           float* dst = static_cast<float*>(a.out) + (long long)m * a.kdim;
@@ -1157,11 +1158,11 @@ cudaError_t launch_gemm_gw_cl(const GemmArgs& ga, cudaStream_t s) {
   a.kdim = g.kdim;
   a.howo = (int)g.howo;
   a.nimg = g.n;
-  a.cin = g.c_in;
+  a.cin = ga.gw_perm ? 0 : g.c_in;
   a.ktaps = g.K;
   a.qblocks = (int)ceil_div_ll(g.howo, kBK);
   a.kb_total = a.qblocks * g.n;
-  a.out = ga.gw;
+  a.out = ga.gw_perm ? ga.gw_perm : ga.gw;
   // all output channels of a column tile in one CTA when C_out > 128 (two
   // halves: the map is read once); the pixels split over CTAs so that the
   // grid is one wave

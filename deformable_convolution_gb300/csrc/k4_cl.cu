@@ -474,9 +474,21 @@ __global__ void __launch_bounds__(288, 1)
 // y, y + 8, ..., then thread row 0 adds the eight group sums (fixed order).
 __global__ void __launch_bounds__(256) k4cl_reduce(const float* __restrict__ part,
                                                    const float* __restrict__ bpart, float* gw_off,
-                                                   float* gb_off, int count, int M, int nchunks) {
+                                                   float* gb_off, int count, int M, int nchunks,
+                                                   const float* __restrict__ gw_perm, float* grad_w,
+                                                   int wcount, int C, int K) {
   __shared__ float red[8][33];
   pdl_wait();
+  // grad_w[o][c][k] = gw_perm[o][k][c] (the main weight gradient, added in
+  // w' order by the GEMM)
+  if (gw_perm) {
+    const int nth = gridDim.x * blockDim.x;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < wcount; e += nth) {
+      const int o = e / (C * K), r = e - o * (C * K);
+      const int c = r / K, k = r - c * K;
+      grad_w[e] = gw_perm[(size_t)o * C * K + (size_t)k * C + c];
+    }
+  }
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int i = blockIdx.x * 32 + tx;
   const bool bias = gb_off != nullptr && blockIdx.x == gridDim.x - 1;  // the last block also sums the bias
@@ -645,7 +657,10 @@ cudaError_t launch_k4cl_reduce(const K4ClArgs& in, cudaStream_t s) {
   float* gw = in.grad_w_off;
   float* gb = in.grad_b_off;
   int count = g.M * g.c_in * g.K, M = g.M, nch = w.nchunks;
-  void* args[] = {&part, &bpart, &gw, &gb, &count, &M, &nch};
+  const float* gwp = in.gw_perm;
+  float* gwd = in.grad_w;
+  int wcount = in.c_out * g.c_in * g.K, C = g.c_in, K = g.K;
+  void* args[] = {&part, &bpart, &gw, &gb, &count, &M, &nch, &gwp, &gwd, &wcount, &C, &K};
   return launch_pdl4((const void*)k4cl_reduce, dim3((unsigned)ceil_div_ll(count, 32)), dim3(256), 0, s,
                      args);
 }
