@@ -226,7 +226,7 @@ struct Cfg {
   // GCOL reduces over C_out only (a few k-blocks): two stages, so that three
   // CTAs fit on an SM; the long reductions keep a deeper ring.
   // GCOL has two k-blocks; four stages let two FWD CTAs share an SM
-  static constexpr int kStages = is_gcol(KIND) ? 2 : 4;
+  static constexpr int kStages = is_gcol(KIND) ? (BN == 256 ? 3 : 2) : 4;
   // tensor-memory columns of one half's accumulator: BN rounded up to a
   // power of two; two accumulators (the epilogue of one tile overlaps the
   // next tile's MMAs), allocated as a power of two
@@ -1133,6 +1133,11 @@ cudaError_t launch_gemm_gcol_cl(const GemmArgs& ga, cudaStream_t s) {
   a.out = ga.gcol;
   a.zero = ga.zero;
   a.gmax = nullptr;
+  if (g.kdim % 256 == 0) {
+    // 256-column tiles: the grad_y tile (A) serves twice the columns
+    dim3 grid((unsigned)(g.kdim / 256), (unsigned)ceil_div_ll(g.howo, kBM), (unsigned)g.n);
+    return launch<GCOLC, 256>(A, B, Cm, a, grid, s);
+  }
   dim3 grid((unsigned)ceil_div_ll(g.kdim, 128), (unsigned)ceil_div_ll(g.howo, kBM), (unsigned)g.n);
   return launch<GCOLC, 128>(A, B, Cm, a, grid, s);
 }
