@@ -14,6 +14,7 @@ namespace dc {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kUnroll = 4;  // 16-byte vectors per thread in flight
 
 // +0 where the value is <= 0, else the value: NaN stays NaN (it is not <= 0),
 // as a training run wants it to; the hardware may return its canonical NaN.
@@ -29,30 +30,40 @@ __device__ __forceinline__ __nv_bfloat16 relu1(__nv_bfloat16 v) {
 // out = max(y, 0) elementwise (NaN stays NaN); out may be y.  Whole 16-byte
 // chunks are vectorised, the last count % (16 / sizeof(T)) elements are not.
 template <typename T>
-__global__ void __launch_bounds__(kThreads) relu_fwd_kernel(const T* y, T* out,
+__global__ void __launch_bounds__(kThreads, 6) relu_fwd_kernel(const T* y, T* out,
                                                             long long count) {
   pdl_wait();
   constexpr int kVec = 16 / sizeof(T);
   const long long nvec = count / kVec;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const long long t0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  for (long long i = t0; i < nvec; i += stride) {
-    uint4 v = reinterpret_cast<const uint4*>(y)[i];
-    if (sizeof(T) == 2) {
-      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+  // kUnroll vectors per thread in flight at once (loads first, then stores)
+  for (long long i0 = t0; i0 < nvec; i0 += kUnroll * stride) {
+    uint4 v[kUnroll];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        // compare the floats the two bf16 halves widen to; keep a half's
-        // bits unless it is <= 0 (so NaN is kept)
-        const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
-        w[e] = (lo <= 0.f ? 0u : (w[e] & 0xffffu)) | (hi <= 0.f ? 0u : (w[e] & 0xffff0000u));
-      }
-    } else {
-      uint32_t* f = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) f[e] = __uint_as_float(f[e]) <= 0.f ? 0u : f[e];
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long i = i0 + u * stride;
+      if (i < nvec) v[u] = reinterpret_cast<const uint4*>(y)[i];
     }
-    reinterpret_cast<uint4*>(out)[i] = v;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const long long i = i0 + u * stride;
+      if (i >= nvec) break;
+      uint32_t* w = reinterpret_cast<uint32_t*>(&v[u]);
+      if (sizeof(T) == 2) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          // compare the floats the two bf16 halves widen to; keep a half's
+          // bits unless it is <= 0 (so NaN is kept)
+          const float lo = __uint_as_float(w[e] << 16), hi = __uint_as_float(w[e] & 0xffff0000u);
+          w[e] = (lo <= 0.f ? 0u : (w[e] & 0xffffu)) | (hi <= 0.f ? 0u : (w[e] & 0xffff0000u));
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) w[e] = __uint_as_float(w[e]) <= 0.f ? 0u : w[e];
+      }
+      reinterpret_cast<uint4*>(out)[i] = v[u];
+    }
   }
   for (long long i = nvec * kVec + t0; i < count; i += stride) out[i] = relu1(y[i]);
   pdl_release();
@@ -61,13 +72,14 @@ __global__ void __launch_bounds__(kThreads) relu_fwd_kernel(const T* y, T* out,
 // grad_in = grad_out where act > 0, else 0, rounded to T (nearest even).
 // act is the activation's output (positive exactly where its input was).
 template <typename T>
-__global__ void __launch_bounds__(kThreads) relu_bwd_kernel(const T* __restrict__ act,
+__global__ void __launch_bounds__(kThreads, 6) relu_bwd_kernel(const T* __restrict__ act,
                                                             const float* __restrict__ gout,
                                                             T* __restrict__ gin, long long count) {
   pdl_wait();
   const long long nvec = count / 8;
   const long long stride = (long long)gridDim.x * blockDim.x;
   const long long t0 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+#pragma unroll 2
   for (long long i = t0; i < nvec; i += stride) {
     const float4 g0 = reinterpret_cast<const float4*>(gout)[2 * i];
     const float4 g1 = reinterpret_cast<const float4*>(gout)[2 * i + 1];
@@ -116,9 +128,10 @@ cudaError_t launch_stream_kernel(K kern, long long count, cudaStream_t s, A... a
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  // 4 CTAs of 256 threads per SM, fewer for small tensors
+  // 8 CTAs of 256 threads per SM (the SM's full 2048 threads), fewer for
+  // small tensors
   long long blocks = ceil_div_ll(ceil_div_ll(count, 8), kThreads);
-  if (blocks > 4LL * sms) blocks = 4LL * sms;
+  if (blocks > 8LL * sms) blocks = 8LL * sms;
   if (blocks < 1) blocks = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
