@@ -44,14 +44,14 @@ def fp32_alu_tflops(dev):
 # dram__bytes_write.sum), keyed by (workload, kernel); valid only while the
 # kernel's source file hashes to the recorded value (else reported as null).
 TRAFFIC = {
-    # ncu --set full, res3 bf16, one launch each.  Writes mostly stay in the
-    # 129 MB L2.
-    ("res3_bf16", "k1_band_sample"): {"bytes": 2193408, "source": "8492705966c2d40d"},
-    ("res3_bf16", "k3_band_bwd"): {"bytes": 20262400, "source": "1a9b981b39ec521e"},
-    ("res3_bf16", "k4_offconv_bwd"): {"bytes": 6218752, "source": "b3d2877a101e5de4"},
-    ("res3_bf16", "gemm_fwd"): {"bytes": 14771968, "source": "f657fe41ae0cab4d"},
-    ("res3_bf16", "gemm_gcol"): {"bytes": 1941248, "source": "f657fe41ae0cab4d"},
-    ("res3_bf16", "gemm_gw"): {"bytes": 17554944, "source": "f657fe41ae0cab4d"},
+    # ncu sections capture of one training step of the stack (cold caches),
+    # one launch each; writes that stay in the 126 MB L2 are not counted.
+    ("stack_bf16", "k3_cl_bwd"): {"bytes": 170828800, "source": "4ef7f561d1f67799"},
+    ("stack_bf16", "k1_cl_sample"): {"bytes": 70471680, "source": "c94cb41769553595"},
+    ("stack_bf16", "k4cl_input"): {"bytes": 27682560, "source": "1899d836b9132317"},
+    ("stack_bf16", "k4cl_weight"): {"bytes": 14779136, "source": "1899d836b9132317"},
+    ("stack_bf16", "gemm_gcol"): {"bytes": 98491136, "source": "46f3bbf5542948f4"},
+    ("stack_bf16", "gemm_gw"): {"bytes": 133973504, "source": "46f3bbf5542948f4"},
 }
 KERNEL_SOURCES = {
     "k1_band_sample": "k1_sample.cu", "k3_band_bwd": "k3_band_bwd.cu",
