@@ -737,14 +737,17 @@ namespace dc {
 // not hold) and unaligned shapes run on CUDA cores.
 cudaError_t launch_gemm_fwd(const GemmArgs& a, dc_dtype dt, cudaStream_t s) {
   if (dt == DC_BF16 && tc_gemm_supported(a.g)) return launch_gemm_fwd_tc(a, s);
+  if (dt == DC_F32 && tf32_gemm_supported(a.g)) return launch_gemm_fwd_tf32(a, s);
   return launch_gemm_fwd_simt(a, dt, s);
 }
 cudaError_t launch_gemm_gcol(const GemmArgs& a, dc_dtype dt, cudaStream_t s) {
   if (dt == DC_BF16 && tc_gemm_supported(a.g)) return launch_gemm_gcol_tc(a, s);
+  if (dt == DC_F32 && tf32_gemm_supported(a.g)) return launch_gemm_gcol_tf32(a, s);
   return launch_gemm_gcol_simt(a, dt, s);
 }
 cudaError_t launch_gemm_gw(const GemmArgs& a, dc_dtype dt, cudaStream_t s) {
   if (dt == DC_BF16 && tc_gemm_supported(a.g)) return launch_gemm_gw_tc(a, s);
+  if (dt == DC_F32 && tf32_gemm_supported(a.g)) return launch_gemm_gw_tf32(a, s);
   return launch_gemm_gw_simt(a, dt, s);
 }
 

@@ -2,6 +2,7 @@
 // kernel launch entry points).  Nothing here is visible through the C ABI.
 #pragma once
 
+#include <climits>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -171,6 +172,12 @@ cudaError_t launch_gemm_gw_cl(const GemmArgs& a, cudaStream_t s);
 bool fwd_sampled_supported(const Geom& g);
 cudaError_t launch_fwd_sampled_tc(const Geom& g, const void* x, const void* w, const float* off,
                                   void* y, cudaStream_t s);
+// float32 problems on the tensor cores (tcgen05 kind::tf32, three-product
+// split); need tf32_gemm_supported(g): kdim and the pixel count multiples of 4.
+bool tf32_gemm_supported(const Geom& g);
+cudaError_t launch_gemm_fwd_tf32(const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_gcol_tf32(const GemmArgs& a, cudaStream_t s);
+cudaError_t launch_gemm_gw_tf32(const GemmArgs& a, cudaStream_t s);
 // CUDA-core (fp32 arithmetic) versions, any layout pitch.
 cudaError_t launch_gemm_fwd_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
 cudaError_t launch_gemm_gcol_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s);
@@ -299,6 +306,7 @@ struct K3ClArgs {
 cudaError_t launch_k3cl(const K3ClArgs& a, cudaStream_t s);
 cudaError_t launch_gx_to_nchw(const float* gx_nhwc, float* grad_x, const Geom& g, cudaStream_t s);
 unsigned int cl3_read_error(int clear);
+unsigned int tf32_read_error(int clear);
 // Backward of the offset convolution on the channels-last path (one offset
 // group, K <= 9 taps): the input part adds into the NHWC grad_x buffer's
 // values and writes grad_x (NCHW) whole; the weight part writes per-chunk

@@ -1242,8 +1242,9 @@ extern "C" dc_status dc_selftest_wait_timeout(unsigned int spins, void* stream) 
 }
 
 // Reads (and optionally clears) the flag bounded device waits raise on expiry.
-// The channels-last kernels keep their own flags (cl_read_error, cl3_read_error,
-// k4cl_read_error: 2 = unreadable).
+// The channels-last kernels and the float32 tensor-core GEMMs keep their own
+// flags (cl_read_error, cl3_read_error, k4cl_read_error, tf32_read_error:
+// 2 = unreadable).
 extern "C" dc_status dc_device_error(int clear) {
   unsigned int v = 0;
   if (cudaMemcpyFromSymbol(&v, dc::g_dc_device_error, sizeof(v)) != cudaSuccess) return DC_ERR_CUDA;
@@ -1255,6 +1256,7 @@ extern "C" dc_status dc_device_error(int clear) {
   const unsigned int c = dc::cl_read_error(clear);
   const unsigned int c3 = dc::cl3_read_error(clear);
   const unsigned int c4 = dc::k4cl_read_error(clear);
-  if (c == 2u || c3 == 2u || c4 == 2u) return DC_ERR_CUDA;
-  return (v || c || c3 || c4) ? DC_ERR_TIMEOUT : DC_OK;
+  const unsigned int t = dc::tf32_read_error(clear);
+  if (c == 2u || c3 == 2u || c4 == 2u || t == 2u) return DC_ERR_CUDA;
+  return (v || c || c3 || c4 || t) ? DC_ERR_TIMEOUT : DC_OK;
 }

@@ -87,6 +87,10 @@ EDGE_GEOMETRIES = [
     (2, 8, 33, 21, 16, 3, 3, 2, 1, 1, 4),
     (1, 3, 11, 40, 2, 5, 5, 1, 2, 1, 1),
     (1, 16, 9, 130, 24, 3, 3, 1, 1, 1, 2),
+    # kdim and the pixel count multiples of 4 (the float32 tensor-core GEMMs),
+    # with ragged k-blocks, pixel tiles and output-channel tiles
+    (2, 12, 10, 14, 40, 3, 3, 1, 1, 1, 1),
+    (1, 20, 12, 12, 136, 3, 3, 1, 1, 1, 2),
 ]
 
 
