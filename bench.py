@@ -40,6 +40,17 @@ def fp32_alu_tflops(dev):
     mhz = measured_peaks()[0].get("sm_max_mhz", 2070.0)
     return sms * 128 * 2 * mhz * 1e6 / 1e12, sms, mhz
 
+# Nominal dense TF32 : bf16 tensor rate of the part (1.1 : 2.25 PFLOP/s).
+TF32_PER_BF16 = 1.1 / 2.25
+
+
+def tf32_path(p):
+    """True when a float32 problem's GEMMs run on the tensor cores (kind::tf32):
+    the library takes that path when kdim and the output pixel count are
+    multiples of 4 (16-byte rows for every tensor map)."""
+    return (p.c_in * p.kh * p.kw) % 4 == 0 and (p.ho * p.wo) % 4 == 0
+
+
 # DRAM traffic of one launch from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum), keyed by (workload, kernel); valid only while the
 # kernel's source file hashes to the recorded value (else reported as null).
@@ -649,8 +660,15 @@ def kernel_breakdown(p, wl, step, dev, stream, flush, iters=40):
     for name in tot:
         ms = tot[name] / cnt[name]
         bound, amount = costs.get(name, ("hbm", 0.0))
-        if bound == "tensor" and p.dtype != 1:
-            # float32 problems run the GEMMs on CUDA cores: FFMA peak of the part
+        if bound == "tensor" and p.dtype != 1 and tf32_path(p):
+            # float32 problems with 16-byte aligned rows: tcgen05 kind::tf32,
+            # three products per multiply (hi*hi + hi*lo + lo*hi)
+            achieved = amount / (ms / 1e3) / 1e12
+            peak, unit = peaks["bf16_tflops"] * TF32_PER_BF16 / 3, "TFLOP/s"
+            peak_src = (f"derived: {src} bf16_tflops (burst) x nominal tf32/bf16 "
+                        f"{TF32_PER_BF16:.3f} / 3 products")
+        elif bound == "tensor" and p.dtype != 1:
+            # other float32 problems run the GEMMs on CUDA cores: FFMA peak of the part
             bound = "alu"
             achieved = amount / (ms / 1e3) / 1e12
             peak, sms, mhz = fp32_alu_tflops(dev)

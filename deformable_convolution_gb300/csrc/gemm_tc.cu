@@ -69,6 +69,7 @@ struct TcArgs {
   // the tile grid (x: column tiles, y: row tiles, z: images or splits); a
   // persistent launch runs tiles blockIdx.x, + gridDim.x, ... of it
   int vgx, vgy, vgz, persistent;
+  int flat;  // FWDC: column tiles run over the flat pixel index b * howo + q of all images
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -217,7 +218,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
 // MH = 2: one CTA computes 256 rows of the output (two M = 128 halves, two
 // accumulators side by side in tensor memory) against one B tile, so the
 // large B operand (the deformed map) is read once instead of once per half.
-template <int KIND, int BN, int MH = 1>
+template <int KIND, int BN, int MH = 1, int NACC = 2>
 struct Cfg {
   static constexpr int kAHalf = kBM * kBK * 2;
   static constexpr int kABytes = MH * kAHalf;
@@ -226,12 +227,16 @@ struct Cfg {
   // GCOL reduces over C_out only (a few k-blocks): two stages, so that three
   // CTAs fit on an SM; the long reductions keep a deeper ring.
   // GCOL has two k-blocks; four stages let two FWD CTAs share an SM
-  static constexpr int kStages = is_gcol(KIND) ? (BN == 256 ? 3 : 2) : 4;
+  // (as many as fit, up to four, for the wide single-wave tiles)
+  static constexpr int kStages =
+      is_gcol(KIND) ? (BN == 256 ? 3 : 2) : ((225 * 1024) / kStage < 4 ? (225 * 1024) / kStage : 4);
   // tensor-memory columns of one half's accumulator: BN rounded up to a
-  // power of two; two accumulators (the epilogue of one tile overlaps the
-  // next tile's MMAs), allocated as a power of two
+  // power of two; NACC accumulators (two: the epilogue of one tile overlaps
+  // the next tile's MMAs; one: wide tiles of a single-wave launch), allocated
+  // as a power of two
   static constexpr int kHS = BN <= 32 ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
-  static constexpr int kTmemCols = 2 * MH * kHS;
+  static constexpr int kTmemCols = NACC * MH * kHS;
+  static_assert(kTmemCols <= 512, "tensor memory holds 512 columns");
   // GCOL's bf16 store staging: 4 warps x BN/64 boxes of 32 x 64
   static constexpr int kStg = is_gcol(KIND) ? 4 * (BN / 64) * 4096 : 0;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStage + kStg + 256;
@@ -239,11 +244,11 @@ struct Cfg {
   static constexpr int kBMn = (KIND == GW || KIND == FWDC) ? 0 : 1;
 };
 
-template <int KIND, int BN, int MH = 1>
+template <int KIND, int BN, int MH = 1, int NACC = 2>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, TcArgs a) {
-  using C = Cfg<KIND, BN, MH>;
+  using C = Cfg<KIND, BN, MH, NACC>;
   static_assert(MH == 1 || KIND == FWDC || KIND == GWC, "two M halves: forward and weight-gradient kinds");
   constexpr uint32_t kAcc = MH * C::kHS;  // tensor-memory columns of one accumulator
   extern __shared__ unsigned char smem_raw[];
@@ -355,7 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // A: w' rows m0.. (and m0 + 128..), k-block kb; B: BN pixels of image z, k-block kb
             tma_2d(sa, &tmA, &full[s], kb * kBK, m0);
             if (MH == 2) tma_2d(sa + C::kAHalf, &tmA, &full[s], kb * kBK, m0 + kBM);
-            tma_3d(sb, &tmB, &full[s], kb * kBK, n0, z);
+            if (a.flat)
+              tma_2d(sb, &tmB, &full[s], kb * kBK, n0);
+            else
+              tma_3d(sb, &tmB, &full[s], kb * kBK, n0, z);
           } else if (KIND == GCOLC) {
             // A: grad_y rows kb*64.. (output channels) x 128 pixels of image z,
             // as two 64-pixel MN chunks; B: w' rows kb*64.. x BN columns
@@ -390,9 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int it = 0;
       for (int j = 0; j < ntiles && ok; ++j) {
         const Tile T = tile(j);
-        const int b = j & 1;
-        // accumulator b was drained by the epilogue (its use two tiles ago)
-        if (j >= 2 && !mbar_wait(&tempty[b], ((j >> 1) - 1) & 1)) {
+        const int b = j % NACC;
+        // accumulator b was drained by the epilogue (its use NACC tiles ago)
+        if (j >= NACC && !mbar_wait(&tempty[b], ((j / NACC) - 1) & 1)) {
           ok = false;
           break;
         }
@@ -438,8 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < ntiles; ++j) {
       const Tile T = tile(j);
       const int m0 = T.m0, n0 = T.n0, z = T.z, nkb = T.nkb;
-      const int b = j & 1;
-      ok = ok && __all_sync(0xffffffffu, mbar_wait(&tfull[b], (j >> 1) & 1));
+      const int b = j % NACC;
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&tfull[b], (j / NACC) & 1));
       if (!ok) break;
       tc_fence_after();
       if (is_gcol(KIND)) {
@@ -468,6 +476,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             float* part = reinterpret_cast<float*>(smem);
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) part[(c * 32 + jj) * kBM + row] = __uint_as_float(r[jj]);
+          }
+        } else if (is_fwd(KIND) && a.flat) {
+          // flat pixel index f = b * howo + q over all images
+          if (m >= a.c_out) continue;
+          const long long total = (long long)a.nimg * a.howo;
+          if (n_first >= total) continue;
+          const int zb = n_first / a.howo, q = n_first - zb * a.howo;
+          __nv_bfloat16* y = static_cast<__nv_bfloat16*>(a.out);
+          if (q + 32 <= a.howo) {
+            store_y_row(y + ((long long)zb * a.c_out + m) * a.howo + q, r, q, a.howo);
+          } else {
+            // the chunk crosses into the next image (or past the last pixel)
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              const int qj = q + jj;
+              const bool next = qj >= a.howo;
+              if (n_first + jj < total)
+                y[((long long)(zb + (next ? 1 : 0)) * a.c_out + m) * a.howo + (next ? qj - a.howo : qj)] =
+                    __float2bfloat16_rn(__uint_as_float(r[jj]));
+            }
           }
         } else if (is_fwd(KIND)) {
           if (m >= a.c_out) continue;
@@ -899,11 +927,11 @@ int gemm_sm_count();
 // `grid` is the tile grid.  Without a cluster the launch is persistent: one
 // CTA per resident slot (shared and tensor memory bound it), each taking
 // tiles blockIdx.x, + gridDim.x, ... of the tile grid.
-template <int KIND, int BN, int MH = 1>
+template <int KIND, int BN, int MH = 1, int NACC = 2>
 cudaError_t launch(const CUtensorMap& A, const CUtensorMap& B, const CUtensorMap& Cm,
                    const TcArgs& args, dim3 grid, cudaStream_t s, int cluster_y = 1) {
-  using C = Cfg<KIND, BN, MH>;
-  auto k = tc_gemm<KIND, BN, MH>;
+  using C = Cfg<KIND, BN, MH, NACC>;
+  auto k = tc_gemm<KIND, BN, MH, NACC>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
   if (e != cudaSuccess) return e;
   TcArgs a = args;
@@ -1103,10 +1131,26 @@ cudaError_t launch_gemm_fwd_cl(const GemmArgs& ga, cudaStream_t s) {
   a.out = ga.y;
   if (bn == 128 && g.c_out > kBM) {
     // all output channels of a pixel tile in one CTA (two halves): the map is
-    // read once; 96-pixel tiles (more tiles than SMs by a finer grain)
+    // read once.  When 192-pixel tiles over the flat pixel index of all
+    // images fit in one wave, those (one accumulator: 2 x 256 tensor-memory
+    // columns; per k-block 56 KB filled for 6.3 MFLOP; a 32-pixel chunk of
+    // the epilogue crosses at most one image boundary); else 96-pixel tiles
+    // per image
+    const long long total = (long long)g.n * g.howo;
+    const long long flat_tiles = ceil_div_ll(total, 192) * ceil_div_ll(g.c_out, 2 * kBM);
+    a.fwd_split = 1;
+    if (flat_tiles <= gemm_sm_count() && total < INT_MAX && g.howo >= 32) {
+      CUtensorMap Bf;
+      const cuuint64_t dims[2] = {(cuuint64_t)g.kdim, (cuuint64_t)total};
+      const cuuint64_t strides[1] = {(cuuint64_t)g.kdim * 2};
+      const cuuint32_t box[2] = {64, 192};
+      if (!make_map(&Bf, ga.col, 2, dims, strides, box)) return cudaErrorInvalidValue;
+      a.flat = 1;
+      dim3 grid((unsigned)ceil_div_ll(total, 192), (unsigned)ceil_div_ll(g.c_out, 2 * kBM), 1);
+      return launch<FWDC, 192, 2, 1>(A, Bf, A, a, grid, s);
+    }
     CUtensorMap B96;
     if (!colc_map(&B96, ga.col, g, 96)) return cudaErrorInvalidValue;
-    a.fwd_split = 1;
     dim3 grid((unsigned)ceil_div_ll(g.howo, 96), (unsigned)ceil_div_ll(g.c_out, 2 * kBM), (unsigned)g.n);
     return launch<FWDC, 96, 2>(A, B96, A, a, grid, s);
   }
@@ -1170,16 +1214,19 @@ cudaError_t launch_gemm_gw_cl(const GemmArgs& ga, cudaStream_t s) {
   a.out = ga.gw_perm ? ga.gw_perm : ga.gw;
   // all output channels of a column tile in one CTA when C_out > 128 (two
   // halves: the map is read once); the pixels split over CTAs so that the
-  // grid is one wave
+  // grid is one wave.  (256-column tiles with one accumulator fill fewer
+  // bytes per flop but need twice the splits, and the float4 atomics that
+  // add the splits into grad_W then cost more than they save.)
   const int mh = g.c_out > kBM ? 2 : 1;
-  const long long tiles = ceil_div_ll(g.kdim, 128) * ceil_div_ll(g.c_out, kBM * mh);
+  const int bn = 128;
+  const long long tiles = ceil_div_ll(g.kdim, bn) * ceil_div_ll(g.c_out, kBM * mh);
   const int sms = gemm_sm_count();
   long long splits = sms / tiles;
   if (splits > a.kb_total) splits = a.kb_total;
   if (splits < 1) splits = 1;
   a.kb_per_split = (int)ceil_div_ll(a.kb_total, splits);
   splits = ceil_div_ll(a.kb_total, a.kb_per_split);
-  dim3 grid((unsigned)ceil_div_ll(g.kdim, 128), (unsigned)ceil_div_ll(g.c_out, kBM * mh), (unsigned)splits);
+  dim3 grid((unsigned)ceil_div_ll(g.kdim, bn), (unsigned)ceil_div_ll(g.c_out, kBM * mh), (unsigned)splits);
   return mh == 2 ? launch<GWC, 128, 2>(A, B, A, a, grid, s) : launch<GWC, 128>(A, B, A, a, grid, s);
 }
 

@@ -466,13 +466,17 @@ def test_sampled_gemm_forward_early_layer_full_batch():
 # channels-last sampling backward (pixel-major gcol from the tensor-core GEMM,
 # grad_x gathered per window position into an NHWC accumulator).  Geometries:
 # 64 / 128 / 256 channels (2, 4, 8 channels per lane), stride 2, dilation 2
-# with a ragged last row of tiles, a 3 x 4 filter; then margin 0 with wide
-# offsets, where most samples leave the window and take the global path.
+# with a ragged last row of tiles, a 3 x 4 filter; 136 output channels over
+# 8 images of 36 x 36 (forward GEMM tiles over the flat pixel index of all
+# images, 32-pixel chunks crossing image boundaries, a ragged second half of
+# output channels); then margin 0 with wide offsets, where most samples leave
+# the window and take the global path.
 CL_BACKWARD_GEOMETRIES = [
     (2, 64, 20, 24, 32, 3, 3, 1, 1, 1, 1),
     (1, 128, 18, 32, 40, 3, 3, 2, 1, 1, 1),
     (2, 256, 15, 16, 24, 3, 3, 1, 2, 2, 1),
     (1, 64, 16, 24, 16, 3, 4, 1, 1, 1, 1),
+    (8, 64, 36, 36, 136, 3, 3, 1, 1, 1, 1),
 ]
 
 
