@@ -23,8 +23,8 @@
 //
 // Weight part (k4cl_weight): the reduction runs over every pixel of the batch,
 // so the CTAs split the pixels into chunks and the channels into slices of
-// 64; each warp owns one tap and keeps D[c][m] = sum_px x[pos(px,k)][c] *
-// goff[m][px] for the slice in registers (mma.sync, A = x^T from the staged
+// 64; two warps own each tap and keep D[c][m] = sum_px x[pos(px,k)][c] *
+// goff[m][px] for 32 channels each in registers (mma.sync, A = x^T from the staged
 // NHWC window by ldmatrix.trans, B = goff).  Each CTA writes its partial sums
 // once; a small kernel adds the chunks (and the bias partials) in a fixed
 // order.
@@ -43,6 +43,7 @@ constexpr int kTY = 8, kTX = 16, kQ = kTY * kTX;  // positions per CTA
 constexpr int kInThreads = 256;
 static_assert(kInThreads % kQ == 0, "each input-part thread keeps one position");
 constexpr int kMaxKMp = 192;  // (tap, offset channel) pairs, padded to 16
+constexpr int kMaxK = 9;      // taps (the offset channels are M = 2K)
 
 __host__ __device__ inline int km_padded(const Geom& g) { return (g.K * g.M + 15) / 16 * 16; }
 __host__ __device__ inline int in_pitch(const Geom& g) { return km_padded(g) + 8; }  // bf16 elements
@@ -131,6 +132,24 @@ __global__ void __launch_bounds__(kInThreads, 2) k4cl_input(K4InArgs a) {
   const int wlo = floor_div(x0 + g.pw - (g.kw - 1) * g.dw, g.sw);
   float* G = reinterpret_cast<float*>(smem + in_g_off(g, CPC));  // [M][GY][GX]
   pdl_wait();  // goff and gx_nhwc from the sampling backward, Bt from the weight part
+  // goff tile: a warp per (m, row), lanes over the columns (GX <= 32), all
+  // rows in flight as 4-byte asynchronous copies (zero-filled outside goff)
+  {
+    const float* gimg = a.goff + (size_t)n * M * g.howo;
+    const int wo = wlo + lane;
+    const bool colok = lane < GX && wo >= 0 && wo < g.wo;
+    if (lane < GX) {
+      for (int r = warp; r < M * GY; r += kInThreads / 32) {
+        const int m = r / GY, ho = hlo + (r - m * GY);
+        const bool ok = colok && ho >= 0 && ho < g.ho;
+        const float* src = ok ? gimg + (size_t)m * g.howo + (size_t)ho * g.wo + wo : gimg;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(px::smem_u32(G + r * GX + lane)),
+                     "l"(src), "r"(ok ? 4 : 0)
+                     : "memory");
+      }
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
   // B rows: Bt[cbeg + c][0 .. KMp) by 16-byte asynchronous copies
   {
     // a warp per row, lanes over its 16-byte pieces (KMp / 8 <= 24)
@@ -143,29 +162,7 @@ __global__ void __launch_bounds__(kInThreads, 2) k4cl_input(K4InArgs a) {
                      : "memory");
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
-  // goff tile: a warp per (m, row), lanes over the columns (GX <= 32), four
-  // rows in flight per warp
-  {
-    const float* gimg = a.goff + (size_t)n * M * g.howo;
-    const int wo = wlo + lane;
-    const bool colok = lane < GX && wo >= 0 && wo < g.wo;
-    for (int r0 = warp; r0 < M * GY; r0 += 4 * (kInThreads / 32)) {
-      float v[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int r = r0 + u * (kInThreads / 32);
-        const int m = r / GY, ho = hlo + (r - m * GY);
-        v[u] = 0.f;
-        if (r < M * GY && colok && ho >= 0 && ho < g.ho)
-          v[u] = __ldg(gimg + (size_t)m * g.howo + (size_t)ho * g.wo + wo);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int r = r0 + u * (kInThreads / 32);
-        if (r < M * GY && lane < GX) G[r * GX + lane] = v[u];
-      }
-    }
-  }
+  asm volatile("cp.async.wait_group 1;" ::: "memory");  // the goff tile (B may still be in flight)
   __syncthreads();
   // A[q][k*M + m] = goff[m][pixel whose tap k reads position q], 0 if none:
   // a thread per (q, k), m pairs written as one word (M is even)
@@ -191,10 +188,13 @@ __global__ void __launch_bounds__(kInThreads, 2) k4cl_input(K4InArgs a) {
     }
     uint32_t* row = reinterpret_cast<uint32_t*>(A + (size_t)q * P + k * M);
     const int plane = GY * GX;
-    for (int m = 0; m < M; m += 2) {
+    const float* gq = G + (gi >= 0 ? gi : 0);
+#pragma unroll
+    for (int m = 0; m < 2 * kMaxK; m += 2) {
+      if (m >= M) break;
       uint32_t w = 0u;
       if (gi >= 0)
-        w = (uint32_t)bf16_bits_rn(G[m * plane + gi]) | ((uint32_t)bf16_bits_rn(G[(m + 1) * plane + gi]) << 16);
+        w = (uint32_t)bf16_bits_rn(gq[m * plane]) | ((uint32_t)bf16_bits_rn(gq[(m + 1) * plane]) << 16);
       row[m >> 1] = w;
     }
   }
@@ -258,13 +258,25 @@ __global__ void __launch_bounds__(kInThreads, 2) k4cl_input(K4InArgs a) {
     }
   }
   __syncthreads();
-  // grad_x rows: a warp per channel at a time, lanes over 32 positions (two
-  // rows of the tile)
+  // grad_x rows: a warp per channel at a time, lanes over four positions
+  // each (one 16-byte store when the row length keeps them aligned), else
+  // over 32 positions (two rows of the tile)
   float* dst = a.grad_x + ((size_t)n * C + cbeg) * g.hw;
-  for (int e = warp; e < CPC * (kQ / 32); e += kInThreads / 32) {
-    const int c = e / (kQ / 32), q = (e - c * (kQ / 32)) * 32 + lane;
+  if (g.w % 4 == 0) {
+    static_assert(kTX % 4 == 0 && kQ == 4 * 32 && TP % 4 == 0, "four positions per lane");
+    const int q = lane * 4;
     const int y = y0 + q / kTX, x = x0 + q % kTX;
-    if (y < g.h && x < g.w) dst[(size_t)c * g.hw + (size_t)y * g.w + x] = T[(size_t)c * TP + q];
+    if (y < g.h && x < g.w) {
+      for (int c = warp; c < CPC; c += kInThreads / 32)
+        *reinterpret_cast<float4*>(dst + (size_t)c * g.hw + (size_t)y * g.w + x) =
+            *reinterpret_cast<const float4*>(T + (size_t)c * TP + q);
+    }
+  } else {
+    for (int e = warp; e < CPC * (kQ / 32); e += kInThreads / 32) {
+      const int c = e / (kQ / 32), q = (e - c * (kQ / 32)) * 32 + lane;
+      const int y = y0 + q / kTX, x = x0 + q % kTX;
+      if (y < g.h && x < g.w) dst[(size_t)c * g.hw + (size_t)y * g.w + x] = T[(size_t)c * TP + q];
+    }
   }
   pdl_release();
 }
@@ -291,9 +303,10 @@ __host__ inline size_t weight_smem(uint32_t win_pitch) {
   return 1024 + kWStages * ((size_t)win_pitch + 24 * kGbPitch * 2) + 64;
 }
 
-// One warp per tap (K warps), M = 2K offset channels: warp k also loads
-// goff rows k and k + K of each tile (lane l: pixels 4l .. 4l + 3).
-__global__ void __launch_bounds__(288, 1)
+// Two warps per tap (2K warps), M = 2K offset channels: warp w takes tap
+// k = w % K for channels 32 hh .. 32 hh + 31 of the slice (hh = w / K) and
+// loads goff row k + hh K of each tile (lane l: pixels 4l .. 4l + 3).
+__global__ void __launch_bounds__(576, 1)
     k4cl_weight(const __grid_constant__ CUtensorMap xmap, K4WArgs a) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = px::align1024(smem_raw);
@@ -309,7 +322,7 @@ __global__ void __launch_bounds__(288, 1)
       reinterpret_cast<unsigned short*>(smem + kWStages * (size_t)a.win_pitch);  // [kWStages][24][pitch]
   uint64_t* wfull = reinterpret_cast<uint64_t*>(gb + kWStages * 24 * kGbPitch);
   const int per_img = a.tiles_x * a.tiles_y;
-  const int k = warp;  // this warp's tap
+  const int k = warp % K, hh = warp / K;  // this warp's tap and channel half
   const int ki = k / g.kw, kj = k - ki * g.kw;
 
   if (tid == 0) {
@@ -337,42 +350,38 @@ __global__ void __launch_bounds__(288, 1)
     px::tma_load_4d(win + (size_t)s * a.win_pitch, &xmap, &wfull[s], cbeg, wo0 * g.sw - g.pw,
                     ho0 * g.sh - g.ph, n);
   };
-  // goff rows k and k + K of a tile, pixels 4l .. 4l + 3 of lane l
-  auto load_goff = [&](int t, float4* v) {
+  // goff row k + hh K of a tile, pixels 4l .. 4l + 3 of lane l
+  const int mrow = k + hh * K;
+  auto load_goff = [&](int t, float4& v) {
     int n, ho0, wo0;
     tile_at(t, n, ho0, wo0);
     const int ho = ho0 + (lane >> 2), wo = wo0 + (lane & 3) * 4;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      v[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (ho < g.ho && wo < g.wo) {
-        const float* src = a.goff + ((size_t)n * M + k + h * K) * g.howo + (size_t)ho * g.wo + wo;
-        if (wo + 3 < g.wo && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
-          v[h] = __ldg(reinterpret_cast<const float4*>(src));
-        } else {
-          v[h].x = __ldg(src);
-          if (wo + 1 < g.wo) v[h].y = __ldg(src + 1);
-          if (wo + 2 < g.wo) v[h].z = __ldg(src + 2);
-          if (wo + 3 < g.wo) v[h].w = __ldg(src + 3);
-        }
+    v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ho < g.ho && wo < g.wo) {
+      const float* src = a.goff + ((size_t)n * M + mrow) * g.howo + (size_t)ho * g.wo + wo;
+      if (wo + 3 < g.wo && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+        v = __ldg(reinterpret_cast<const float4*>(src));
+      } else {
+        v.x = __ldg(src);
+        if (wo + 1 < g.wo) v.y = __ldg(src + 1);
+        if (wo + 2 < g.wo) v.z = __ldg(src + 2);
+        if (wo + 3 < g.wo) v.w = __ldg(src + 3);
       }
     }
   };
-  float bsum[2] = {0.f, 0.f};
-  auto store_goff = [&](int s, const float4* v) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      bsum[h] += (v[h].x + v[h].y) + (v[h].z + v[h].w);
-      uint2 w;
-      w.x = (uint32_t)bf16_bits_rn(v[h].x) | ((uint32_t)bf16_bits_rn(v[h].y) << 16);
-      w.y = (uint32_t)bf16_bits_rn(v[h].z) | ((uint32_t)bf16_bits_rn(v[h].w) << 16);
-      reinterpret_cast<uint2*>(gb + ((size_t)s * 24 + k + h * K) * kGbPitch)[lane] = w;
-    }
+  float bsum = 0.f;
+  auto store_goff = [&](int s, const float4& v) {
+    bsum += (v.x + v.y) + (v.z + v.w);
+    uint2 w;
+    w.x = (uint32_t)bf16_bits_rn(v.x) | ((uint32_t)bf16_bits_rn(v.y) << 16);
+    w.y = (uint32_t)bf16_bits_rn(v.z) | ((uint32_t)bf16_bits_rn(v.w) << 16);
+    reinterpret_cast<uint2*>(gb + ((size_t)s * 24 + mrow) * kGbPitch)[lane] = w;
   };
 
-  float acc[4][3][4];
+  // D[c][m] for this warp's 32 channels (two 16-channel tiles) and tap
+  float acc[2][3][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 2; ++i)
 #pragma unroll
     for (int j = 0; j < 3; ++j)
 #pragma unroll
@@ -395,7 +404,7 @@ __global__ void __launch_bounds__(288, 1)
     }
   }
   pdl_wait();  // goff comes from the sampling backward
-  float4 g1[2], g2[2];  // goff of the next two tiles
+  float4 g1, g2;  // goff of the next two tiles
   if (tb < te) {
     if (tid == 0) {
       issue(tb, 0);
@@ -430,9 +439,9 @@ __global__ void __launch_bounds__(288, 1)
         ldsm_x2(gbb + (uint32_t)(((16 + (lane & 7)) * kGbPitch + pr * kWX + ((lane >> 3) & 1) * 8) * 2),
                 bf + 4);
 #pragma unroll
-        for (int ct = 0; ct < 4; ++ct) {
+        for (int ct = 0; ct < 2; ++ct) {
           uint32_t af[4];
-          const uint32_t piece = (uint32_t)(ct * 2 + a_half);
+          const uint32_t piece = (uint32_t)((2 * hh + ct) * 2 + a_half);
           ldsm_x4_t(wb + pos * 128u + ((piece ^ (pos & 7u)) << 4), af);
           mma16816(acc[ct][0], af, bf[0], bf[1]);
           mma16816(acc[ct][1], af, bf[2], bf[3]);
@@ -441,30 +450,26 @@ __global__ void __launch_bounds__(288, 1)
       }
     }
     if (t + 1 < te) store_goff((i + 1) % kWStages, g1);
-    g1[0] = g2[0];
-    g1[1] = g2[1];
+    g1 = g2;
   }
   // this CTA's partial sums: D[c][m] of tap k -> part[chunk][m][c][k]
   float* dst = a.part + (size_t)chunk * M * C * K;
   const int gid = lane >> 2, tig = lane & 3;
 #pragma unroll
-  for (int ct = 0; ct < 4; ++ct)
+  for (int ct = 0; ct < 2; ++ct)
 #pragma unroll
     for (int nt = 0; nt < 3; ++nt)
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int c = cbeg + ct * 16 + gid + 8 * (r >> 1);
+        const int c = cbeg + (2 * hh + ct) * 16 + gid + 8 * (r >> 1);
         const int m = nt * 8 + 2 * tig + (r & 1);
         if (m < M) dst[((size_t)m * C + c) * K + k] = acc[ct][nt][r];
       }
   if (slice == 0) {
+    float v = bsum;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float v = bsum[h];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) a.bpart[(size_t)chunk * M + k + h * K] = v;
-    }
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) a.bpart[(size_t)chunk * M + mrow] = v;
   }
   pdl_release();
 }
@@ -565,7 +570,7 @@ WeightShape weight_shape(const Geom& g, int sms) {
 }  // namespace
 
 bool k4cl_supported(const Geom& g) {
-  if (g.groups != 1 || g.M != 2 * g.K || g.K > 9 || km_padded(g) > kMaxKMp) return false;
+  if (g.groups != 1 || g.M != 2 * g.K || g.K > kMaxK || km_padded(g) > kMaxKMp) return false;
   if (g.c_in % 64 != 0 || g.c_in > 256) return false;
   const int sms = sm_count4();
   if (sms <= 0) return false;
@@ -644,7 +649,7 @@ cudaError_t launch_k4cl_weight(const K4ClArgs& in, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   void* args[] = {&xmap, &a};
   return launch_pdl4((const void*)k4cl_weight, dim3((unsigned)w.slices, (unsigned)w.nchunks),
-                     dim3((unsigned)(32 * g.K)), smem, s, args);
+                     dim3((unsigned)(64 * g.K)), smem, s, args);
 }
 
 cudaError_t launch_k4cl_reduce(const K4ClArgs& in, cudaStream_t s) {
