@@ -44,6 +44,7 @@ constexpr int kInThreads = 256;
 static_assert(kInThreads % kQ == 0, "each input-part thread keeps one position");
 constexpr int kMaxKMp = 192;  // (tap, offset channel) pairs, padded to 16
 constexpr int kMaxK = 9;      // taps (the offset channels are M = 2K)
+constexpr int kPermCh = 128;  // input channels per block of the grad_w permutation
 
 __host__ __device__ inline int km_padded(const Geom& g) { return (g.K * g.M + 15) / 16 * 16; }
 __host__ __device__ inline int in_pitch(const Geom& g) { return km_padded(g) + 8; }  // bf16 elements
@@ -483,20 +484,29 @@ __global__ void __launch_bounds__(256) k4cl_reduce(const float* __restrict__ par
                                                    const float* __restrict__ gw_perm, float* grad_w,
                                                    int wcount, int C, int K) {
   __shared__ float red[8][33];
+  __shared__ float tr[kPermCh * kMaxK];
   pdl_wait();
-  // grad_w[o][c][k] = gw_perm[o][k][c] (the main weight gradient, added in
-  // w' order by the GEMM)
-  if (gw_perm) {
-    const int nth = gridDim.x * blockDim.x;
-    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < wcount; e += nth) {
-      const int o = e / (C * K), r = e - o * (C * K);
-      const int c = r / K, k = r - c * K;
-      grad_w[e] = gw_perm[(size_t)o * C * K + (size_t)k * C + c];
-    }
+  const int nred = (count + 31) / 32;
+  if ((int)blockIdx.x >= nred) {
+    // grad_w[o][c][k] = gw_perm[o][k][c] (the main weight gradient, added in
+    // w' order by the GEMM): one block per (o, kPermCh channels), the slice
+    // [K][kPermCh] read by rows and written as one run of kPermCh * K floats
+    const int b = (int)blockIdx.x - nred;
+    const int cch = (C + kPermCh - 1) / kPermCh;
+    const int o = b / cch, c0 = (b - o * cch) * kPermCh;
+    const int nc = min(kPermCh, C - c0);
+    const float* src = gw_perm + (size_t)o * C * K;
+    for (int k = 0; k < K; ++k)
+      for (int c = threadIdx.x; c < nc; c += blockDim.x) tr[c * K + k] = src[(size_t)k * C + c0 + c];
+    __syncthreads();
+    float* dst = grad_w + ((size_t)o * C + c0) * K;
+    for (int e = threadIdx.x; e < nc * K; e += blockDim.x) dst[e] = tr[e];
+    pdl_release();
+    return;
   }
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int i = blockIdx.x * 32 + tx;
-  const bool bias = gb_off != nullptr && blockIdx.x == gridDim.x - 1;  // the last block also sums the bias
+  const bool bias = gb_off != nullptr && (int)blockIdx.x == nred - 1;  // the last sum block also adds the bias
   float v = 0.f, vb = 0.f;
   if (i < count)
     for (int c = ty; c < nchunks; c += 8) v += part[(size_t)c * count + i];
@@ -666,8 +676,11 @@ cudaError_t launch_k4cl_reduce(const K4ClArgs& in, cudaStream_t s) {
   float* gwd = in.grad_w;
   int wcount = in.c_out * g.c_in * g.K, C = g.c_in, K = g.K;
   void* args[] = {&part, &bpart, &gw, &gb, &count, &M, &nch, &gwp, &gwd, &wcount, &C, &K};
-  return launch_pdl4((const void*)k4cl_reduce, dim3((unsigned)ceil_div_ll(count, 32)), dim3(256), 0, s,
-                     args);
+  // blocks [0, count / 32): the chunk sums; then, with gw_perm, one block per
+  // (output channel, kPermCh input channels) for the permutation
+  const long long nperm = gwp ? (long long)in.c_out * ceil_div_ll(g.c_in, kPermCh) : 0;
+  return launch_pdl4((const void*)k4cl_reduce, dim3((unsigned)(ceil_div_ll(count, 32) + nperm)), dim3(256), 0,
+                     s, args);
 }
 
 // This file's share of dc_device_error.
