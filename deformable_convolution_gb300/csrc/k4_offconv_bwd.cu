@@ -27,8 +27,11 @@ struct Plan {
   int ps;  // pixel stride of the fp32 goff array
   int cpc, nslices;
   int rows, cols, plane;  // staged window: the band's receptive field
-  size_t off_halo, off_gx, off_goff, off_tab, smem;
+  size_t off_halo, off_gx, off_goff, off_tab, off_w, smem;
 };
+
+// offset channels per pass of the input gradient (w_off staged per pass)
+constexpr int kMc = 12;
 
 __host__ Plan make_plan(const Geom& g, dc_dtype dt) {
   const bool bf16 = dt == DC_BF16;
@@ -57,6 +60,9 @@ __host__ Plan make_plan(const Geom& g, dc_dtype dt) {
       at += (size_t)(p.ps + g.K) * 4;
       p.off_goff = at;
       at += (size_t)g.M * p.ps * 4;
+      at = (at + 15) / 16 * 16;
+      p.off_w = at;  // w_off of the slice for one pass: [cpc][K][kMc] fp32
+      at += (size_t)cpc * g.K * kMc * 4;
       p.smem = at;
       if (best.smem == 0 || p.smem < best.smem) best = p;
       if (p.smem <= kSmemBudget) return p;
@@ -120,28 +126,39 @@ __global__ void __launch_bounds__(kThreads) k4_offconv_bwd(OffconvBwdArgs a, Pla
     __syncthreads();
     // ---------------------------------------------------------------- offset-conv input gradient
     // for each (channel, pixel): sum over offset channels of goff * w_off at every
-    // tap, added to the window position that tap reads
-    constexpr int kMc = 12;
+    // tap, added to the window position that tap reads; per pass of kMc offset
+    // channels the slice's w_off is staged as [channel][tap][m] (zeros past M
+    // and past the last channel), so the kMc-term sums add in the same order
     {
-      const long long mstride = (long long)g.c_in * g.K;
-      band::Walk2 w;
-      w.init(tid, kThreads, npx);
-      while (w.a < ncur) {
-        const int cl = w.a, px = w.b;
-        w.next();
-        const int e = pix[px];
-        const int pos = ((e >> 16) * g.sh + margin) * pl.cols + (e & 0xffff) * g.sw + margin;
-        const T* wc = w_off + (long long)(c_begin + cl) * g.K;
-        float* gp = gxs + cl * PL + pos;
-        for (int m0 = 0; m0 < M; m0 += kMc) {
+      float* wsm = reinterpret_cast<float*>(smem + pl.off_w);
+      const int wn = pl.cpc * g.K * kMc;
+      for (int m0 = 0; m0 < M; m0 += kMc) {
+        __syncthreads();  // the previous pass is done with wsm
+        for (int idx = tid; idx < wn; idx += kThreads) {
+          const int cl = idx / (g.K * kMc), r = idx - cl * (g.K * kMc);
+          const int k = r / kMc, t = r - k * kMc;
+          wsm[idx] = (cl < ncur && m0 + t < M)
+                         ? ld_f(w_off + ((long long)(m0 + t) * g.c_in + c_begin + cl) * g.K + k)
+                         : 0.f;
+        }
+        __syncthreads();
+        band::Walk2 w;
+        w.init(tid, kThreads, npx);
+        while (w.a < ncur) {
+          const int cl = w.a, px = w.b;
+          w.next();
+          const int e = pix[px];
+          const int pos = ((e >> 16) * g.sh + margin) * pl.cols + (e & 0xffff) * g.sw + margin;
+          float* gp = gxs + cl * PL + pos;
           float gv[kMc];
   #pragma unroll
           for (int t = 0; t < kMc; ++t) gv[t] = (m0 + t < M) ? goff[(m0 + t) * PS + px] : 0.f;
+          const float* wk = wsm + cl * g.K * kMc;
           for (int k = 0; k < g.K; ++k) {
             float s = 0.f;
   #pragma unroll
             for (int t = 0; t < kMc; ++t)
-              if (m0 + t < M) s = __fmaf_rn(gv[t], ld_f(wc + (long long)(m0 + t) * mstride + k), s);
+              if (m0 + t < M) s = __fmaf_rn(gv[t], wk[k * kMc + t], s);
             if (s != 0.f) atomicAdd(gp + tapoff[k], s);
           }
         }
