@@ -530,9 +530,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!p_sync_and(ok)) break;  // a wait expired: every P thread leaves together
       prefetch_oin(t + tstep, s ^ 1);
       const float* oin_t = oin + (size_t)s * M * pl.npx;
+      // the copy of the next tile's window (tile i + 1), into the buffer of
+      // tile i + 1 - nstages once the S warps are done with that tile: thread
+      // 0 polls for that after each phase of this tile and issues it as soon
+      // as the buffer is free (the last check waits), so that the window has
+      // landed when this tile is done
+      const int tn = t + tstep;
+      const int jn = i + 1 - pl.nstages;  // the tile that last used that buffer
+      bool pend = (sampling || pl.nstages == 1) && jn >= 0 && tn < pl.tiles && tid == 0;
+      const int wbn = pl.nstages == 2 ? (s ^ 1) : 0;
+      const uint32_t epar = (uint32_t)(pl.nstages == 2 ? (jn >> 1) : jn) & 1u;
+      auto try_issue = [&](bool block) {
+        // offsets only, one buffer: the P warps themselves read it, so the
+        // copy waits for the end of the tile
+        if (!pend || (!block && !sampling)) return;
+        const bool ready = !sampling || (block ? px::mbar_wait(&wempty[wbn], epar, &g_cl_error)
+                                               : px::mbar_try_wait(&wempty[wbn], epar));
+        if (ready) {
+          issue(tn, wbn);
+          ++issued[wbn];
+          pend = false;
+        } else if (block) {
+          pend = false;  // the wait expired (flag raised): no copy
+        }
+      };
       if (!kReplay) {
         // ---------------------------------------------------- offset convolution
         offconv_slices<NT, CPS>(pl, g, a.margin, win_u32, wb_u32, toff, partk, warp, lane);
+        try_issue(false);
         p_sync();
         // the slices' partial sums in a fixed order: this CTA's share of the
         // offsets (to part, and into the peer's exchange buffer) or all of them
@@ -552,6 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (pl.csplit == 2) {
           mbar_arrive_remote(mapa(px::smem_u32(&xfull[s]), (uint32_t)peer));
+          try_issue(false);
           const bool okx = mbar_wait_cluster(&xfull[s], par);
           if (!p_sync_and(okx)) break;
           // both halves' sums, identical on both CTAs (a + b == b + a)
@@ -626,19 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         p_sync();
         if (tid == 0) mbar_arrive(&tfull[s]);
       }
-      // the copy of the next tile's window (tile i + 1), into the buffer of
-      // tile i + 1 - nstages once the S warps are done with that tile
-      const int tn = t + tstep;
-      const int jn = i + 1 - pl.nstages;  // the tile that last used that buffer
-      if ((sampling || pl.nstages == 1) && jn >= 0 && tn < pl.tiles && tid == 0) {
-        const int wb = pl.nstages == 2 ? (s ^ 1) : 0;
-        const uint32_t epar = (uint32_t)(pl.nstages == 2 ? (jn >> 1) : jn) & 1u;
-        const bool ok2 = !sampling || px::mbar_wait(&wempty[wb], epar, &g_cl_error);
-        if (ok2) {
-          issue(tn, wb);
-          ++issued[wb];
-        }
-      }
+      try_issue(true);
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     if (tid == 0) {
