@@ -7,10 +7,10 @@
 //   forward  y[b][o][q]     = sum_r w[o][r] * col[r][b][q]
 //   backward gcol[r][b][q]  = sum_o w[o][r] * gy[b][o][q]
 //            gw[o][r]      += sum_{b,q} gy[b][o][q] * col[r][b][q]
-// This file is the float32 path (a bf16/tf32 tensor-core contraction would
-// not hold the float32 tolerance) and the path for bf16 shapes whose rows are
-// not 16-byte aligned; other bf16 problems use the tcgen05 kernels in
-// gemm_tc.cu.
+// This file serves the shapes whose rows are not 16-byte aligned, float32
+// (C_in * K or Ho * Wo not a multiple of 4) and bf16 (not a multiple of 8);
+// other problems use the tcgen05 kernels of gemm_tc.cu (bf16) and
+// gemm_tf32.cu (float32, three-product TF32 split).
 #include "dc_common.cuh"
 
 namespace dc {
