@@ -23,9 +23,11 @@
 //                (sample, corner) pair that lands in the window and in the
 //                image, bucketed by window position (counts and ranks from
 //                shared-memory atomics, a scan, a scatter);
-//   S warps (12) per tile: lanes in groups of cpc / 8 (eight channels
-//                each); the bucketed pairs are split evenly over the groups
-//                and walked in batches of 8: per pair, the sample's gcol
+//   S warps (12) per tile: lanes in groups of cpc / 16 (sixteen channels
+//                each, two 8-channel pieces half a slice apart; eight
+//                channels for 64-channel slices); the bucketed pairs are
+//                split evenly over the groups and walked in batches of 4
+//                (8): per pair, the sample's gcol
 //                slice from shared memory, w * gcol accumulated in registers
 //                (packed fp32 FMAs) for the current position (added to a
 //                float32 NHWC buffer with vector float atomics when the
@@ -250,25 +252,6 @@ __device__ __forceinline__ void xstep(float* v, int lane, int o) {
   }
 }
 
-// Sums each of NB (8 or 16) per-lane values over the warp: lane l returns
-// the total of v[l >> (5 - log2 NB)] (NB shuffles for NB sums).
-template <int NB>
-__device__ __forceinline__ float warp_sum_transpose(float* v, int lane) {
-  if constexpr (NB == 16) {
-    xstep<8>(v, lane, 16);  // entry bit 3 = lane bit 4
-    xstep<4>(v, lane, 8);   // entry bit 2 = lane bit 3
-    xstep<2>(v, lane, 4);   // entry bit 1 = lane bit 2
-    xstep<1>(v, lane, 2);   // entry bit 0 = lane bit 1
-    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
-  } else {
-    xstep<4>(v, lane, 16);  // entry bit 2 = lane bit 4
-    xstep<2>(v, lane, 8);   // entry bit 1 = lane bit 3
-    xstep<1>(v, lane, 4);   // entry bit 0 = lane bit 2
-    float r = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 2);
-    return r + __shfl_xor_sync(0xffffffffu, r, 1);
-  }
-}
-
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
   float2 d;
   asm("{.reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2,%3};\n mov.b64 rb, {%4,%5};\n"
@@ -280,16 +263,17 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 
 __device__ __forceinline__ float2 bf2(uint32_t w) { return make_float2(bf_lo(w), bf_hi(w)); }
 
-// Sums each of 8 per-lane values over a group of L consecutive lanes (L = 8,
-// 16 or 32): lane l of the group returns the total of v[l >> log2(L / 8)].
-template <int L>
-__device__ __forceinline__ float group_sum_transpose8(float* v, int lane) {
-  xstep<4>(v, lane, L / 2);
-  xstep<2>(v, lane, L / 4);
-  xstep<1>(v, lane, L / 8);
+// Sums each of NBV (a power of two, at most L) per-lane values over a group
+// of L consecutive lanes: lane l of the group returns the total of
+// v[l >> log2(L / NBV)].
+template <int NBV, int L>
+__device__ __forceinline__ float group_sum_t(float* v, int lane) {
+  if constexpr (NBV >= 8) xstep<NBV / 2>(v, lane, L / 2);
+  if constexpr (NBV >= 4) xstep<(NBV >= 8 ? NBV / 4 : NBV / 2)>(v, lane, NBV >= 8 ? L / 4 : L / 2);
+  if constexpr (NBV >= 2) xstep<1>(v, lane, L / NBV);
   float r = v[0];
 #pragma unroll
-  for (int o = L / 16; o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  for (int o = L / (2 * NBV); o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
   return r;
 }
 
@@ -563,11 +547,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // lane l holds channels cbeg + l * CPL .. + CPL - 1
     const int sw = warp - kPWarps;
     const int cl = lane * CPL;
-    // lanes in groups of L = cpc / 8, eight channels each
-    constexpr int L = CPL * 4;
-    constexpr int G = 32 / L;  // groups per warp
-    const int gl = lane & (L - 1);
-    const int gid = sw * G + (lane / L);
 
     const uint32_t row_bytes = (uint32_t)pl.cpc * 2u;
     for (int i = 0, t = t0; t < pl.tiles; ++i, t += tstep) {
@@ -590,77 +569,107 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = tid - kPThreads; e < items * 4; e += kSThreads) Dt[e] = 0.f;
       s_sync();
       // ---------------------------------------------- pairs, by window position
-      // Lanes in groups of L = cpc / 8, eight channels each; every group walks
-      // its own contiguous run of the bucketed pairs (the runs split them
-      // evenly over the CTA's groups), eight pairs per batch: per pair the
+      // Lanes in groups of L = cpc / W, W channels each (16 when the slice has
+      // 128 or more channels: a pair's fixed work is shared by twice the
+      // channels and its two halves are independent chains).  Lane l of a
+      // group holds the 8-channel pieces l * 8 + v * cpc / 2 (v < W / 8), so
+      // each 16-byte load of 8 lanes covers one contiguous 128 bytes; every group
+      // walks its own contiguous run of the bucketed pairs (the runs split
+      // them evenly over the CTA's groups), NB pairs per batch: per pair the
       // gradient at its position accumulates in registers (added to the NHWC
       // buffer when the position changes) and the lanes' partial dot products
       // with x at that position are kept; one transposing butterfly per batch
       // sums them over the group.
       {
-        constexpr int NB = 8;
-        const uint32_t xo = (uint32_t)(gl >> 3) * pl.chunk_pitch;
-        const uint32_t xp = (uint32_t)(gl & 7) << 4;
+        constexpr int W = CPL >= 4 ? 16 : 8;  // channels per lane
+        constexpr int NV = W / 8;              // 16-byte pieces per lane
+        constexpr int LW = CPL * 32 / W;       // lanes per group
+        constexpr int GW = 32 / LW;            // groups per warp
+        constexpr int NB = W == 16 ? 4 : 8;  // pairs per batch (registers)
+        const int glw = lane & (LW - 1);
+        const int gidw = sw * GW + (lane / LW);
+        // piece v: channels cp[v] .. + 7 of the slice; its x line offset in
+        // the window (chunk) and 16-byte piece within the swizzled line
+        int cp[NV];
+        uint32_t xo[NV], xpv[NV];
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+          cp[v] = v * (LW * 8) + glw * 8;
+          xo[v] = (uint32_t)(cp[v] >> 6) * pl.chunk_pitch;
+          xpv[v] = (uint32_t)((cp[v] & 63) >> 3) << 4;
+        }
         const int E = pst[npos];
-        const int ngroups = kSWarps * G;
-        const int ebeg = (int)((long long)E * gid / ngroups);
-        const int eend = (int)((long long)E * (gid + 1) / ngroups);
+        const int ngroups = kSWarps * GW;
+        const int ebeg = (int)((long long)E * gidw / ngroups);
+        const int eend = (int)((long long)E * (gidw + 1) / ngroups);
         const int minlen = E / ngroups, maxlen = (E + ngroups - 1) / ngroups;
-        const uint32_t gs = px::smem_u32(gsm0) + (uint32_t)gl * 16u;
-        const uint32_t xs = px::smem_u32(xsm0) + xo;
+        const uint32_t gs = px::smem_u32(gsm0);
+        const uint32_t xs = px::smem_u32(xsm0);
         float* gxrow = a.gx + (((long long)tx.n * g.h + tx.ylo) * g.w + tx.xlo) * C + cbeg;
         int cur = -1;
-        float2 xv[4], acc[4];
+        float2 xv[W / 2], acc[W / 2];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) xv[c] = acc[c] = make_float2(0.f, 0.f);
+        for (int c = 0; c < W / 2; ++c) xv[c] = acc[c] = make_float2(0.f, 0.f);
         // the group's gradient at `pos` into the NHWC buffer (vector float atomics)
         auto flush = [&](int pos) {
-          red_add<8>(gxrow + (long long)pixoff[pos] * C + gl * 8, reinterpret_cast<const float*>(acc));
+          float* dst = gxrow + (long long)pixoff[pos] * C;
+#pragma unroll
+          for (int v = 0; v < NV; ++v) red_add<8>(dst + cp[v], reinterpret_cast<const float*>(acc + 4 * v));
         };
-        // the sample's gcol slice of a pair
-        auto row = [&](const int2 en) {
-          uint4 gw;
-          asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-              : "=r"(gw.x), "=r"(gw.y), "=r"(gw.z), "=r"(gw.w)
-              : "r"(gs + (uint32_t)((en.x & 0xffff) >> 2) * row_bytes));
-          return gw;
+        // the sample's gcol slice of a pair (NV 16-byte pieces)
+        auto row = [&](const int2 en, uint4* gw) {
+          const uint32_t ra = gs + (uint32_t)((en.x & 0xffff) >> 2) * row_bytes;
+#pragma unroll
+          for (int v = 0; v < NV; ++v)
+            asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                : "=r"(gw[v].x), "=r"(gw[v].y), "=r"(gw[v].z), "=r"(gw[v].w)
+                : "r"(ra + (uint32_t)(cp[v] * 2)));
         };
         // one pair: its gradient at the current position, its partial dot product
-        auto pair = [&](const int2 en, const uint4 gw, bool valid, float& dpj) {
+        auto pair = [&](const int2 en, const uint4* gw, bool valid, float& dpj) {
           const int pos = (int)((uint32_t)en.x >> 16);
           if (valid && pos != cur) {
             if (cur >= 0) flush(cur);
             cur = pos;
-            uint4 xw;
-            asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                : "=r"(xw.x), "=r"(xw.y), "=r"(xw.z), "=r"(xw.w)
-                : "r"(xs + (line_off((uint32_t)cur) ^ xp)));
-            xv[0] = bf2(xw.x);
-            xv[1] = bf2(xw.y);
-            xv[2] = bf2(xw.z);
-            xv[3] = bf2(xw.w);
+            const uint32_t lo = line_off((uint32_t)cur);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) acc[c] = make_float2(0.f, 0.f);
+            for (int v = 0; v < NV; ++v) {
+              uint4 xw;
+              asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                  : "=r"(xw.x), "=r"(xw.y), "=r"(xw.z), "=r"(xw.w)
+                  : "r"(xs + xo[v] + (lo ^ xpv[v])));
+              xv[4 * v] = bf2(xw.x);
+              xv[4 * v + 1] = bf2(xw.y);
+              xv[4 * v + 2] = bf2(xw.z);
+              xv[4 * v + 3] = bf2(xw.w);
+            }
+#pragma unroll
+            for (int c = 0; c < W / 2; ++c) acc[c] = make_float2(0.f, 0.f);
           }
           const float w = __int_as_float(en.y);
           const float2 w2 = make_float2(w, w);
-          const float2 g0 = bf2(gw.x), g1 = bf2(gw.y), g2 = bf2(gw.z), g3 = bf2(gw.w);
-          acc[0] = ffma2(w2, g0, acc[0]);
-          acc[1] = ffma2(w2, g1, acc[1]);
-          acc[2] = ffma2(w2, g2, acc[2]);
-          acc[3] = ffma2(w2, g3, acc[3]);
-          float2 d2 = ffma2(g0, xv[0], make_float2(0.f, 0.f));
-          d2 = ffma2(g1, xv[1], d2);
-          d2 = ffma2(g2, xv[2], d2);
-          d2 = ffma2(g3, xv[3], d2);
-          dpj = d2.x + d2.y;
+          float dsum = 0.f;
+#pragma unroll
+          for (int v = 0; v < NV; ++v) {
+            const float2 g0 = bf2(gw[v].x), g1 = bf2(gw[v].y), g2 = bf2(gw[v].z), g3 = bf2(gw[v].w);
+            acc[4 * v] = ffma2(w2, g0, acc[4 * v]);
+            acc[4 * v + 1] = ffma2(w2, g1, acc[4 * v + 1]);
+            acc[4 * v + 2] = ffma2(w2, g2, acc[4 * v + 2]);
+            acc[4 * v + 3] = ffma2(w2, g3, acc[4 * v + 3]);
+            float2 d2 = ffma2(g0, xv[4 * v], make_float2(0.f, 0.f));
+            d2 = ffma2(g1, xv[4 * v + 1], d2);
+            d2 = ffma2(g2, xv[4 * v + 2], d2);
+            d2 = ffma2(g3, xv[4 * v + 3], d2);
+            dsum += d2.x + d2.y;
+          }
+          dpj = dsum;
         };
         // the batch's dot products summed over the group, to the D table
         auto finish = [&](float* dp, int b) {
-          const float dsum = group_sum_transpose8<L>(dp, lane);
-          constexpr int kSh = L == 8 ? 0 : (L == 16 ? 1 : 2);
-          const int e = ebeg + b + (gl >> kSh);
-          if ((gl & ((1 << kSh) - 1)) == 0 && e < eend) Dt[ent[e].x & 0xffff] = dsum;
+          const float dsum = group_sum_t<NB, LW>(dp, lane);
+          constexpr int kSh = (LW / NB) == 1 ? 0 : ((LW / NB) == 2 ? 1 : ((LW / NB) == 4 ? 2 : 3));
+          const int e = ebeg + b + (glw >> kSh);
+          if ((glw & ((1 << kSh) - 1)) == 0 && e < eend) Dt[ent[e].x & 0xffff] = dsum;
         };
         // full batches (every group has NB pairs left), software-pipelined:
         // the next batch's pairs load while this one computes; then one
@@ -673,11 +682,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < fullb; b += NB) {
           int2 en[NB];
-          uint4 gw[NB];
+          uint4 gw[NB][NV];
 #pragma unroll
           for (int j = 0; j < NB; ++j) {
             en[j] = enn[j];
-            gw[j] = row(en[j]);
+            row(en[j], gw[j]);
           }
           if (b + NB < fullb) {
 #pragma unroll
@@ -695,7 +704,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int e = ebeg + fullb + j;
             const bool valid = e < eend;
             const int2 en = valid ? ent[e] : make_int2(0, 0);
-            const uint4 gw = valid ? row(en) : make_uint4(0u, 0u, 0u, 0u);
+            uint4 gw[NV];
+            if (valid) {
+              row(en, gw);
+            } else {
+#pragma unroll
+              for (int v = 0; v < NV; ++v) gw[v] = make_uint4(0u, 0u, 0u, 0u);
+            }
             pair(en, gw, valid, dp[j]);
           }
           finish(dp, fullb);
