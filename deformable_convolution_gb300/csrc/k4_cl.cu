@@ -282,243 +282,6 @@ __global__ void __launch_bounds__(kInThreads, 2) k4cl_input(K4InArgs a) {
   pdl_release();
 }
 
-// ------------------------------------------------------------------ input part, tcgen05
-// The same contraction on the 5th-generation tensor cores: the threads build
-// A = im2col(goff) [kQ positions][(k, m)] and copy B = w_off [CPC channels]
-// [(k, m)] straight into the K-major 128-byte-swizzled layout of a tcgen05
-// operand (three 64-wide k-chunks, zero beyond K * M), one thread issues the
-// 12 MMAs (M = kQ = 128, N = CPC, K = 16 each) into a tensor-memory
-// accumulator of CPC columns, and the epilogue reads it back with
-// tcgen05.ld, adds the sampling backward's NHWC part and writes grad_x
-// through the same shared-memory transpose.  No fragment registers: the
-// accumulator lives in tensor memory while the threads stage and drain.
-constexpr int kKChunks = kMaxKMp / 64;  // k-chunks of 64 bf16 (one 128-byte row each)
-
-__host__ __device__ inline size_t in_tc_g_off(int cpc) { return (size_t)kKChunks * (kQ + cpc) * 128; }
-__host__ inline size_t input_tc_smem(const Geom& g, int cpc) {
-  const size_t gbytes = ((size_t)g.M * in_gy(g) * in_gx(g) * 4 + 15) / 16 * 16;
-  return 1024 + in_tc_g_off(cpc) + gbytes + 16;
-}
-
-__device__ __forceinline__ uint64_t tc_sdesc(uint32_t addr) {
-  // K-major, 128-byte swizzle: 8-row atoms 1024 bytes apart, leading offset unused
-  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-         (1ull << 46) | (2ull << 61);
-}
-
-// kind::f16 instruction descriptor: bf16 A and B (K-major), fp32 D, M = 128, N = n
-__host__ __device__ constexpr uint32_t tc_idesc(int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
-}
-
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-template <int CPC>
-__global__ void __launch_bounds__(kInThreads, 2) k4cl_input_tc(K4InArgs a) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = px::align1024(smem_raw);
-  const Geom g = a.g;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ty = blockIdx.x / a.tiles_x, tx = blockIdx.x - ty * a.tiles_x;
-  const int y0 = ty * kTY, x0 = tx * kTX;
-  const int cbeg = blockIdx.y * CPC;
-  const int n = blockIdx.z;
-  const int M = g.M, K = g.K, C = g.c_in;
-  const int KM = K * M, KMp = km_padded(g);
-  unsigned char* Ab = smem;                                // [kKChunks][kQ][128 B]
-  unsigned char* Bb = smem + (size_t)kKChunks * kQ * 128;  // [kKChunks][CPC][128 B]
-  float* G = reinterpret_cast<float*>(smem + in_tc_g_off(CPC));  // [M][GY][GX]
-  const int GY = in_gy(g), GX = in_gx(g);
-  uint64_t* mbar = reinterpret_cast<uint64_t*>(
-      smem + in_tc_g_off(CPC) + ((size_t)M * GY * GX * 4 + 15) / 16 * 16);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
-  // byte offset of element (row, kk) of a K-major swizzled operand with `rows` rows
-  auto sw_off = [](int row, int kk, int rows) {
-    return (uint32_t)((kk >> 6) * rows * 128 + row * 128 + ((((kk & 63) >> 3) ^ (row & 7)) << 4) + (kk & 7) * 2);
-  };
-
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     px::smem_u32(tslot)),
-                 "r"((uint32_t)CPC)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  if (tid == 32) {
-    px::mbar_init(mbar, 1);
-    px::fence_mbar_init();
-  }
-  // zero 16-byte pieces of A at or beyond K * M (the build fills the rest of
-  // a straddling piece) and of B beyond KMp (the copies fill the rest)
-  {
-    const int pa0 = KM / 8, pb0 = KMp / 8, np = kKChunks * 8;
-    for (int e = tid; e < kQ * (np - pa0); e += kInThreads) {
-      const int q = e / (np - pa0), pc = pa0 + (e - q * (np - pa0));
-      *reinterpret_cast<uint4*>(Ab + sw_off(q, pc * 8, kQ)) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    for (int e = tid; e < CPC * (np - pb0); e += kInThreads) {
-      const int c = e / (np - pb0), pc = pb0 + (e - c * (np - pb0));
-      *reinterpret_cast<uint4*>(Bb + sw_off(c, pc * 8, CPC)) = make_uint4(0u, 0u, 0u, 0u);
-    }
-  }
-  const int hlo = floor_div(y0 + g.ph - (g.kh - 1) * g.dh, g.sh);
-  const int wlo = floor_div(x0 + g.pw - (g.kw - 1) * g.dw, g.sw);
-  pdl_wait();  // goff and gx_nhwc from the sampling backward, Bt from the weight part
-  // goff tile (zero-filled 4-byte copies), then B's 16-byte pieces
-  {
-    const float* gimg = a.goff + (size_t)n * M * g.howo;
-    const int wo = wlo + lane;
-    const bool colok = lane < GX && wo >= 0 && wo < g.wo;
-    if (lane < GX) {
-      for (int r = warp; r < M * GY; r += kInThreads / 32) {
-        const int m = r / GY, ho = hlo + (r - m * GY);
-        const bool ok = colok && ho >= 0 && ho < g.ho;
-        const float* src = ok ? gimg + (size_t)m * g.howo + (size_t)ho * g.wo + wo : gimg;
-        asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(px::smem_u32(G + r * GX + lane)),
-                     "l"(src), "r"(ok ? 4 : 0)
-                     : "memory");
-      }
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    const unsigned short* src = a.bt + (size_t)cbeg * KMp;
-    for (int c = warp; c < CPC; c += kInThreads / 32)
-      if (lane < KMp / 8)
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                         px::smem_u32(Bb + sw_off(c, lane * 8, CPC))),
-                     "l"(src + (size_t)c * KMp + lane * 8)
-                     : "memory");
-    asm volatile("cp.async.commit_group;" ::: "memory");
-  }
-  asm volatile("cp.async.wait_group 1;" ::: "memory");  // the goff tile (B may still be in flight)
-  __syncthreads();
-  // A[q][k*M + m] = goff[m][pixel whose tap k reads position q], 0 if none
-  {
-    const int q = tid % kQ;
-    const int yq = y0 + q / kTX + g.ph, xq = x0 + q % kTX + g.pw;
-    int ki = 0, kj = tid / kQ;
-    while (kj >= g.kw) {
-      kj -= g.kw;
-      ++ki;
-    }
-    for (int k = tid / kQ; k < K; k += kInThreads / kQ) {
-      const int ty_ = yq - ki * g.dh, tx_ = xq - kj * g.dw;
-      kj += kInThreads / kQ;
-      while (kj >= g.kw) {
-        kj -= g.kw;
-        ++ki;
-      }
-      int gi = -1;
-      if (ty_ >= 0 && tx_ >= 0 && (g.sh == 1 || ty_ % g.sh == 0) && (g.sw == 1 || tx_ % g.sw == 0)) {
-        const int ho = ty_ / g.sh, wo = tx_ / g.sw;
-        if (ho < g.ho && wo < g.wo) gi = (ho - hlo) * GX + (wo - wlo);
-      }
-      const int plane = GY * GX;
-      const float* gq = G + (gi >= 0 ? gi : 0);
-#pragma unroll
-      for (int m = 0; m < 2 * kMaxK; m += 2) {
-        if (m >= M) break;
-        uint32_t w = 0u;
-        if (gi >= 0)
-          w = (uint32_t)bf16_bits_rn(gq[m * plane]) | ((uint32_t)bf16_bits_rn(gq[(m + 1) * plane]) << 16);
-        *reinterpret_cast<uint32_t*>(Ab + sw_off(q, k * M + m, kQ)) = w;
-      }
-    }
-  }
-  asm volatile("cp.async.wait_group 0;" ::: "memory");
-  // the threads' shared-memory writes and copies are visible to the tensor core
-  px::fence_proxy_async();
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  const uint32_t tmem = *tslot;
-  // ---------------------------------------------------------------- MMA (one thread)
-  if (tid == 0) {
-    const uint32_t ab = px::smem_u32(Ab), bb = px::smem_u32(Bb);
-    const int nch = (KMp + 63) / 64;
-#pragma unroll 1
-    for (int ch = 0; ch < nch; ++ch)
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const uint64_t da = tc_sdesc(ab + (uint32_t)(ch * kQ * 128 + kk * 32));
-        const uint64_t db = tc_sdesc(bb + (uint32_t)(ch * CPC * 128 + kk * 32));
-        const uint32_t acc = (ch > 0 || kk > 0) ? 1u : 0u;
-        asm volatile(
-            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-            " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem),
-            "l"(da), "l"(db), "r"(tc_idesc(CPC)), "r"(acc)
-            : "memory");
-      }
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     px::smem_u32(mbar))
-                 : "memory");
-  }
-  const bool done = __all_sync(0xffffffffu, px::mbar_wait(mbar, 0, &g_k4cl_error));
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-
-  // ---------------------------------------------------------------- epilogue
-  // warp w reads accumulator lanes 32 (w % 4) .. (its positions) and columns
-  // (channels) (w / 4) * CPC / 2 .., adds the sampling backward's part and
-  // writes them transposed, T[c][q] (pitch kQ + 4, over A and B)
-  float* T = reinterpret_cast<float*>(smem);
-  constexpr int TP = kQ + 4;
-  if (done) {
-    const int q = (warp & 3) * 32 + lane;
-    const int y = y0 + q / kTX, x = x0 + q % kTX;
-    const bool in = y < g.h && x < g.w;
-    const float* gsrc = a.gx_nhwc + (((size_t)n * g.h + y) * g.w + x) * C + cbeg;
-#pragma unroll 1
-    for (int c0 = (warp >> 2) * (CPC / 2); c0 < (warp >> 2) * (CPC / 2) + CPC / 2; c0 += 32) {
-      uint32_t r[32];
-      tc_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)c0, r);
-#pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (in) s4 = __ldg(reinterpret_cast<const float4*>(gsrc + c0 + 4 * v));
-        T[(size_t)(c0 + 4 * v) * TP + q] = __uint_as_float(r[4 * v]) + s4.x;
-        T[(size_t)(c0 + 4 * v + 1) * TP + q] = __uint_as_float(r[4 * v + 1]) + s4.y;
-        T[(size_t)(c0 + 4 * v + 2) * TP + q] = __uint_as_float(r[4 * v + 2]) + s4.z;
-        T[(size_t)(c0 + 4 * v + 3) * TP + q] = __uint_as_float(r[4 * v + 3]) + s4.w;
-      }
-    }
-  }
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-  __syncthreads();
-  if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"((uint32_t)CPC)
-                 : "memory");
-  if (done) {
-    float* dst = a.grad_x + ((size_t)n * C + cbeg) * g.hw;
-    if (g.w % 4 == 0) {
-      const int q = lane * 4;
-      const int y = y0 + q / kTX, x = x0 + q % kTX;
-      if (y < g.h && x < g.w) {
-        for (int c = warp; c < CPC; c += kInThreads / 32)
-          *reinterpret_cast<float4*>(dst + (size_t)c * g.hw + (size_t)y * g.w + x) =
-              *reinterpret_cast<const float4*>(T + (size_t)c * TP + q);
-      }
-    } else {
-      for (int e = warp; e < CPC * (kQ / 32); e += kInThreads / 32) {
-        const int c = e / (kQ / 32), q = (e - c * (kQ / 32)) * 32 + lane;
-        const int y = y0 + q / kTX, x = x0 + q % kTX;
-        if (y < g.h && x < g.w) dst[(size_t)c * g.hw + (size_t)y * g.w + x] = T[(size_t)c * TP + q];
-      }
-    }
-  }
-  pdl_release();
-}
-
 // ------------------------------------------------------------------ weight part
 constexpr int kWY = 8, kWX = 16, kWP = kWY * kWX;  // output pixels per tile
 constexpr int kWCh = 64;                           // channels per CTA
@@ -824,7 +587,7 @@ bool k4cl_supported(const Geom& g) {
   const WeightShape w = weight_shape(g, sms);
   if (w.rows > 256 || w.cols > 256 || weight_smem(w.win_pitch) > 225 * 1024) return false;
   const int cpc = g.c_in >= 128 ? 128 : 64;
-  return in_gx(g) <= 32 && input_smem(g, cpc) <= 113 * 1024 && input_tc_smem(g, cpc) <= 113 * 1024;
+  return in_gx(g) <= 32 && input_smem(g, cpc) <= 113 * 1024;
 }
 
 // The workspace region: chunk partials [nchunks][M][C][K], bias partials
@@ -854,8 +617,8 @@ cudaError_t launch_k4cl_input(const K4ClArgs& in, cudaStream_t s) {
   a.tiles_x = (int)ceil_div_ll(g.w, kTX);
   a.cpc = cpc;
   const int tiles_y = (int)ceil_div_ll(g.h, kTY);
-  const size_t smem = input_tc_smem(g, cpc);
-  const void* func = cpc == 128 ? (const void*)k4cl_input_tc<128> : (const void*)k4cl_input_tc<64>;
+  const size_t smem = input_smem(g, cpc);
+  const void* func = cpc == 128 ? (const void*)k4cl_input<128> : (const void*)k4cl_input<64>;
   cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   void* args[] = {&a};
