@@ -33,9 +33,15 @@ struct Plan {
 // offset channels per pass of the input gradient (w_off staged per pass)
 constexpr int kMc = 12;
 
+// The largest band and channel slice that fit and still give the grid at
+// least two CTAs per SM (each CTA's phases are latency chains; a grid below
+// the SM count leaves SMs idle); if none does, the fitting plan with the most
+// CTAs; if nothing fits, the smallest.
 __host__ Plan make_plan(const Geom& g, dc_dtype dt) {
+  constexpr long long kMinGrid = 2 * 152;
   const bool bf16 = dt == DC_BF16;
-  Plan best{};
+  Plan best{}, most{};
+  long long most_grid = 0;
   for (int px = kMaxPx; px >= 32; px /= 2) {
     const band::Shape sh = band::make_shape(g, 0, px);
     for (int cpc = 32; cpc >= 16; cpc -= 16) {
@@ -65,10 +71,17 @@ __host__ Plan make_plan(const Geom& g, dc_dtype dt) {
       at += (size_t)cpc * g.K * kMc * 4;
       p.smem = at;
       if (best.smem == 0 || p.smem < best.smem) best = p;
-      if (p.smem <= kSmemBudget) return p;
+      if (p.smem <= kSmemBudget) {
+        const long long grid = (long long)p.nslices * p.tiles_w * p.tiles_h * g.n;
+        if (grid >= kMinGrid) return p;
+        if (grid > most_grid) {
+          most = p;
+          most_grid = grid;
+        }
+      }
     }
   }
-  return best;
+  return most_grid > 0 ? most : best;
 }
 
 template <typename T>
