@@ -49,13 +49,17 @@ struct Plan {
   size_t off_halo, off_gx, off_offs, off_part, off_tab, off_q, smem;
 };
 
-// Largest band (128, 64 or 32 pixels) whose shared memory fits, with slices
-// of 16 channels: staged input, grad_x window, offsets, this CTA's partial
-// offset gradient, pixel table and the slow-tap queue.
+// Largest band (128, 64 or 32 pixels) whose shared memory fits and that
+// still gives the grid at least two CTAs per SM (else the fitting band with
+// the most CTAs), with slices of 16 channels: staged input, grad_x window,
+// offsets, this CTA's partial offset gradient, pixel table and the slow-tap
+// queue.
 __host__ Plan make_plan(const Geom& g, dc_dtype dt, int margin) {
+  constexpr long long kMinGrid = 2 * 152;
   const bool bf16 = dt == DC_BF16;
   const int cpc = 16;
-  Plan best{};
+  Plan best{}, most{};
+  long long most_grid = 0;
   for (int px = kMaxPx; px >= 32; px /= 2) {
     const band::Shape sh = band::make_shape(g, margin, px);
     Plan p{};
@@ -93,9 +97,16 @@ __host__ Plan make_plan(const Geom& g, dc_dtype dt, int margin) {
     at += (size_t)(1 + p.qcap) * 4;
     p.smem = at;
     if (best.smem == 0 || p.smem < best.smem) best = p;
-    if (p.smem <= kSmemBudget) return p;
+    if (p.smem <= kSmemBudget) {
+      const long long grid = (long long)p.csize * p.tiles_w * p.tiles_h * g.n;
+      if (grid >= kMinGrid) return p;
+      if (grid > most_grid) {
+        most = p;
+        most_grid = grid;
+      }
+    }
   }
-  return best;  // over budget: the caller rejects the problem
+  return most_grid > 0 ? most : best;  // over budget: the caller rejects the problem
 }
 
 __device__ __forceinline__ void gadd(float* plane, const Geom& g, int y, int x, float v) {
