@@ -87,15 +87,19 @@ __host__ size_t plan_bytes(Plan& p, const Geom& g, bool bf16, bool replay) {
 }
 
 // Largest band (128, 64 or 32 pixels) and widest channel slice (32 or 16, and
-// wider when 8 CTAs of 32 would not cover C_in) whose shared memory fits.  (Slices
-// of 16 double the CTAs per band, but 8-CTA clusters then no longer fit in one
-// wave on GB300.)
+// wider when 8 CTAs of 32 would not cover C_in) whose shared memory fits and
+// that still give the grid a CTA per SM (else the fitting plan with the most
+// CTAs; measured: smaller bands than that only add halo).  (Slices of 16
+// double the CTAs per band, but 8-CTA clusters then no longer fit in one wave
+// on GB300.)
 __host__ Plan make_plan(const Geom& g, dc_dtype dt, int margin, bool replay) {
+  constexpr long long kMinGrid = 152;
   const bool bf16 = dt == DC_BF16;
   const int c16 = (g.c_in + 15) / 16 * 16;
   int cmin = 16;
   while ((c16 + cmin - 1) / cmin > kMaxCluster) cmin += 16;
-  Plan best{};
+  Plan best{}, most{};
+  long long most_grid = 0;
   for (int px = kMaxPx; px >= 32; px /= 2) {
     const band::Shape sh = band::make_shape(g, margin, px);
     for (int cpc = (c16 <= 16 ? 16 : (cmin > 32 ? cmin : 32)); cpc >= cmin; cpc -= 16) {
@@ -114,10 +118,17 @@ __host__ Plan make_plan(const Geom& g, dc_dtype dt, int margin, bool replay) {
       p.csize = (g.c_in + cpc - 1) / cpc;
       plan_bytes(p, g, bf16, replay);
       if (best.smem == 0 || p.smem < best.smem) best = p;
-      if (p.smem <= kSmemBudget) return p;
+      if (p.smem <= kSmemBudget) {
+        const long long grid = (long long)p.csize * p.tiles_w * p.tiles_h * g.n;
+        if (grid >= kMinGrid) return p;
+        if (grid > most_grid) {
+          most = p;
+          most_grid = grid;
+        }
+      }
     }
   }
-  return best;  // over budget: the caller rejects the problem
+  return most_grid > 0 ? most : best;  // over budget: the caller rejects the problem
 }
 
 __device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
