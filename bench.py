@@ -970,8 +970,8 @@ def e2e_stack(job, dev, stream, iters=10):
                 hbuf[f"g{l}"].copy_(dbuf[f"g{l}"], non_blocking=True)
             if l > 0:
                 B.dc_relu_bwd(st.x[l], st.gx[l], st.gy[l - 1])
-        dv["gx"]["gx"].copy_(st.gx[0])
-        hbuf["gx"].copy_(dbuf["gx"], non_blocking=True)
+        # one tensor: straight into its pinned host view, no packing copy
+        hv["gx"]["gx"].copy_(st.gx[0], non_blocking=True)
         cur.wait_stream(cs)
 
     with torch.cuda.stream(stream):
