@@ -483,10 +483,9 @@ __global__ void __launch_bounds__(256) k4cl_reduce(const float* __restrict__ par
                                                    float* gb_off, int count, int M, int nchunks,
                                                    const float* __restrict__ gw_perm, float* grad_w,
                                                    int wcount, int C, int K) {
-  __shared__ float red[8][33];
   __shared__ float tr[kPermCh * kMaxK];
   pdl_wait();
-  const int nred = (count + 31) / 32;
+  const int nred = (count + 255) / 256;
   if ((int)blockIdx.x >= nred) {
     // grad_w[o][c][k] = gw_perm[o][k][c] (the main weight gradient, added in
     // w' order by the GEMM): one block per (o, kPermCh channels), the slice
@@ -504,32 +503,26 @@ __global__ void __launch_bounds__(256) k4cl_reduce(const float* __restrict__ par
     pdl_release();
     return;
   }
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int i = blockIdx.x * 32 + tx;
-  const bool bias = gb_off != nullptr && (int)blockIdx.x == nred - 1;  // the last sum block also adds the bias
-  float v = 0.f, vb = 0.f;
-  if (i < count)
-    for (int c = ty; c < nchunks; c += 8) v += part[(size_t)c * count + i];
-  if (bias && tx < M)
-    for (int c = ty; c < nchunks; c += 8) vb += bpart[(size_t)c * M + tx];
-  red[ty][tx] = v;
-  __syncthreads();
-  if (ty == 0 && i < count) {
-    float r = 0.f;
+  // one output per thread: the chunks' partials added in chunk order, eight
+  // loads in flight; the last sum block's first M threads also add the bias
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  if (i < count) {
+    float v = 0.f;
+    int c = 0;
+    for (; c + 8 <= nchunks; c += 8) {
+      float t[8];
 #pragma unroll
-    for (int y = 0; y < 8; ++y) r += red[y][tx];
-    gw_off[i] = r;
-  }
-  if (bias) {
-    __syncthreads();
-    red[ty][tx] = vb;
-    __syncthreads();
-    if (ty == 0 && tx < M) {
-      float r = 0.f;
+      for (int u = 0; u < 8; ++u) t[u] = part[(size_t)(c + u) * count + i];
 #pragma unroll
-      for (int y = 0; y < 8; ++y) r += red[y][tx];
-      gb_off[tx] = r;
+      for (int u = 0; u < 8; ++u) v += t[u];
     }
+    for (; c < nchunks; ++c) v += part[(size_t)c * count + i];
+    gw_off[i] = v;
+  }
+  if (gb_off != nullptr && (int)blockIdx.x == nred - 1 && (int)threadIdx.x < M) {
+    float v = 0.f;
+    for (int c = 0; c < nchunks; ++c) v += bpart[(size_t)c * M + threadIdx.x];
+    gb_off[threadIdx.x] = v;
   }
   pdl_release();
 }
@@ -676,10 +669,10 @@ cudaError_t launch_k4cl_reduce(const K4ClArgs& in, cudaStream_t s) {
   float* gwd = in.grad_w;
   int wcount = in.c_out * g.c_in * g.K, C = g.c_in, K = g.K;
   void* args[] = {&part, &bpart, &gw, &gb, &count, &M, &nch, &gwp, &gwd, &wcount, &C, &K};
-  // blocks [0, count / 32): the chunk sums; then, with gw_perm, one block per
+  // blocks [0, count / 256): the chunk sums; then, with gw_perm, one block per
   // (output channel, kPermCh input channels) for the permutation
   const long long nperm = gwp ? (long long)in.c_out * ceil_div_ll(g.c_in, kPermCh) : 0;
-  return launch_pdl4((const void*)k4cl_reduce, dim3((unsigned)(ceil_div_ll(count, 32) + nperm)), dim3(256), 0,
+  return launch_pdl4((const void*)k4cl_reduce, dim3((unsigned)(ceil_div_ll(count, 256) + nperm)), dim3(256), 0,
                      s, args);
 }
 
