@@ -401,6 +401,7 @@ def job_config(wl, stacked):
                         "input in every layer; measured std per layer in offset_std_per_layer)")
         c["init"] = "He (main weights N(0, 2/(9 C_in)))"
         c["backward"] = "deform_conv_bwd_after_fwd per layer, dc_relu_bwd between layers"
+        c["forward"] = "deform_conv_fwd per layer, the ReLU between layers fused into its GEMM epilogue (out_relu)"
     else:
         c["offsets"] = f"N(0,{wl.sigma}) px" + (
             f" + {wl.outlier_p:.0%} outliers at +-{wl.outlier_px} px" if wl.outlier_p else "")
@@ -945,14 +946,14 @@ def e2e_stack(job, dev, stream, iters=10):
         dbuf["in0"].copy_(hbuf["in0"], non_blocking=True)
         st.x[0] = x_dev
         q = st.params[0]
-        B.deform_conv_fwd(p, x_dev, q["w_off"], q["b_off"], q["w"], None, st.y[0], st.off[0],
-                          None, st.ws[0])
+        # layers below the last write relu(y) into the next layer's input (fused)
+        B.deform_conv_fwd(st.p_relu if L > 1 else p, x_dev, q["w_off"], q["b_off"], q["w"], None,
+                          st.x[1] if L > 1 else st.y[0], st.off[0], None, st.ws[0])
         cur.wait_event(e_rest)
         for l in range(1, L):
-            B.dc_relu_fwd(st.y[l - 1], st.x[l])
-            q = st.params[l]
-            B.deform_conv_fwd(p, st.x[l], q["w_off"], q["b_off"], q["w"], None, st.y[l],
-                              st.off[l], None, st.ws[l])
+            q, last = st.params[l], l + 1 == L
+            B.deform_conv_fwd(p if last else st.p_relu, st.x[l], q["w_off"], q["b_off"], q["w"], None,
+                              st.y[l] if last else st.x[l + 1], st.off[l], None, st.ws[l])
         dv["yout"]["y"].copy_(st.y[-1])
         e_fwd.record(cur)
         cs.wait_event(e_fwd)

@@ -36,7 +36,7 @@ class DcProblem(ctypes.Structure):
     """Mirror of ``dc_problem``."""
     _fields_ = [(name, ctypes.c_int) for name in (
         "n", "c_in", "h", "w", "c_out", "kh", "kw", "stride_h", "stride_w",
-        "pad_h", "pad_w", "dil_h", "dil_w", "offset_groups", "dtype", "halo_margin")]
+        "pad_h", "pad_w", "dil_h", "dil_w", "offset_groups", "dtype", "halo_margin", "out_relu")]
 
 
 class DcError(RuntimeError):
@@ -165,6 +165,7 @@ class Problem:
     offset_groups: int = 1
     dtype: int = DC_F32
     halo_margin: int = -1
+    out_relu: int = 0  # 1: the forward writes relu(y) (a following ReLU fused into its epilogue)
 
     def __post_init__(self):
         for f in ("stride", "pad", "dil"):
@@ -176,7 +177,7 @@ class Problem:
         return DcProblem(self.n, self.c_in, self.h, self.w, self.c_out, self.kh, self.kw,
                          self.stride[0], self.stride[1], self.pad[0], self.pad[1],
                          self.dil[0], self.dil[1], self.offset_groups, self.dtype,
-                         self.halo_margin)
+                         self.halo_margin, self.out_relu)
 
     @property
     def torch_dtype(self):

@@ -92,6 +92,7 @@ dc_status make_geom(const dc_problem* p, Geom* g, int* margin) {
     return DC_ERR_INVALID_ARG;
   if (p->dtype != DC_F32 && p->dtype != DC_BF16) return DC_ERR_INVALID_ARG;
   if (p->halo_margin < -1) return DC_ERR_INVALID_ARG;
+  if (p->out_relu != 0 && p->out_relu != 1) return DC_ERR_INVALID_ARG;
   const long long eh = (long long)p->h + 2LL * p->pad_h - (long long)p->dil_h * (p->kh - 1) - 1;
   const long long ew = (long long)p->w + 2LL * p->pad_w - (long long)p->dil_w * (p->kw - 1) - 1;
   if (eh < 0 || ew < 0) return DC_ERR_INVALID_ARG;
@@ -117,6 +118,7 @@ dc_status make_geom(const dc_problem* p, Geom* g, int* margin) {
   g->kdim = p->c_in * g->K;
   g->hw = (long long)p->h * p->w;
   g->howo = (long long)g->ho * g->wo;
+  g->relu = p->out_relu;
   // limits of this build
   if (g->K > kMaxTaps) return DC_ERR_UNSUPPORTED;
   if ((long long)p->c_in * g->K > (1LL << 30) || (long long)p->n * p->c_in * g->hw > (1LL << 40) ||

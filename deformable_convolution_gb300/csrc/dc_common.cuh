@@ -23,6 +23,7 @@ struct Geom {
   int cg;    // input channels per offset group
   int kdim;  // main-GEMM reduction length, c_in * K
   long long hw, howo;
+  int relu;  // forward: the main GEMM's epilogue writes max(y, 0) (NaN kept)
 };
 
 // Pitches of the deformed map ("column") buffer [kdim][n][howo(+pad)]:

@@ -29,6 +29,7 @@ struct StridedGemm {
   int atomic;  // 1: atomically add fp32 into C, 0: store
   ZeroArgs zero;  // buffers this launch clears as a side job (GCOL)
   int ksplit;     // K ranges per batch entry along blockIdx.z (needs atomic when > 1)
+  int relu;       // stores only: max(value, 0), NaN kept (the forward's fused activation)
 };
 
 template <typename TA, typename TB, typename TC>
@@ -98,10 +99,13 @@ __global__ void __launch_bounds__(kThreads)
       const int nidx = n0 + tc * TN + j;
       if (nidx >= p.N) continue;
       TC* dst = Cz + m * p.c_m + nidx * p.c_n;
-      if (p.atomic)
+      if (p.atomic) {
         atomicAdd(reinterpret_cast<float*>(dst), acc[i][j]);
-      else
-        *dst = from_f<TC>(acc[i][j]);
+      } else {
+        float v = acc[i][j];
+        if (p.relu && !(v > 0.f) && v == v) v = 0.f;
+        *dst = from_f<TC>(v);
+      }
     }
   }
 }
@@ -128,6 +132,7 @@ cudaError_t launch_gemm_fwd_simt(const GemmArgs& a, dc_dtype dt, cudaStream_t s)
   p.b_z = a.col_layout.img; p.b_k = a.col_layout.row; p.b_n = 1;
   p.c_z = (long long)g.c_out * g.howo; p.c_m = g.howo; p.c_n = 1;
   p.atomic = 0;
+  p.relu = g.relu;
   if (dt == DC_BF16)
     return run<__nv_bfloat16, __nv_bfloat16, __nv_bfloat16>(p, g.n, a.w, a.col, a.y, s);
   return run<float, float, float>(p, g.n, a.w, a.col, a.y, s);

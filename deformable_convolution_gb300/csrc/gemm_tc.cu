@@ -70,6 +70,7 @@ struct TcArgs {
   // persistent launch runs tiles blockIdx.x, + gridDim.x, ... of it
   int vgx, vgy, vgz, persistent;
   int flat;  // FWDC: column tiles run over the flat pixel index b * howo + q of all images
+  int relu;  // FWD / FWDC: y = max(y, 0) in the epilogue
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -126,6 +127,16 @@ __device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, uint64
       "{%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
       "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+
+// ReLU on 32 fp32 values in place (the forward's fused activation): positive
+// values and NaN kept, everything else (-0 included) +0.
+__device__ __forceinline__ void relu32(uint32_t* r) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float v = __uint_as_float(r[j]);
+    if (!(v > 0.f) && v == v) r[j] = 0u;
+  }
 }
 
 // Row m of y (bf16), columns n_first .. n_first + 31, from 32 fp32 values.
@@ -515,6 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (is_fwd(KIND) && a.flat) {
           // flat pixel index f = b * howo + q over all images
           if (m >= a.c_out) continue;
+          if (a.relu) relu32(r);
           const long long total = (long long)a.nimg * a.howo;
           if (n_first >= total) continue;
           const int zb = n_first / a.howo, q = n_first - zb * a.howo;
@@ -534,6 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else if (is_fwd(KIND)) {
           if (m >= a.c_out) continue;
+          if (a.relu) relu32(r);
           store_y_row(static_cast<__nv_bfloat16*>(a.out) + ((long long)z * a.c_out + m) * a.howo + n_first,
                       r, n_first, a.howo);
         } else if (is_gcol(KIND)) {
@@ -641,6 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             r[j] = __float_as_uint(__uint_as_float(r[j]) + peer[(c * 32 + j) * kBM + row]);
         }
         const int n_first = n0 + c * 32;
+        if (a.relu) relu32(r);
         if (m < a.c_out)
           store_y_row(static_cast<__nv_bfloat16*>(a.out) + ((long long)z * a.c_out + m) * a.howo + n_first,
                       r, n_first, a.howo);
@@ -911,6 +925,7 @@ __global__ void __launch_bounds__(kFsThreads, 1)
         tmem_ld32(tbase + c * 32, r);
         if (!ok || nkb == 0 || m >= g.c_out) continue;
         const int n_first = n0 + c * 32;
+        if (g.relu) relu32(r);
         store_y_row(a.y + ((long long)n * g.c_out + m) * g.howo + n_first, r, n_first, (int)g.howo);
       }
     }
@@ -1075,6 +1090,7 @@ cudaError_t launch_gemm_fwd_tc(const GemmArgs& ga, cudaStream_t s) {
   a.nimg = g.n;
   a.kb_total = (int)ceil_div_ll(g.kdim, kBK);
   a.out = ga.y;
+  a.relu = g.relu;
   const int bn = pick_fwd_bn(g);
   const long long tiles = ceil_div_ll(g.howo, bn) * ceil_div_ll(g.c_out, kBM) * g.n;
   // fewer output tiles than SMs and a long reduction: split the k-blocks over
@@ -1164,6 +1180,7 @@ cudaError_t launch_gemm_fwd_cl(const GemmArgs& ga, cudaStream_t s) {
   a.nimg = g.n;
   a.kb_total = (int)ceil_div_ll(g.kdim, kBK);
   a.out = ga.y;
+  a.relu = g.relu;
   if (bn == 128 && g.c_out > kBM) {
     // all output channels of a pixel tile in one CTA (two halves): the map is
     // read once.  When 192-pixel tiles over the flat pixel index of all

@@ -59,6 +59,7 @@ struct Tf32Args {
   long long out_row, out_img;  // GCOL: gcol pitches (elements)
   ZeroArgs zero;               // GCOL: buffers the rest of the backward accumulates into
   int vgx, vgy, vgz;           // tile grid: x column tiles, y row tiles, z images or splits
+  int relu;                    // FWD: y = max(y, 0) in the epilogue (NaN kept)
 };
 
 template <int KIND, int BN>
@@ -435,6 +436,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (T.nkb == 0) continue;
         const int n_first = T.n0 + c * 32;
         if (KIND == FWD) {
+          if (a.relu) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float v = __uint_as_float(r[j]);
+              if (!(v > 0.f) && v == v) r[j] = 0u;
+            }
+          }
           if (m < a.c_out) store_row(a.out + ((long long)T.z * a.c_out + m) * a.howo + n_first, r, n_first, a.howo);
         } else if (KIND == GCOL) {
           if (m < a.kdim) store_row(a.out + m * a.out_row + T.z * a.out_img + n_first, r, n_first, a.howo);
@@ -587,6 +595,7 @@ cudaError_t launch_gemm_fwd_tf32(const GemmArgs& ga, cudaStream_t s) {
   Tf32Args a = base_args(g);
   a.kb_total = (int)ceil_div_ll(g.kdim, kBK);
   a.out = static_cast<float*>(ga.y);
+  a.relu = g.relu;
   return launch<FWD, 64>(A, B, a, ceil_div_ll(g.howo, 64), ceil_div_ll(g.c_out, kBM), g.n, s);
 }
 

@@ -7,15 +7,20 @@ throughout a ResNet; "Why it works / Fixing the slowest stage lifts the whole
 layer": training time of a fully deformable ResNet).  This module chains the C
 ABI's calls for such a stack: per layer the forward (``deform_conv_fwd``) and
 the backward that reuses the forward's deformed map
-(``deform_conv_bwd_after_fwd``), with ``dc_relu_fwd`` / ``dc_relu_bwd``
-between layers.  Marshalling only: buffers come from PyTorch, every step of
-the arithmetic runs in the library's kernels.
+(``deform_conv_bwd_after_fwd``), with the ReLU between layers: in the forward
+fused into the layer's main GEMM epilogue (``out_relu``, bit for bit
+``dc_relu_fwd`` of the plain output), in the backward ``dc_relu_bwd``.
+Marshalling only: buffers come from PyTorch, every step of the arithmetic runs
+in the library's kernels.
 
-Layer l's input is x[l] (x[0] is the caller's); x[l + 1] = relu(y[l]).  The
+Layer l's input is x[l] (x[0] is the caller's); x[l + 1] = relu(y[l]), which
+the forward of layer l writes directly; y is kept for the last layer.  The
 backward runs from the top: layer l's grad_y is the caller's grad_y for the
 last layer, else relu'(x[l + 1]) * grad_x[l + 1], rounded to the dtype.
 """
 from __future__ import annotations
+
+import dataclasses
 
 import torch
 
@@ -36,6 +41,7 @@ class Stack:
         if s["x"] != s["y"]:
             raise ValueError("stacked layers need C_in = C_out and an unchanged size")
         self.p, self.params, self.L = p, params, len(params)
+        self.p_relu = dataclasses.replace(p, out_relu=1)  # forward with the ReLU fused
         dt, f32 = p.torch_dtype, torch.float32
         self.x = [None] + [torch.empty(s["x"], dtype=dt, device=device) for _ in range(self.L - 1)]
         self.y = [torch.empty(s["y"], dtype=dt, device=device) for _ in range(self.L)]
@@ -52,12 +58,10 @@ class Stack:
         """Runs every layer's forward; returns the last layer's output y."""
         self.x[0] = x0
         for l in range(self.L):
-            q = self.params[l]
-            B.deform_conv_fwd(self.p, self.x[l], q["w_off"], q["b_off"], q["w"],
-                              offset_add if l == 0 else None, self.y[l], self.off[l], None,
-                              self.ws[l])
-            if l + 1 < self.L:
-                B.dc_relu_fwd(self.y[l], self.x[l + 1])
+            q, last = self.params[l], l + 1 == self.L
+            B.deform_conv_fwd(self.p if last else self.p_relu, self.x[l], q["w_off"], q["b_off"],
+                              q["w"], offset_add if l == 0 else None,
+                              self.y[l] if last else self.x[l + 1], self.off[l], None, self.ws[l])
         return self.y[-1]
 
     def backward(self, grad_y):

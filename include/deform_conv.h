@@ -67,13 +67,19 @@ typedef enum { DC_F32 = 0, DC_BF16 = 1 } dc_dtype;
  * the fused sampling kernel stages around each output tile's receptive field
  * ("The idea": tile padding sized to the offset distribution); -1 selects the
  * library default (3 px).  It changes speed only, never results: taps that
- * fall outside the staged tile are read from global memory. */
+ * fall outside the staged tile are read from global memory.
+ * out_relu (0 or 1): the forward calls write y = max(conv, 0) instead of the
+ * convolution, a following ReLU fused into the main GEMM's epilogue; the
+ * result is bit for bit dc_relu_fwd of the plain forward (NaN kept, -0 -> +0).
+ * The backward calls ignore it: their grad_y is the gradient with respect to
+ * the convolution's output, as without it. */
 typedef struct {
   int n, c_in, h, w, c_out, kh, kw;
   int stride_h, stride_w, pad_h, pad_w, dil_h, dil_w;
   int offset_groups;
   dc_dtype dtype;
   int halo_margin;
+  int out_relu;
 } dc_problem;
 
 /* Output height/width of the problem (0 if the problem is invalid). */

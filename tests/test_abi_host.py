@@ -59,6 +59,7 @@ def ws_size(p, backward=False):
     (dict(stride=0), B.DC_ERR_INVALID_ARG),
     (dict(dtype=7), B.DC_ERR_INVALID_ARG),
     (dict(halo_margin=-2), B.DC_ERR_INVALID_ARG),
+    (dict(out_relu=2), B.DC_ERR_INVALID_ARG),
     (dict(kh=9, kw=9, pad=4), B.DC_ERR_UNSUPPORTED),
     (dict(halo_margin=1000), B.DC_ERR_UNSUPPORTED),
 ])

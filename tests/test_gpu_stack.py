@@ -27,6 +27,53 @@ pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
 
 
+# The forward with the following ReLU fused into its main GEMM's epilogue
+# (out_relu) is bit for bit dc_relu_fwd of the plain forward, on every
+# forward GEMM: the channels-last tcgen05 GEMM (per-image tiles, and tiles over
+# the flat pixel index of all images with chunks crossing image boundaries),
+# the plane-major bf16 tcgen05 GEMM, the float32 TF32 GEMM, the CUDA-core GEMM
+# (rows that are not 16-byte aligned) and the sampled-operand forward.
+FUSED_RELU_CASES = [
+    ((2, 64, 20, 24, 32, 3, 3, 1, 1, 1, 1), B.DC_BF16, "fwd"),
+    ((8, 64, 36, 36, 136, 3, 3, 1, 1, 1, 1), B.DC_BF16, "fwd"),
+    ((2, 16, 12, 10, 24, 3, 3, 1, 1, 1, 2), B.DC_BF16, "fwd"),
+    ((2, 12, 10, 14, 40, 3, 3, 1, 1, 1, 1), B.DC_F32, "fwd"),
+    ((1, 5, 17, 19, 7, 3, 3, 1, 1, 1, 1), B.DC_F32, "fwd"),
+    ((2, 16, 12, 10, 24, 3, 3, 1, 1, 1, 2), B.DC_BF16, "sampled"),
+]
+
+
+@pytest.mark.parametrize("geom,dtype,entry", FUSED_RELU_CASES)
+def test_fused_relu_forward_is_relu_of_the_forward(geom, dtype, entry):
+    import dataclasses
+    n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups = geom
+    p = B.Problem(n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups, dtype)
+    pr = dataclasses.replace(p, out_relu=1)
+    g = torch.Generator().manual_seed(31 + c_in + c_out)
+    sh = p.shapes()
+    dt = p.torch_dtype
+    x = torch.randn(sh["x"], generator=g).to(dt).cuda()
+    w_off = (0.05 * torch.randn(sh["w_off"], generator=g)).to(dt).cuda()
+    b_off = torch.zeros(sh["b_off"]).cuda()
+    wm = (torch.randn(sh["w"], generator=g) / (c_in * kh * kw) ** 0.5).to(dt).cuda()
+    outs = []
+    for q in (p, pr):
+        y = torch.empty(sh["y"], dtype=dt, device="cuda")
+        off = torch.empty(sh["offset"], dtype=torch.float32, device="cuda")
+        if entry == "sampled":
+            B.deform_conv_fwd_sampled_gemm(q, x, w_off, b_off, wm, None, y, off)
+        else:
+            ws = B.workspace(q, False, "cuda")
+            B.deform_conv_fwd(q, x, w_off, b_off, wm, None, y, off, None, ws)
+        outs.append(y)
+    ref = torch.empty_like(outs[0])
+    B.dc_relu_fwd(outs[0], ref)
+    torch.cuda.synchronize()
+    bits = torch.int16 if dtype == B.DC_BF16 else torch.int32
+    assert (outs[0] < 0).any() and (outs[0] > 0).any()
+    assert torch.equal(outs[1].view(bits), ref.view(bits))
+
+
 def to_bf16_via_f32(a):
     """fp64 -> float32 -> bf16 (nearest even at each step), back as fp64."""
     return torch.from_numpy(np.asarray(a, dtype=np.float64)).float().to(torch.bfloat16).double().numpy()
