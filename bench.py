@@ -400,7 +400,8 @@ def job_config(wl, stacked):
         c["offsets"] = (f"N(0,{wl.sigma}) px (offset weights scaled for a post-ReLU N(0,1) "
                         "input in every layer; measured std per layer in offset_std_per_layer)")
         c["init"] = "He (main weights N(0, 2/(9 C_in)))"
-        c["backward"] = "deform_conv_bwd_after_fwd per layer, dc_relu_bwd between layers"
+        c["backward"] = ("deform_conv_bwd_after_fwd per layer, the ReLU between layers fused into "
+                         "the grad_x store of the layer above (in_relu)")
         c["forward"] = "deform_conv_fwd per layer, the ReLU between layers fused into its GEMM epilogue (out_relu)"
     else:
         c["offsets"] = f"N(0,{wl.sigma}) px" + (
@@ -620,6 +621,7 @@ def kernel_costs(p, has_add):
         "gx_to_nchw": ("hbm", 2 * gx_b),
         "k4_offconv_bwd": ("hbm", k4),
         # input part: read goff, w_off and the NHWC grad_x buffer, write grad_x
+        # (float32; through the fused ReLU read x, write bf16: the same bytes)
         "k4cl_input": ("hbm", off_b + woff_b + 2 * gx_b),
         # weight part: read x (NHWC) and goff, write the chunk partials
         "k4cl_weight": ("hbm", x_b + off_b + k4cl_chunks * p.n_off * (kdim + 1) * 4),
@@ -961,16 +963,11 @@ def e2e_stack(job, dev, stream, iters=10):
             hbuf["yout"].copy_(dbuf["yout"], non_blocking=True)
         st.gy[-1] = gy_dev
         for l in reversed(range(L)):
-            q, g = st.params[l], st.grads[l]
-            B.deform_conv_bwd(p, st.x[l], q["w_off"], q["w"], st.off[l], st.gy[l], st.gx[l],
-                              g["grad_w_off"], g["grad_b_off"], g["grad_w"], None, st.ws[l],
-                              after_fwd=True)
+            st.backward_layer(l)  # layer l - 1's grad_y through the ReLU, fused
             e_layer[l].record(cur)
             cs.wait_event(e_layer[l])
             with torch.cuda.stream(cs):
                 hbuf[f"g{l}"].copy_(dbuf[f"g{l}"], non_blocking=True)
-            if l > 0:
-                B.dc_relu_bwd(st.x[l], st.gx[l], st.gy[l - 1])
         # one tensor: straight into its pinned host view, no packing copy
         hv["gx"]["gx"].copy_(st.gx[0], non_blocking=True)
         cur.wait_stream(cs)

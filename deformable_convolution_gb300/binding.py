@@ -36,7 +36,8 @@ class DcProblem(ctypes.Structure):
     """Mirror of ``dc_problem``."""
     _fields_ = [(name, ctypes.c_int) for name in (
         "n", "c_in", "h", "w", "c_out", "kh", "kw", "stride_h", "stride_w",
-        "pad_h", "pad_w", "dil_h", "dil_w", "offset_groups", "dtype", "halo_margin", "out_relu")]
+        "pad_h", "pad_w", "dil_h", "dil_w", "offset_groups", "dtype", "halo_margin", "out_relu",
+        "in_relu")]
 
 
 class DcError(RuntimeError):
@@ -166,6 +167,7 @@ class Problem:
     dtype: int = DC_F32
     halo_margin: int = -1
     out_relu: int = 0  # 1: the forward writes relu(y) (a following ReLU fused into its epilogue)
+    in_relu: int = 0   # 1: x = relu(z); the backward writes dL/dz in the dtype as grad_x
 
     def __post_init__(self):
         for f in ("stride", "pad", "dil"):
@@ -177,7 +179,7 @@ class Problem:
         return DcProblem(self.n, self.c_in, self.h, self.w, self.c_out, self.kh, self.kw,
                          self.stride[0], self.stride[1], self.pad[0], self.pad[1],
                          self.dil[0], self.dil[1], self.offset_groups, self.dtype,
-                         self.halo_margin, self.out_relu)
+                         self.halo_margin, self.out_relu, self.in_relu)
 
     @property
     def torch_dtype(self):
@@ -281,7 +283,8 @@ def deform_conv_fwd_noalloc(p: Problem, x, w_off, b_off, w, offset_add, y, offse
 def deform_conv_bwd(p: Problem, x, w_off, w, offset, grad_y, grad_x, grad_w_off, grad_b_off,
                     grad_w, grad_offset=None, ws=None, stream=None, after_fwd=False):
     """after_fwd: `ws` still holds the deformed map of the deform_conv_fwd call
-    for these inputs (deform_conv_bwd_after_fwd); the map is not replayed."""
+    for these inputs (deform_conv_bwd_after_fwd); the map is not replayed.
+    grad_x is float32, or of the problem dtype when ``p.in_relu``."""
     s = p.shapes()
     dt, f32 = p.torch_dtype, torch.float32
     st = p.c_struct()
@@ -290,7 +293,7 @@ def deform_conv_bwd(p: Problem, x, w_off, w, offset, grad_y, grad_x, grad_w_off,
     _check(fn(
         ctypes.byref(st), _ptr(x, "x", s["x"], dt), _ptr(w_off, "w_off", s["w_off"], dt),
         _ptr(w, "w", s["w"], dt), _ptr(offset, "offset", s["offset"], f32),
-        _ptr(grad_y, "grad_y", s["y"], dt), _ptr(grad_x, "grad_x", s["x"], f32),
+        _ptr(grad_y, "grad_y", s["y"], dt), _ptr(grad_x, "grad_x", s["x"], dt if p.in_relu else f32),
         _ptr(grad_w_off, "grad_w_off", s["w_off"], f32),
         _ptr(grad_b_off, "grad_b_off", s["b_off"], f32, True),
         _ptr(grad_w, "grad_w", s["w"], f32),
@@ -436,7 +439,8 @@ def backward(p: Problem, x, w_off, w, offset, grad_y, ws=None, stream=None):
     """Returns dict(grad_x, grad_w_off, grad_b_off, grad_w, grad_offset)."""
     s = p.shapes()
     dev = x.device
-    out = dict(grad_x=torch.empty(s["x"], dtype=torch.float32, device=dev),
+    out = dict(grad_x=torch.empty(s["x"], dtype=p.torch_dtype if p.in_relu else torch.float32,
+                                  device=dev),
                grad_w_off=torch.empty(s["w_off"], dtype=torch.float32, device=dev),
                grad_b_off=torch.empty(s["b_off"], dtype=torch.float32, device=dev),
                grad_w=torch.empty(s["w"], dtype=torch.float32, device=dev),

@@ -93,6 +93,7 @@ dc_status make_geom(const dc_problem* p, Geom* g, int* margin) {
   if (p->dtype != DC_F32 && p->dtype != DC_BF16) return DC_ERR_INVALID_ARG;
   if (p->halo_margin < -1) return DC_ERR_INVALID_ARG;
   if (p->out_relu != 0 && p->out_relu != 1) return DC_ERR_INVALID_ARG;
+  if (p->in_relu != 0 && p->in_relu != 1) return DC_ERR_INVALID_ARG;
   const long long eh = (long long)p->h + 2LL * p->pad_h - (long long)p->dil_h * (p->kh - 1) - 1;
   const long long ew = (long long)p->w + 2LL * p->pad_w - (long long)p->dil_w * (p->kw - 1) - 1;
   if (eh < 0 || ew < 0) return DC_ERR_INVALID_ARG;
@@ -119,6 +120,7 @@ dc_status make_geom(const dc_problem* p, Geom* g, int* margin) {
   g->hw = (long long)p->h * p->w;
   g->howo = (long long)g->ho * g->wo;
   g->relu = p->out_relu;
+  g->in_relu = p->in_relu;
   // limits of this build
   if (g->K > kMaxTaps) return DC_ERR_UNSUPPORTED;
   if ((long long)p->c_in * g->K > (1LL << 30) || (long long)p->n * p->c_in * g->hw > (1LL << 40) ||
@@ -142,7 +144,7 @@ struct Plan {
   bool k4cl;  // channels-last offset-convolution backward (writes grad_x from that accumulator)
   ColLayout col, gcol;
   size_t col_off, gcol_off, off_off, gmax_off, gwo_img_off, xc_off, wp_off, wfrag_off, gxc_off, k4part_off,
-      gwp_off,
+      gwp_off, gxr_off,
       total;
   int gmax_tx, gmax_ty;
 };
@@ -187,6 +189,10 @@ Plan make_plan(const Geom& g, dc_dtype dt, int backward, int margin) {
   pl.gwo_img_off = backward && !pl.k4cl && offconv_bwd_tc_supported(g, dt)
                        ? take((size_t)g.n * gwo_frag_count(g.M, g.c_in, g.K) * sizeof(float))
                        : 0;
+  // float32 grad_x ahead of the fused ReLU backward (in_relu) where the
+  // kernels accumulate into grad_x itself; last, so the regions before it are
+  // where the forward pass put them
+  pl.gxr_off = backward && g.in_relu && !pl.k4cl ? take((size_t)g.n * g.c_in * g.hw * sizeof(float)) : 0;
   pl.total = at;
   return pl;
 }
@@ -241,7 +247,7 @@ namespace {
 // The backward pass; with reuse_map the deformed map the forward pass left in
 // the workspace feeds the weight-gradient GEMM and K3 does not replay it.
 dc_status backward(const dc_problem* prob, const void* x, const void* w_off, const void* w,
-                   const float* offset, const void* grad_y, float* grad_x, float* grad_w_off,
+                   const float* offset, const void* grad_y, void* grad_x, float* grad_w_off,
                    float* grad_b_off, float* grad_w, float* grad_offset, void* ws,
                    size_t ws_bytes, void* stream, bool reuse_map) {
   Geom g;
@@ -262,6 +268,10 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* wsb = static_cast<char*>(ws);
   float* goff = grad_offset ? grad_offset : reinterpret_cast<float*>(wsb + pl.off_off);
+  // float32 grad_x: the caller's buffer, or with in_relu the scratch the
+  // ReLU backward reads at the end (the channels-last offset-convolution
+  // backward applies it while writing grad_x and needs neither)
+  float* gx32 = pl.gxr_off ? reinterpret_cast<float*>(wsb + pl.gxr_off) : static_cast<float*>(grad_x);
   if (pl.cl && !reuse_map) {
     // the pixel-major map for the weight-gradient GEMM, sampled at the given
     // offsets, and the permuted weights
@@ -285,7 +295,7 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
   // from it)
   float* gxc = pl.k3cl ? reinterpret_cast<float*>(wsb + pl.gxc_off) : nullptr;
   if (pl.k3cl) ga.w = wsb + pl.wp_off;
-  ga.zero.p[0] = pl.k3cl ? gxc : grad_x;
+  ga.zero.p[0] = pl.k3cl ? gxc : gx32;
   ga.zero.n[0] = (long long)g.n * g.c_in * g.hw;
   float* gw_perm = pl.k4cl ? reinterpret_cast<float*>(wsb + pl.gwp_off) : nullptr;
   ga.zero.p[1] = pl.k4cl ? gw_perm : grad_w;
@@ -333,6 +343,7 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
       k4.w_off = w_off;
       k4.goff = goff;
       k4.gx_nhwc = gxc;
+      k4.x = x;
       k4.grad_x = grad_x;
       k4.grad_w_off = grad_w_off;
       k4.grad_b_off = grad_b_off;
@@ -349,7 +360,7 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
       if (st != DC_OK) return st;
       return cuda_status(timed("k4cl_reduce", s, [&] { return launch_k4cl_reduce(k4, s); }));
     }
-    st = cuda_status(timed("gx_to_nchw", s, [&] { return launch_gx_to_nchw(gxc, grad_x, g, s); }));
+    st = cuda_status(timed("gx_to_nchw", s, [&] { return launch_gx_to_nchw(gxc, gx32, g, s); }));
     if (st != DC_OK) return st;
   }
 
@@ -362,7 +373,7 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
   ba.gcol_layout = pl.gcol;
   ba.col = (reuse_map || pl.cl) ? nullptr : wsb + pl.col_off;
   ba.col_layout = pl.col;
-  ba.gx = grad_x;
+  ba.gx = gx32;
   ba.goff = goff;
   ba.margin = margin;
   ba.gmax = ga.gmax;
@@ -379,7 +390,7 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
   oa.x = x;
   oa.w_off = w_off;
   oa.goff = goff;
-  oa.gx = grad_x;
+  oa.gx = gx32;
   oa.gw_off = grad_w_off;
   oa.gb_off = grad_b_off;
   oa.gw_off_img = gwo_img;
@@ -398,10 +409,17 @@ dc_status backward(const dc_problem* prob, const void* x, const void* w_off, con
   st = cuda_status(timed("gemm_gw", s, [&] {
     return pl.cl ? launch_gemm_gw_cl(ga, s) : launch_gemm_gw(ga, prob->dtype, s);
   }));
-  if (st != DC_OK || !gwo_img || gw_reduces) return st;
-
-  // grad_w_off from K4's per-image partials
-  return cuda_status(timed("gw_off_reduce", s, [&] { return launch_gw_off_reduce(oa, s); }));
+  if (st != DC_OK) return st;
+  if (gwo_img && !gw_reduces) {
+    // grad_w_off from K4's per-image partials
+    st = cuda_status(timed("gw_off_reduce", s, [&] { return launch_gw_off_reduce(oa, s); }));
+    if (st != DC_OK) return st;
+  }
+  if (!pl.gxr_off) return DC_OK;
+  // the ReLU backward of the layer before, on the completed grad_x
+  return cuda_status(timed("relu_bwd", s, [&] {
+    return launch_relu_bwd(x, gx32, grad_x, (long long)g.n * g.c_in * g.hw, prob->dtype, s);
+  }));
 }
 
 }  // namespace
@@ -493,7 +511,7 @@ dc_status deform_conv_fwd(const dc_problem* prob, const void* x, const void* w_o
 }
 
 dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_off, const void* w,
-                          const float* offset, const void* grad_y, float* grad_x,
+                          const float* offset, const void* grad_y, void* grad_x,
                           float* grad_w_off, float* grad_b_off, float* grad_w,
                           float* grad_offset, void* ws, size_t ws_bytes, void* stream) {
   return dc::backward(prob, x, w_off, w, offset, grad_y, grad_x, grad_w_off, grad_b_off, grad_w,
@@ -502,7 +520,7 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
 
 dc_status deform_conv_bwd_after_fwd(const dc_problem* prob, const void* x, const void* w_off,
                                     const void* w, const float* offset, const void* grad_y,
-                                    float* grad_x, float* grad_w_off, float* grad_b_off,
+                                    void* grad_x, float* grad_w_off, float* grad_b_off,
                                     float* grad_w, float* grad_offset, void* ws, size_t ws_bytes,
                                     void* stream) {
   return dc::backward(prob, x, w_off, w, offset, grad_y, grad_x, grad_w_off, grad_b_off, grad_w,

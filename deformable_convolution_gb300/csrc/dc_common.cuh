@@ -24,6 +24,7 @@ struct Geom {
   int kdim;  // main-GEMM reduction length, c_in * K
   long long hw, howo;
   int relu;  // forward: the main GEMM's epilogue writes max(y, 0) (NaN kept)
+  int in_relu;  // backward: grad_x masked by x > 0 and written in the problem dtype
 };
 
 // Pitches of the deformed map ("column") buffer [kdim][n][howo(+pad)]:
@@ -321,7 +322,8 @@ struct K4ClArgs {
   const void* w_off;    // [M][C_in][K] bf16
   const float* goff;    // [n][M][Ho][Wo]
   const float* gx_nhwc; // the sampling backward's grad_x, NHWC float32
-  float* grad_x;        // [n][C_in][H][W]
+  const void* x;        // x, NCHW bf16 (the ReLU mask when g.in_relu)
+  void* grad_x;         // [n][C_in][H][W] float32, or bf16 masked by x > 0 when g.in_relu
   float* grad_w_off;    // [M][C_in][K]
   float* grad_b_off;    // [M] or null
   float* part;          // workspace, k4cl_part_bytes

@@ -19,7 +19,8 @@
 // part, which runs first), multiplies them on the tensor cores (mma.sync
 // m16n8k16, fp32 accumulate), adds the sampling backward's contribution from
 // its NHWC float32 buffer and writes grad_x (NCHW) once: no atomics, no
-// separate transpose.
+// separate transpose.  When x is a ReLU's output (in_relu), that store is the
+// ReLU's backward: bf16, zero where x is not above zero.
 //
 // Weight part (k4cl_weight): the reduction runs over every pixel of the batch,
 // so the CTAs split the pixels into chunks and the channels into slices of
@@ -100,9 +101,19 @@ struct K4InArgs {
   const float* goff;                // [n][M][Ho][Wo]
   const unsigned short* bt;         // [C][KMp] bf16 bits: w_off as B (written by k4cl_weight)
   const float* gx_nhwc;             // sampling backward's grad_x, [n][H][W][C]
-  float* grad_x;                    // [n][C][H][W]
+  const unsigned short* x;          // [n][C][H][W] bf16 bits, the ReLU mask (g.in_relu)
+  void* grad_x;                     // [n][C][H][W] float32, or bf16 masked by x > 0 (g.in_relu)
   int tiles_x, cpc;
 };
+
+// The ReLU backward fused into the grad_x store: v where the activation x is
+// above zero, else 0, rounded to bf16 (nearest even) -- the same value the
+// stand-alone ReLU backward kernel writes for v.
+__device__ __forceinline__ unsigned int relu_grad2(float v0, float v1, unsigned int x2) {
+  const float a0 = __uint_as_float(x2 << 16), a1 = __uint_as_float(x2 & 0xffff0000u);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(a0 > 0.f ? v0 : 0.f, a1 > 0.f ? v1 : 0.f);
+  return *reinterpret_cast<const unsigned int*>(&b);
+}
 
 // CPC channels per CTA (64 or 128).  Warps: 8 m-tiles of 16 positions x
 // CPC/8 n-tiles of 8 channels; a warp holds MTW m-tiles x 8 n-tiles.
@@ -132,6 +143,21 @@ __global__ void __launch_bounds__(kInThreads, 2) k4cl_input(K4InArgs a) {
   const int hlo = floor_div(y0 + g.ph - (g.kh - 1) * g.dh, g.sh);
   const int wlo = floor_div(x0 + g.pw - (g.kw - 1) * g.dw, g.sw);
   float* G = reinterpret_cast<float*>(smem + in_g_off(g, CPC));  // [M][GY][GX]
+  if (g.in_relu) {
+    // the ReLU mask x of the grad_x store, into L2 while the tile is built:
+    // per (channel, row of the tile) the row's first and last element (x was
+    // written before this backward began; a prefetch changes no data)
+    const unsigned short* p0 = a.x + ((size_t)n * C + cbeg) * g.hw;
+    const int xl = min(x0 + kTX, g.w) - 1;
+    for (int e = tid; e < CPC * kTY; e += kInThreads) {
+      const int c = e / kTY, y = y0 + (e - c * kTY);
+      if (y < g.h) {
+        const unsigned short* row = p0 + (size_t)c * g.hw + (size_t)y * g.w;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + x0));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + xl));
+      }
+    }
+  }
   pdl_wait();  // goff and gx_nhwc from the sampling backward, Bt from the weight part
   // goff tile: a warp per (m, row), lanes over the columns (GX <= 32), all
   // rows in flight as 4-byte asynchronous copies (zero-filled outside goff)
@@ -262,7 +288,45 @@ __global__ void __launch_bounds__(kInThreads, 2) k4cl_input(K4InArgs a) {
   // grad_x rows: a warp per channel at a time, lanes over four positions
   // each (one 16-byte store when the row length keeps them aligned), else
   // over 32 positions (two rows of the tile)
-  float* dst = a.grad_x + ((size_t)n * C + cbeg) * g.hw;
+  const size_t plane0 = ((size_t)n * C + cbeg) * g.hw;
+  if (g.in_relu) {
+    // the ReLU backward of the layer before: bf16, masked by x > 0 (x read
+    // at the same positions, four per lane in one 8-byte load when aligned)
+    unsigned short* dst = static_cast<unsigned short*>(a.grad_x) + plane0;
+    const unsigned short* act = a.x + plane0;
+    if (g.w % 4 == 0) {
+      const int q = lane * 4;
+      const int y = y0 + q / kTX, x = x0 + q % kTX;
+      if (y < g.h && x < g.w) {
+        // every load of x in flight before the first store
+        constexpr int kIt = CPC / (kInThreads / 32);
+        const size_t pos = (size_t)y * g.w + x;
+        uint2 xa[kIt];
+#pragma unroll
+        for (int i = 0; i < kIt; ++i)
+          xa[i] = __ldg(reinterpret_cast<const uint2*>(act + (size_t)(warp + i * (kInThreads / 32)) * g.hw + pos));
+#pragma unroll
+        for (int i = 0; i < kIt; ++i) {
+          const int c = warp + i * (kInThreads / 32);
+          const float4 v = *reinterpret_cast<const float4*>(T + (size_t)c * TP + q);
+          *reinterpret_cast<uint2*>(dst + (size_t)c * g.hw + pos) =
+              make_uint2(relu_grad2(v.x, v.y, xa[i].x), relu_grad2(v.z, v.w, xa[i].y));
+        }
+      }
+    } else {
+      for (int e = warp; e < CPC * (kQ / 32); e += kInThreads / 32) {
+        const int c = e / (kQ / 32), q = (e - c * (kQ / 32)) * 32 + lane;
+        const int y = y0 + q / kTX, x = x0 + q % kTX;
+        if (y < g.h && x < g.w) {
+          const size_t at = (size_t)c * g.hw + (size_t)y * g.w + x;
+          dst[at] = (unsigned short)relu_grad2(T[(size_t)c * TP + q], 0.f, act[at]);
+        }
+      }
+    }
+    pdl_release();
+    return;
+  }
+  float* dst = static_cast<float*>(a.grad_x) + plane0;
   if (g.w % 4 == 0) {
     static_assert(kTX % 4 == 0 && kQ == 4 * 32 && TP % 4 == 0, "four positions per lane");
     const int q = lane * 4;
@@ -606,6 +670,7 @@ cudaError_t launch_k4cl_input(const K4ClArgs& in, cudaStream_t s) {
   a.bt = reinterpret_cast<const unsigned short*>(reinterpret_cast<const char*>(in.part) +
                                                  bt_offset_bytes(g, weight_shape(g, sms).nchunks));
   a.gx_nhwc = in.gx_nhwc;
+  a.x = static_cast<const unsigned short*>(in.x);
   a.grad_x = in.grad_x;
   a.tiles_x = (int)ceil_div_ll(g.w, kTX);
   a.cpc = cpc;

@@ -72,7 +72,15 @@ typedef enum { DC_F32 = 0, DC_BF16 = 1 } dc_dtype;
  * convolution, a following ReLU fused into the main GEMM's epilogue; the
  * result is bit for bit dc_relu_fwd of the plain forward (NaN kept, -0 -> +0).
  * The backward calls ignore it: their grad_y is the gradient with respect to
- * the convolution's output, as without it. */
+ * the convolution's output, as without it.
+ * in_relu (0 or 1): x is the output of a ReLU, x = max(z, 0), and the backward
+ * calls return the gradient with respect to z instead of x:
+ * grad_x[i] = x[i] > 0 ? dL/dx[i] : 0, written in the problem dtype (the
+ * grad_x buffer of a bf16 problem then holds bf16 elements), what
+ * dc_relu_bwd(x, dL/dx) gives for the float32 dL/dx the call computes -- the
+ * previous layer's ReLU backward fused into this layer's grad_x epilogue.  The backward workspace query counts it (problems
+ * off the channels-last backward need a float32 grad_x scratch); the forward
+ * calls ignore it. */
 typedef struct {
   int n, c_in, h, w, c_out, kh, kw;
   int stride_h, stride_w, pad_h, pad_w, dil_h, dil_w;
@@ -80,6 +88,7 @@ typedef struct {
   dc_dtype dtype;
   int halo_margin;
   int out_relu;
+  int in_relu;
 } dc_problem;
 
 /* Output height/width of the problem (0 if the problem is invalid). */
@@ -117,7 +126,8 @@ dc_status deform_conv_fwd(const dc_problem* prob, const void* x, const void* w_o
  *   x, w_off, w   as in the forward pass
  *   offset        [N, 2GK, Ho, Wo] float32, required: offset_out of the forward
  *   grad_y        [N, C_out, Ho, Wo] dtype, required
- *   grad_x        [N, C_in, H, W] float32, required (sampling + offset-conv paths)
+ *   grad_x        [N, C_in, H, W] float32, required (sampling + offset-conv paths);
+ *                 the problem dtype, masked by x > 0, when prob->in_relu = 1
  *   grad_w_off    [2GK, C_in, Kh, Kw] float32, required
  *   grad_b_off    [2GK] float32, NULL = not returned
  *   grad_w        [C_out, C_in, Kh, Kw] float32, required
@@ -128,7 +138,7 @@ dc_status deform_conv_fwd(const dc_problem* prob, const void* x, const void* w_o
  * summation order. */
 dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_off,
                           const void* w, const float* offset, const void* grad_y,
-                          float* grad_x, float* grad_w_off, float* grad_b_off,
+                          void* grad_x, float* grad_w_off, float* grad_b_off,
                           float* grad_w, float* grad_offset, void* ws, size_t ws_bytes,
                           void* stream);
 
@@ -142,7 +152,7 @@ dc_status deform_conv_bwd(const dc_problem* prob, const void* x, const void* w_o
  * library cannot check this: a stale map gives a wrong grad_w only. */
 dc_status deform_conv_bwd_after_fwd(const dc_problem* prob, const void* x, const void* w_off,
                                     const void* w, const float* offset, const void* grad_y,
-                                    float* grad_x, float* grad_w_off, float* grad_b_off,
+                                    void* grad_x, float* grad_w_off, float* grad_b_off,
                                     float* grad_w, float* grad_offset, void* ws, size_t ws_bytes,
                                     void* stream);
 

@@ -60,6 +60,7 @@ def ws_size(p, backward=False):
     (dict(dtype=7), B.DC_ERR_INVALID_ARG),
     (dict(halo_margin=-2), B.DC_ERR_INVALID_ARG),
     (dict(out_relu=2), B.DC_ERR_INVALID_ARG),
+    (dict(in_relu=-1), B.DC_ERR_INVALID_ARG),
     (dict(kh=9, kw=9, pad=4), B.DC_ERR_UNSUPPORTED),
     (dict(halo_margin=1000), B.DC_ERR_UNSUPPORTED),
 ])
@@ -83,6 +84,21 @@ def _call_fwd(p, ptrs, ws_bytes):
     vp = ctypes.c_void_p
     return B.lib().deform_conv_fwd(ctypes.byref(st), *[vp(v) if v else None for v in ptrs],
                                    ctypes.c_size_t(ws_bytes), None)
+
+
+@pytest.mark.parametrize("kw", [dict(dtype=B.DC_F32), dict(dtype=B.DC_BF16, offset_groups=2)])
+def test_in_relu_backward_workspace_holds_a_float32_grad_x(kw):
+    # problems off the channels-last backward accumulate grad_x in a float32
+    # scratch at the workspace's end, which the ReLU backward then reads; the
+    # forward workspace and every region before it are unchanged
+    import dataclasses
+    p = problem(**kw)
+    q = dataclasses.replace(p, in_relu=1)
+    scratch = p.n * p.c_in * p.h * p.w * 4
+    assert ws_size(q, False) == ws_size(p, False)
+    (s0, b0), (s1, b1) = ws_size(p, True), ws_size(q, True)
+    assert s0 == s1 == B.DC_OK
+    assert scratch <= b1 - b0 < scratch + 256
 
 
 def test_fwd_argument_checks_fail_before_any_launch():

@@ -8,10 +8,13 @@ The oracle runs the stack layer by layer in fp64 on image 0; each activation
 and each gradient between layers is stored in the layers' dtype (bf16) on both
 sides, so the oracle rounds it the same way (to float32, then to bf16,
 nearest even).  The CUDA path is compared layer by layer at the oracle's
-inputs (forward, backward at the oracle's float32 offsets, and the ReLU
-kernels bit for bit), then as a chain through the stack runner on the
-one-image slice and at full batch (forward output of image 0, and the top
-layer's weight gradient, which depends on no offset gradient)."""
+inputs (forward, backward at the oracle's float32 offsets, the ReLU kernels
+bit for bit, and the backward with the ReLU below fused), then as a chain
+through the stack runner on the one-image slice and at full batch (forward
+output of image 0, and the top layer's weight gradient, which depends on no
+offset gradient)."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -72,6 +75,69 @@ def test_fused_relu_forward_is_relu_of_the_forward(geom, dtype, entry):
     bits = torch.int16 if dtype == B.DC_BF16 else torch.int32
     assert (outs[0] < 0).any() and (outs[0] > 0).any()
     assert torch.equal(outs[1].view(bits), ref.view(bits))
+
+
+# The backward through the ReLU below (in_relu): grad_x in the layer's dtype,
+# +0 where x is not above zero and elsewhere the float32 grad_x rounded as
+# dc_relu_bwd rounds it.  Where the channels-last offset-convolution backward
+# writes grad_x, it applies the ReLU in that store (16-byte rows, and a row
+# length that is not a multiple of four: the per-element store; 64 and 128
+# channels per CTA); the others (a channels-last problem with stride 2, the
+# plane-major ones) accumulate grad_x in a float32 scratch and run the ReLU
+# kernel.  Columns: geometry, dtype, channels-last, ReLU in the grad_x store.
+FUSED_RELU_BWD_CASES = [
+    ((2, 64, 20, 24, 32, 3, 3, 1, 1, 1, 1), B.DC_BF16, True, True),
+    ((2, 64, 20, 22, 32, 3, 3, 1, 1, 1, 1), B.DC_BF16, True, True),
+    ((1, 128, 16, 32, 40, 3, 3, 1, 1, 1, 1), B.DC_BF16, True, True),
+    ((1, 128, 18, 32, 40, 3, 3, 2, 1, 1, 1), B.DC_BF16, True, False),
+    ((2, 16, 12, 10, 24, 3, 3, 1, 1, 1, 2), B.DC_BF16, False, False),
+    ((2, 12, 10, 14, 40, 3, 3, 1, 1, 1, 1), B.DC_F32, False, False),
+    ((1, 5, 17, 19, 7, 3, 3, 1, 1, 1, 1), B.DC_F32, False, False),
+]
+
+
+@pytest.mark.parametrize("geom,dtype,channels_last,in_store", FUSED_RELU_BWD_CASES)
+def test_fused_relu_backward_is_relu_bwd_of_the_backward(geom, dtype, channels_last, in_store):
+    import dataclasses
+    n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups = geom
+    p = B.Problem(n, c_in, h, w, c_out, kh, kw, s, pad, dil, groups, dtype)
+    pr = dataclasses.replace(p, in_relu=1)
+    assert (B.col_layout(p) == B.DC_COL_PIXEL_MAJOR) == channels_last
+    g = torch.Generator().manual_seed(53 + c_in + w)
+    sh = p.shapes()
+    dt = p.torch_dtype
+    x = torch.relu(torch.randn(sh["x"], generator=g)).to(dt).cuda()  # a ReLU's output
+    w_off = (0.05 * torch.randn(sh["w_off"], generator=g)).to(dt).cuda()
+    wm = (torch.randn(sh["w"], generator=g) / (c_in * kh * kw) ** 0.5).to(dt).cuda()
+    off = (0.7 * torch.randn(sh["offset"], generator=g)).cuda()
+    gy = torch.randn(sh["y"], generator=g).to(dt).cuda()
+    plain = B.backward(p, x, w_off, wm, off, gy)
+    B.kernel_timing(True)
+    fused = B.backward(pr, x, w_off, wm, off, gy)
+    names = [k for k, _ in B.kernel_times()]
+    B.kernel_timing(False)
+    ref = torch.empty_like(x)
+    B.dc_relu_bwd(x, plain["grad_x"], ref)
+    torch.cuda.synchronize()
+    assert fused["grad_x"].dtype == dt
+    # a separate ReLU kernel only where grad_x is not written by the
+    # channels-last offset-convolution backward
+    assert ("relu_bwd" in names) == (not in_store), names
+    assert ("k4cl_input" in names) == in_store, names
+    got, want = fused["grad_x"].double().cpu(), ref.double().cpu()
+    masked = x.cpu() <= 0
+    assert masked.any() and (~masked).any()
+    bits = torch.int16 if dtype == B.DC_BF16 else torch.int32
+    assert torch.all(fused["grad_x"].cpu()[masked].view(bits) == 0)  # +0
+    # float32 atomics sum grad_x in a run-dependent order: the float32 values
+    # differ by summation rounding (1e-5 of the tensor's scale bounds it,
+    # cancellation included), then by one bf16 rounding step at most
+    scale = float(want.abs().max())
+    assert scale > 0
+    rel = 2.0 ** -7 if dtype == B.DC_BF16 else 0.0
+    assert torch.all((got - want).abs() <= rel * torch.maximum(got.abs(), want.abs()) + 1e-5 * scale)
+    for k in ("grad_w", "grad_w_off", "grad_b_off", "grad_offset"):
+        assert rel_err(f64(fused[k]), f64(plain[k])) <= 1e-4, k
 
 
 def to_bf16_via_f32(a):
@@ -161,8 +227,13 @@ def test_stack_layer_by_layer_and_chained_on_one_image():
         if l > 0:
             gin = torch.empty(p1.shapes()["y"], dtype=dt, device="cuda")
             B.dc_relu_bwd(bf(xs[l]), torch.from_numpy(grads[l]["grad_x"]).float().cuda(), gin)
+            # the same gradient from the backward with the ReLU fused (in_relu)
+            gf = B.backward(dataclasses.replace(p1, in_relu=1), bf(xs[l]), q["w_off"], q["w"],
+                            torch.from_numpy(offs[l]).float().cuda(), bf(gys[l]))
             torch.cuda.synchronize()
             assert np.array_equal(f64(gin), gys[l - 1]), l
+            assert rel_err(f64(gf["grad_x"]), gys[l - 1]) <= tol, l
+            assert np.all(f64(gf["grad_x"])[xs[l] <= 0] == 0), l
     # the chain through the stack runner, on the same image
     st = S.Stack(p1, dev_layers, "cuda")
     st.step(x0.cuda(), gy.cuda())
