@@ -22,7 +22,8 @@
 //   P warps (4)  per tile: the sampling taps from the given offsets and every
 //                (sample, corner) pair that lands in the window and in the
 //                image, bucketed by window position (counts and ranks from
-//                shared-memory atomics, a scan, a scatter);
+//                shared-memory atomics, a scan, a scatter); D_j(s) = 0 for
+//                the corners outside the image;
 //   S warps (12) per tile: lanes in groups of cpc / 16 (sixteen channels
 //                each, two 8-channel pieces half a slice apart; eight
 //                channels for 64-channel slices); the bucketed pairs are
@@ -116,7 +117,7 @@ __host__ K3Plan k3_plan_for(const Geom& g, int margin, int TH, int TW, int cspli
   at += (size_t)p.items * 16;
   p.off_otab = at;  // [M * npx] int2 {offset-map element from the tile's first, pixel row | col << 16}
   at += (size_t)g.M * p.npx * 8;
-  p.off_D = at;  // [2][items * 4] D_j(s) (S only)
+  p.off_D = at;  // [2][items * 4] D_j(s) (S; P writes the zeros of corners outside the image)
   at += 2 * (size_t)p.items * 4 * 4;
   p.off_slow = at;  // [2][items + 1] samples read from global memory (count first)
   at += 2 * (size_t)(p.items + 1) * 4;
@@ -443,6 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int2* ent = ent0 + (size_t)s * items * 4;
       int* pst = pst0 + (size_t)s * (npos + 1);
       int* slow = slow0 + (size_t)s * (items + 1);
+      float* Dz = D0 + (size_t)s * items * 4;  // S's D table of this tile
       if (tid == 0) slow[0] = 0;
       for (int e = tid; e <= npos; e += kPThreads) cnt[e] = 0;
       p_sync();
@@ -478,6 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (yy >= 0 && yy < g.h && xx >= 0 && xx < g.w) {
                   const int pos = (ry + (j >> 1)) * pl.cols + rx + (j & 1);
                   pr[u][j] = (uint32_t)pos | ((uint32_t)atomicAdd(&cnt[pos], 1) << 16);
+                } else {
+                  Dz[it * 4 + j] = 0.f;  // no pair: D_j(s) = 0 (S writes the others)
                 }
               }
             } else {
@@ -566,8 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const unsigned char* gsm0 = smem + pl.off_gc + (size_t)s * gc_pitch;
       const unsigned char* gsm = gsm0 + cl * 2;
       float* gximg = a.gx + (long long)tx.n * g.hw * C + cbeg + cl;
-      for (int e = tid - kPThreads; e < items * 4; e += kSThreads) Dt[e] = 0.f;
-      s_sync();
+      // every D_j(s) the offset gradients read is written once this tile:
+      // by the pair walk, the global path, or (corners outside the image) P
       // ---------------------------------------------- pairs, by window position
       // Lanes in groups of L = cpc / W, W channels each (16 when the slice has
       // 128 or more channels: a pair's fixed work is shared by twice the

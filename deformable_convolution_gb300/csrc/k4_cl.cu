@@ -553,32 +553,43 @@ __global__ void __launch_bounds__(256) k4cl_reduce(const float* __restrict__ par
   if ((int)blockIdx.x >= nred) {
     // grad_w[o][c][k] = gw_perm[o][k][c] (the main weight gradient, added in
     // w' order by the GEMM): one block per (o, kPermCh channels), the slice
-    // [K][kPermCh] read by rows and written as one run of kPermCh * K floats
+    // [K][kPermCh] read by rows (every load of the block in flight at once)
+    // and written as one run of kPermCh * K floats
     const int b = (int)blockIdx.x - nred;
     const int cch = (C + kPermCh - 1) / kPermCh;
     const int o = b / cch, c0 = (b - o * cch) * kPermCh;
     const int nc = min(kPermCh, C - c0);
     const float* src = gw_perm + (size_t)o * C * K;
-    for (int k = 0; k < K; ++k)
-      for (int c = threadIdx.x; c < nc; c += blockDim.x) tr[c * K + k] = src[(size_t)k * C + c0 + c];
+    constexpr int kPer = (kPermCh * kMaxK + 255) / 256;  // elements per thread
+    float v[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = (int)threadIdx.x + 256 * u, k = e / nc;
+      if (k < K) v[u] = src[(size_t)k * C + c0 + (e - k * nc)];
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = (int)threadIdx.x + 256 * u, k = e / nc;
+      if (k < K) tr[(e - k * nc) * K + k] = v[u];
+    }
     __syncthreads();
     float* dst = grad_w + ((size_t)o * C + c0) * K;
     for (int e = threadIdx.x; e < nc * K; e += blockDim.x) dst[e] = tr[e];
     pdl_release();
     return;
   }
-  // one output per thread: the chunks' partials added in chunk order, eight
+  // one output per thread: the chunks' partials added in chunk order, sixteen
   // loads in flight; the last sum block's first M threads also add the bias
   const int i = blockIdx.x * 256 + threadIdx.x;
   if (i < count) {
     float v = 0.f;
     int c = 0;
-    for (; c + 8 <= nchunks; c += 8) {
-      float t[8];
+    for (; c + 16 <= nchunks; c += 16) {
+      float t[16];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) t[u] = part[(size_t)(c + u) * count + i];
+      for (int u = 0; u < 16; ++u) t[u] = part[(size_t)(c + u) * count + i];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) v += t[u];
+      for (int u = 0; u < 16; ++u) v += t[u];
     }
     for (; c < nchunks; ++c) v += part[(size_t)c * count + i];
     gw_off[i] = v;
