@@ -335,6 +335,8 @@ cudaError_t launch_k4cl_input(const K4ClArgs& a, cudaStream_t s);
 cudaError_t launch_k4cl_weight(const K4ClArgs& a, cudaStream_t s);
 cudaError_t launch_k4cl_reduce(const K4ClArgs& a, cudaStream_t s);
 unsigned int k4cl_read_error(int clear);
+bool make_tmap_f32(CUtensorMap* m, const void* base, int rank, const unsigned long long* dims,
+                   const unsigned long long* strides_bytes, const unsigned int* box);
 bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const unsigned long long* dims,
                     const unsigned long long* strides_bytes, const unsigned int* box,
                     bool swizzle128);

@@ -909,6 +909,33 @@ EncodeTiledFnCl encode_cl() {
 }
 }  // namespace
 
+namespace {
+bool make_tmap_dt(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank,
+                  const unsigned long long* dims, const unsigned long long* strides_bytes,
+                  const unsigned int* box, bool swizzle128) {
+  EncodeTiledFnCl fn = encode_cl();
+  if (!fn) return false;
+  cuuint64_t d[5];
+  cuuint64_t st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) st[i] = strides_bytes[i];
+  }
+  return fn(m, dt, (cuuint32_t)rank, const_cast<void*>(base), d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+// fp32 tensor map, no swizzle (zero fill outside the tensor).
+bool make_tmap_f32(CUtensorMap* m, const void* base, int rank, const unsigned long long* dims,
+                   const unsigned long long* strides_bytes, const unsigned int* box) {
+  return make_tmap_dt(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, rank, dims, strides_bytes, box, false);
+}
+
 // bf16 tensor map (zero fill outside the tensor); 128-byte swizzle or none.
 bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const unsigned long long* dims,
                     const unsigned long long* strides_bytes, const unsigned int* box,

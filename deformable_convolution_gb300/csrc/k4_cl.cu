@@ -29,6 +29,8 @@
 // NHWC window by ldmatrix.trans, B = goff).  Each CTA writes its partial sums
 // once; a small kernel adds the chunks (and the bias partials) in a fixed
 // order.
+#include <string.h>
+
 #include "dc_band.cuh"
 #include "dc_tma.cuh"
 
@@ -53,17 +55,27 @@ __host__ __device__ inline int in_pitch(const Geom& g) { return km_padded(g) + 8
 // goff rows / columns read by a tile of positions
 __host__ __device__ inline int in_gy(const Geom& g) { return (kTY - 1 + (g.kh - 1) * g.dh) / g.sh + 2; }
 __host__ __device__ inline int in_gx(const Geom& g) { return (kTX - 1 + (g.kw - 1) * g.dw) / g.sw + 2; }
+// The goff tile arrives by one TMA box when goff's rows are 16-byte aligned
+// (Wo a multiple of 4): the box starts at the column rounded down to a
+// multiple of 4 and is as many columns wider, a multiple of 4 in all.
+__host__ __device__ inline bool in_goff_tma(const Geom& g) { return g.wo % 4 == 0; }
+__host__ __device__ inline int in_gxp(const Geom& g) {
+  return in_goff_tma(g) ? (in_gx(g) + 3 + 3) / 4 * 4 : in_gx(g);
+}
 __host__ __device__ inline int floor_div(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
 // shared memory: A [kQ][pitch] and B [cpc][pitch] (bf16), then the goff tile
 // (float); the transposed result later lies over A and B
+// (offsets from the dynamic array advanced to a 128-byte boundary; the goff
+// tile is a TMA destination, its mbarrier follows it)
 __host__ __device__ inline size_t in_g_off(const Geom& g, int cpc) {
   const size_t ab = (size_t)(kQ + cpc) * in_pitch(g) * 2;
   const size_t t = (size_t)cpc * (kQ + 4) * 4;
-  return ((ab > t ? ab : t) + 15) / 16 * 16;
+  return ((ab > t ? ab : t) + 127) / 128 * 128;
 }
-__host__ inline size_t input_smem(const Geom& g, int cpc) {
-  return in_g_off(g, cpc) + (size_t)g.M * in_gy(g) * in_gx(g) * 4;
+__host__ __device__ inline size_t in_bar_off(const Geom& g, int cpc) {
+  return in_g_off(g, cpc) + ((size_t)g.M * in_gy(g) * in_gxp(g) * 4 + 7) / 8 * 8;
 }
+__host__ inline size_t input_smem(const Geom& g, int cpc) { return in_bar_off(g, cpc) + 8 + 128; }
 
 __device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -117,9 +129,13 @@ __device__ __forceinline__ unsigned int relu_grad2(float v0, float v1, unsigned 
 
 // CPC channels per CTA (64 or 128).  Warps: 8 m-tiles of 16 positions x
 // CPC/8 n-tiles of 8 channels; a warp holds MTW m-tiles x 8 n-tiles.
+// gmap: goff [n][M][Ho][Wo] fp32, box {GXP, GY, M, 1}, used when in_goff_tma.
 template <int CPC>
-__global__ void __launch_bounds__(kInThreads, 2) k4cl_input(K4InArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
+__global__ void __launch_bounds__(kInThreads, 2)
+    k4cl_input(const __grid_constant__ CUtensorMap gmap, K4InArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const uint32_t raw = px::smem_u32(smem_raw);
+  unsigned char* smem = smem_raw + (((raw + 127u) & ~127u) - raw);
   constexpr int MTW = CPC / 64;  // m-tiles per warp (2 or 1)
   const Geom g = a.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -142,7 +158,17 @@ __global__ void __launch_bounds__(kInThreads, 2) k4cl_input(K4InArgs a) {
   const int GY = in_gy(g), GX = in_gx(g);  // GX <= 32 (k4cl_supported)
   const int hlo = floor_div(y0 + g.ph - (g.kh - 1) * g.dh, g.sh);
   const int wlo = floor_div(x0 + g.pw - (g.kw - 1) * g.dw, g.sw);
-  float* G = reinterpret_cast<float*>(smem + in_g_off(g, CPC));  // [M][GY][GX]
+  const bool tma = in_goff_tma(g);
+  const int GXP = in_gxp(g), wlo0 = tma ? (wlo & ~3) : wlo;  // the tile's first column and pitch
+  float* G = reinterpret_cast<float*>(smem + in_g_off(g, CPC));  // [M][GY][GXP]
+  uint64_t* gbar = reinterpret_cast<uint64_t*>(smem + in_bar_off(g, CPC));
+  if (tma) {
+    if (tid == 0) {
+      px::mbar_init(gbar, 1);
+      px::fence_mbar_init();
+    }
+    __syncthreads();
+  }
   if (g.in_relu) {
     // the ReLU mask x of the grad_x store, into L2 while the tile is built:
     // per (channel, row of the tile) the row's first and last element (x was
@@ -159,9 +185,15 @@ __global__ void __launch_bounds__(kInThreads, 2) k4cl_input(K4InArgs a) {
     }
   }
   pdl_wait();  // goff and gx_nhwc from the sampling backward, Bt from the weight part
-  // goff tile: a warp per (m, row), lanes over the columns (GX <= 32), all
-  // rows in flight as 4-byte asynchronous copies (zero-filled outside goff)
-  {
+  // goff tile: one TMA box (zero outside goff), or else a warp per (m, row),
+  // lanes over the columns (GX <= 32), all rows in flight as 4-byte
+  // asynchronous copies (zero-filled outside goff)
+  if (tma) {
+    if (tid == 0) {
+      px::mbar_expect_tx(gbar, (uint32_t)(M * GY * GXP * 4));
+      px::tma_load_4d(G, &gmap, gbar, wlo0, hlo, 0, n);
+    }
+  } else {
     const float* gimg = a.goff + (size_t)n * M * g.howo;
     const int wo = wlo + lane;
     const bool colok = lane < GX && wo >= 0 && wo < g.wo;
@@ -189,8 +221,20 @@ __global__ void __launch_bounds__(kInThreads, 2) k4cl_input(K4InArgs a) {
                      : "memory");
     asm volatile("cp.async.commit_group;" ::: "memory");
   }
-  asm volatile("cp.async.wait_group 1;" ::: "memory");  // the goff tile (B may still be in flight)
-  __syncthreads();
+  if (tma) {
+    // the goff tile (B may still be in flight); on a wait that gave up, the
+    // copy this CTA issued is waited for once more (bounded) before leaving
+    const bool ok = px::mbar_wait(gbar, 0, &g_k4cl_error);
+    if (!__syncthreads_and(ok)) {
+      if (tid == 0 && !ok) px::mbar_wait(gbar, 0, &g_k4cl_error);
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+      pdl_release();
+      return;
+    }
+  } else {
+    asm volatile("cp.async.wait_group 1;" ::: "memory");  // the goff tile (B may still be in flight)
+    __syncthreads();
+  }
   // A[q][k*M + m] = goff[m][pixel whose tap k reads position q], 0 if none:
   // a thread per (q, k), m pairs written as one word (M is even)
   // (kInThreads is a multiple of kQ: each thread keeps its position q)
@@ -211,10 +255,10 @@ __global__ void __launch_bounds__(kInThreads, 2) k4cl_input(K4InArgs a) {
     int gi = -1;
     if (ty_ >= 0 && tx_ >= 0 && (g.sh == 1 || ty_ % g.sh == 0) && (g.sw == 1 || tx_ % g.sw == 0)) {
       const int ho = ty_ / g.sh, wo = tx_ / g.sw;
-      if (ho < g.ho && wo < g.wo) gi = (ho - hlo) * GX + (wo - wlo);
+      if (ho < g.ho && wo < g.wo) gi = (ho - hlo) * GXP + (wo - wlo0);
     }
     uint32_t* row = reinterpret_cast<uint32_t*>(A + (size_t)q * P + k * M);
-    const int plane = GY * GX;
+    const int plane = GY * GXP;
     const float* gq = G + (gi >= 0 ? gi : 0);
 #pragma unroll
     for (int m = 0; m < 2 * kMaxK; m += 2) {
@@ -687,10 +731,20 @@ cudaError_t launch_k4cl_input(const K4ClArgs& in, cudaStream_t s) {
   a.cpc = cpc;
   const int tiles_y = (int)ceil_div_ll(g.h, kTY);
   const size_t smem = input_smem(g, cpc);
+  CUtensorMap gmap;
+  memset(&gmap, 0, sizeof(gmap));
+  if (in_goff_tma(g)) {
+    const unsigned long long dims[4] = {(unsigned long long)g.wo, (unsigned long long)g.ho,
+                                        (unsigned long long)g.M, (unsigned long long)g.n};
+    const unsigned long long strides[3] = {(unsigned long long)g.wo * 4, (unsigned long long)g.howo * 4,
+                                           (unsigned long long)g.M * g.howo * 4};
+    const unsigned int box[4] = {(unsigned)in_gxp(g), (unsigned)in_gy(g), (unsigned)g.M, 1u};
+    if (!make_tmap_f32(&gmap, in.goff, 4, dims, strides, box)) return cudaErrorInvalidValue;
+  }
   const void* func = cpc == 128 ? (const void*)k4cl_input<128> : (const void*)k4cl_input<64>;
   cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  void* args[] = {&a};
+  void* args[] = {&gmap, &a};
   return launch_pdl4(func, dim3((unsigned)(a.tiles_x * tiles_y), (unsigned)(g.c_in / cpc), (unsigned)g.n),
                      dim3(kInThreads), smem, s, args);
 }
