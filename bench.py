@@ -896,10 +896,12 @@ def e2e_stack(job, dev, stream, iters=10):
     uploads layer 0's input, every layer's weights and grad_y from pinned host
     memory and reads back the last layer's output, grad_x of layer 0 and every
     layer's weight gradients.  One CUDA graph per step over two streams:
-    layer 0's input and weights go up first on the compute stream; the other
-    layers' weights and grad_y go up on a copy stream while layer 0's forward
-    runs; the output comes back on the copy stream while the backward runs,
-    and each layer's weight gradients come back on it as soon as that layer's
+    layer 0's input and weights go up first on the compute stream, alone, so
+    the forward starts as early as the link allows; then, on a copy stream
+    while layer 0's forward runs, the other layers' weights (the next
+    forward waits for them) and grad_y (the backward waits for it); the
+    output comes back on the copy stream while the backward runs, and each
+    layer's weight gradients come back on it as soon as that layer's
     backward is done.  Each group of tensors is one packed buffer on both
     sides, so each group is one copy."""
     import torch
@@ -911,9 +913,9 @@ def e2e_stack(job, dev, stream, iters=10):
     x0h, layers_h, gyh = job.host
     groups = {"in0": [("x", tuple(s["x"]), dt)] + [(f"{k}0", tuple(v.shape), v.dtype)
                                                    for k, v in layers_h[0].items()],
-              "rest": [("gy", tuple(s["y"]), dt)] + [(f"{k}{l}", tuple(v.shape), v.dtype)
-                                                     for l in range(1, L)
-                                                     for k, v in layers_h[l].items()],
+              "wrest": [(f"{k}{l}", tuple(v.shape), v.dtype) for l in range(1, L)
+                        for k, v in layers_h[l].items()],
+              "gyin": [("gy", tuple(s["y"]), dt)],
               "yout": [("y", tuple(s["y"]), dt)], "gx": [("gx", tuple(s["x"]), f32)]}
     for l in range(L):
         groups[f"g{l}"] = [("grad_w_off", tuple(s["w_off"]), f32),
@@ -923,45 +925,53 @@ def e2e_stack(job, dev, stream, iters=10):
         hbuf[gname], hv[gname] = _packed(specs, "cpu", True)
         dbuf[gname], dv[gname] = _packed(specs, dev, False)
     hv["in0"]["x"].copy_(x0h)
-    hv["rest"]["gy"].copy_(gyh)
+    hv["gyin"]["gy"].copy_(gyh)
     for l in range(L):
         for k, v in layers_h[l].items():
-            hv["in0" if l == 0 else "rest"][f"{k}{l}"].copy_(v)
-    params = [{k: dv["in0" if l == 0 else "rest"][f"{k}{l}"] for k in ("w_off", "b_off", "w")}
+            hv["in0" if l == 0 else "wrest"][f"{k}{l}"].copy_(v)
+    params = [{k: dv["in0" if l == 0 else "wrest"][f"{k}{l}"] for k in ("w_off", "b_off", "w")}
               for l in range(L)]
     saved = st.params, st.grads
     st.params = params
     st.grads = [dv[f"g{l}"] for l in range(L)]
-    h2d = sum(b.numel() for g, b in hbuf.items() if g in ("in0", "rest"))
-    d2h = sum(b.numel() for g, b in hbuf.items() if g not in ("in0", "rest"))
+    up = ("in0", "wrest", "gyin")
+    h2d = sum(b.numel() for g, b in hbuf.items() if g in up)
+    d2h = sum(b.numel() for g, b in hbuf.items() if g not in up)
     cs = torch.cuda.Stream(device=dev)
-    e_rest = torch.cuda.Event()
+    e_in0, e_wrest, e_gy = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
     e_fwd = torch.cuda.Event()
     e_layer = [torch.cuda.Event() for _ in range(L)]
-    x_dev, gy_dev = dv["in0"]["x"], dv["rest"]["gy"]
+    x_dev, gy_dev = dv["in0"]["x"], dv["gyin"]["gy"]
 
     def one():
         cur = torch.cuda.current_stream(dev)
-        cs.wait_stream(cur)
-        with torch.cuda.stream(cs):
-            dbuf["rest"].copy_(hbuf["rest"], non_blocking=True)
-            e_rest.record(cs)
         dbuf["in0"].copy_(hbuf["in0"], non_blocking=True)
+        e_in0.record(cur)
+        cs.wait_event(e_in0)
+        with torch.cuda.stream(cs):
+            if L > 1:
+                dbuf["wrest"].copy_(hbuf["wrest"], non_blocking=True)
+                e_wrest.record(cs)
+            dbuf["gyin"].copy_(hbuf["gyin"], non_blocking=True)
+            e_gy.record(cs)
         st.x[0] = x_dev
         q = st.params[0]
         # layers below the last write relu(y) into the next layer's input (fused)
         B.deform_conv_fwd(st.p_relu if L > 1 else p, x_dev, q["w_off"], q["b_off"], q["w"], None,
                           st.x[1] if L > 1 else st.y[0], st.off[0], None, st.ws[0])
-        cur.wait_event(e_rest)
+        if L > 1:
+            cur.wait_event(e_wrest)
         for l in range(1, L):
             q, last = st.params[l], l + 1 == L
             B.deform_conv_fwd(p if last else st.p_relu, st.x[l], q["w_off"], q["b_off"], q["w"], None,
                               st.y[l] if last else st.x[l + 1], st.off[l], None, st.ws[l])
-        dv["yout"]["y"].copy_(st.y[-1])
         e_fwd.record(cur)
         cs.wait_event(e_fwd)
         with torch.cuda.stream(cs):
-            hbuf["yout"].copy_(dbuf["yout"], non_blocking=True)
+            # the output straight into its pinned host view (the backward
+            # reads the forward's workspace, not y)
+            hv["yout"]["y"].copy_(st.y[-1], non_blocking=True)
+        cur.wait_event(e_gy)
         st.gy[-1] = gy_dev
         for l in reversed(range(L)):
             st.backward_layer(l)  # layer l - 1's grad_y through the ReLU, fused
@@ -999,15 +1009,15 @@ def e2e_stack(job, dev, stream, iters=10):
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / iters
     # the read-back is complete: the host copies equal the device buffers
-    assert torch.equal(hv["yout"]["y"], dv["yout"]["y"].cpu()), "e2e read-back mismatch"
+    assert torch.equal(hv["yout"]["y"], st.y[-1].cpu()), "e2e read-back mismatch"
     assert torch.equal(hv["g0"]["grad_w"], dv["g0"]["grad_w"].cpu()), "e2e read-back mismatch"
     st.params, st.grads = saved
     return {"value": job.flops_step / (ms / 1e3) / 1e9, "unit": "GFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "method": how + ": layer 0's input and weights up on the compute stream, the other "
-                            "layers' weights and grad_y up on a copy stream during layer 0's "
-                            "forward; the output, each layer's weight gradients (as soon as its "
-                            "backward is done) and grad_x of layer 0 back, packed groups"}
+            "method": how + ": layer 0's input and weights up on the compute stream first, then "
+                            "the other layers' weights and grad_y up on a copy stream during "
+                            "layer 0's forward; the output, each layer's weight gradients (as soon "
+                            "as its backward is done) and grad_x of layer 0 back, packed groups"}
 
 
 def e2e(p, d, dev, stream, flops_step, iters=20):

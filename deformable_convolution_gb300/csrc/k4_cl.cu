@@ -169,21 +169,6 @@ __global__ void __launch_bounds__(kInThreads, 2)
     }
     __syncthreads();
   }
-  if (g.in_relu) {
-    // the ReLU mask x of the grad_x store, into L2 while the tile is built:
-    // per (channel, row of the tile) the row's first and last element (x was
-    // written before this backward began; a prefetch changes no data)
-    const unsigned short* p0 = a.x + ((size_t)n * C + cbeg) * g.hw;
-    const int xl = min(x0 + kTX, g.w) - 1;
-    for (int e = tid; e < CPC * kTY; e += kInThreads) {
-      const int c = e / kTY, y = y0 + (e - c * kTY);
-      if (y < g.h) {
-        const unsigned short* row = p0 + (size_t)c * g.hw + (size_t)y * g.w;
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + x0));
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(row + xl));
-      }
-    }
-  }
   pdl_wait();  // goff and gx_nhwc from the sampling backward, Bt from the weight part
   // goff tile: one TMA box (zero outside goff), or else a warp per (m, row),
   // lanes over the columns (GX <= 32), all rows in flight as 4-byte
