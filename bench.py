@@ -891,6 +891,26 @@ def _packed(specs, device, pinned):
     return buf, views
 
 
+def _timed_runs(step, stream, dev, iters, runs=3):
+    """ms per step of `iters` steps timed with CUDA events on `stream`, three
+    times: the median, and every run (the host link is shared with other work
+    on the machine, so a single run can catch a slow moment)."""
+    import statistics
+
+    import torch
+    out = []
+    for _ in range(runs):
+        with torch.cuda.stream(stream):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(iters):
+                step()
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        out.append(a.elapsed_time(b) / iters)
+    return statistics.median(out), out
+
+
 def e2e_stack(job, dev, stream, iters=10):
     """The stack's training step through the ABI with host buffers: every step
     uploads layer 0's input, every layer's weights and grad_y from pinned host
@@ -1001,19 +1021,14 @@ def e2e_stack(job, dev, stream, iters=10):
         for _ in range(2):
             step()
         torch.cuda.synchronize(dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(iters):
-            step()
-        b.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b) / iters
+    ms, runs = _timed_runs(step, stream, dev, iters)
     # the read-back is complete: the host copies equal the device buffers
     assert torch.equal(hv["yout"]["y"], st.y[-1].cpu()), "e2e read-back mismatch"
     assert torch.equal(hv["g0"]["grad_w"], dv["g0"]["grad_w"].cpu()), "e2e read-back mismatch"
     st.params, st.grads = saved
     return {"value": job.flops_step / (ms / 1e3) / 1e9, "unit": "GFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "runs_ms_per_step": runs, "timing": f"median of {len(runs)} runs of {iters} steps",
             "method": how + ": layer 0's input and weights up on the compute stream first, then "
                             "the other layers' weights and grad_y up on a copy stream during "
                             "layer 0's forward; the output, each layer's weight gradients (as soon "
@@ -1102,19 +1117,14 @@ def e2e(p, d, dev, stream, flops_step, iters=20):
         for _ in range(3):
             step()
         torch.cuda.synchronize(dev)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(iters):
-            step()
-        b.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b) / iters
+    ms, runs = _timed_runs(step, stream, dev, iters)
     # the read-back is complete: the last step's y and grad_x on the host equal
     # the device copies
     assert torch.equal(hv["y"], outs["y"].cpu()), "e2e read-back mismatch"
     assert torch.equal(hv["gx"], outs["gx"].cpu()), "e2e read-back mismatch"
     return {"value": flops_step / (ms / 1e3) / 1e9, "unit": "GFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "runs_ms_per_step": runs, "timing": f"median of {len(runs)} runs of {iters} steps",
             "method": how + ": forward inputs up (one packed copy), forward, backward, gradients "
                             "back (one packed copy) on the compute stream; grad_y up and y/offsets "
                             "back on a copy stream beside it"}
