@@ -613,8 +613,8 @@ def kernel_costs(p, has_add):
         "k1_band_sample": ("hbm", k1_bytes(p, has_add)),
         "k1_cl_sample": ("hbm", k1_bytes(p, has_add)),
         "k1_cl_offsets": ("hbm", x_b + woff_b + off_b * (2 if has_add else 1)),
-        "cl_prep_x": ("hbm", 2 * x_b),
-        "cl_prep_weights": ("hbm", 2 * w_b + 2 * woff_b),
+        # x to its NHWC copy, w permuted, w_off laid out: one launch
+        "cl_prep": ("hbm", 2 * x_b + 2 * w_b + 2 * woff_b),
         "gemm_fwd": ("tensor", gemm), "gemm_gcol": ("tensor", gemm), "gemm_gw": ("tensor", gemm),
         "k3_band_bwd": ("hbm", k3),
         # read x (NHWC), offsets, gcol; grad_x into the NHWC float32 buffer, goff
@@ -751,7 +751,7 @@ def k1_roofline(p, t, dev, stream, flush, wl, iters=200):
     cl = B.col_layout(p) == B.DC_COL_PIXEL_MAJOR
     name = "k1_cl_sample" if cl else "k1_band_sample"
     traffic = traffic_for(wl.name, name)
-    what = ("cl_prep_x (x to NHWC) + cl_prep_weights + k1_cl_sample (offset conv + bilinear "
+    what = ("cl_prep (x to NHWC, weight layouts) + k1_cl_sample (offset conv + bilinear "
             "sampling), one deform_conv_sample call" if cl
             else "k1_band_sample (offset conv + bilinear sampling)")
     return {"kernel": what, "bound": "hbm",

@@ -204,24 +204,20 @@ dc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DC_OK : DC_ERR_
 }  // namespace
 
 namespace {
-// The channels-last sampling stage: x to NHWC; in one launch the main weights
+// The channels-last sampling stage: in one launch x to NHWC, the main weights
 // permuted (when `w` is given) and w_off in mma fragment order (unless in
 // replay mode); then K1 over the staged windows.
 dc_status cl_stage(const Geom& g, int margin, const Plan& pl, char* wsb, const void* x,
                    const void* w_off, const void* w, const float* b_off, const float* off_add,
                    const float* off_in, void* col, float* off_out, unsigned long long* slow,
                    cudaStream_t s) {
-  dc_status st = cuda_status(timed("cl_prep_x", s, [&] {
-    return launch_cl_prep_x(x, wsb + pl.xc_off, g, s);
+  // x to NHWC and (unless replaying without new weights) the weight layouts
+  const bool weights = !off_in || w;
+  dc_status st = cuda_status(timed("cl_prep", s, [&] {
+    return launch_cl_prep(x, wsb + pl.xc_off, weights ? w : nullptr, wsb + pl.wp_off, w_off,
+                          weights && !off_in ? wsb + pl.wfrag_off : nullptr, g, margin, s);
   }));
   if (st != DC_OK) return st;
-  if (!off_in || w) {
-    st = cuda_status(timed("cl_prep_weights", s, [&] {
-      return launch_cl_prep_weights(w, wsb + pl.wp_off, w_off, off_in ? nullptr : wsb + pl.wfrag_off,
-                                    g, margin, s);
-    }));
-    if (st != DC_OK) return st;
-  }
   ClArgs ca{};
   ca.g = g;
   ca.xc = wsb + pl.xc_off;

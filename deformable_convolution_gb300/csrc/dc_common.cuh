@@ -285,11 +285,10 @@ struct ClArgs {
   unsigned long long* slow_count;
   int margin;
 };
-cudaError_t launch_cl_prep_x(const void* x, void* xc, const Geom& g, cudaStream_t s);
-// w [o][c][tap] -> w' [o][tap][c] (w non-null), and w_off in mma B-fragment
-// order (frag non-null), in one launch
-cudaError_t launch_cl_prep_weights(const void* w, void* wp, const void* w_off, void* frag,
-                                   const Geom& g, int margin, cudaStream_t s);
+// In one launch: x (NCHW) to its NHWC copy xc; w [o][c][tap] -> w' [o][tap][c]
+// (w non-null); w_off in mma B-fragment order (frag non-null).
+cudaError_t launch_cl_prep(const void* x, void* xc, const void* w, void* wp, const void* w_off,
+                           void* frag, const Geom& g, int margin, cudaStream_t s);
 cudaError_t launch_cl_sample(const ClArgs& a, cudaStream_t s);
 unsigned int cl_read_error(int clear);
 // Backward of the sampling step on the channels-last path (one offset group):

@@ -756,13 +756,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 // channels of one pixel.  C % 64 == 0 and H * W % 8 == 0 (cl_supported).
 constexpr int kTrPx = 128;
 constexpr int kTrPitch = 36;  // words per tile row: 32 channel pairs + 4 (16-byte rows, banks shifted)
-__global__ void __launch_bounds__(256) nchw_to_nhwc(const __nv_bfloat16* __restrict__ x,
-                                                    __nv_bfloat16* __restrict__ xc, int C,
-                                                    long long HW) {
-  __shared__ __align__(16) uint32_t tile[kTrPx * kTrPitch];
-  pdl_wait();
-  const int n = blockIdx.z, c0 = blockIdx.y * 64;
-  const long long p0 = (long long)blockIdx.x * kTrPx;
+__device__ __forceinline__ void nchw_to_nhwc_tile(const __nv_bfloat16* __restrict__ x,
+                                                  __nv_bfloat16* __restrict__ xc, int C, long long HW,
+                                                  int bx, int by, int bz, uint32_t* tile) {
+  const int n = bz, c0 = by * 64;
+  const long long p0 = (long long)bx * kTrPx;
   const int t = threadIdx.x;
   {
     const int cp = t & 31, g16 = t >> 5;
@@ -797,7 +795,6 @@ __global__ void __launch_bounds__(256) nchw_to_nhwc(const __nv_bfloat16* __restr
       *reinterpret_cast<uint4*>(xc + ((long long)n * HW + p) * C + c0 + 8 * j) =
           *reinterpret_cast<const uint4*>(tile + pp * kTrPitch + 4 * j);
   }
-  pdl_release();
 }
 
 // Weight preparation, one launch.  Blocks [0, O): row o of the main weights
@@ -808,16 +805,15 @@ __global__ void __launch_bounds__(256) nchw_to_nhwc(const __nv_bfloat16* __restr
 // channels, lane (gid, tig) holds {w(m, c0 + 2tig, k), w(m, c0 + 2tig + 1, k)}
 // and the same at c0 + 8, m = 8q + gid; zero for m >= M.  The steps are
 // ordered by channel slice (the channels one CTA of a tile holds), then tap.
-__global__ void __launch_bounds__(256) prep_weights(const unsigned short* __restrict__ w,
-                                                    unsigned short* __restrict__ wp,
-                                                    const unsigned short* __restrict__ w_off,
-                                                    uint2* __restrict__ frag, int O, int C, int K,
-                                                    int M, int ntiles, int cpc) {
-  extern __shared__ __align__(16) unsigned short row[];  // C * K
-  pdl_wait();
+__device__ __forceinline__ void prep_weights_block(const unsigned short* __restrict__ w,
+                                                   unsigned short* __restrict__ wp,
+                                                   const unsigned short* __restrict__ w_off,
+                                                   uint2* __restrict__ frag, int O, int C, int K,
+                                                   int M, int ntiles, int cpc, int wb,
+                                                   unsigned short* row) {
   const int CK = C * K;
-  if ((int)blockIdx.x < O) {
-    const int o = blockIdx.x;
+  if (wb < O) {
+    const int o = wb;
     const uint4* src = reinterpret_cast<const uint4*>(w + (long long)o * CK);
     for (int e = threadIdx.x; e < CK / 8; e += blockDim.x) reinterpret_cast<uint4*>(row)[e] = __ldg(src + e);
     __syncthreads();
@@ -833,7 +829,7 @@ __global__ void __launch_bounds__(256) prep_weights(const unsigned short* __rest
   } else if (frag) {
     // reduction step ks of channel slice r (slices of cpc channels, in slice
     // order): tap k, channels r * cpc + 16 * (step within the tap) ..
-    const int ks_all = blockIdx.x - O;
+    const int ks_all = wb - O;
     const int kstl = K * cpc / 16, r = ks_all / kstl, ks = ks_all - r * kstl;
     const int cps = cpc / 16;
     const int k = ks / cps;
@@ -850,6 +846,27 @@ __global__ void __launch_bounds__(256) prep_weights(const unsigned short* __rest
       frag[(long long)ks_all * ntiles * 32 + e] = v;
     }
   }
+}
+
+// The channels-last preparation in one launch: blocks [0, nxb) the NHWC copy
+// of x (block b: pixel tile b % ntx, channel chunk (b / ntx) % nty, image
+// b / (ntx * nty)), the rest the weight layouts (two independent jobs that
+// the sampling stage both waits for).
+__global__ void __launch_bounds__(256) cl_prep(const __nv_bfloat16* __restrict__ x,
+                                               __nv_bfloat16* __restrict__ xc, long long HW, int ntx,
+                                               int nty, int nxb, const unsigned short* __restrict__ w,
+                                               unsigned short* __restrict__ wp,
+                                               const unsigned short* __restrict__ w_off,
+                                               uint2* __restrict__ frag, int O, int C, int K, int M,
+                                               int ntiles, int cpc) {
+  __shared__ __align__(16) uint32_t tile[kTrPx * kTrPitch];
+  extern __shared__ __align__(16) unsigned short row[];  // C * K (weight blocks)
+  pdl_wait();
+  const int b = (int)blockIdx.x;
+  if (b < nxb)
+    nchw_to_nhwc_tile(x, xc, C, HW, b % ntx, (b / ntx) % nty, b / (ntx * nty), tile);
+  else
+    prep_weights_block(w, wp, w_off, frag, O, C, K, M, ntiles, cpc, b - nxb, row);
   pdl_release();
 }
 
@@ -979,36 +996,28 @@ size_t cl_wfrag_bytes(const Geom& g) {
   return (size_t)(g.K * g.c_in / 16) * ((g.M + 7) / 8) * 32 * sizeof(uint2);
 }
 
-cudaError_t launch_cl_prep_x(const void* x, void* xc, const Geom& g, cudaStream_t s) {
+cudaError_t launch_cl_prep(const void* x, void* xc, const void* w, void* wp, const void* w_off,
+                           void* frag, const Geom& g, int margin, cudaStream_t s) {
   const __nv_bfloat16* xp = static_cast<const __nv_bfloat16*>(x);
   __nv_bfloat16* xcp = static_cast<__nv_bfloat16*>(xc);
-  int C = g.c_in;
-  long long HW = g.hw;
-  void* args[] = {&xp, &xcp, &C, &HW};
-  return launch_pdl((const void*)nchw_to_nhwc,
-                    dim3((unsigned)ceil_div_ll(g.hw, kTrPx), (unsigned)(g.c_in / 64), (unsigned)g.n),
-                    dim3(256), 0, s, args);
-}
-
-cudaError_t launch_cl_prep_weights(const void* w, void* wp, const void* w_off, void* frag,
-                                   const Geom& g, int margin, cudaStream_t s) {
   const unsigned short* a = static_cast<const unsigned short*>(w);
   unsigned short* b = static_cast<unsigned short*>(wp);
   const unsigned short* c = static_cast<const unsigned short*>(w_off);
   uint2* f = static_cast<uint2*>(frag);
+  long long HW = g.hw;
+  int ntx = (int)ceil_div_ll(g.hw, kTrPx), nty = g.c_in / 64;
+  int nxb = ntx * nty * g.n;
   int O = w ? g.c_out : 0, C = g.c_in, K = g.K, M = g.M, nt = (g.M + 7) / 8;
   const int sms = sm_count();
   // the fragments are ordered by the channel slices the sampling stage's plan uses
   const ClPlan pl = cl_make_plan(g, margin, sms > 0 ? sms : 152);
   int cpc = pl.csplit > 0 ? g.c_in / pl.csplit : g.c_in;
-  const int blocks = O + (frag ? g.K * g.c_in / 16 : 0);
-  if (blocks == 0) return cudaSuccess;
+  const long long blocks = (long long)nxb + O + (frag ? g.K * g.c_in / 16 : 0);
   const size_t smem = (size_t)C * K * 2;
-  cudaError_t e = cudaFuncSetAttribute((const void*)prep_weights,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute((const void*)cl_prep, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  void* args[] = {&a, &b, &c, &f, &O, &C, &K, &M, &nt, &cpc};
-  return launch_pdl((const void*)prep_weights, dim3((unsigned)blocks), dim3(256), smem, s, args);
+  void* args[] = {&xp, &xcp, &HW, &ntx, &nty, &nxb, &a, &b, &c, &f, &O, &C, &K, &M, &nt, &cpc};
+  return launch_pdl((const void*)cl_prep, dim3((unsigned)blocks), dim3(256), smem, s, args);
 }
 
 cudaError_t launch_cl_sample(const ClArgs& in, cudaStream_t s) {
