@@ -60,7 +60,7 @@ TRAFFIC = {
     # 126 MB L2 are not counted (k4cl_input: layer 3's store with the ReLU
     # below fused, whose bf16 output stays in L2 for the next backward).
     ("stack_bf16", "k3_cl_bwd"): {"bytes": 171687424, "source": "02a91a919a0f90c2"},
-    ("stack_bf16", "k1_cl_sample"): {"bytes": 69343232, "source": "b041d0c0472493d0"},
+    ("stack_bf16", "k1_cl_sample"): {"bytes": 69400064, "source": "cbee7b1732934ddc"},
     ("stack_bf16", "k4cl_input"): {"bytes": 40613888, "source": "1f46bd658bb5b517"},
     ("stack_bf16", "k4cl_weight"): {"bytes": 14768640, "source": "1f46bd658bb5b517"},
     ("stack_bf16", "gemm_fwd"): {"bytes": 120043008, "source": "d21b94d0b4d051a4"},
